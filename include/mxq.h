@@ -1,0 +1,229 @@
+/*
+ * mxq.h -- C ABI of the GB300 (sm_103a) MXFP8 grouped-quantization and
+ * grouped-GEMM library for mixture-of-experts expert layers.
+ *
+ * The operations follow three TransformerEngine pull-request pages:
+ *   [RQ] PR #3244 "[Pytorch] Add support for row-wise quanted input for
+ *        grouped gemm" -- the description (fprop/dgrad read the rowwise
+ *        prequantized input directly; wgrad needs a columnwise copy made by
+ *        dequantize + columnwise requantize), the review threads on
+ *        prepare_prequantized_mxfp8_grouped_input (compact scale shape
+ *        (round_up(tokens,128), round_up(cols/32,4)); 128-token per-expert
+ *        alignment and hidden % 512 from the dispatch; dense swizzle of the
+ *        dispatch's rowwise scales; "group_quantize + swizzle fusion" for the
+ *        columnwise scales; compact scales required for dequantization) and
+ *        the Greptile flowchart (bias and routing-scale reductions from the
+ *        dequantized tensor).
+ *   [FM] PR #3545 "Fix distributed BF16 weights and trim NVFP4 saved state
+ *        in the fused grouped MLP" -- forward GEMMs read rowwise weights, the
+ *        columnwise weight copy exists for dgrad, every wgrad path reads
+ *        only columnwise input tiles; FC1 -> activation -> FC2.
+ *   [DI] PR #3224 "Improve device-init grouped linear module with single
+ *        grouped weight support" -- device-resident int64 m_splits (host
+ *        m_splits rejected), one grouped weight (E, out, in) and a 2-D
+ *        grouped bias (E, out), group_quantize output= reuse (caller-owned
+ *        outputs, stable pointers) and noop_flag for graph replay,
+ *        per-member swizzled scale bases in group_quantize_mxfp8, explicit
+ *        errors instead of silent fallbacks.
+ *
+ * Formats. E4M3 data bytes; one E8M0 scale byte (2^(code-127)) per 32
+ * contiguous elements: "rowwise" blocks run along the last dimension,
+ * "colwise" blocks along tokens (the first dimension) inside one expert.
+ * Colwise data bytes keep the (rows, cols) row-major byte order of the
+ * source. Shared exponent s = floor(log2(amax)) - 8 (clamped to
+ * [-127,127]; all-zero block -> code 0x00); elements are cast with
+ * round-to-nearest-even, saturating at +-448, sign kept (OCP MX v1.0).
+ *
+ * Scale layouts.
+ *   compact rowwise (R, C=cols/32) : (round_up(R,128), round_up(C,4)) bytes,
+ *                                    row-major, zero padded   [RQ]
+ *   compact colwise                : (round_up(R/32,4), round_up(cols,128))
+ *   swizzled                       : 128x4 tensor-core atoms (512 B): logical
+ *        S[r][c] of an (R, C) matrix lives at byte
+ *        ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4.
+ *        Rowwise scales of a grouped tensor are swizzled as one (R, cols/32)
+ *        matrix (valid because every m_e % 128 == 0 [RQ]); colwise scales
+ *        are swizzled PER EXPERT as the (cols, m_e/32) matrix
+ *        S_e[k][i] = scale of token block i of expert e at column k, placed
+ *        at byte cols*off_e/32 (off_e = tokens before expert e) [DI].
+ *
+ * Grouping contract: E >= 1 (<= MXQ_MAX_EXPERTS); every m_e >= 0 and a
+ * multiple of 128; sum(m_e) == M. cols (K, N) multiples of 128 for the
+ * quantizers; the GEMMs additionally need the output-tile width (the
+ * dimension written as 256-column tiles) to be a multiple of 256.
+ *
+ * Ownership. The caller allocates every input, output and workspace (device
+ * memory, 16-byte aligned); the library allocates nothing and keeps no
+ * state between calls other than a per-device cache of device attributes.
+ * Every call is asynchronous on `stream` and never synchronizes, except
+ * mxq_status_read.
+ *
+ * Errors. Host-detectable faults return a negative mxq error code before
+ * anything is launched. Data-dependent faults (m_splits on the device) are
+ * OR-ed into the caller's device status word *d_status (may be NULL to
+ * skip reporting); the work that depends on the bad data is skipped and its
+ * outputs are left untouched.
+ */
+#ifndef MXQ_H
+#define MXQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mxq_stream_t; /* identical to cudaStream_t */
+
+#if defined(__GNUC__)
+#define MXQ_API __attribute__((visibility("default")))
+#else
+#define MXQ_API
+#endif
+
+#define MXQ_MAX_EXPERTS 1024
+
+/* host return codes */
+enum {
+    MXQ_OK = 0,
+    MXQ_ERR_NULL = -1,         /* a required pointer is NULL */
+    MXQ_ERR_SHAPE = -2,        /* a dimension breaks the contract above */
+    MXQ_ERR_HOST_POINTER = -3, /* m_splits (or data) is not device memory [DI] */
+    MXQ_ERR_ARCH = -4,         /* current device is not sm_103 (GB300) */
+    MXQ_ERR_WORKSPACE = -5,    /* workspace smaller than mxq_workspace_bytes() */
+    MXQ_ERR_LAUNCH = -6,       /* a CUDA call failed (see mxq_last_cuda_error) */
+    MXQ_ERR_FLAGS = -7,        /* unknown or inconsistent flags */
+    MXQ_ERR_ALIGN = -8         /* a pointer is not 16-byte aligned */
+};
+
+/* device status word bits (sticky; OR-ed by the kernels) */
+enum {
+    MXQ_STATUS_SPLIT_UNALIGNED = 1, /* some m_e % 128 != 0 */
+    MXQ_STATUS_SPLIT_NEGATIVE = 2,  /* some m_e < 0 */
+    MXQ_STATUS_SPLIT_SUM = 4,       /* sum(m_e) != M */
+    MXQ_STATUS_WAIT_TIMEOUT = 8     /* a bounded on-chip wait expired (the kernel bailed out) */
+};
+
+/* flags */
+enum {
+    MXQ_ROWWISE = 1,      /* group_quantize: emit the rowwise copy;
+                             requant: emit the swizzled copy of the rowwise scales */
+    MXQ_COLWISE = 2,      /* emit the colwise copy */
+    MXQ_SWIZZLE = 4,      /* scales in the swizzled GEMM layout (else compact) */
+    MXQ_DEQUANT_OUT = 8,  /* requant: also write the dequantized bf16 tensor */
+    MXQ_ACCUMULATE = 16,  /* wgrad: dW += product (else dW = product) */
+    MXQ_OUT_BF16 = 32     /* wgrad: dW in bf16 (else fp32) */
+};
+
+/* operation ids for mxq_workspace_bytes */
+enum {
+    MXQ_OP_GROUP_QUANTIZE = 1,
+    MXQ_OP_REQUANT_COLWISE = 2,
+    MXQ_OP_GROUPED_DBIAS = 3,
+    MXQ_OP_GEMM_FPROP = 4,
+    MXQ_OP_GEMM_DGRAD = 5,
+    MXQ_OP_GEMM_WGRAD = 6
+};
+
+/* Library version (major*10000 + minor*100 + patch). */
+MXQ_API int mxq_version(void);
+
+/* Bytes of one scale buffer for an (rows, cols) tensor: the padded compact
+ * shape of [RQ]; for rows % 128 == 0 and cols % 128 == 0 the swizzled
+ * layout has the same size. colwise != 0 selects the colwise shape. */
+MXQ_API size_t mxq_scale_bytes(int64_t rows, int64_t cols, int colwise);
+
+/* Workspace bytes `op` needs for these sizes and flags (0 if none). For
+ * group_quantize / requant it is nonzero only when dbias is requested:
+ * fp32 column partial sums of every 128-row tile, (M/128) * K * 4 bytes. */
+MXQ_API size_t mxq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int flags);
+
+/* group_quantize [RQ][DI]: bf16 x (M, K) row-major, split into E experts by
+ * the device int64 array d_m_splits (NULL: E uniform members of M/E rows,
+ * the weight case (E*N, K) -- then M/E must be a multiple of 128) into
+ * MXFP8. flags: MXQ_ROWWISE and/or MXQ_COLWISE, optional MXQ_SWIZZLE.
+ *   row_data (M,K) E4M3, row_scale mxq_scale_bytes(M,K,0) bytes;
+ *   col_data (M,K) E4M3, col_scale mxq_scale_bytes(M,K,1) bytes;
+ *   dbias_out (E,K) fp32 or NULL: per-expert column sums of x (needs ws);
+ *   d_noop: NULL or a device int32; when it is nonzero the call writes
+ *   nothing (graph replay with a skipped step [DI]).
+ * Unused outputs may be NULL. Returns MXQ_OK or a negative code. */
+MXQ_API int mxq_group_quantize(const void* x_bf16, int64_t M, int64_t K, int E, const int64_t* d_m_splits, int flags,
+                       void* row_data, void* row_scale, void* col_data, void* col_scale, float* dbias_out,
+                       const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream);
+
+/* requant_colwise [RQ]: from a rowwise-prequantized grouped input (the
+ * expert-parallel FP8 dispatch's wire format: row_data (M,K) E4M3 with
+ * COMPACT scales row_scale_compact) build the colwise copy wgrad needs by
+ * dequantizing (exactly) and quantizing the dequantized values colwise.
+ *   flags: MXQ_COLWISE (col_data + col_scale, layout per MXQ_SWIZZLE),
+ *          MXQ_ROWWISE (row_scale_swizzled_out: the rowwise scales in the
+ *          GEMM layout, for fprop/dgrad on the rowwise data),
+ *          MXQ_DEQUANT_OUT (dequant_bf16_out (M,K)).
+ *   dbias_out (E,K) fp32 or NULL: per-expert sums of the dequantized
+ *   values (the "ordinary dbias" reduced without a wgrad stage; needs ws). */
+MXQ_API int mxq_requant_colwise(const void* row_data, const void* row_scale_compact, int64_t M, int64_t K, int E,
+                        const int64_t* d_m_splits, int flags, void* col_data, void* col_scale,
+                        void* row_scale_swizzled_out, float* dbias_out, void* dequant_bf16_out,
+                        const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream);
+
+/* grouped_dbias [RQ]: db[e, n] = sum over expert e's rows of dy[m, n];
+ * dy bf16 (M, N); out fp32 (E, N); an empty expert gets 0. Deterministic
+ * (fixed-order tree per 128-row tile, fp64 across tiles); needs ws. */
+MXQ_API int mxq_grouped_dbias(const void* dy_bf16, int64_t M, int64_t N, int E, const int64_t* d_m_splits, float* dbias_out,
+                      int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream);
+
+/* grouped fprop [RQ][DI]: Y[m, :] = X[m, :] . W[e(m)]^T (+ bias[e(m)]),
+ * X rowwise (M,K) E4M3 + swizzled rowwise scales; W rowwise (E,N,K) E4M3
+ * + swizzled rowwise scales of the (E*N, K) matrix; bias bf16 (E,N) or
+ * NULL (added in fp32 before rounding); Y bf16 (M,N). N % 256 == 0. */
+MXQ_API int mxq_grouped_gemm_fprop(const void* x_data, const void* x_scale, const void* w_data, const void* w_scale,
+                           const void* bias_bf16, int64_t M, int64_t N, int64_t K, int E,
+                           const int64_t* d_m_splits, void* y_bf16, int32_t* d_status, void* ws,
+                           size_t ws_bytes, mxq_stream_t stream);
+
+/* grouped dgrad [RQ][FM]: dX[m, :] = dY[m, :] . W[e(m)], dY rowwise (M,N)
+ * + swizzled rowwise scales; W colwise (E,N,K) E4M3 (W's byte order,
+ * blocks along N) + per-expert swizzled colwise scales (expert e: logical
+ * (K, N/32) at byte e*K*N/32); dX bf16 (M,K). K % 256 == 0. */
+MXQ_API int mxq_grouped_gemm_dgrad(const void* dy_data, const void* dy_scale, const void* w_col_data,
+                           const void* w_col_scale, int64_t M, int64_t N, int64_t K, int E,
+                           const int64_t* d_m_splits, void* dx_bf16, int32_t* d_status, void* ws,
+                           size_t ws_bytes, mxq_stream_t stream);
+
+/* grouped wgrad [RQ][FM]: dW[e] = dY_e^T . X_e over expert e's tokens,
+ * from the colwise copies only: dY colwise (M,N) + per-expert swizzled
+ * colwise scales, X colwise (M,K) + per-expert swizzled colwise scales.
+ * dW (E,N,K) fp32 (bf16 with MXQ_OUT_BF16); MXQ_ACCUMULATE adds into dW.
+ * An empty expert gets dW[e] = 0 (unchanged with MXQ_ACCUMULATE).
+ * K % 256 == 0. */
+MXQ_API int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_scale, const void* x_col_data,
+                           const void* x_col_scale, int64_t M, int64_t N, int64_t K, int E,
+                           const int64_t* d_m_splits, int flags, void* dw, int32_t* d_status, void* ws,
+                           size_t ws_bytes, mxq_stream_t stream);
+
+/* SwiGLU between FC1 and FC2 of the fused grouped MLP [FM] (reading: the
+ * first F columns of the FC1 output are the gate):
+ *   fwd: y (M, 2F) bf16 -> h (M, F) bf16, h = silu(g) * u;
+ *   bwd: dh (M, F), y (M, 2F) -> dy (M, 2F) = [dh*u*silu'(g) | dh*silu(g)].
+ * fp32 math, bf16 I/O. F % 8 == 0. */
+MXQ_API int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream);
+MXQ_API int mxq_swiglu_bwd(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F, void* dy_bf16,
+                   mxq_stream_t stream);
+
+/* Copy the device status word to *h_out after `stream` drains (the only
+ * synchronizing call). */
+MXQ_API int mxq_status_read(const int32_t* d_status, int32_t* h_out, mxq_stream_t stream);
+
+/* Text for a host return code. */
+MXQ_API const char* mxq_error_string(int code);
+
+/* The last CUDA error code seen by the library on this thread (0 if none). */
+MXQ_API int mxq_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXQ_H */

@@ -1,0 +1,270 @@
+// mxq_api.cu -- extern "C" entry points declared in include/mxq.h: host-side
+// validation (pointers, alignment, shapes, device residency of m_splits,
+// device architecture, workspace size), then one launch sequence on the
+// caller's stream. Nothing here synchronizes except mxq_status_read; nothing
+// here allocates.
+#include <cuda_runtime.h>
+
+#include "../../include/mxq.h"
+#include "mxq_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+int fail_cuda(cudaError_t e) {
+    g_last_cuda = (int)e;
+    return MXQ_ERR_LAUNCH;
+}
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device attribute cache: 1 = sm_103 (GB300), -1 = other, 0 = unknown.
+int arch_ok() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 64 && cache[dev]) return cache[dev] > 0;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    const int ok = (major == 10 && minor == 3) ? 1 : -1;
+    if (dev < 64) cache[dev] = ok;
+    return ok > 0;
+}
+
+// m_splits must be reachable from the device without a host round trip
+// [DI: host m_splits are rejected on the device-init path].
+bool device_pointer(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+int check_common(int64_t M, int64_t K, int E, const int64_t* m_splits, bool splits_required) {
+    if (!arch_ok()) return MXQ_ERR_ARCH;
+    if (M < 0 || K <= 0 || M % 128 || K % 128) return MXQ_ERR_SHAPE;
+    if (E < 1 || E > MXQ_MAX_EXPERTS) return MXQ_ERR_SHAPE;
+    if (M > ((int64_t)1 << 31) - 128 || K > ((int64_t)1 << 31) - 128) return MXQ_ERR_SHAPE;
+    if (m_splits == nullptr) {
+        if (splits_required) return MXQ_ERR_NULL;
+        if (M % E || (M / E) % 128) return MXQ_ERR_SHAPE;
+    } else if (!device_pointer(m_splits)) {
+        return MXQ_ERR_HOST_POINTER;
+    }
+    return MXQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxq_version(void) { return 100; }
+
+size_t mxq_scale_bytes(int64_t rows, int64_t cols, int colwise) {
+    auto up = [](int64_t a, int64_t b) { return (a + b - 1) / b * b; };
+    if (rows < 0 || cols < 0) return 0;
+    if (!colwise) return (size_t)(up(rows, 128) * up(cols / 32, 4));
+    return (size_t)(up(rows / 32, 4) * up(cols, 128));
+}
+
+size_t mxq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int flags) {
+    (void)E;
+    (void)flags;
+    switch (op) {
+        case MXQ_OP_GROUP_QUANTIZE:
+        case MXQ_OP_REQUANT_COLWISE: return (size_t)(M / 128) * (size_t)K * sizeof(float);
+        case MXQ_OP_GROUPED_DBIAS: return (size_t)(M / 128) * (size_t)N * sizeof(float);
+        default: return 0;
+    }
+}
+
+int mxq_group_quantize(const void* x_bf16, int64_t M, int64_t K, int E, const int64_t* d_m_splits, int flags,
+                       void* row_data, void* row_scale, void* col_data, void* col_scale, float* dbias_out,
+                       const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
+    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE)) return MXQ_ERR_FLAGS;
+    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE;
+    if (!row && !col && !dbias_out) return MXQ_ERR_FLAGS;
+    if (!x_bf16 || (row && (!row_data || !row_scale)) || (col && (!col_data || !col_scale))) return MXQ_ERR_NULL;
+    if (int r = check_common(M, K, E, d_m_splits, false)) return r;
+    if (!aligned16(x_bf16) || !aligned16(row_data) || !aligned16(row_scale) || !aligned16(col_data) ||
+        !aligned16(col_scale) || !aligned16(dbias_out) || !aligned16(ws))
+        return MXQ_ERR_ALIGN;
+    if (dbias_out && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GROUP_QUANTIZE, M, 0, K, E, flags)))
+        return MXQ_ERR_WORKSPACE;
+    mxq::QuantCall c{};
+    c.x = x_bf16;
+    c.M = M;
+    c.K = K;
+    c.E = E;
+    c.m_splits = d_m_splits;
+    c.row_q = row ? row_data : nullptr;
+    c.row_s = row ? row_scale : nullptr;
+    c.col_q = col ? col_data : nullptr;
+    c.col_s = col ? col_scale : nullptr;
+    c.dbias = dbias_out;
+    c.partials = dbias_out ? static_cast<float*>(ws) : nullptr;
+    c.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    c.noop = d_noop;
+    c.status = d_status;
+    cudaError_t e = mxq::run_group_quantize(c, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_requant_colwise(const void* row_data, const void* row_scale_compact, int64_t M, int64_t K, int E,
+                        const int64_t* d_m_splits, int flags, void* col_data, void* col_scale,
+                        void* row_scale_swizzled_out, float* dbias_out, void* dequant_bf16_out,
+                        const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
+    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE | MXQ_DEQUANT_OUT)) return MXQ_ERR_FLAGS;
+    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE, deq = flags & MXQ_DEQUANT_OUT;
+    if (!row && !col && !deq && !dbias_out) return MXQ_ERR_FLAGS;
+    if (!row_data || !row_scale_compact || (col && (!col_data || !col_scale)) || (row && !row_scale_swizzled_out) ||
+        (deq && !dequant_bf16_out))
+        return MXQ_ERR_NULL;
+    if (int r = check_common(M, K, E, d_m_splits, false)) return r;
+    if (!aligned16(row_data) || !aligned16(row_scale_compact) || !aligned16(col_data) || !aligned16(col_scale) ||
+        !aligned16(row_scale_swizzled_out) || !aligned16(dbias_out) || !aligned16(dequant_bf16_out) ||
+        !aligned16(ws))
+        return MXQ_ERR_ALIGN;
+    if (dbias_out && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_REQUANT_COLWISE, M, 0, K, E, flags)))
+        return MXQ_ERR_WORKSPACE;
+    mxq::RequantCall c{};
+    c.row_q = row_data;
+    c.row_s_compact = row_scale_compact;
+    c.M = M;
+    c.K = K;
+    c.E = E;
+    c.m_splits = d_m_splits;
+    c.col_q = col ? col_data : nullptr;
+    c.col_s = col ? col_scale : nullptr;
+    c.row_s_swizzled = row ? row_scale_swizzled_out : nullptr;
+    c.dbias = dbias_out;
+    c.partials = dbias_out ? static_cast<float*>(ws) : nullptr;
+    c.deq_out = deq ? dequant_bf16_out : nullptr;
+    c.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    c.noop = d_noop;
+    c.status = d_status;
+    cudaError_t e = mxq::run_requant(c, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_grouped_dbias(const void* dy_bf16, int64_t M, int64_t N, int E, const int64_t* d_m_splits, float* dbias_out,
+                      int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
+    if (!dy_bf16 || !dbias_out) return MXQ_ERR_NULL;
+    if (int r = check_common(M, N, E, d_m_splits, true)) return r;
+    if (!aligned16(dy_bf16) || !aligned16(dbias_out) || !aligned16(ws)) return MXQ_ERR_ALIGN;
+    if (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GROUPED_DBIAS, M, N, 0, E, 0)) return MXQ_ERR_WORKSPACE;
+    cudaError_t e = mxq::run_grouped_dbias(dy_bf16, M, N, E, d_m_splits, dbias_out, static_cast<float*>(ws), d_status,
+                                           (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+static int gemm_common(int mode, const void* a, const void* as, const void* b, const void* bs, const void* bias,
+                       int64_t M, int64_t N, int64_t K, int E, const int64_t* m_splits, void* out, int accumulate,
+                       int out_bf16, int32_t* d_status, mxq_stream_t stream) {
+    if (!a || !as || !b || !bs || !out) return MXQ_ERR_NULL;
+    if (int r = check_common(M, K, E, m_splits, true)) return r;
+    if (N <= 0 || N % 128 || N > ((int64_t)1 << 31) / 128) return MXQ_ERR_SHAPE;
+    if ((int64_t)E * N > ((int64_t)1 << 31) - 256) return MXQ_ERR_SHAPE;
+    if (mode == mxq::kFprop && N % 256) return MXQ_ERR_SHAPE;
+    if (mode != mxq::kFprop && K % 256) return MXQ_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(as) || !aligned16(b) || !aligned16(bs) || !aligned16(bias) || !aligned16(out))
+        return MXQ_ERR_ALIGN;
+    mxq::GemmCall c{};
+    c.mode = mode;
+    c.a_data = a;
+    c.a_scale = as;
+    c.b_data = b;
+    c.b_scale = bs;
+    c.bias = bias;
+    c.M = M;
+    c.N = N;
+    c.K = K;
+    c.E = E;
+    c.m_splits = m_splits;
+    c.out = out;
+    c.accumulate = accumulate;
+    c.out_bf16 = out_bf16;
+    c.status = d_status;
+    cudaError_t e = mxq::run_grouped_gemm(c, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_grouped_gemm_fprop(const void* x_data, const void* x_scale, const void* w_data, const void* w_scale,
+                           const void* bias_bf16, int64_t M, int64_t N, int64_t K, int E,
+                           const int64_t* d_m_splits, void* y_bf16, int32_t* d_status, void* ws,
+                           size_t ws_bytes, mxq_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    return gemm_common(mxq::kFprop, x_data, x_scale, w_data, w_scale, bias_bf16, M, N, K, E, d_m_splits, y_bf16, 0, 1,
+                       d_status, stream);
+}
+
+int mxq_grouped_gemm_dgrad(const void* dy_data, const void* dy_scale, const void* w_col_data,
+                           const void* w_col_scale, int64_t M, int64_t N, int64_t K, int E,
+                           const int64_t* d_m_splits, void* dx_bf16, int32_t* d_status, void* ws,
+                           size_t ws_bytes, mxq_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    return gemm_common(mxq::kDgrad, dy_data, dy_scale, w_col_data, w_col_scale, nullptr, M, N, K, E, d_m_splits,
+                       dx_bf16, 0, 1, d_status, stream);
+}
+
+int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_scale, const void* x_col_data,
+                           const void* x_col_scale, int64_t M, int64_t N, int64_t K, int E,
+                           const int64_t* d_m_splits, int flags, void* dw, int32_t* d_status, void* ws,
+                           size_t ws_bytes, mxq_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (flags & ~(MXQ_ACCUMULATE | MXQ_OUT_BF16)) return MXQ_ERR_FLAGS;
+    return gemm_common(mxq::kWgrad, dy_col_data, dy_col_scale, x_col_data, x_col_scale, nullptr, M, N, K, E,
+                       d_m_splits, dw, (flags & MXQ_ACCUMULATE) != 0, (flags & MXQ_OUT_BF16) != 0, d_status, stream);
+}
+
+int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream) {
+    if (!y_bf16 || !h_bf16) return MXQ_ERR_NULL;
+    if (!arch_ok()) return MXQ_ERR_ARCH;
+    if (M < 0 || F <= 0 || F % 8) return MXQ_ERR_SHAPE;
+    if (!aligned16(y_bf16) || !aligned16(h_bf16)) return MXQ_ERR_ALIGN;
+    cudaError_t e = mxq::run_swiglu_fwd(y_bf16, M, F, h_bf16, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_swiglu_bwd(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F, void* dy_bf16,
+                   mxq_stream_t stream) {
+    if (!dh_bf16 || !y_bf16 || !dy_bf16) return MXQ_ERR_NULL;
+    if (!arch_ok()) return MXQ_ERR_ARCH;
+    if (M < 0 || F <= 0 || F % 8) return MXQ_ERR_SHAPE;
+    if (!aligned16(dh_bf16) || !aligned16(y_bf16) || !aligned16(dy_bf16)) return MXQ_ERR_ALIGN;
+    cudaError_t e = mxq::run_swiglu_bwd(dh_bf16, y_bf16, M, F, dy_bf16, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_status_read(const int32_t* d_status, int32_t* h_out, mxq_stream_t stream) {
+    if (!d_status || !h_out) return MXQ_ERR_NULL;
+    cudaError_t e = cudaMemcpyAsync(h_out, d_status, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+const char* mxq_error_string(int code) {
+    switch (code) {
+        case MXQ_OK: return "ok";
+        case MXQ_ERR_NULL: return "a required pointer is NULL";
+        case MXQ_ERR_SHAPE: return "a dimension breaks the shape contract";
+        case MXQ_ERR_HOST_POINTER: return "m_splits must be device memory (host m_splits are rejected)";
+        case MXQ_ERR_ARCH: return "the current device is not sm_103 (GB300)";
+        case MXQ_ERR_WORKSPACE: return "workspace missing or smaller than mxq_workspace_bytes()";
+        case MXQ_ERR_LAUNCH: return "a CUDA call failed (see mxq_last_cuda_error)";
+        case MXQ_ERR_FLAGS: return "unknown or inconsistent flags";
+        case MXQ_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        default: return "unknown error";
+    }
+}
+
+int mxq_last_cuda_error(void) { return g_last_cuda; }
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// mxq_common.cuh -- device helpers shared by the MXFP8 kernels of this library.
+//
+// MX conventions (OCP MX v1.0, E4M3 elements, E8M0 scales; the pages name
+// MXFP8 E4M3 with one scale per 32 elements -- TransformerEngine PR #3244,
+// "[Pytorch] Add support for row-wise quanted input for grouped gemm",
+// review on the compact scale shape `cols // 32`):
+//   shared exponent s = floor(log2(amax)) - 8, clamped to [-127, 127];
+//   all-zero block -> code 0; code = s + 127;
+//   element = cvt.rn.satfinite.e4m3(x * 2^-s) (RNE, saturating, sign kept).
+// The exponent is read from the bits of amax: for a finite non-negative
+// IEEE value with biased exponent field F (bias 127), floor(log2) = F - 127
+// for normals and < -126 for subnormals, so code = max(F - 8, 0) for both
+// bf16 (F = bits >> 7) and fp32 (F = bits >> 23).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mxq.h"
+
+namespace mxq {
+
+constexpr int kTile = 128;  // rows x cols of one quantization tile
+
+__device__ __forceinline__ uint32_t scale_code_from_bf16_absbits(uint32_t absbits) {
+    int f = (int)(absbits >> 7);
+    return (uint32_t)max(f - 8, 0);
+}
+__device__ __forceinline__ uint32_t scale_code_from_f32_absbits(uint32_t absbits) {
+    int f = (int)(absbits >> 23);
+    return (uint32_t)max(f - 8, 0);
+}
+// 2^-s as an fp32 for code = s + 127 in [0, 246]: exponent field 254 - code.
+__device__ __forceinline__ float inv_scale_from_code(uint32_t code) {
+    return __uint_as_float((254u - code) << 23);
+}
+// 2^s as an fp32 for any code in [0, 254] (code 0 -> 2^-127, an fp32 subnormal).
+__device__ __forceinline__ float scale_from_code(uint32_t code) {
+    return __uint_as_float(code ? (code << 23) : 0x00400000u);
+}
+
+// Two fp32 -> two E4M3 bytes (lo = a, hi = b), RNE, saturating finite.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return (uint32_t)r;
+}
+// Two E4M3 bytes (lo, hi of v) -> two fp32, exact.
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint16_t v) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    __half2 h = *reinterpret_cast<__half2*>(&h2);
+    return __half22float2(h);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Per-CTA view of the grouping: exclusive token offsets off[0..E] in shared
+// memory. d_m_splits == nullptr means E uniform members of M/E rows.
+// Validates the contract (m_e >= 0, m_e % 128 == 0, sum == M) and returns a
+// status bit mask (0 = valid). Must be called by all threads of the block.
+__device__ __forceinline__ int load_offsets(const int64_t* __restrict__ d_m_splits, int E, int64_t M,
+                                            int64_t* s_off) {
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    if (tid < 32) {
+        const int lane = tid;
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int64_t local = 0;
+        int bad = 0;
+        for (int e = lo; e < hi; ++e) {
+            int64_t v = d_m_splits ? d_m_splits[e] : M / E;
+            if (v < 0) bad |= MXQ_STATUS_SPLIT_NEGATIVE;
+            if (v % 128) bad |= MXQ_STATUS_SPLIT_UNALIGNED;
+            local += v;
+        }
+        int64_t incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int64_t run = incl - local;
+        for (int e = lo; e < hi; ++e) {
+            s_off[e] = run;
+            run += d_m_splits ? d_m_splits[e] : M / E;
+        }
+        int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+        bad = __reduce_or_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            s_off[E] = total;
+            if (total != M) bad |= MXQ_STATUS_SPLIT_SUM;
+            s_bad = bad;
+        }
+    }
+    __syncthreads();
+    return s_bad;
+}
+
+// Expert owning row `row` (0 <= row < M): the e with off[e] <= row < off[e+1].
+__device__ __forceinline__ int expert_of(const int64_t* s_off, int E, int64_t row) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {  // first e with off[e+1] > row
+        int mid = (lo + hi) >> 1;
+        if (s_off[mid + 1] > row) hi = mid;
+        else lo = mid + 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void report_status(int32_t* d_status, int bits) {
+    if (d_status && bits && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(d_status, bits);
+}
+
+}  // namespace mxq

@@ -1,0 +1,625 @@
+// mxq_gemm.cu -- grouped MXFP8 GEMMs of an MoE expert layer on GB300 (sm_103a):
+//   fprop  Y[m,:]  = X[m,:]  . W[e(m)]^T (+ b[e(m)])   rowwise X, rowwise W
+//   dgrad  dX[m,:] = dY[m,:] . W[e(m)]                 rowwise dY, colwise W
+//   wgrad  dW[e]   = dY_e^T . X_e                      colwise dY, colwise X
+// (TransformerEngine PR #3244, "[Pytorch] Add support for row-wise quanted
+// input for grouped gemm": fprop/dgrad on the rowwise copy, wgrad on the
+// columnwise copy; PR #3545, "Fix distributed BF16 weights and trim NVFP4
+// saved state in the fused grouped MLP": the columnwise weight copy exists for
+// dgrad, wgrad reads only columnwise tiles; PR #3224, "Improve device-init
+// grouped linear module with single grouped weight support": device m_splits
+// read without a host sync, one grouped weight (E,out,in), 2-D grouped bias.)
+//
+// Kernel: persistent, one CTA (192 threads) per SM, warp-specialised.
+//   warp 0      TMA producer: 128x128-byte E4M3 boxes (128B swizzle) for A and
+//               two for B per 128-deep K block, plus the 512-byte scale atoms
+//               (already in the tensor-core 128x4 layout) by bulk copy;
+//   warp 1      owns TMEM (512 columns) and, from one lane, issues
+//               tcgen05.cp (scales -> TMEM) and tcgen05.mma
+//               .kind::mxf8f6f4.block_scale (M=128, N=256, K=32, fp32 accum);
+//   warps 2..5  epilogue: tcgen05.ld the 128x256 fp32 accumulator, add bias,
+//               convert, store to global.
+// A 4-stage shared-memory ring (mbarrier full/empty) feeds the tensor core;
+// the accumulator is released to the MMA warp as soon as it has been read
+// into registers, so the next tile's MMAs overlap the global stores.
+//
+// Operand majorness: K-major (A of fprop/dgrad, B of fprop) and MN-major (B of
+// dgrad, A and B of wgrad: the columnwise copies keep the source's byte
+// order, so their contiguous dimension is the MMA's M or N). Both use the
+// 128-byte swizzle; MN-major tiles are read straight from the un-transposed
+// colwise copy.
+//
+// Tile schedule: fprop/dgrad are a dense grid of 128-row x 256-col tiles over
+// the M routed rows (a 128-row tile never straddles two experts because every
+// m_e % 128 == 0; its expert comes from an on-chip prefix sum of the device
+// m_splits). wgrad tiles are (expert, 128 rows of N, 256 cols of K) with a
+// K loop of m_e/128 blocks; they are ordered heaviest expert first and dealt
+// to CTAs in a serpentine so that per-CTA work is balanced.
+//
+// Every wait on an mbarrier is bounded (about 2 s of wall time); on expiry the
+// kernel sets MXQ_STATUS_WAIT_TIMEOUT, stops issuing work, frees its TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "mxq_common.cuh"
+#include "mxq_internal.h"
+
+namespace mxq {
+namespace gemm {
+
+constexpr int BM = 128;               // MMA M (rows of A per tile)
+constexpr int BN = 256;               // MMA N (cols of the output tile)
+constexpr int BK = 128;               // K elements (bytes) per pipeline stage
+constexpr int UMMA_K = 32;            // K per tcgen05.mma for 8-bit operands
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;      // 16 KB
+constexpr int B_BYTES = BN * BK;      // 32 KB
+constexpr int SFA_OFF = A_BYTES + B_BYTES;
+constexpr int SFB_OFF = SFA_OFF + 512;
+constexpr int STAGE_BYTES = 51200;    // 50 KB: keeps every stage 1024-aligned
+constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + 512 + 1024;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int TMEM_SFA = 256;         // scale columns after the accumulator
+constexpr int TMEM_SFB = 264;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+struct Params {
+    int mode;
+    int64_t M, N, K;
+    int E;
+    const int64_t* m_splits;
+    const uint8_t* sfa;  // scale base of A
+    const uint8_t* sfb;  // scale base of B
+    const __nv_bfloat16* bias;
+    void* out;
+    int accumulate, out_bf16;
+    int32_t* status;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: true when the phase with `parity` completed; false after
+// ~2 s or once another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 63) == 63) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start>>4 [0,14), LBO>>4 [16,30),
+// SBO>>4 [32,46), version 1 [46,48), layout [61,64) (2 = 128B swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)(layout & 7u) << 61;
+    return d;
+}
+
+// Instruction descriptor for kind::mxf8f6f4 (E4M3 x E4M3, fp32 accum,
+// UE8M0 scales): b_sf_id [4,6), a_fmt [7,10)=0, b_fmt [10,13)=0,
+// a_major [15], b_major [16], N>>3 [17,23), scale type UE8M0 [23],
+// M>>4 [24,29), a_sf_id [29,31).
+__device__ __forceinline__ uint32_t idesc(uint32_t a_mn, uint32_t b_mn, uint32_t sf_id) {
+    return (sf_id << 4) | (a_mn << 15) | (b_mn << 16) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(accum), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+#define TMEM_LD32(taddr, r)                                                                                     \
+    asm volatile(                                                                                              \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17," \
+        "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                                      \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),         \
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), \
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),           \
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),           \
+          "=r"(r[30]), "=r"(r[31])                                                                              \
+        : "r"(taddr))
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------ tile schedule
+struct Tile {
+    int64_t a_row;   // fprop/dgrad: first token row; wgrad: first N row
+    int64_t b_col;   // first output column (N for fprop, K for dgrad/wgrad)
+    int e;
+    int64_t off, me; // expert token offset / count
+    int nk;          // number of 128-deep K blocks
+    bool valid;
+};
+
+struct Sched {
+    int mode;
+    int64_t M, N, K;
+    int E;
+    const int64_t* off;     // shared: exclusive offsets
+    const int16_t* order;   // shared (wgrad): experts sorted by load, heaviest first
+    int64_t tiles_n;        // fprop/dgrad: output col tiles; wgrad: tiles per expert
+    int64_t total;
+
+    __device__ void init(int mode_, int64_t M_, int64_t N_, int64_t K_, int E_, const int64_t* off_,
+                         const int16_t* order_) {
+        mode = mode_; M = M_; N = N_; K = K_; E = E_; off = off_; order = order_;
+        if (mode == kFprop) { tiles_n = N / BN; total = (M / BM) * tiles_n; }
+        else if (mode == kDgrad) { tiles_n = K / BN; total = (M / BM) * tiles_n; }
+        else { tiles_n = (N / BM) * (K / BN); total = (int64_t)E * tiles_n; }
+    }
+    // i-th tile of CTA `cta` among `ncta` (serpentine deal over the ordered list)
+    __device__ int64_t pick(int64_t i, int cta, int ncta) const {
+        const int64_t round = i, base = round * ncta;
+        return (round & 1) ? base + (ncta - 1 - cta) : base + cta;
+    }
+    __device__ Tile get(int64_t t) const {
+        Tile T;
+        T.valid = t < total;
+        if (!T.valid) return T;
+        if (mode != kWgrad) {
+            const int64_t mt = t / tiles_n, nt = t % tiles_n;
+            T.a_row = mt * BM;
+            T.b_col = nt * BN;
+            T.e = expert_of(off, E, T.a_row);
+            T.off = off[T.e];
+            T.me = off[T.e + 1] - T.off;
+            T.nk = (int)((mode == kFprop ? K : N) / BK);
+        } else {
+            const int64_t ei = t / tiles_n, r = t % tiles_n;
+            const int64_t kt = K / BN;
+            T.e = order[ei];
+            T.a_row = (r / kt) * BM;
+            T.b_col = (r % kt) * BN;
+            T.off = off[T.e];
+            T.me = off[T.e + 1] - T.off;
+            T.nk = (int)(T.me / BK);
+        }
+        return T;
+    }
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int64_t s_off[MXQ_MAX_EXPERTS + 1];
+    __shared__ int16_t s_order[MXQ_MAX_EXPERTS];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bad = load_offsets(p.m_splits, p.E, p.M, s_off);
+    if (bad) {
+        report_status(p.status, bad);
+        return;
+    }
+    if (p.mode == kWgrad) {
+        // rank experts by token count, heaviest first (ties: lower index first)
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+            const int64_t me = s_off[e + 1] - s_off[e];
+            int rank = 0;
+            for (int f = 0; f < p.E; ++f) {
+                const int64_t mf = s_off[f + 1] - s_off[f];
+                rank += (mf > me) || (mf == me && f < e);
+            }
+            s_order[rank] = (int16_t)e;
+        }
+    }
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+    const uint32_t acc_full = smem_u32(bars + 2 * STAGES), acc_empty = smem_u32(bars + 2 * STAGES + 1);
+    volatile int* abort_flag = &s_abort;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = s_tmem;
+
+    Sched S;
+    S.init(p.mode, p.M, p.N, p.K, p.E, s_off, s_order);
+    const int ncta = gridDim.x, cta = blockIdx.x;
+    const uint32_t a_mn = (p.mode == kWgrad) ? 1u : 0u;
+    const uint32_t b_mn = (p.mode == kFprop) ? 0u : 1u;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t i = 0;; ++i) {
+                const Tile T = S.get(S.pick(i, cta, ncta));
+                if (!T.valid) break;
+                for (int kb = 0; kb < T.nk; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) goto done_producer;
+                    const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, STAGE_TX);
+                    const uint8_t *sfa, *sfb0, *sfb1;
+                    if (p.mode == kFprop) {
+                        const int64_t kbs = p.K / BK;
+                        tma_load_2d(sb, &tmA, fb, kb * BK, (int)T.a_row);
+                        const int64_t wrow = (int64_t)T.e * p.N + T.b_col;
+                        tma_load_2d(sb + A_BYTES, &tmB, fb, kb * BK, (int)wrow);
+                        tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, kb * BK, (int)(wrow + 128));
+                        sfa = p.sfa + ((T.a_row / 128) * kbs + kb) * 512;
+                        sfb0 = p.sfb + ((wrow / 128) * kbs + kb) * 512;
+                        sfb1 = p.sfb + ((wrow / 128 + 1) * kbs + kb) * 512;
+                    } else if (p.mode == kDgrad) {
+                        const int64_t kbs = p.N / BK;
+                        tma_load_2d(sb, &tmA, fb, kb * BK, (int)T.a_row);
+                        const int64_t wrow = (int64_t)T.e * p.N + kb * BK;
+                        tma_load_2d(sb + A_BYTES, &tmB, fb, (int)T.b_col, (int)wrow);
+                        tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, (int)(T.b_col + 128), (int)wrow);
+                        sfa = p.sfa + ((T.a_row / 128) * kbs + kb) * 512;
+                        const uint8_t* wb = p.sfb + (int64_t)T.e * p.K * (p.N / 32);
+                        sfb0 = wb + ((T.b_col / 128) * kbs + kb) * 512;
+                        sfb1 = wb + ((T.b_col / 128 + 1) * kbs + kb) * 512;
+                    } else {
+                        const int64_t kbs = T.me / BK;
+                        const int64_t trow = T.off + (int64_t)kb * BK;
+                        tma_load_2d(sb, &tmA, fb, (int)T.a_row, (int)trow);
+                        tma_load_2d(sb + A_BYTES, &tmB, fb, (int)T.b_col, (int)trow);
+                        tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, (int)(T.b_col + 128), (int)trow);
+                        const uint8_t* ab = p.sfa + p.N * T.off / 32;
+                        const uint8_t* bb = p.sfb + p.K * T.off / 32;
+                        sfa = ab + ((T.a_row / 128) * kbs + kb) * 512;
+                        sfb0 = bb + ((T.b_col / 128) * kbs + kb) * 512;
+                        sfb1 = bb + ((T.b_col / 128 + 1) * kbs + kb) * 512;
+                    }
+                    bulk_load(sb + SFA_OFF, sfa, 512, fb);
+                    bulk_load(sb + SFB_OFF, sfb0, 512, fb);
+                    bulk_load(sb + SFB_OFF + 512, sfb1, 512, fb);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        done_producer:;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, aphase = 0;
+            // per-k-step descriptor advance: K-major +32 B; MN-major +32 rows (4 KB)
+            const uint32_t a_step = a_mn ? 4096u : 32u, b_step = b_mn ? 4096u : 32u;
+            for (int64_t i = 0;; ++i) {
+                const Tile T = S.get(S.pick(i, cta, ncta));
+                if (!T.valid) break;
+                if (!mbar_wait(acc_empty, aphase ^ 1, abort_flag)) break;
+                fence_after();
+                if (T.nk == 0) {
+                    mbar_arrive(acc_full);
+                } else {
+                    for (int kb = 0; kb < T.nk; ++kb) {
+                        if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) goto done_mma;
+                        fence_after();
+                        const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
+                        tmem_cp_sf(tmem + TMEM_SFA, smem_desc(sb + SFA_OFF, 0, 128, 0));
+                        tmem_cp_sf(tmem + TMEM_SFB, smem_desc(sb + SFB_OFF, 0, 128, 0));
+                        tmem_cp_sf(tmem + TMEM_SFB + 4, smem_desc(sb + SFB_OFF + 512, 0, 128, 0));
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            const uint64_t ad = a_mn ? smem_desc(sb + k * a_step, BK * 128, 1024, 2)
+                                                     : smem_desc(sb + k * a_step, 16, 1024, 2);
+                            const uint64_t bd = b_mn ? smem_desc(sb + A_BYTES + k * b_step, BK * 128, 1024, 2)
+                                                     : smem_desc(sb + A_BYTES + k * b_step, 16, 1024, 2);
+                            mma_mxf8(tmem, ad, bd, idesc(a_mn, b_mn, (uint32_t)k), tmem + TMEM_SFA, tmem + TMEM_SFB,
+                                     (kb | k) != 0);
+                        }
+                        mma_commit(empty0 + 8 * stage);
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    mma_commit(acc_full);
+                }
+                aphase ^= 1;
+            }
+        done_mma:;
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        uint32_t aphase = 0;
+        for (int64_t i = 0;; ++i) {
+            const Tile T = S.get(S.pick(i, cta, ncta));
+            if (!T.valid) break;
+            const bool ok = mbar_wait(acc_full, aphase, abort_flag);
+            __syncwarp();
+            if (!ok || *abort_flag) break;
+            fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+            if (p.mode != kWgrad) {
+                const int64_t row = T.a_row + row_in_tile;
+                const int64_t ldo = (p.mode == kFprop) ? p.N : p.K;
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + row * ldo + T.b_col;
+                const __nv_bfloat16* bias =
+                    (p.mode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    TMEM_LD32(tbase + c * 32, r);
+                    tmem_wait_ld();
+                    if (c == BN / 32 - 1) {
+                        fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
+                    }
+                    float f[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+                    if (bias) {
+                        const uint4* bp = reinterpret_cast<const uint4*>(bias + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint4 bw = __ldg(bp + v);
+                            const uint32_t ws[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                f[8 * v + 2 * j] += __uint_as_float(ws[j] << 16);
+                                f[8 * v + 2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
+                            }
+                        }
+                    }
+                    uint32_t h[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+                        h[j] = *reinterpret_cast<uint32_t*>(&b2);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                }
+            } else {
+                const int64_t row = T.a_row + row_in_tile;  // n
+                const int64_t base = ((int64_t)T.e * p.N + row) * p.K + T.b_col;
+                const bool zero = (T.nk == 0);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    if (!zero) {
+                        TMEM_LD32(tbase + c * 32, r);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+                    if (c == BN / 32 - 1) {
+                        fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
+                    }
+                    if (zero && p.accumulate) continue;
+                    if (p.out_bf16) {
+                        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base + c * 32;
+                        uint4* dst = reinterpret_cast<uint4*>(out);
+                        float f[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+                        if (p.accumulate) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const uint4 o = dst[v];
+                                const uint32_t ws[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    f[8 * v + 2 * j] += __uint_as_float(ws[j] << 16);
+                                    f[8 * v + 2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
+                                }
+                            }
+                        }
+                        uint32_t h[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+                            h[j] = *reinterpret_cast<uint32_t*>(&b2);
+                        }
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base + c * 32);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                            if (p.accumulate) {
+                                const float4 old = dst[v];
+                                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+                            }
+                            dst[v] = o;
+                        }
+                    }
+                }
+            }
+            aphase ^= 1;
+        }
+    }
+
+    fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0 && p.status) atomicOr(p.status, MXQ_STATUS_WAIT_TIMEOUT);
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// 2-D uint8 tensor (outer rows x inner cols, row-major), box 128 x 128, 128B swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return v;
+}
+
+}  // namespace gemm
+
+cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
+    using namespace gemm;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    CUtensorMap ta, tb;
+    bool ok;
+    if (c.mode == kFprop) {
+        ok = make_map(&ta, c.a_data, c.M, c.K) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
+    } else if (c.mode == kDgrad) {
+        ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
+    } else {
+        ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, c.M, c.K);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+
+    Params p{};
+    p.mode = c.mode;
+    p.M = c.M;
+    p.N = c.N;
+    p.K = c.K;
+    p.E = c.E;
+    p.m_splits = c.m_splits;
+    p.sfa = static_cast<const uint8_t*>(c.a_scale);
+    p.sfb = static_cast<const uint8_t*>(c.b_scale);
+    p.bias = static_cast<const __nv_bfloat16*>(c.bias);
+    p.out = c.out;
+    p.accumulate = c.accumulate;
+    p.out_bf16 = c.out_bf16;
+    p.status = c.status;
+
+    int64_t tiles;
+    if (c.mode == kFprop) tiles = (c.M / BM) * (c.N / BN);
+    else if (c.mode == kDgrad) tiles = (c.M / BM) * (c.K / BN);
+    else tiles = (int64_t)c.E * (c.N / BM) * (c.K / BN);
+    if (tiles == 0) return cudaSuccess;
+    const int grid = (int)std::min<int64_t>(tiles, sm_count());
+    grouped_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace mxq

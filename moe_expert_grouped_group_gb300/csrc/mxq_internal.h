@@ -1,0 +1,60 @@
+// mxq_internal.h -- launcher interfaces between the C ABI (mxq_api.cu) and
+// the kernel translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mxq {
+
+struct QuantCall {
+    const void* x;
+    int64_t M, K;
+    int E;
+    const int64_t* m_splits;
+    void *row_q, *row_s, *col_q, *col_s;
+    float* dbias;
+    float* partials;  // workspace, (M/128)*K fp32, when dbias != nullptr
+    int swizzle;
+    const int32_t* noop;
+    int32_t* status;
+};
+
+struct RequantCall {
+    const void* row_q;
+    const void* row_s_compact;
+    int64_t M, K;
+    int E;
+    const int64_t* m_splits;
+    void *col_q, *col_s, *row_s_swizzled;
+    float* dbias;
+    float* partials;
+    void* deq_out;
+    int swizzle;
+    const int32_t* noop;
+    int32_t* status;
+};
+
+enum GemmMode { kFprop = 0, kDgrad = 1, kWgrad = 2 };
+
+struct GemmCall {
+    int mode;
+    const void *a_data, *a_scale, *b_data, *b_scale;
+    const void* bias;  // fprop only
+    int64_t M, N, K;
+    int E;
+    const int64_t* m_splits;
+    void* out;
+    int accumulate, out_bf16;  // wgrad only
+    int32_t* status;
+};
+
+cudaError_t run_group_quantize(const QuantCall& c, cudaStream_t s);
+cudaError_t run_requant(const RequantCall& c, cudaStream_t s);
+cudaError_t run_grouped_dbias(const void* dy, int64_t M, int64_t N, int E, const int64_t* m_splits, float* out,
+                              float* partials, int32_t* status, cudaStream_t s);
+cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s);
+cudaError_t run_swiglu_fwd(const void* y, int64_t M, int64_t F, void* h, cudaStream_t s);
+cudaError_t run_swiglu_bwd(const void* dh, const void* y, int64_t M, int64_t F, void* dy, cudaStream_t s);
+
+}  // namespace mxq

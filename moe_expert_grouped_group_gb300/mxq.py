@@ -1,0 +1,252 @@
+"""Thin Python binding of libmxq.so (the C ABI in include/mxq.h).
+
+Argument marshalling only: PyTorch supplies device memory and the current
+CUDA stream; every step of the path runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or the device is not a
+GB300 (sm_103), calls raise.
+
+Tensors: activations/weights bf16; E4M3 data and E8M0 scales are uint8;
+m_splits is a CUDA int64 tensor (host m_splits are rejected by the library).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB
+
+ROWWISE, COLWISE, SWIZZLE, DEQUANT_OUT, ACCUMULATE, OUT_BF16 = 1, 2, 4, 8, 16, 32
+OP_GROUP_QUANTIZE, OP_REQUANT_COLWISE, OP_GROUPED_DBIAS = 1, 2, 3
+OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD = 4, 5, 6
+STATUS_SPLIT_UNALIGNED, STATUS_SPLIT_NEGATIVE, STATUS_SPLIT_SUM, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
+
+SYMBOLS = [
+    "mxq_version", "mxq_scale_bytes", "mxq_workspace_bytes", "mxq_group_quantize", "mxq_requant_colwise",
+    "mxq_grouped_dbias", "mxq_grouped_gemm_fprop", "mxq_grouped_gemm_dgrad", "mxq_grouped_gemm_wgrad",
+    "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
+]
+
+
+class MXQError(RuntimeError):
+    pass
+
+
+_lib = None
+_P, _I64, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+
+
+def load(path: str = LIB) -> ctypes.CDLL:
+    """Load libmxq.so and declare every exported symbol (no GPU needed)."""
+    if not os.path.exists(path):
+        raise MXQError(f"{path} is missing: build it with moe_expert_grouped_group_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    L.mxq_version.restype = _INT
+    L.mxq_scale_bytes.argtypes = [_I64, _I64, _INT]
+    L.mxq_scale_bytes.restype = _SZ
+    L.mxq_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64, _INT, _INT]
+    L.mxq_workspace_bytes.restype = _SZ
+    L.mxq_group_quantize.argtypes = [_P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.mxq_requant_colwise.argtypes = [_P, _P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_dbias.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_gemm_fprop.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_gemm_dgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_gemm_wgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
+    L.mxq_swiglu_fwd.argtypes = [_P, _I64, _I64, _P, _P]
+    L.mxq_swiglu_bwd.argtypes = [_P, _P, _I64, _I64, _P, _P]
+    L.mxq_status_read.argtypes = [_P, _P, _P]
+    L.mxq_error_string.argtypes = [_INT]
+    L.mxq_error_string.restype = ctypes.c_char_p
+    L.mxq_last_cuda_error.restype = _INT
+    for a in ("mxq_group_quantize", "mxq_requant_colwise", "mxq_grouped_dbias", "mxq_grouped_gemm_fprop",
+              "mxq_grouped_gemm_dgrad", "mxq_grouped_gemm_wgrad", "mxq_swiglu_fwd", "mxq_swiglu_bwd",
+              "mxq_status_read"):
+        getattr(L, a).restype = _INT
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = load()
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise MXQError("tensor arguments must be CUDA tensors")
+    if not t.is_contiguous():
+        raise MXQError("tensor arguments must be contiguous")
+    return t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        L = lib()
+        msg = L.mxq_error_string(rc).decode()
+        cuda = L.mxq_last_cuda_error()
+        raise MXQError(f"{what}: {msg} (code {rc}{', cuda error %d' % cuda if rc == -6 else ''})")
+
+
+def _splits(m_splits):
+    if m_splits is None:
+        return None
+    if not isinstance(m_splits, torch.Tensor) or not m_splits.is_cuda or m_splits.dtype != torch.int64:
+        raise MXQError("m_splits must be a CUDA int64 tensor (host m_splits are rejected)")
+    return m_splits
+
+
+def scale_bytes(rows: int, cols: int, colwise: bool) -> int:
+    return int(lib().mxq_scale_bytes(rows, cols, int(colwise)))
+
+
+def workspace_bytes(op: int, M: int, N: int, K: int, E: int, flags: int = 0) -> int:
+    return int(lib().mxq_workspace_bytes(op, M, N, K, E, flags))
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def status_read(status: torch.Tensor) -> int:
+    out = ctypes.c_int32(0)
+    _check(lib().mxq_status_read(_ptr(status), ctypes.byref(out), _stream()), "mxq_status_read")
+    return int(out.value)
+
+
+def _u8(n, dev):
+    return torch.empty(n, dtype=torch.uint8, device=dev)
+
+
+def group_quantize(x, m_splits=None, E=None, rowwise=True, colwise=True, swizzle=True, dbias=False,
+                   noop=None, status=None, out=None, workspace=None):
+    """bf16 x (M, K) -> dict(row_data, row_scale, col_data, col_scale, dbias)."""
+    M, K = x.shape
+    m_splits = _splits(m_splits)
+    if E is None:
+        if m_splits is None:
+            raise MXQError("E is required for uniform members")
+        E = m_splits.numel()
+    dev = x.device
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
+    o = dict(out or {})
+    if rowwise:
+        o.setdefault("row_data", _u8((M, K), dev))
+        o.setdefault("row_scale", _u8(scale_bytes(M, K, False), dev))
+    if colwise:
+        o.setdefault("col_data", _u8((M, K), dev))
+        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+    ws = None
+    if dbias:
+        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+        ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_GROUP_QUANTIZE, M, 0, K, E)), dev)
+    rc = lib().mxq_group_quantize(
+        _ptr(x), M, K, E, _ptr(m_splits), flags, _ptr(o.get("row_data")), _ptr(o.get("row_scale")),
+        _ptr(o.get("col_data")), _ptr(o.get("col_scale")), _ptr(o.get("dbias")), _ptr(noop), _ptr(status),
+        _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream())
+    _check(rc, "mxq_group_quantize")
+    return o
+
+
+def requant_colwise(row_data, row_scale_compact, m_splits, colwise=True, swizzle=True, row_scale_swizzled=True,
+                    dbias=False, dequant=False, noop=None, status=None, out=None, workspace=None):
+    """Rowwise E4M3 (M, K) + compact scales -> dict(col_data, col_scale, row_scale_swizzled, dbias, dequant)."""
+    M, K = row_data.shape
+    m_splits = _splits(m_splits)
+    E = m_splits.numel()
+    dev = row_data.device
+    flags = ((COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0) | (ROWWISE if row_scale_swizzled else 0)
+             | (DEQUANT_OUT if dequant else 0))
+    o = dict(out or {})
+    if colwise:
+        o.setdefault("col_data", _u8((M, K), dev))
+        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+    if row_scale_swizzled:
+        o.setdefault("row_scale_swizzled", _u8(scale_bytes(M, K, False), dev))
+    if dequant:
+        o.setdefault("dequant", torch.empty((M, K), dtype=torch.bfloat16, device=dev))
+    ws = None
+    if dbias:
+        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+        ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_REQUANT_COLWISE, M, 0, K, E)), dev)
+    rc = lib().mxq_requant_colwise(
+        _ptr(row_data), _ptr(row_scale_compact), M, K, E, _ptr(m_splits), flags, _ptr(o.get("col_data")),
+        _ptr(o.get("col_scale")), _ptr(o.get("row_scale_swizzled")), _ptr(o.get("dbias")), _ptr(o.get("dequant")),
+        _ptr(noop), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream())
+    _check(rc, "mxq_requant_colwise")
+    return o
+
+
+def grouped_dbias(dy, m_splits, status=None, out=None, workspace=None):
+    M, N = dy.shape
+    m_splits = _splits(m_splits)
+    E = m_splits.numel()
+    out = out if out is not None else torch.empty((E, N), dtype=torch.float32, device=dy.device)
+    ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_GROUPED_DBIAS, M, N, 0, E)), dy.device)
+    rc = lib().mxq_grouped_dbias(_ptr(dy), M, N, E, _ptr(m_splits), _ptr(out), _ptr(status), _ptr(ws),
+                                 ws.numel(), _stream())
+    _check(rc, "mxq_grouped_dbias")
+    return out
+
+
+def grouped_gemm_fprop(x_data, x_scale, w_data, w_scale, m_splits, bias=None, status=None, out=None):
+    """Y = X W_e^T (+ b_e). x_data (M,K) u8, w_data (E,N,K) u8, swizzled scales."""
+    M, K = x_data.shape
+    E, N, _ = w_data.shape
+    m_splits = _splits(m_splits)
+    out = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x_data.device)
+    rc = lib().mxq_grouped_gemm_fprop(_ptr(x_data), _ptr(x_scale), _ptr(w_data), _ptr(w_scale), _ptr(bias), M, N, K,
+                                      E, _ptr(m_splits), _ptr(out), _ptr(status), None, 0, _stream())
+    _check(rc, "mxq_grouped_gemm_fprop")
+    return out
+
+
+def grouped_gemm_dgrad(dy_data, dy_scale, w_col_data, w_col_scale, m_splits, status=None, out=None):
+    """dX = dY W_e. dy_data (M,N) rowwise, w_col_data (E,N,K) colwise."""
+    M, N = dy_data.shape
+    E, _, K = w_col_data.shape
+    m_splits = _splits(m_splits)
+    out = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dy_data.device)
+    rc = lib().mxq_grouped_gemm_dgrad(_ptr(dy_data), _ptr(dy_scale), _ptr(w_col_data), _ptr(w_col_scale), M, N, K,
+                                      E, _ptr(m_splits), _ptr(out), _ptr(status), None, 0, _stream())
+    _check(rc, "mxq_grouped_gemm_dgrad")
+    return out
+
+
+def grouped_gemm_wgrad(dy_col_data, dy_col_scale, x_col_data, x_col_scale, m_splits, accumulate=False,
+                       out_bf16=False, status=None, out=None):
+    """dW_e = dY_e^T X_e from the colwise copies; out (E, N, K) fp32 (or bf16)."""
+    M, N = dy_col_data.shape
+    K = x_col_data.shape[1]
+    m_splits = _splits(m_splits)
+    E = m_splits.numel()
+    if out is None:
+        out = torch.empty((E, N, K), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dy_col_data.device)
+    flags = (ACCUMULATE if accumulate else 0) | (OUT_BF16 if out_bf16 else 0)
+    rc = lib().mxq_grouped_gemm_wgrad(_ptr(dy_col_data), _ptr(dy_col_scale), _ptr(x_col_data), _ptr(x_col_scale), M,
+                                      N, K, E, _ptr(m_splits), flags, _ptr(out), _ptr(status), None, 0, _stream())
+    _check(rc, "mxq_grouped_gemm_wgrad")
+    return out
+
+
+def swiglu_fwd(y, out=None):
+    M, F2 = y.shape
+    out = out if out is not None else torch.empty((M, F2 // 2), dtype=torch.bfloat16, device=y.device)
+    _check(lib().mxq_swiglu_fwd(_ptr(y), M, F2 // 2, _ptr(out), _stream()), "mxq_swiglu_fwd")
+    return out
+
+
+def swiglu_bwd(dh, y, out=None):
+    M, F2 = y.shape
+    out = out if out is not None else torch.empty((M, F2), dtype=torch.bfloat16, device=y.device)
+    _check(lib().mxq_swiglu_bwd(_ptr(dh), _ptr(y), M, F2 // 2, _ptr(out), _stream()), "mxq_swiglu_bwd")
+    return out
