@@ -1,0 +1,463 @@
+"""Benchmark: one grouped MXFP8 linear training step of an MoE expert layer.
+
+Workload (8 experts, hidden 2048, out 4096, 16384 routed tokens, uniform
+multinomial routing rounded to 128-token multiples, X arriving rowwise-
+quantized as an expert-parallel FP8 dispatch delivers it). One step is the
+whole hot path over one batch:
+
+    requant X (rowwise wire format -> colwise copy + swizzled rowwise scales)
+    group_quantize W (rowwise + colwise, uniform members)
+    group_quantize dY (rowwise + colwise)
+    grouped fprop  Y  = X W_e^T
+    grouped dgrad  dX = dY W_e
+    grouped wgrad  dW = dY_e^T X_e (fp32)
+
+value = GEMM flops of the step (6*M*N*K) / step time (whole step), in
+TFLOP/s. L2 is flushed (256 MiB write) before every timed step; the flush is
+outside the per-step CUDA-event brackets. Per-kernel times come from events
+on the launching stream. `--impl reference` times the CPU oracle instead.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (the grouped path has no exchange step of its own); rank 0 prints
+the aggregate (weak scaling, max time over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "e8_h2048_n4096_t16k_prequant"
+METRIC = "grouped MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad); group_quantize HBM GB/s"
+UNIT = "TFLOP/s"
+MXFP8_OVER_BF16 = 2.0   # nominal dense MXFP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops", FALLBACK_BF16_TFLOPS), d.get("hbm_gbs", FALLBACK_HBM_GBS), "measured"
+    return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# --------------------------------------------------------------- workload
+def make_host_workload():
+    from synth import WORKLOADS, make_inputs
+
+    w = WORKLOADS[WORKLOAD]
+    d = make_inputs(w, which=("x", "w", "dy"))
+    return w, d
+
+
+class NativeStep:
+    """Device-resident inputs/outputs of one step and the calls that run it."""
+
+    def __init__(self, w, d, dev):
+        import torch
+
+        import moe_expert_grouped_group_gb300 as mxq
+
+        self.torch, self.mxq, self.w, self.dev = torch, mxq, w, dev
+        E, N, K, M = w.E, w.N, w.K, w.M
+        tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        self.ms = torch.from_numpy(d["m_splits"]).to(dev)
+        self.x_bf16 = tb(d["x"])
+        self.wt = tb(d["w"]).view(E * N, K)
+        self.dy = tb(d["dy"])
+        # The dispatch wire format (rowwise E4M3 + compact scales), made once
+        # by the library itself (setup, untimed).
+        q = mxq.group_quantize(self.x_bf16, self.ms, rowwise=True, colwise=False, swizzle=False)
+        self.x_row, self.x_row_scale = q["row_data"], q["row_scale"]
+        u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+        self.rq = {"col_data": u8((M, K)), "col_scale": u8(mxq.scale_bytes(M, K, True)),
+                   "row_scale_swizzled": u8(mxq.scale_bytes(M, K, False))}
+        self.qw = {"row_data": u8((E * N, K)), "row_scale": u8(mxq.scale_bytes(E * N, K, False)),
+                   "col_data": u8((E * N, K)), "col_scale": u8(mxq.scale_bytes(E * N, K, True))}
+        self.qdy = {"row_data": u8((M, N)), "row_scale": u8(mxq.scale_bytes(M, N, False)),
+                    "col_data": u8((M, N)), "col_scale": u8(mxq.scale_bytes(M, N, True))}
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((E, N, K), dtype=torch.float32, device=dev)
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 6
+
+    def run(self, events=None):
+        mxq, w = self.mxq, self.w
+        E, N, K = w.E, w.N, w.K
+        rec = (lambda i: events[i].record()) if events else (lambda i: None)
+        rec(0)
+        mxq.requant_colwise(self.x_row, self.x_row_scale, self.ms, out=self.rq)
+        rec(1)
+        mxq.group_quantize(self.wt, None, E=E, out=self.qw)
+        rec(2)
+        mxq.group_quantize(self.dy, self.ms, out=self.qdy)
+        rec(3)
+        mxq.grouped_gemm_fprop(self.x_row, self.rq["row_scale_swizzled"], self.qw["row_data"].view(E, N, K),
+                               self.qw["row_scale"], self.ms, out=self.y)
+        rec(4)
+        mxq.grouped_gemm_dgrad(self.qdy["row_data"], self.qdy["row_scale"], self.qw["col_data"].view(E, N, K),
+                               self.qw["col_scale"], self.ms, out=self.dx)
+        rec(5)
+        mxq.grouped_gemm_wgrad(self.qdy["col_data"], self.qdy["col_scale"], self.rq["col_data"],
+                               self.rq["col_scale"], self.ms, out=self.dw)
+        rec(6)
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+
+
+KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
+
+
+def algorithmic(w):
+    M, N, K, E = w.M, w.N, w.K, w.E
+    flops = {"fprop": 2.0 * M * N * K, "dgrad": 2.0 * M * N * K, "wgrad": 2.0 * M * N * K}
+    bytes_ = {"requant_x": 2.09375 * M * K, "quantize_w": 4.0625 * E * N * K, "quantize_dy": 4.0625 * M * N}
+    return flops, bytes_
+
+
+def time_native(st, steps, warmup, sampler):
+    torch = st.torch
+    for _ in range(warmup):
+        st.flush()
+        st.run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        st.flush()
+        st.run(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    per_step = [evs[i][0].elapsed_time(evs[i][6]) for i in range(steps)]
+    per_kernel = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+                  for j, k in enumerate(KERNELS)}
+    return per_step, per_kernel, wall, clocks
+
+
+def time_e2e(st, steps, warmup, d):
+    """Through the public API from pinned host memory: H2D of the step's
+    inputs (wire-format X, its scales, W, dY, m_splits), the step, D2H of its
+    results (Y, dX, dW)."""
+    torch = st.torch
+    host_in = {
+        "x_row": st.x_row.cpu().pin_memory(), "x_row_scale": st.x_row_scale.cpu().pin_memory(),
+        "wt": st.wt.cpu().pin_memory(), "dy": st.dy.cpu().pin_memory(), "ms": st.ms.cpu().pin_memory(),
+    }
+    host_out = {"y": torch.empty_like(st.y, device="cpu").pin_memory(),
+                "dx": torch.empty_like(st.dx, device="cpu").pin_memory(),
+                "dw": torch.empty_like(st.dw, device="cpu").pin_memory()}
+    dev_in = {"x_row": st.x_row, "x_row_scale": st.x_row_scale, "wt": st.wt, "dy": st.dy, "ms": st.ms}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def one():
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        st.run()
+        host_out["y"].copy_(st.y, non_blocking=True)
+        host_out["dx"].copy_(st.dx, non_blocking=True)
+        host_out["dw"].copy_(st.dw, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# ------------------------------------------------------------- CPU oracle
+class OracleSample:
+    """The CPU oracle on a bounded sample of one step, scaled to a full step.
+
+    Sample: quantize/requant on a 1/32 row slice of X and dY and of W's rows;
+    each GEMM on `entries` output entries, each a full-length dot product.
+    The sampled rows all belong to one expert (so only that expert's weights
+    are needed); per-entry cost does not depend on which expert it is."""
+
+    def __init__(self, w, d, frac_rows=1 / 32, entries=1 << 18):
+        import oracle as orc
+
+        self.orc, self.w, self.d = orc, w, d
+        M, N, K, E = w.M, w.N, w.K, w.E
+        self.frac = frac_rows
+        self.rows = int(M * frac_rows) // 128 * 128
+        self.wrows = int(E * N * frac_rows) // 128 * 128
+        rows = self.rows
+        self.wire = orc.group_quantize(d["x"][:rows], [rows], rowwise=True, colwise=False)
+        self.cx = orc.group_quantize(d["x"][:rows], [rows])
+        self.cdy = orc.group_quantize(d["dy"][:rows], [rows])
+        self.cw = orc.quantize_weights(d["w"][:1])
+        rng = np.random.default_rng(0)
+        self.r = rng.integers(0, rows, entries)
+        self.cn = rng.integers(0, N, entries)
+        self.ck = rng.integers(0, K, entries)
+        self.n_w = max(16, entries // 8)
+        self.wn = rng.integers(0, N, self.n_w)
+        self.wk = rng.integers(0, K, self.n_w)
+        self.cores = orc.num_threads()
+        self.sample = (f"quantize/requant on {rows}/{M} activation rows and {self.wrows}/{E * N} weight rows; "
+                       f"{entries} fprop and dgrad entries and {self.n_w} wgrad entries (full-length dot "
+                       f"products); scaled to one full step")
+
+    def run(self):
+        orc, w, d = self.orc, self.w, self.d
+        M, N, K, E = w.M, w.N, w.K, w.E
+        rows, t = self.rows, {}
+        t1 = time.perf_counter()
+        orc.requant_colwise(self.wire["row_q"], self.wire["row_s"], [rows], swizzled=True)
+        t["requant_x"] = (time.perf_counter() - t1) * M / rows
+        t1 = time.perf_counter()
+        orc.group_quantize(d["w"].reshape(E * N, K)[:self.wrows], [self.wrows], swizzled=True)
+        t["quantize_w"] = (time.perf_counter() - t1) * (E * N) / self.wrows
+        t1 = time.perf_counter()
+        orc.group_quantize(d["dy"][:rows], [rows], swizzled=True)
+        t["quantize_dy"] = (time.perf_counter() - t1) * M / rows
+        cx, cdy, cw = self.cx, self.cdy, self.cw
+        t1 = time.perf_counter()
+        orc.fprop_entries(cx["row_q"], cx["row_s"], cw["row_q"].reshape(1, N, K), cw["row_s"], [rows],
+                          self.r, self.cn)
+        t["fprop"] = (time.perf_counter() - t1) * (M * N) / self.r.size
+        t1 = time.perf_counter()
+        orc.dgrad_entries(cdy["row_q"], cdy["row_s"], cw["col_q"].reshape(1, N, K), cw["col_s"], [rows],
+                          self.r, self.ck)
+        t["dgrad"] = (time.perf_counter() - t1) * (M * K) / self.r.size
+        t1 = time.perf_counter()
+        orc.wgrad_entries(cdy["col_q"], cdy["col_s"], cx["col_q"], cx["col_s"], [rows],
+                          np.zeros(self.n_w, np.int64), self.wn, self.wk)
+        # a sampled wgrad entry reduces over `rows` tokens, a full-size one
+        # over m_e = M/E tokens on average
+        t["wgrad"] = (time.perf_counter() - t1) * (E * N * K) / self.n_w * (M / E) / rows
+        return t
+
+
+# --------------------------------------------------------------- dist
+_PG = None
+
+
+def barrier():
+    if _PG is not None:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float) -> float:
+    if _PG is None:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: float, world: int, t_max_s: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return per_rank_units * world / t_max_s
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    w, d = make_host_workload()
+    flops, _ = algorithmic(w)
+    step_flops = sum(flops.values())
+    sample = OracleSample(w, d)
+    for _ in range(args.warmup):
+        sample.run()
+    times = [sum(sample.run().values()) for _ in range(args.steps)]
+    ms = statistics.mean(times) * 1e3
+    value = step_flops / (ms * 1e-3) / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+                             "sample": sample.sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    global _PG
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        _PG = dist.group.WORLD
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from __graft_entry__ import build
+
+    build()
+    w, d = make_host_workload()
+    st = NativeStep(w, d, dev)
+    flops, bytes_ = algorithmic(w)
+    step_flops = sum(flops.values())
+
+    sampler = ClockSampler(local if world > 1 else 0) if rank == 0 else None
+    per_step, per_kernel, wall, clocks = time_native(st, args.steps, max(3, args.warmup), sampler)
+    ms_step = statistics.mean(per_step)
+    ms_step_max = max_over_ranks(ms_step)
+    value = aggregate(step_flops, world, ms_step_max * 1e-3) / 1e12
+
+    gemm_ms = per_kernel["fprop"] + per_kernel["dgrad"] + per_kernel["wgrad"]
+    gemm_tflops = step_flops / (gemm_ms * 1e-3) / 1e12
+    quant_gbs = {k: bytes_[k] / (per_kernel[k] * 1e-3) / 1e9 for k in bytes_}
+
+    e2e = None
+    if not args.no_e2e:
+        ms_e2e, h2d, d2h = time_e2e(st, max(5, args.steps // 5), 2, d)
+        ms_e2e = max_over_ranks(ms_e2e)
+        e2e = {"value": aggregate(step_flops, world, ms_e2e * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+
+    if rank != 0:
+        return
+    bf16_peak, hbm_peak, src = peaks()
+    mx_peak = bf16_peak * MXFP8_OVER_BF16
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if os.path.exists(tpath):
+        from moe_expert_grouped_group_gb300.build import _stamp
+
+        with open(tpath) as f:
+            tj = json.load(f)
+        if tj.get("source_stamp") == _stamp() and tj.get("workload") == WORKLOAD:
+            traffic = tj.get("dram_bytes_per_launch")
+    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": mx_peak, "unit": "TFLOP/s",
+                "frac": gemm_tflops / mx_peak, "traffic": traffic,
+                "kernel": "grouped_gemm_kernel (fprop+dgrad+wgrad launches of one step)",
+                "peak_source": f"{src} bf16 burst {bf16_peak} TFLOP/s x {MXFP8_OVER_BF16} (nominal MXFP8/BF16)"}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        t0 = time.perf_counter()
+        sample = OracleSample(w, d, frac_rows=1 / 8, entries=1 << 21)
+        t = sample.run()
+        cpu_ms = sum(t.values()) * 1e3
+        cpu = {"value": step_flops / (cpu_ms * 1e-3) / 1e12, "unit": UNIT, "cores": sample.cores,
+               "kind": "oracle", "sample": sample.sample, "ms_per_step_extrapolated": cpu_ms,
+               "per_kernel_ms_extrapolated": {k: v * 1e3 for k, v in t.items()},
+               "wall_s": time.perf_counter() - t0}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8_e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
+                   "m_splits": [int(v) for v in d["m_splits"]],
+                   "step": "requant X + quantize W (row+col) + quantize dY (row+col) + fprop + dgrad + wgrad (fp32 dW)",
+                   "l2": "256 MiB buffer written before every timed step (outside the event brackets)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": st.launches_per_step * args.steps,
+        "clocks": clocks,
+        "kernels_ms": per_kernel, "gemm_tflops": gemm_tflops,
+        "group_quantize_gbs": quant_gbs, "hbm_peak_gbs": hbm_peak,
+        "group_quantize_frac": {k: v / hbm_peak for k, v in quant_gbs.items()},
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -88,12 +88,14 @@ int mxq_group_quantize(const void* x_bf16, int64_t M, int64_t K, int E, const in
     if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE)) return MXQ_ERR_FLAGS;
     const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE;
     if (!row && !col && !dbias_out) return MXQ_ERR_FLAGS;
-    if (!x_bf16 || (row && (!row_data || !row_scale)) || (col && (!col_data || !col_scale))) return MXQ_ERR_NULL;
+    // With M == 0 every data buffer is empty (and may be NULL).
+    if (M != 0 && (!x_bf16 || (row && (!row_data || !row_scale)) || (col && (!col_data || !col_scale))))
+        return MXQ_ERR_NULL;
     if (int r = check_common(M, K, E, d_m_splits, false)) return r;
     if (!aligned16(x_bf16) || !aligned16(row_data) || !aligned16(row_scale) || !aligned16(col_data) ||
         !aligned16(col_scale) || !aligned16(dbias_out) || !aligned16(ws))
         return MXQ_ERR_ALIGN;
-    if (dbias_out && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GROUP_QUANTIZE, M, 0, K, E, flags)))
+    if (dbias_out && M != 0 && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GROUP_QUANTIZE, M, 0, K, E, flags)))
         return MXQ_ERR_WORKSPACE;
     mxq::QuantCall c{};
     c.x = x_bf16;
@@ -121,15 +123,15 @@ int mxq_requant_colwise(const void* row_data, const void* row_scale_compact, int
     if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE | MXQ_DEQUANT_OUT)) return MXQ_ERR_FLAGS;
     const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE, deq = flags & MXQ_DEQUANT_OUT;
     if (!row && !col && !deq && !dbias_out) return MXQ_ERR_FLAGS;
-    if (!row_data || !row_scale_compact || (col && (!col_data || !col_scale)) || (row && !row_scale_swizzled_out) ||
-        (deq && !dequant_bf16_out))
+    if (M != 0 && (!row_data || !row_scale_compact || (col && (!col_data || !col_scale)) ||
+                   (row && !row_scale_swizzled_out) || (deq && !dequant_bf16_out)))
         return MXQ_ERR_NULL;
     if (int r = check_common(M, K, E, d_m_splits, false)) return r;
     if (!aligned16(row_data) || !aligned16(row_scale_compact) || !aligned16(col_data) || !aligned16(col_scale) ||
         !aligned16(row_scale_swizzled_out) || !aligned16(dbias_out) || !aligned16(dequant_bf16_out) ||
         !aligned16(ws))
         return MXQ_ERR_ALIGN;
-    if (dbias_out && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_REQUANT_COLWISE, M, 0, K, E, flags)))
+    if (dbias_out && M != 0 && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_REQUANT_COLWISE, M, 0, K, E, flags)))
         return MXQ_ERR_WORKSPACE;
     mxq::RequantCall c{};
     c.row_q = row_data;
@@ -153,10 +155,10 @@ int mxq_requant_colwise(const void* row_data, const void* row_scale_compact, int
 
 int mxq_grouped_dbias(const void* dy_bf16, int64_t M, int64_t N, int E, const int64_t* d_m_splits, float* dbias_out,
                       int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
-    if (!dy_bf16 || !dbias_out) return MXQ_ERR_NULL;
+    if ((M != 0 && !dy_bf16) || !dbias_out) return MXQ_ERR_NULL;
     if (int r = check_common(M, N, E, d_m_splits, true)) return r;
     if (!aligned16(dy_bf16) || !aligned16(dbias_out) || !aligned16(ws)) return MXQ_ERR_ALIGN;
-    if (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GROUPED_DBIAS, M, N, 0, E, 0)) return MXQ_ERR_WORKSPACE;
+    if (M != 0 && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GROUPED_DBIAS, M, N, 0, E, 0))) return MXQ_ERR_WORKSPACE;
     cudaError_t e = mxq::run_grouped_dbias(dy_bf16, M, N, E, d_m_splits, dbias_out, static_cast<float*>(ws), d_status,
                                            (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
@@ -165,7 +167,12 @@ int mxq_grouped_dbias(const void* dy_bf16, int64_t M, int64_t N, int E, const in
 static int gemm_common(int mode, const void* a, const void* as, const void* b, const void* bs, const void* bias,
                        int64_t M, int64_t N, int64_t K, int E, const int64_t* m_splits, void* out, int accumulate,
                        int out_bf16, int32_t* d_status, mxq_stream_t stream) {
-    if (!a || !as || !b || !bs || !out) return MXQ_ERR_NULL;
+    // With M == 0 the token-major operands (and fprop/dgrad outputs) are empty.
+    const bool a_empty_ok = (M == 0), b_empty_ok = (M == 0 && mode == mxq::kWgrad);
+    const bool out_empty_ok = (M == 0 && mode != mxq::kWgrad);
+    if ((!a && !a_empty_ok) || (!as && !a_empty_ok) || (!b && !b_empty_ok) || (!bs && !b_empty_ok) ||
+        (!out && !out_empty_ok))
+        return MXQ_ERR_NULL;
     if (int r = check_common(M, K, E, m_splits, true)) return r;
     if (N <= 0 || N % 128 || N > ((int64_t)1 << 31) / 128) return MXQ_ERR_SHAPE;
     if ((int64_t)E * N > ((int64_t)1 << 31) - 256) return MXQ_ERR_SHAPE;

@@ -586,6 +586,17 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     });
     if (attr_err != cudaSuccess) return attr_err;
 
+    int64_t tiles;
+    if (c.mode == kFprop) tiles = (c.M / BM) * (c.N / BN);
+    else if (c.mode == kDgrad) tiles = (c.M / BM) * (c.K / BN);
+    else tiles = (int64_t)c.E * (c.N / BM) * (c.K / BN);
+    if (tiles == 0) return cudaSuccess;
+    if (c.mode == kWgrad && c.M == 0) {
+        // no tokens: every expert is empty, dW = 0 (unchanged when accumulating)
+        if (c.accumulate) return cudaSuccess;
+        return cudaMemsetAsync(c.out, 0, (size_t)c.E * c.N * c.K * (c.out_bf16 ? 2 : 4), s);
+    }
+
     CUtensorMap ta, tb;
     bool ok;
     if (c.mode == kFprop) {
@@ -612,11 +623,6 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     p.out_bf16 = c.out_bf16;
     p.status = c.status;
 
-    int64_t tiles;
-    if (c.mode == kFprop) tiles = (c.M / BM) * (c.N / BN);
-    else if (c.mode == kDgrad) tiles = (c.M / BM) * (c.K / BN);
-    else tiles = (int64_t)c.E * (c.N / BM) * (c.K / BN);
-    if (tiles == 0) return cudaSuccess;
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
     grouped_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, p);
     return cudaGetLastError();

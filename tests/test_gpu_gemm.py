@@ -230,3 +230,21 @@ def test_full_size_sampled(mxq, name):
             assert bool((dw[e] == 0).all())
         del dw
         torch.cuda.empty_cache()
+
+
+def test_empty_token_batch(mxq):
+    """No routed tokens: fprop/dgrad produce empty outputs, wgrad writes dW = 0."""
+    E, N, K = 3, 256, 256
+    ms = dev_i64([0, 0, 0])
+    e8 = torch.empty((0, K), dtype=torch.uint8, device="cuda")
+    e8n = torch.empty((0, N), dtype=torch.uint8, device="cuda")
+    es = torch.empty(0, dtype=torch.uint8, device="cuda")
+    w = torch.zeros((E, N, K), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(mxq.scale_bytes(E * N, K, False), dtype=torch.uint8, device="cuda")
+    y = mxq.grouped_gemm_fprop(e8, es, w, ws, ms)
+    dx = mxq.grouped_gemm_dgrad(e8n, es, w, ws, ms)
+    dw = torch.full((E, N, K), 3.0, dtype=torch.float32, device="cuda")
+    mxq.grouped_gemm_wgrad(e8n, es, e8, es, ms, out=dw)
+    torch.cuda.synchronize()
+    assert y.shape == (0, N) and dx.shape == (0, K)
+    assert bool((dw == 0).all())
