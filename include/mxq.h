@@ -94,7 +94,8 @@ enum {
     MXQ_ERR_WORKSPACE = -5,    /* workspace smaller than mxq_workspace_bytes() */
     MXQ_ERR_LAUNCH = -6,       /* a CUDA call failed (see mxq_last_cuda_error) */
     MXQ_ERR_FLAGS = -7,        /* unknown or inconsistent flags */
-    MXQ_ERR_ALIGN = -8         /* a pointer is not 16-byte aligned */
+    MXQ_ERR_ALIGN = -8,        /* a pointer is not 16-byte aligned */
+    MXQ_ERR_SCRATCH_LIMIT = -9 /* problem larger than mxq_grouped_dbias_noalloc's fixed scratch */
 };
 
 /* device status word bits (sticky; OR-ed by the kernels) */
@@ -202,6 +203,21 @@ MXQ_API int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_s
                            const void* x_col_scale, int64_t M, int64_t N, int64_t K, int E,
                            const int64_t* d_m_splits, int flags, void* dw, int32_t* d_status, void* ws,
                            size_t ws_bytes, mxq_stream_t stream);
+
+/* grouped_dbias without any allocation, for callers that cannot allocate
+ * device memory (code running where no allocator may be called, or with no
+ * access to one). The pages have no counterpart: this is a library
+ * convenience. Same result as mxq_grouped_dbias, but the per-tile partial
+ * sums live in a fixed 8 MiB file-scope device array that every GPU loading
+ * the library holds until the process exits:
+ *   - (M/128) * N must be <= 2,097,152, else MXQ_ERR_SCRATCH_LIMIT;
+ *   - the first call on a device looks up the array's device address (once
+ *     per device), so make it before any stream capture;
+ *   - all calls share the array (it keeps the last call's partials, which the
+ *     next call overwrites before reading); calls that overlap on the GPU
+ *     race, so serialise them. */
+MXQ_API int mxq_grouped_dbias_noalloc(const void* dy_bf16, int64_t M, int64_t N, int E, const int64_t* d_m_splits,
+                                      float* dbias_out, int32_t* d_status, mxq_stream_t stream);
 
 /* SwiGLU between FC1 and FC2 of the fused grouped MLP [FM] (reading: the
  * first F columns of the FC1 output are the gate):

@@ -268,6 +268,8 @@ const char* mxq_error_string(int code) {
         case MXQ_ERR_LAUNCH: return "a CUDA call failed (see mxq_last_cuda_error)";
         case MXQ_ERR_FLAGS: return "unknown or inconsistent flags";
         case MXQ_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case MXQ_ERR_SCRATCH_LIMIT:
+            return "(M/128)*N exceeds the 2,097,152-float scratch of mxq_grouped_dbias_noalloc";
         default: return "unknown error";
     }
 }

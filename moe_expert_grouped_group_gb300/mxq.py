@@ -26,6 +26,7 @@ SYMBOLS = [
     "mxq_version", "mxq_scale_bytes", "mxq_workspace_bytes", "mxq_group_quantize", "mxq_requant_colwise",
     "mxq_grouped_dbias", "mxq_grouped_gemm_fprop", "mxq_grouped_gemm_dgrad", "mxq_grouped_gemm_wgrad",
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
+    "mxq_grouped_dbias_noalloc",
 ]
 
 
@@ -53,6 +54,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_grouped_gemm_fprop.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_wgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_dbias_noalloc.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P]
+    L.mxq_grouped_dbias_noalloc.restype = _INT
     L.mxq_swiglu_fwd.argtypes = [_P, _I64, _I64, _P, _P]
     L.mxq_swiglu_bwd.argtypes = [_P, _P, _I64, _I64, _P, _P]
     L.mxq_status_read.argtypes = [_P, _P, _P]
