@@ -10,18 +10,20 @@
 // grouped linear module with single grouped weight support": device m_splits
 // read without a host sync, one grouped weight (E,out,in), 2-D grouped bias.)
 //
-// Kernel: persistent, one CTA (192 threads) per SM, warp-specialised.
+// Kernel: persistent, one CTA (320 threads) per SM, warp-specialised.
 //   warp 0      TMA producer: 128x128-byte E4M3 boxes (128B swizzle) for A and
 //               two for B per 128-deep K block, plus the 512-byte scale atoms
 //               (already in the tensor-core 128x4 layout) by bulk copy;
 //   warp 1      owns TMEM (512 columns) and, from one lane, issues
 //               tcgen05.cp (scales -> TMEM) and tcgen05.mma
 //               .kind::mxf8f6f4.block_scale (M=128, N=256, K=32, fp32 accum);
-//   warps 2..5  epilogue: tcgen05.ld the 128x256 fp32 accumulator, add bias,
-//               convert, store to global.
+//   warps 2..9  epilogue: two warps per TMEM lane quarter each pull a 32x128
+//               slice of the 128x256 fp32 accumulator into registers
+//               (tcgen05.ld), release the accumulator, then add bias,
+//               convert and store to global.
 // A 4-stage shared-memory ring (mbarrier full/empty) feeds the tensor core;
-// the accumulator is released to the MMA warp as soon as it has been read
-// into registers, so the next tile's MMAs overlap the global stores.
+// because the accumulator is released as soon as it sits in registers, the
+// next tile's MMAs overlap the conversion and the global stores.
 //
 // Operand majorness: K-major (A of fprop/dgrad, B of fprop) and MN-major (B of
 // dgrad, A and B of wgrad: the columnwise copies keep the source's byte
@@ -62,7 +64,8 @@ constexpr int SFA_OFF = A_BYTES + B_BYTES;
 constexpr int SFB_OFF = SFA_OFF + 512;
 constexpr int STAGE_BYTES = 51200;    // 50 KB: keeps every stage 1024-aligned
 constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + 512 + 1024;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;      // producer, MMA, 8 epilogue warps
+constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SFA = 256;         // scale columns after the accumulator
 constexpr int TMEM_SFB = 264;
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(empty0 + 8 * s, 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        mbar_init(acc_empty, EPI_WARPS);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
@@ -408,8 +411,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         // ------------------------------------------------------ epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // Warp w may read TMEM lanes 32*(w%4)..+31 (its quarter of the 128
+        // accumulator rows); the two warps of a quarter split the 256 columns.
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row_in_tile = q * 32 + lane;
+        const int col0 = half * (BN / 2);
         uint32_t aphase = 0;
         for (int64_t i = 0;; ++i) {
             const Tile T = S.get(S.pick(i, cta, ncta));
@@ -418,108 +425,95 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (!ok || *abort_flag) break;
             fence_after();
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+            // Pull this warp's 32 x 128 slice of the accumulator into registers,
+            // then hand the accumulator back to the MMA warp before storing.
+            uint32_t r[BN / 2];
+            const bool zero = (p.mode == kWgrad && T.nk == 0);
+            if (!zero) {
+                const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + col0;
+                TMEM_LD32(tbase + 0, (r + 0));
+                TMEM_LD32(tbase + 32, (r + 32));
+                TMEM_LD32(tbase + 64, (r + 64));
+                TMEM_LD32(tbase + 96, (r + 96));
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < BN / 2; ++j) r[j] = 0u;
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+
             if (p.mode != kWgrad) {
                 const int64_t row = T.a_row + row_in_tile;
                 const int64_t ldo = (p.mode == kFprop) ? p.N : p.K;
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + row * ldo + T.b_col;
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + row * ldo + T.b_col + col0;
                 const __nv_bfloat16* bias =
-                    (p.mode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col : nullptr;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    TMEM_LD32(tbase + c * 32, r);
-                    tmem_wait_ld();
-                    if (c == BN / 32 - 1) {
-                        fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
-                    }
-                    float f[32];
+                    (p.mode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col + col0 : nullptr;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+                for (int c = 0; c < BN / 2; c += 8) {
+                    float f[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[c + j]);
                     if (bias) {
-                        const uint4* bp = reinterpret_cast<const uint4*>(bias + c * 32);
+                        const uint4 bw = __ldg(reinterpret_cast<const uint4*>(bias + c));
+                        const uint32_t ws[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint4 bw = __ldg(bp + v);
-                            const uint32_t ws[4] = {bw.x, bw.y, bw.z, bw.w};
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                f[8 * v + 2 * j] += __uint_as_float(ws[j] << 16);
-                                f[8 * v + 2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
-                            }
+                        for (int j = 0; j < 4; ++j) {
+                            f[2 * j] += __uint_as_float(ws[j] << 16);
+                            f[2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
                         }
                     }
-                    uint32_t h[16];
+                    uint32_t h[4];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
+                    for (int j = 0; j < 4; ++j) {
                         __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
                         h[j] = *reinterpret_cast<uint32_t*>(&b2);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+                    *reinterpret_cast<uint4*>(out + c) = make_uint4(h[0], h[1], h[2], h[3]);
                 }
-            } else {
+            } else if (!(zero && p.accumulate)) {
                 const int64_t row = T.a_row + row_in_tile;  // n
-                const int64_t base = ((int64_t)T.e * p.N + row) * p.K + T.b_col;
-                const bool zero = (T.nk == 0);
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    if (!zero) {
-                        TMEM_LD32(tbase + c * 32, r);
-                        tmem_wait_ld();
-                    } else {
+                const int64_t base = ((int64_t)T.e * p.N + row) * p.K + T.b_col + col0;
+                if (p.out_bf16) {
+                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = 0u;
-                    }
-                    if (c == BN / 32 - 1) {
-                        fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
-                    }
-                    if (zero && p.accumulate) continue;
-                    if (p.out_bf16) {
-                        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base + c * 32;
-                        uint4* dst = reinterpret_cast<uint4*>(out);
-                        float f[32];
+                    for (int c = 0; c < BN / 2; c += 8) {
+                        float f[8];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[c + j]);
+                        uint4* dst = reinterpret_cast<uint4*>(out + c);
                         if (p.accumulate) {
+                            const uint4 o = *dst;
+                            const uint32_t ws[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                const uint4 o = dst[v];
-                                const uint32_t ws[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    f[8 * v + 2 * j] += __uint_as_float(ws[j] << 16);
-                                    f[8 * v + 2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
-                                }
+                            for (int j = 0; j < 4; ++j) {
+                                f[2 * j] += __uint_as_float(ws[j] << 16);
+                                f[2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
                             }
                         }
-                        uint32_t h[16];
+                        uint32_t h[4];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
+                        for (int j = 0; j < 4; ++j) {
                             __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
                             h[j] = *reinterpret_cast<uint32_t*>(&b2);
                         }
+                        *dst = make_uint4(h[0], h[1], h[2], h[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base + c * 32);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                            if (p.accumulate) {
-                                const float4 old = dst[v];
-                                o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-                            }
-                            dst[v] = o;
+                    for (int v = 0; v < BN / 8; ++v) {
+                        float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                        if (p.accumulate) {
+                            const float4 old = dst[v];
+                            o.x += old.x;
+                            o.y += old.y;
+                            o.z += old.z;
+                            o.w += old.w;
                         }
+                        dst[v] = o;
                     }
                 }
             }

@@ -16,17 +16,20 @@
 //   dbias          : per-expert column sums (PR #3244, ordinary dbias reduced
 //                    directly, without a wgrad stage).
 //
-// Design (HBM-bound): one CTA of 8 warps handles a 128x128 tile. Warp w owns
-// rows 32*(w/2)..+31 and columns 64*(w%2)..+63; lane l owns one row of that
-// strip (128 contiguous input bytes). Rowwise amax is thread-local; the
-// colwise amax of a 32-row block is one warp-wide redux.sync per column. A
-// 128x128 tile produces exactly one 512-byte rowwise scale atom and one
-// 512-byte colwise scale atom of the swizzled layout; both are assembled in
-// shared memory and written with 16-byte stores. Because every expert's row
-// count is a multiple of 128, a tile never straddles two experts. dbias uses
-// a fixed-order butterfly over lanes, a fixed-order sum over the four row
-// groups (fp32 partial per 128-row tile, kept in the caller's workspace) and
-// an fp64 ordered sum over each expert's tiles -- deterministic run to run.
+// Design (HBM-bound): one CTA of 8 warps handles a 128x128 tile; lane l of
+// warp w owns columns 64*(w%2) + 2l, +1 of rows 32*(w/2)..+31, so every
+// warp-wide load and store is one contiguous stretch of a row. The colwise
+// amax of a 32-row block and the dbias column sums are thread-local; the
+// rowwise block spans a half-warp. The E8M0 code depends only on the largest exponent field of the
+// block, so rowwise maxima are reduced as packed 8-bit exponents (4 rows per
+// word, byte-wise max shuffles). A 128x128 tile produces exactly one
+// 512-byte rowwise and one 512-byte colwise scale atom of the swizzled
+// layout; both are assembled in shared memory and written with 16-byte
+// stores. Because every expert's row count is a multiple of 128, a tile never
+// straddles two experts. dbias sums each lane's 32 rows in order, then the
+// four row groups in order (fp32 partial per 128-row tile, kept in the
+// caller's workspace), then each expert's tiles in order in fp64 --
+// deterministic run to run.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -54,14 +57,32 @@ struct TileArgs {
     int32_t* status;
 };
 
-__device__ __forceinline__ uint4 ldg_nc(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
     return r;
 }
 
+// Byte-wise max of 4 packed 8-bit exponents across the 16 lanes of a half-warp.
+__device__ __forceinline__ uint32_t group16_max_u8x4(uint32_t v) {
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) v = __vmaxu4(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// One CTA (8 warps) handles a 128x128 tile. Warp w owns rows 32*(w/2)..+31
+// and the 64 columns 64*(w%2)..+63; lane l owns columns 2l, 2l+1 of that
+// strip in every one of its 32 rows, so each warp-wide load or store is one
+// contiguous stretch of a row. The colwise amax of a 32-row block and the
+// dbias column sums are thread-local (over the lane's 32 rows); a rowwise
+// block of 32 columns spans one half-warp, whose exponents are reduced four
+// rows at a time with byte-wise max shuffles (the scale depends only on the
+// block's largest exponent field).
 template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq>
 __global__ void __launch_bounds__(256, 2) mx_tile_kernel(TileArgs a) {
     __shared__ int64_t s_off[MXQ_MAX_EXPERTS + 1];
@@ -77,156 +98,134 @@ __global__ void __launch_bounds__(256, 2) mx_tile_kernel(TileArgs a) {
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = warp >> 1, ch = warp & 1;
+    const int blk = ch * 2 + (lane >> 4);  // 32-column block of the tile holding this lane's columns
     const int64_t K = a.K;
     const int64_t tilesK = K / kTile;
     const int64_t tiles = (a.M / kTile) * tilesK;
 
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t mt = t / tilesK, kt = t % tilesK;
-        const int64_t row = mt * kTile + rg * 32 + lane;
-        const int64_t col = kt * kTile + ch * 64;
+        const int64_t r0 = mt * kTile + rg * 32;             // this warp's first row
+        const int64_t col = kt * kTile + ch * 64 + lane * 2;  // this lane's first column
 
-        float v[64];
-        uint32_t in_code[2] = {0, 0};
+        // ------------------------------------------------------------ load
+        uint32_t raw[32];   // bf16x2, or two E4M3 bytes in the low half
+        float rsc[kReq ? 32 : 1];
+        (void)rsc;
         if constexpr (!kReq) {
-            const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.src) + row * K + col);
-            uint4 w[8];
+            const uint16_t* p = static_cast<const uint16_t*>(a.src) + r0 * K + col;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = ldg_nc(p + i);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    v[8 * i + 2 * j] = bf16lo(ws[j]);
-                    v[8 * i + 2 * j + 1] = bf16hi(ws[j]);
-                }
-            }
+            for (int r = 0; r < 32; ++r) raw[r] = ldg_nc_u32(p + r * K);
         } else {
-            const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.src) + row * K + col);
-            uint4 w[4];
+            const uint8_t* p = static_cast<const uint8_t*>(a.src) + r0 * K + col;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) w[i] = ldg_nc(p + i);
-            const uint16_t sc = *reinterpret_cast<const uint16_t*>(a.src_scale + row * (K / 32) + kt * 4 + ch * 2);
-            in_code[0] = sc & 0xFF;
-            in_code[1] = sc >> 8;
-            const float s0 = scale_from_code(in_code[0]), s1 = scale_from_code(in_code[1]);
+            for (int r = 0; r < 32; ++r) raw[r] = __ldg(reinterpret_cast<const unsigned short*>(p + r * K));
+            // lane l reads the 4 compact rowwise scale codes of row r0 + l
+            const uint32_t sw = ldg_nc_u32(a.src_scale + (r0 + lane) * (K / 32) + kt * 4);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 lo = e4m3x2_to_f32((uint16_t)(ws[j] & 0xFFFF));
-                    const float2 hi = e4m3x2_to_f32((uint16_t)(ws[j] >> 16));
-                    const int c = 16 * i + 4 * j;
-                    const float s = (c < 32) ? s0 : s1;
-                    v[c] = lo.x * s;
-                    v[c + 1] = lo.y * s;
-                    v[c + 2] = hi.x * s;
-                    v[c + 3] = hi.y * s;
-                }
+            for (int r = 0; r < 32; ++r) {
+                const uint32_t word = __shfl_sync(0xffffffffu, sw, r);
+                rsc[r] = scale_from_code((word >> (8 * blk)) & 0xFFu);
+            }
+            if constexpr (kRow) {
+                if (ch == 0) *reinterpret_cast<uint32_t*>(&s_rs[lane * 16 + rg * 4]) = sw;
             }
         }
+        // values of row r, exact fp32
+        auto val2 = [&](int r) -> float2 {
+            if constexpr (!kReq) {
+                return make_float2(bf16lo(raw[r]), bf16hi(raw[r]));
+            } else {
+                const float2 f = e4m3x2_to_f32((uint16_t)raw[r]);
+                return make_float2(f.x * rsc[r], f.y * rsc[r]);
+            }
+        };
 
         // ---------------------------------------------------------- rowwise
         if constexpr (kRow && !kReq) {
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                uint32_t amax = 0;
+            for (int r4 = 0; r4 < 32; r4 += 4) {
+                uint32_t packed = 0;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) amax = max(amax, __float_as_uint(v[32 * b + i]) & 0x7FFFFFFFu);
-                const uint32_t code = scale_code_from_f32_absbits(amax);
-                const float inv = inv_scale_from_code(code);
-                uint32_t q[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t lo = cvt_e4m3x2(v[32 * b + 4 * i] * inv, v[32 * b + 4 * i + 1] * inv);
-                    const uint32_t hi = cvt_e4m3x2(v[32 * b + 4 * i + 2] * inv, v[32 * b + 4 * i + 3] * inv);
-                    q[i] = lo | (hi << 16);
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t w = raw[r4 + k] & 0x7FFF7FFFu;
+                    packed |= (max(w & 0xFFFFu, w >> 16) >> 7) << (8 * k);  // bf16 exponent field
                 }
-                uint4* dst = reinterpret_cast<uint4*>(a.row_q + row * K + col + 32 * b);
-                dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-                dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-                if (a.swizzle) s_rs[lane * 16 + rg * 4 + ch * 2 + b] = (uint8_t)code;
-                else a.row_s[row * (K / 32) + kt * 4 + ch * 2 + b] = (uint8_t)code;
+                packed = group16_max_u8x4(packed);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
+                    const float inv = inv_scale_from_code(code);
+                    const float2 v = val2(r4 + k);
+                    *reinterpret_cast<uint16_t*>(a.row_q + (r0 + r4 + k) * K + col) =
+                        (uint16_t)cvt_e4m3x2(v.x * inv, v.y * inv);
+                    if ((lane & 15) == 0) {
+                        if (a.swizzle) s_rs[(r4 + k) * 16 + rg * 4 + blk] = (uint8_t)code;
+                        else a.row_s[(r0 + r4 + k) * (K / 32) + kt * 4 + blk] = (uint8_t)code;
+                    }
+                }
             }
-        }
-        if constexpr (kRow && kReq) {
-            // swizzled copy of the compact rowwise scales of the wire format
-            *reinterpret_cast<uint16_t*>(&s_rs[lane * 16 + rg * 4 + ch * 2]) =
-                (uint16_t)(in_code[0] | (in_code[1] << 8));
         }
 
         // ---------------------------------------------------------- colwise
         if constexpr (kCol) {
-            uint32_t my_code[2] = {0, 0};
-            uint32_t q[16];
+            uint32_t e0, e1;  // largest exponent field of each of the 2 columns
+            if constexpr (!kReq) {
+                uint32_t m = 0;
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-                const uint32_t m0 = __reduce_max_sync(0xffffffffu, __float_as_uint(v[c]) & 0x7FFFFFFFu);
-                const uint32_t m1 = __reduce_max_sync(0xffffffffu, __float_as_uint(v[c + 1]) & 0x7FFFFFFFu);
-                const uint32_t c0 = scale_code_from_f32_absbits(m0);
-                const uint32_t c1 = scale_code_from_f32_absbits(m1);
-                if (lane == (c & 31)) my_code[c >> 5] = c0;
-                if (lane == ((c + 1) & 31)) my_code[(c + 1) >> 5] = c1;
-                const uint32_t pair = cvt_e4m3x2(v[c] * inv_scale_from_code(c0), v[c + 1] * inv_scale_from_code(c1));
-                if ((c & 2) == 0) q[c >> 2] = pair;
-                else q[c >> 2] |= pair << 16;
-            }
-            uint4* dst = reinterpret_cast<uint4*>(a.col_q + row * K + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(q[4 * i], q[4 * i + 1], q[4 * i + 2], q[4 * i + 3]);
-            if (a.swizzle) {
-                s_cs[lane * 16 + (ch * 2) * 4 + rg] = (uint8_t)my_code[0];
-                s_cs[lane * 16 + (ch * 2 + 1) * 4 + rg] = (uint8_t)my_code[1];
+                for (int r = 0; r < 32; ++r) m = __vmaxu2(m, raw[r] & 0x7FFF7FFFu);
+                e0 = (m >> 7) & 0xFFu;
+                e1 = (m >> 23) & 0xFFu;
             } else {
-                uint8_t* cs = a.col_s + (mt * 4 + rg) * K + col;
-                cs[lane] = (uint8_t)my_code[0];
-                cs[32 + lane] = (uint8_t)my_code[1];
+                uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const float2 v = val2(r);
+                    m0 = max(m0, __float_as_uint(v.x) & 0x7FFFFFFFu);
+                    m1 = max(m1, __float_as_uint(v.y) & 0x7FFFFFFFu);
+                }
+                e0 = m0 >> 23;
+                e1 = m1 >> 23;
+            }
+            const uint32_t c0 = (uint32_t)max((int)e0 - 8, 0), c1 = (uint32_t)max((int)e1 - 8, 0);
+            const float i0 = inv_scale_from_code(c0), i1 = inv_scale_from_code(c1);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                const float2 v = val2(r);
+                *reinterpret_cast<uint16_t*>(a.col_q + (r0 + r) * K + col) = (uint16_t)cvt_e4m3x2(v.x * i0, v.y * i1);
+            }
+            if (a.swizzle) {
+                const int cc = (2 * lane) & 31, cb = blk;  // both columns share the 32-column block
+                s_cs[cc * 16 + cb * 4 + rg] = (uint8_t)c0;
+                s_cs[(cc + 1) * 16 + cb * 4 + rg] = (uint8_t)c1;
+            } else {
+                *reinterpret_cast<uint16_t*>(a.col_s + (mt * 4 + rg) * K + col) = (uint16_t)(c0 | (c1 << 8));
             }
         }
 
         // ------------------------------------------------- dequant output
         if constexpr (kDeq) {
-            uint32_t h[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                h[i] = *reinterpret_cast<uint32_t*>(&b2);
+            for (int r = 0; r < 32; ++r) {
+                const float2 v = val2(r);
+                __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+                *reinterpret_cast<__nv_bfloat162*>(a.deq_out + (r0 + r) * K + col) = b;
             }
-            uint4* dst = reinterpret_cast<uint4*>(a.deq_out + row * K + col);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
         }
 
         // ------------------------------------------------- dbias partials
         if constexpr (kBias) {
-            // butterfly over lanes: after step `o`, each lane keeps the half
-            // of its columns selected by (lane & o); lane l ends with the
-            // 32-row sums of columns 2l and 2l+1 of the warp's 64.
-            float r[64];
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) r[i] = v[i];
-            int n = 64;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const bool upper = (lane & o) != 0;
-                n >>= 1;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if (i < n) {
-                        const float send = upper ? r[i] : r[n + i];
-                        const float keep = upper ? r[n + i] : r[i];
-                        r[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                    }
-                }
+            for (int r = 0; r < 32; ++r) {
+                const float2 v = val2(r);
+                s0 += v.x;
+                s1 += v.y;
             }
-            s_red[rg][ch * 64 + 2 * lane] = r[0];
-            s_red[rg][ch * 64 + 2 * lane + 1] = r[1];
+            *reinterpret_cast<float2*>(&s_red[rg][ch * 64 + lane * 2]) = make_float2(s0, s1);
         }
 
-        if constexpr (kBias || kRow || kCol) __syncthreads();
-
+        __syncthreads();
         if constexpr (kBias) {
             if (threadIdx.x < kTile) {
                 const int c = threadIdx.x;
@@ -234,25 +233,23 @@ __global__ void __launch_bounds__(256, 2) mx_tile_kernel(TileArgs a) {
             }
         }
         if constexpr (kRow) {
-            if (a.swizzle || kReq) {
-                if (threadIdx.x < 32) {
-                    uint4* dst = reinterpret_cast<uint4*>(a.row_s + (mt * tilesK + kt) * 512);
-                    dst[threadIdx.x] = reinterpret_cast<const uint4*>(s_rs)[threadIdx.x];
-                }
+            if ((a.swizzle || kReq) && threadIdx.x < 32) {
+                uint4* dst = reinterpret_cast<uint4*>(a.row_s + (mt * tilesK + kt) * 512);
+                dst[threadIdx.x] = reinterpret_cast<const uint4*>(s_rs)[threadIdx.x];
             }
         }
         if constexpr (kCol) {
             if (a.swizzle && threadIdx.x >= 32 && threadIdx.x < 64) {
-                const int64_t r0 = mt * kTile;
-                const int e = expert_of(s_off, a.E, r0);
+                const int64_t rt0 = mt * kTile;
+                const int e = expert_of(s_off, a.E, rt0);
                 const int64_t off = s_off[e], me = s_off[e + 1] - off;
                 const int64_t base = K * off / 32;
-                const int64_t atom = kt * (me / kTile) + (r0 - off) / kTile;
+                const int64_t atom = kt * (me / kTile) + (rt0 - off) / kTile;
                 uint4* dst = reinterpret_cast<uint4*>(a.col_s + base + atom * 512);
                 dst[threadIdx.x - 32] = reinterpret_cast<const uint4*>(s_cs)[threadIdx.x - 32];
             }
         }
-        if constexpr (kBias || kRow || kCol) __syncthreads();
+        __syncthreads();
     }
 }
 
@@ -288,7 +285,7 @@ template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq>
 static cudaError_t launch_tile(const TileArgs& a, cudaStream_t s) {
     const int64_t tiles = (a.M / kTile) * (a.K / kTile);
     if (tiles == 0) return cudaSuccess;
-    const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms() * 2);
+    const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms() * 4);
     mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq><<<(unsigned)grid, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
