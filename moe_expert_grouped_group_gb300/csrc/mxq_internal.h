@@ -2,6 +2,7 @@
 // the kernel translation units. Not installed; not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,6 +49,12 @@ struct GemmCall {
     int accumulate, out_bf16;  // wgrad only
     int32_t* status;
 };
+
+// Encodes a 2-D row-major tensor map (rows x cols elements of elem_bytes)
+// with a box of box_rows x box_cols; swizzle128 selects the 128-byte
+// swizzle (box_cols * elem_bytes must then be 128). False on failure.
+bool encode_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int elem_bytes, int box_cols,
+                    int box_rows, bool swizzle128);
 
 cudaError_t run_group_quantize(const QuantCall& c, cudaStream_t s);
 cudaError_t run_requant(const RequantCall& c, cudaStream_t s);

@@ -16,11 +16,12 @@
 //   dbias          : per-expert column sums (PR #3244, ordinary dbias reduced
 //                    directly, without a wgrad stage).
 //
-// Design (HBM-bound): one CTA of 8 warps handles a 128x128 tile; lane l of
-// warp w owns columns 64*(w%2) + 2l, +1 of rows 32*(w/2)..+31, so every
-// warp-wide load and store is one contiguous stretch of a row. The colwise
-// amax of a 32-row block and the dbias column sums are thread-local; the
-// rowwise block spans a half-warp. The E8M0 code depends only on the largest exponent field of the
+// Design (HBM-bound): persistent CTAs (several per SM) stream 128x128 input
+// tiles through a TMA-fed shared-memory ring while 4 compute warps quantize;
+// lane l of warp w owns columns 4l..4l+3 of rows 32w..32w+31, so every
+// warp-wide store is one contiguous stretch of a row. The colwise amax of a
+// 32-row block and the dbias column sums are thread-local; the rowwise block
+// spans 8 lanes. The E8M0 code depends only on the largest exponent field of the
 // block, so rowwise maxima are reduced as packed 8-bit exponents (4 rows per
 // word, byte-wise max shuffles). A 128x128 tile produces exactly one
 // 512-byte rowwise and one 512-byte colwise scale atom of the swizzled
@@ -57,38 +58,65 @@ struct TileArgs {
     int32_t* status;
 };
 
-__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
-    uint2 r;
-    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-    return r;
-}
-__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
-    uint32_t r;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
-}
-
-// Byte-wise max of 4 packed 8-bit exponents across the 16 lanes of a half-warp.
-__device__ __forceinline__ uint32_t group16_max_u8x4(uint32_t v) {
+// Byte-wise max of 4 packed 8-bit exponents across the 8 lanes of a group.
+__device__ __forceinline__ uint32_t group8_max_u8x4(uint32_t v) {
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) v = __vmaxu4(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = 4; o >= 1; o >>= 1) v = __vmaxu4(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
 
-// One CTA (8 warps) handles a 128x128 tile. Warp w owns rows 32*(w/2)..+31
-// and the 64 columns 64*(w%2)..+63; lane l owns columns 2l, 2l+1 of that
-// strip in every one of its 32 rows, so each warp-wide load or store is one
-// contiguous stretch of a row. The colwise amax of a 32-row block and the
-// dbias column sums are thread-local (over the lane's 32 rows); a rowwise
-// block of 32 columns spans one half-warp, whose exponents are reduced four
-// rows at a time with byte-wise max shuffles (the scale depends only on the
-// block's largest exponent field).
+// Persistent CTAs, several per SM: warp 4 is a TMA producer that keeps the
+// next 128x128 input tiles in flight in a small shared-memory ring; warps 0..3
+// compute. Warp w owns rows 32w..32w+31 of a tile and lane l owns its columns
+// 4l..4l+3, so shared-memory reads are conflict-free and every global store
+// of a warp is one contiguous stretch of a row. The tile is read from shared
+// memory twice: pass 1 takes the colwise amax (thread-local over the lane's
+// 32 rows) and the dbias column sums, pass 2 encodes. A rowwise block of 32
+// columns spans 8 lanes, whose exponents are reduced four rows at a time as
+// packed bytes (the E8M0 code depends only on the block's largest exponent).
+template <bool kReq>
+struct TileShape {
+    static constexpr int kInBytes = kReq ? 1 : 2;          // input element size
+    static constexpr int kRowBytes = kTile * kInBytes;     // one tile row in shared memory
+    static constexpr int kStageBytes = kTile * kRowBytes;  // 16 KB (E4M3) or 32 KB (bf16)
+    static constexpr int kStages = kReq ? 3 : 2;
+    static constexpr int kSmem = kStages * kStageBytes + 2 * kStages * 8 + 128;
+};
+constexpr int kComputeWarps = 4;
+constexpr int kTileThreads = (kComputeWarps + 1) * 32;
+
+__device__ __forceinline__ void compute_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kComputeWarps * 32) : "memory");
+}
+// Barrier over the compute warps that also ORs a predicate across them, so
+// that they all take the same exit decision.
+__device__ __forceinline__ bool compute_bar_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(kComputeWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
 template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq>
-__global__ void __launch_bounds__(256, 2) mx_tile_kernel(TileArgs a) {
-    __shared__ int64_t s_off[MXQ_MAX_EXPERTS + 1];
+__global__ void __launch_bounds__(kTileThreads)
+    mx_tile_kernel(const __grid_constant__ CUtensorMap tm_in, TileArgs a) {
+    using Sh = TileShape<kReq>;
+    extern __shared__ uint8_t q_smem_raw[];
     __shared__ __align__(16) uint8_t s_rs[512];
     __shared__ __align__(16) uint8_t s_cs[512];
-    __shared__ float s_red[4][kTile];
+    __shared__ __align__(16) float s_red[4][kTile];
+    __shared__ int s_abort;
+
+    // dynamic shared memory: [input stages][full/empty barriers][expert offsets (E+1)]
+    uint8_t* q_smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + Sh::kStages * Sh::kStageBytes);
+    int64_t* s_off = reinterpret_cast<int64_t*>(bars + 2 * Sh::kStages);
 
     if (a.noop && *a.noop) return;
     const int bad = load_offsets(a.m_splits, a.E, a.M, s_off);
@@ -97,140 +125,187 @@ __global__ void __launch_bounds__(256, 2) mx_tile_kernel(TileArgs a) {
         return;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rg = warp >> 1, ch = warp & 1;
-    const int blk = ch * 2 + (lane >> 4);  // 32-column block of the tile holding this lane's columns
     const int64_t K = a.K;
     const int64_t tilesK = K / kTile;
     const int64_t tiles = (a.M / kTile) * tilesK;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + Sh::kStages);
+    volatile int* abort_flag = &s_abort;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int st = 0; st < Sh::kStages; ++st) {
+            mbar_init(full0 + 8 * st, 1);
+            mbar_init(empty0 + 8 * st, kComputeWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tm_in) : "memory");
+    }
+    __syncthreads();
 
-    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int64_t mt = t / tilesK, kt = t % tilesK;
-        const int64_t r0 = mt * kTile + rg * 32;             // this warp's first row
-        const int64_t col = kt * kTile + ch * 64 + lane * 2;  // this lane's first column
-
-        // ------------------------------------------------------------ load
-        uint32_t raw[32];   // bf16x2, or two E4M3 bytes in the low half
-        float rsc[kReq ? 32 : 1];
-        (void)rsc;
-        if constexpr (!kReq) {
-            const uint16_t* p = static_cast<const uint16_t*>(a.src) + r0 * K + col;
-#pragma unroll
-            for (int r = 0; r < 32; ++r) raw[r] = ldg_nc_u32(p + r * K);
-        } else {
-            const uint8_t* p = static_cast<const uint8_t*>(a.src) + r0 * K + col;
-#pragma unroll
-            for (int r = 0; r < 32; ++r) raw[r] = __ldg(reinterpret_cast<const unsigned short*>(p + r * K));
-            // lane l reads the 4 compact rowwise scale codes of row r0 + l
-            const uint32_t sw = ldg_nc_u32(a.src_scale + (r0 + lane) * (K / 32) + kt * 4);
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const uint32_t word = __shfl_sync(0xffffffffu, sw, r);
-                rsc[r] = scale_from_code((word >> (8 * blk)) & 0xFFu);
-            }
-            if constexpr (kRow) {
-                if (ch == 0) *reinterpret_cast<uint32_t*>(&s_rs[lane * 16 + rg * 4]) = sw;
+    if (warp == kComputeWarps) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+                if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) break;
+                const uint32_t fb = full0 + 8 * stage;
+                mbar_expect_tx(fb, Sh::kStageBytes);
+                tma_load_2d(smem_u32(q_smem + stage * Sh::kStageBytes), &tm_in, fb, (int)((t % tilesK) * kTile),
+                            (int)((t / tilesK) * kTile));
+                if (++stage == Sh::kStages) { stage = 0; phase ^= 1; }
             }
         }
-        // values of row r, exact fp32
-        auto val2 = [&](int r) -> float2 {
+        return;
+    }
+
+    const int rg = warp;         // 32-row group of the tile
+    const int blk = lane >> 3;   // 32-column block of the tile holding this lane's 4 columns
+    const uint32_t Ku = (uint32_t)K;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t mt = t / tilesK, kt = t % tilesK;
+        const int64_t r0 = mt * kTile + rg * 32;        // this warp's first row
+        const int64_t col = kt * kTile + lane * 4;       // this lane's first column
+
+        // requant: lane l reads the 4 compact rowwise scale codes of row r0 + l
+        uint32_t sw = 0;
+        if constexpr (kReq) sw = __ldg(reinterpret_cast<const unsigned int*>(a.src_scale + (r0 + lane) * (K / 32) + kt * 4));
+
+        const bool ok = mbar_wait(full0 + 8 * stage, phase, abort_flag);
+        if (compute_bar_any(!ok)) break;
+        const uint8_t* src = q_smem + stage * Sh::kStageBytes + (rg * 32) * Sh::kRowBytes + lane * 4 * Sh::kInBytes;
+
+        // raw bits of row r: bf16 x4 (two words) or E4M3 x4 (one word)
+        auto ld_row = [&](int r) -> uint2 {
+            if constexpr (!kReq) return *reinterpret_cast<const uint2*>(src + r * Sh::kRowBytes);
+            else return make_uint2(*reinterpret_cast<const uint32_t*>(src + r * Sh::kRowBytes), 0u);
+        };
+        // exact fp32 values of row r
+        auto vals = [&](int r, uint2 u, float* v) {
             if constexpr (!kReq) {
-                return make_float2(bf16lo(raw[r]), bf16hi(raw[r]));
+                v[0] = bf16lo(u.x);
+                v[1] = bf16hi(u.x);
+                v[2] = bf16lo(u.y);
+                v[3] = bf16hi(u.y);
             } else {
-                const float2 f = e4m3x2_to_f32((uint16_t)raw[r]);
-                return make_float2(f.x * rsc[r], f.y * rsc[r]);
+                const float sc = scale_from_code((__shfl_sync(0xffffffffu, sw, r) >> (8 * blk)) & 0xFFu);
+                const float2 lo = e4m3x2_to_f32((uint16_t)(u.x & 0xFFFFu));
+                const float2 hi = e4m3x2_to_f32((uint16_t)(u.x >> 16));
+                v[0] = lo.x * sc;
+                v[1] = lo.y * sc;
+                v[2] = hi.x * sc;
+                v[3] = hi.y * sc;
             }
         };
 
-        // ---------------------------------------------------------- rowwise
-        if constexpr (kRow && !kReq) {
+        // ------------------------------------ pass 1: colwise amax, dbias
+        uint32_t ccode[4] = {0, 0, 0, 0};
+        float cinv[4] = {1.f, 1.f, 1.f, 1.f};
+        if constexpr (kCol || kBias) {
+            uint32_t m[4] = {0, 0, 0, 0};
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) {
+                const uint2 u = ld_row(r);
+                if constexpr (!kReq && !kBias) {
+                    m[0] = __vmaxu2(m[0], u.x & 0x7FFF7FFFu);
+                    m[1] = __vmaxu2(m[1], u.y & 0x7FFF7FFFu);
+                } else {
+                    float v[4];
+                    vals(r, u, v);
 #pragma unroll
-            for (int r4 = 0; r4 < 32; r4 += 4) {
-                uint32_t packed = 0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t w = raw[r4 + k] & 0x7FFF7FFFu;
-                    packed |= (max(w & 0xFFFFu, w >> 16) >> 7) << (8 * k);  // bf16 exponent field
+                    for (int j = 0; j < 4; ++j) {
+                        m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
+                        sum[j] += v[j];
+                    }
                 }
-                packed = group16_max_u8x4(packed);
+            }
+            if constexpr (kCol) {
+                uint32_t e[4];
+                if constexpr (!kReq && !kBias) {
+                    e[0] = (m[0] >> 7) & 0xFFu;
+                    e[1] = (m[0] >> 23) & 0xFFu;
+                    e[2] = (m[1] >> 7) & 0xFFu;
+                    e[3] = (m[1] >> 23) & 0xFFu;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) e[j] = m[j] >> 23;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    ccode[j] = (uint32_t)max((int)e[j] - 8, 0);
+                    cinv[j] = inv_scale_from_code(ccode[j]);
+                }
+                if (a.swizzle) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) s_cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
+                } else {
+                    *reinterpret_cast<uint32_t*>(a.col_s + (mt * 4 + rg) * K + col) =
+                        ccode[0] | (ccode[1] << 8) | (ccode[2] << 16) | (ccode[3] << 24);
+                }
+            }
+            if constexpr (kBias) *reinterpret_cast<float4*>(&s_red[rg][lane * 4]) = make_float4(sum[0], sum[1], sum[2], sum[3]);
+        }
+        if constexpr (kReq && kRow) *reinterpret_cast<uint32_t*>(&s_rs[lane * 16 + rg * 4]) = sw;
+
+        // ------------------------------------------------- pass 2: encode
+        if constexpr ((kRow && !kReq) || kCol || kDeq) {
+            uint8_t* rq = kRow && !kReq ? a.row_q + r0 * K + col : nullptr;
+            uint8_t* cq = kCol ? a.col_q + r0 * K + col : nullptr;
+            __nv_bfloat16* dq = kDeq ? a.deq_out + r0 * K + col : nullptr;
+#pragma unroll 2
+            for (int r4 = 0; r4 < 32; r4 += 4) {
+                uint2 u[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) u[k] = ld_row(r4 + k);
+                uint32_t packed = 0;
+                if constexpr (kRow && !kReq) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t w2 = __vmaxu2(u[k].x & 0x7FFF7FFFu, u[k].y & 0x7FFF7FFFu);
+                        packed |= (max(w2 & 0xFFFFu, w2 >> 16) >> 7) << (8 * k);  // bf16 exponent field
+                    }
+                    packed = group8_max_u8x4(packed);
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
-                    const float inv = inv_scale_from_code(code);
-                    const float2 v = val2(r4 + k);
-                    *reinterpret_cast<uint16_t*>(a.row_q + (r0 + r4 + k) * K + col) =
-                        (uint16_t)cvt_e4m3x2(v.x * inv, v.y * inv);
-                    if ((lane & 15) == 0) {
-                        if (a.swizzle) s_rs[(r4 + k) * 16 + rg * 4 + blk] = (uint8_t)code;
-                        else a.row_s[(r0 + r4 + k) * (K / 32) + kt * 4 + blk] = (uint8_t)code;
+                    const int r = r4 + k;
+                    float v[4];
+                    vals(r, u[k], v);
+                    if constexpr (kRow && !kReq) {
+                        const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
+                        const float inv = inv_scale_from_code(code);
+                        *reinterpret_cast<uint32_t*>(rq + r * Ku) =
+                            cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+                        if ((lane & 7) == 0) {
+                            if (a.swizzle) s_rs[r * 16 + rg * 4 + blk] = (uint8_t)code;
+                            else a.row_s[(r0 + r) * (K / 32) + kt * 4 + blk] = (uint8_t)code;
+                        }
+                    }
+                    if constexpr (kCol) {
+                        *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) |
+                                                                    (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
+                    }
+                    if constexpr (kDeq) {
+                        __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]);
+                        __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2], v[3]);
+                        uint2 o;
+                        o.x = *reinterpret_cast<uint32_t*>(&b0);
+                        o.y = *reinterpret_cast<uint32_t*>(&b1);
+                        *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = o;
                     }
                 }
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);  // this warp is done with the stage
+        if (++stage == Sh::kStages) { stage = 0; phase ^= 1; }
 
-        // ---------------------------------------------------------- colwise
-        if constexpr (kCol) {
-            uint32_t e0, e1;  // largest exponent field of each of the 2 columns
-            if constexpr (!kReq) {
-                uint32_t m = 0;
-#pragma unroll
-                for (int r = 0; r < 32; ++r) m = __vmaxu2(m, raw[r] & 0x7FFF7FFFu);
-                e0 = (m >> 7) & 0xFFu;
-                e1 = (m >> 23) & 0xFFu;
-            } else {
-                uint32_t m0 = 0, m1 = 0;
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    const float2 v = val2(r);
-                    m0 = max(m0, __float_as_uint(v.x) & 0x7FFFFFFFu);
-                    m1 = max(m1, __float_as_uint(v.y) & 0x7FFFFFFFu);
-                }
-                e0 = m0 >> 23;
-                e1 = m1 >> 23;
-            }
-            const uint32_t c0 = (uint32_t)max((int)e0 - 8, 0), c1 = (uint32_t)max((int)e1 - 8, 0);
-            const float i0 = inv_scale_from_code(c0), i1 = inv_scale_from_code(c1);
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const float2 v = val2(r);
-                *reinterpret_cast<uint16_t*>(a.col_q + (r0 + r) * K + col) = (uint16_t)cvt_e4m3x2(v.x * i0, v.y * i1);
-            }
-            if (a.swizzle) {
-                const int cc = (2 * lane) & 31, cb = blk;  // both columns share the 32-column block
-                s_cs[cc * 16 + cb * 4 + rg] = (uint8_t)c0;
-                s_cs[(cc + 1) * 16 + cb * 4 + rg] = (uint8_t)c1;
-            } else {
-                *reinterpret_cast<uint16_t*>(a.col_s + (mt * 4 + rg) * K + col) = (uint16_t)(c0 | (c1 << 8));
-            }
-        }
-
-        // ------------------------------------------------- dequant output
-        if constexpr (kDeq) {
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const float2 v = val2(r);
-                __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
-                *reinterpret_cast<__nv_bfloat162*>(a.deq_out + (r0 + r) * K + col) = b;
-            }
-        }
-
-        // ------------------------------------------------- dbias partials
+        compute_bar();
         if constexpr (kBias) {
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const float2 v = val2(r);
-                s0 += v.x;
-                s1 += v.y;
-            }
-            *reinterpret_cast<float2*>(&s_red[rg][ch * 64 + lane * 2]) = make_float2(s0, s1);
-        }
-
-        __syncthreads();
-        if constexpr (kBias) {
-            if (threadIdx.x < kTile) {
-                const int c = threadIdx.x;
-                a.partials[mt * K + kt * kTile + c] = ((s_red[0][c] + s_red[1][c]) + s_red[2][c]) + s_red[3][c];
-            }
+            const int c = threadIdx.x;  // 0..127
+            a.partials[mt * K + kt * kTile + c] = ((s_red[0][c] + s_red[1][c]) + s_red[2][c]) + s_red[3][c];
         }
         if constexpr (kRow) {
             if ((a.swizzle || kReq) && threadIdx.x < 32) {
@@ -249,8 +324,9 @@ __global__ void __launch_bounds__(256, 2) mx_tile_kernel(TileArgs a) {
                 dst[threadIdx.x - 32] = reinterpret_cast<const uint4*>(s_cs)[threadIdx.x - 32];
             }
         }
-        __syncthreads();
+        compute_bar();
     }
+    if (threadIdx.x == 0 && s_abort && a.status) atomicOr(a.status, MXQ_STATUS_WAIT_TIMEOUT);
 }
 
 // Second dbias stage: out[e, c] = sum over expert e's 128-row tiles of the
@@ -283,10 +359,20 @@ static int num_sms() {
 
 template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq>
 static cudaError_t launch_tile(const TileArgs& a, cudaStream_t s) {
+    using Sh = TileShape<kReq>;
     const int64_t tiles = (a.M / kTile) * (a.K / kTile);
     if (tiles == 0) return cudaSuccess;
-    const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms() * 4);
-    mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq><<<(unsigned)grid, 256, 0, s>>>(a);
+    const int smem = Sh::kSmem + (a.E + 1) * 8;
+    const cudaError_t attr = cudaFuncSetAttribute(mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (attr != cudaSuccess) return attr;
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, a.src, a.M, a.K, Sh::kInBytes, kTile, kTile, false)) return cudaErrorInvalidValue;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq>,
+                                                  kTileThreads, smem);
+    const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms() * std::max(per_sm, 1));
+    mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq><<<(unsigned)grid, kTileThreads, smem, s>>>(tm, a);
     return cudaGetLastError();
 }
 
