@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "mxq_common.cuh"
@@ -58,18 +59,23 @@ constexpr int BN = 256;               // MMA N (cols of the output tile)
 constexpr int BK = 128;               // K elements (bytes) per pipeline stage
 constexpr int UMMA_K = 32;            // K per tcgen05.mma for 8-bit operands
 constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 8;
 constexpr int A_BYTES = BM * BK;      // 16 KB
 constexpr int B_BYTES = BN * BK;      // 32 KB
-constexpr int SFA_OFF = A_BYTES + B_BYTES;
-constexpr int SFB_OFF = SFA_OFF + 512;
-constexpr int STAGE_BYTES = 51200;    // 50 KB: keeps every stage 1024-aligned
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB: every stage stays 1024-aligned
+constexpr int SF_STAGE_BYTES = 1536;            // scale atoms of a stage: A (512), B (2 x 512)
 constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES + 512 + 1024;
 constexpr int NUM_THREADS = 320;      // producer, MMA, 8 epilogue warps
-constexpr int EPI_WARPS = 8;
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SFA = 256;         // scale columns after the accumulator
 constexpr int TMEM_SFB = 264;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr int EPI_STAGE_BYTES = 2048;           // per epilogue warp: one 32-row output box
+// dynamic shared memory: [A/B stages][scale atoms][barriers][epilogue staging][expert tables]
+constexpr int SF_REGION = STAGES * STAGE_BYTES;
+constexpr int BAR_REGION = SF_REGION + STAGES * SF_STAGE_BYTES;
+constexpr int EPI_REGION = BAR_REGION + 256;
+constexpr int TABLE_REGION = EPI_REGION + EPI_WARPS * EPI_STAGE_BYTES;
+__host__ __device__ constexpr int smem_bytes(int E) { return 1024 + TABLE_REGION + 8 * (E + 1) + 2 * E; }
 
 struct Params {
     int mode;
@@ -81,6 +87,7 @@ struct Params {
     const __nv_bfloat16* bias;
     void* out;
     int accumulate, out_bf16;
+    int tma_store;  // 1: outputs leave through TMA bulk-tensor stores of staged boxes
     int32_t* status;
 };
 
@@ -203,10 +210,11 @@ struct Sched {
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        Params p) {
+                        const __grid_constant__ CUtensorMap tmOut, Params p) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int64_t s_off[MXQ_MAX_EXPERTS + 1];
-    __shared__ int16_t s_order[MXQ_MAX_EXPERTS];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int64_t* s_off = reinterpret_cast<int64_t*>(smem + TABLE_REGION);
+    int16_t* s_order = reinterpret_cast<int16_t*>(s_off + p.E + 1);
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -229,8 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
 
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_REGION);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
     const uint32_t acc_full = smem_u32(bars + 2 * STAGES), acc_empty = smem_u32(bars + 2 * STAGES + 1);
     volatile int* abort_flag = &s_abort;
@@ -246,6 +253,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+        if (p.tma_store) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmOut) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
@@ -309,9 +317,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         sfb0 = bb + ((T.b_col / 128) * kbs + kb) * 512;
                         sfb1 = bb + ((T.b_col / 128 + 1) * kbs + kb) * 512;
                     }
-                    bulk_load(sb + SFA_OFF, sfa, 512, fb);
-                    bulk_load(sb + SFB_OFF, sfb0, 512, fb);
-                    bulk_load(sb + SFB_OFF + 512, sfb1, 512, fb);
+                    const uint32_t sfs = smem_u32(smem + SF_REGION + stage * SF_STAGE_BYTES);
+                    bulk_load(sfs, sfa, 512, fb);
+                    bulk_load(sfs + 512, sfb0, 512, fb);
+                    bulk_load(sfs + 1024, sfb1, 512, fb);
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
@@ -336,9 +345,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) goto done_mma;
                         fence_after();
                         const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
-                        tmem_cp_sf(tmem + TMEM_SFA, smem_desc(sb + SFA_OFF, 0, 128, 0));
-                        tmem_cp_sf(tmem + TMEM_SFB, smem_desc(sb + SFB_OFF, 0, 128, 0));
-                        tmem_cp_sf(tmem + TMEM_SFB + 4, smem_desc(sb + SFB_OFF + 512, 0, 128, 0));
+                        const uint32_t sfs = smem_u32(smem + SF_REGION + stage * SF_STAGE_BYTES);
+                        tmem_cp_sf(tmem + TMEM_SFA, smem_desc(sfs, 0, 128, 0));
+                        tmem_cp_sf(tmem + TMEM_SFB, smem_desc(sfs + 512, 0, 128, 0));
+                        tmem_cp_sf(tmem + TMEM_SFB + 4, smem_desc(sfs + 1024, 0, 128, 0));
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k) {
                             const uint64_t ad = a_mn ? smem_desc(sb + k * a_step, BK * 128, 1024, 2)
@@ -365,6 +375,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int half = (warp - 2) >> 2;
         const int row_in_tile = q * 32 + lane;
         const int col0 = half * (BN / 2);
+        uint8_t* epi_buf = smem + EPI_REGION + (warp - 2) * EPI_STAGE_BYTES;
         uint32_t aphase = 0;
         for (int64_t i = 0;; ++i) {
             const Tile T = S.get(S.pick(i, cta, ncta));
@@ -392,8 +403,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
 
-            if (p.mode != kWgrad) {
-                const int64_t row = T.a_row + row_in_tile;
+            const int64_t row = T.a_row + row_in_tile;
+            if (p.tma_store) {
+                // Stage 32-row boxes in this warp's buffer and write each with one
+                // TMA store: a box is 32 columns (bf16) or 16 columns (fp32).
+                const bool f32 = (p.mode == kWgrad && !p.out_bf16);
+                const int box_cols = f32 ? 16 : 32;
+                const int out_row0 = (int)((p.mode == kWgrad ? (int64_t)T.e * p.N : 0) + T.a_row + q * 32);
+                const __nv_bfloat16* bias =
+                    (p.mode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col + col0 : nullptr;
+#pragma unroll
+                for (int c = 0; c < BN / 2; c += 16) {
+                    if (!f32 && (c & 31)) continue;
+                    uint32_t w16[16];
+                    if (f32) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w16[j] = r[c + j];
+                    } else {
+                        float f[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[(c + j) & (BN / 2 - 1)]);
+                        if (bias) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const uint4 bw = __ldg(reinterpret_cast<const uint4*>(bias + c) + v);
+                                const uint32_t ws[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    f[8 * v + 2 * j] += __uint_as_float(ws[j] << 16);
+                                    f[8 * v + 2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+                            w16[j] = *reinterpret_cast<uint32_t*>(&b2);
+                        }
+                    }
+                    // the previous box of this buffer must have been read out
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    __syncwarp();
+                    uint4* dst = reinterpret_cast<uint4*>(epi_buf + lane * 64);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        asm volatile(
+                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                                (uint64_t)&tmOut),
+                            "r"((int)(T.b_col + col0 + c)), "r"(out_row0), "r"(smem_u32(epi_buf))
+                            : "memory");
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                    (void)box_cols;
+                }
+            } else if (p.mode != kWgrad) {
                 const int64_t ldo = (p.mode == kFprop) ? p.N : p.K;
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + row * ldo + T.b_col + col0;
                 const __nv_bfloat16* bias =
@@ -421,7 +487,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     *reinterpret_cast<uint4*>(out + c) = make_uint4(h[0], h[1], h[2], h[3]);
                 }
             } else if (!(zero && p.accumulate)) {
-                const int64_t row = T.a_row + row_in_tile;  // n
+                // accumulate into dW: read-modify-write with plain loads and stores
                 const int64_t base = ((int64_t)T.e * p.N + row) * p.K + T.b_col + col0;
                 if (p.out_bf16) {
                     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base;
@@ -467,6 +533,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             aphase ^= 1;
         }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
 
     fence_before();
@@ -534,7 +602,7 @@ static int sm_count() {
 cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     using namespace gemm;
     const cudaError_t attr_err =
-        cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MXQ_MAX_EXPERTS));
     if (attr_err != cudaSuccess) return attr_err;
 
     int64_t tiles;
@@ -559,6 +627,18 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     }
     if (!ok) return cudaErrorInvalidValue;
 
+    // Output boxes for the TMA-store epilogue (not used when accumulating).
+    CUtensorMap to;
+    memset(&to, 0, sizeof(to));
+    const int tma_store = !c.accumulate;
+    if (tma_store) {
+        if (c.mode == kFprop) ok = encode_tmap_2d(&to, c.out, c.M, c.N, 2, 32, 32, false);
+        else if (c.mode == kDgrad) ok = encode_tmap_2d(&to, c.out, c.M, c.K, 2, 32, 32, false);
+        else if (c.out_bf16) ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 2, 32, 32, false);
+        else ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 4, 16, 32, false);
+        if (!ok) return cudaErrorInvalidValue;
+    }
+
     Params p{};
     p.mode = c.mode;
     p.M = c.M;
@@ -572,10 +652,11 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     p.out = c.out;
     p.accumulate = c.accumulate;
     p.out_bf16 = c.out_bf16;
+    p.tma_store = tma_store;
     p.status = c.status;
 
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
-    grouped_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ta, tb, p);
+    grouped_gemm_kernel<<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
     return cudaGetLastError();
 }
 
