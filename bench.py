@@ -420,11 +420,11 @@ def main():
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if os.path.exists(tpath):
-        from moe_expert_grouped_group_gb300.build import _stamp
+        from moe_expert_grouped_group_gb300.build import source_stamp
 
         with open(tpath) as f:
             tj = json.load(f)
-        if tj.get("source_stamp") == _stamp() and tj.get("workload") == WORKLOAD:
+        if tj.get("source_stamp") == source_stamp() and tj.get("workload") == WORKLOAD:
             traffic = tj.get("dram_bytes_per_launch")
     roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": mx_peak, "unit": "TFLOP/s",
                 "frac": gemm_tflops / mx_peak, "traffic": traffic,

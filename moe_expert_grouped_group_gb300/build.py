@@ -47,6 +47,16 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+def source_stamp(files=("mxq_gemm.cu", "mxq_common.cuh", "mxq_internal.h")) -> str:
+    """Hash of the named kernel sources (identifies the code an ncu capture measured)."""
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     stamp_path = os.path.join(OUT_DIR, "stamp")
