@@ -338,7 +338,8 @@ def max_over_ranks(v: float) -> float:
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -355,7 +356,7 @@ def reference_arm(args, rank, world):
     w, d = make_host_workload()
     flops, _ = algorithmic(w)
     step_flops = sum(flops.values())
-    sample = OracleSample(w, d)
+    sample = OracleSample(w, d, entries=1 << 16)
     for _ in range(args.warmup):
         sample.run()
     times = [sum(sample.run().values()) for _ in range(args.steps)]

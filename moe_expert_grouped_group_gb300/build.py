@@ -22,6 +22,8 @@ SOURCES = ["mxq_api.cu", "mxq_quant.cu", "mxq_gemm.cu", "mxq_swiglu.cu", "mxq_no
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-I", os.path.join(ROOT, "include")]
+# Optional extra nvcc flags (e.g. -D overrides of tuning constants) for tuning builds.
+FLAGS += os.environ.get("MXQ_NVCC_EXTRA", "").split()
 
 
 def nvcc() -> str:

@@ -242,3 +242,52 @@ def test_full_size_quantize_activation(mxq, name):
     else:
         q = mxq.group_quantize(dev_bf16(x), dev_i64(ms))
         _compare_quant(q, orc.group_quantize(x, ms, swizzled=True), name)
+
+
+def _dbias_ok(got, ref, src_abs_colsum):
+    return np.all(np.abs(got - ref) <= 1e-5 * src_abs_colsum + 1e-30)
+
+
+def test_full_size_mlp_backward_quantizers(mxq):
+    """64 experts, 83968 routed rows: requant of the rowwise-prequantized FC2
+    gradient (3072 wide) with fused dbias, and group_quantize of the FC1
+    gradient (2048 wide, synthetic) with fused dbias."""
+    w = WORKLOADS["e64_h3072_f1024_t84k_prequant"]
+    d = make_inputs(w, which=("dy", "dy2"))
+    ms = d["m_splits"]
+    off = np.concatenate([[0], np.cumsum(ms)])
+    # FC2 grad arrives rowwise-quantized (the combine's backward)
+    wire = orc.group_quantize(d["dy2"], ms, rowwise=True, colwise=False, swizzled=False)
+    r = mxq.requant_colwise(dev_u8(wire["row_q"]), dev_u8(wire["row_s"]), dev_i64(ms), dbias=True)
+    o = orc.requant_colwise(wire["row_q"], wire["row_s"], ms, swizzled=True, dbias=True)
+    assert np.array_equal(host(r["col_data"]), o["col_q"])
+    assert np.array_equal(host(r["col_scale"]), o["col_s"])
+    assert np.array_equal(host(r["row_scale_swizzled"]), o["row_s_swizzled"])
+    deq = orc.dequant_rowwise(wire["row_q"], wire["row_s"])
+    got = host(r["dbias"]).astype(np.float64)
+    for e in range(w.E):
+        assert _dbias_ok(got[e], o["dbias"][e], np.abs(deq[off[e]:off[e + 1]]).sum(axis=0)), e
+    del deq
+    # FC1 grad (M, 2F) quantized row+col with fused dbias
+    q = mxq.group_quantize(dev_bf16(d["dy"]), dev_i64(ms), dbias=True)
+    _compare_quant(q, orc.group_quantize(d["dy"], ms, swizzled=True), "dY1")
+    ref = orc.grouped_dbias(d["dy"], ms)
+    got = host(q["dbias"]).astype(np.float64)
+    f = np.abs(bf16_to_f64(d["dy"]))
+    for e in range(w.E):
+        assert _dbias_ok(got[e], ref[e], f[off[e]:off[e + 1]].sum(axis=0)), e
+
+
+def test_full_size_swiglu(mxq):
+    """SwiGLU fwd/bwd at 83968 x (2 x 1024)."""
+    rng = np.random.default_rng(18)
+    M, F = 83968, 1024
+    y = bf16_bits_from_f32((2 * rng.standard_normal((M, 2 * F))).astype(np.float32))
+    dh = bf16_bits_from_f32(rng.standard_normal((M, F)).astype(np.float32))
+    h = host(mxq.swiglu_fwd(dev_bf16(y)))
+    dy = host(mxq.swiglu_bwd(dev_bf16(dh), dev_bf16(y)))
+    for got, ref in ((h, orc.swiglu_fwd(y)), (dy, orc.swiglu_bwd(dh, y))):
+        d_ = np.abs(got.astype(np.int32) - ref.astype(np.int32))
+        same_sign = (got >> 15) == (ref >> 15)
+        ok = (d_ <= 1) & same_sign | ((got & 0x7FFF) <= 1) & ((ref & 0x7FFF) <= 1)
+        assert ok.all(), first_diff(got, ref)
