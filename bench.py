@@ -53,6 +53,7 @@ def parse():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
     return p.parse_args()
 
 
@@ -181,6 +182,130 @@ class NativeStep:
 
     def flush(self):
         self.flush_buf.fill_(1)
+
+
+MLP_WORKLOAD = "e64_h3072_f1024_t84k_prequant"
+MLP_STAGES = ["requant_x", "quantize_w1_w2", "fc1_fprop", "swiglu_fwd", "quantize_h", "fc2_fprop",
+              "requant_dy2_dbias", "fc2_dgrad", "fc2_wgrad", "swiglu_bwd", "quantize_dy1_dbias", "fc1_dgrad",
+              "fc1_wgrad"]
+
+
+class MLPStep:
+    """Forward + backward of a grouped MoE MLP (FC1 -> SwiGLU -> FC2) with
+    per-expert biases; X and the FC2 gradient arrive rowwise-quantized (the
+    expert-parallel dispatch and the combine's backward). Covers every step
+    of the path: requant (+fused dbias), weight and activation quantize
+    (+fused dbias), the three grouped GEMMs of both linears, SwiGLU."""
+
+    def __init__(self, dev, seed=0):
+        import torch
+
+        import moe_expert_grouped_group_gb300 as mxq
+        from synth import WORKLOADS, make_inputs
+
+        self.torch, self.mxq = torch, mxq
+        w = self.w = WORKLOADS[MLP_WORKLOAD]
+        d = make_inputs(w, seed=seed, which=("x", "w", "dy", "w2", "dy2", "b1", "b2"))
+        E, H, F, M = w.E, w.K, w.F, w.M
+        self.E, self.H, self.F, self.M = E, H, F, M
+        tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        self.ms = torch.from_numpy(d["m_splits"]).to(dev)
+        self.w1 = tb(d["w"]).view(E * 2 * F, H)
+        self.w2 = tb(d["w2"]).view(E * H, F)
+        self.b1, self.b2 = tb(d["b1"]), tb(d["b2"])
+        qx = mxq.group_quantize(tb(d["x"]), self.ms, rowwise=True, colwise=False, swizzle=False)
+        qd = mxq.group_quantize(tb(d["dy2"]), self.ms, rowwise=True, colwise=False, swizzle=False)
+        self.x_row, self.x_rs = qx["row_data"], qx["row_scale"]
+        self.dy2_row, self.dy2_rs = qd["row_data"], qd["row_scale"]
+        u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+        bf = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=dev)
+        sb = mxq.scale_bytes
+
+        def q(rows, cols):
+            return {"row_data": u8((rows, cols)), "row_scale": u8(sb(rows, cols, False)),
+                    "col_data": u8((rows, cols)), "col_scale": u8(sb(rows, cols, True))}
+
+        self.rqx = {"col_data": u8((M, H)), "col_scale": u8(sb(M, H, True)), "row_scale_swizzled": u8(sb(M, H, False))}
+        self.rqd = {"col_data": u8((M, H)), "col_scale": u8(sb(M, H, True)), "row_scale_swizzled": u8(sb(M, H, False)),
+                    "dbias": torch.empty((E, H), dtype=torch.float32, device=dev)}
+        self.qw1, self.qw2 = q(E * 2 * F, H), q(E * H, F)
+        self.qh = q(M, F)
+        self.qdy1 = q(M, 2 * F)
+        self.qdy1["dbias"] = torch.empty((E, 2 * F), dtype=torch.float32, device=dev)
+        self.ws = u8(max(mxq.workspace_bytes(2, M, 0, H, E), mxq.workspace_bytes(1, M, 0, 2 * F, E)))
+        self.y1, self.h, self.y2 = bf(M, 2 * F), bf(M, F), bf(M, H)
+        self.dh, self.dy1, self.dx = bf(M, F), bf(M, 2 * F), bf(M, H)
+        self.dw1 = torch.empty((E, 2 * F, H), dtype=torch.float32, device=dev)
+        self.dw2 = torch.empty((E, H, F), dtype=torch.float32, device=dev)
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 16
+
+    def flops(self):
+        return 6.0 * self.M * (2 * self.F * self.H + self.H * self.F)
+
+    def run(self, ev=None):
+        mxq, E, H, F = self.mxq, self.E, self.H, self.F
+        rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
+        rec(0)
+        mxq.requant_colwise(self.x_row, self.x_rs, self.ms, out=self.rqx)
+        rec(1)
+        mxq.group_quantize(self.w1, None, E=E, out=self.qw1)
+        mxq.group_quantize(self.w2, None, E=E, out=self.qw2)
+        rec(2)
+        mxq.grouped_gemm_fprop(self.x_row, self.rqx["row_scale_swizzled"], self.qw1["row_data"].view(E, 2 * F, H),
+                               self.qw1["row_scale"], self.ms, bias=self.b1, out=self.y1)
+        rec(3)
+        mxq.swiglu_fwd(self.y1, out=self.h)
+        rec(4)
+        mxq.group_quantize(self.h, self.ms, out=self.qh)
+        rec(5)
+        mxq.grouped_gemm_fprop(self.qh["row_data"], self.qh["row_scale"], self.qw2["row_data"].view(E, H, F),
+                               self.qw2["row_scale"], self.ms, bias=self.b2, out=self.y2)
+        rec(6)
+        mxq.requant_colwise(self.dy2_row, self.dy2_rs, self.ms, dbias=True, out=self.rqd, workspace=self.ws)
+        rec(7)
+        mxq.grouped_gemm_dgrad(self.dy2_row, self.rqd["row_scale_swizzled"], self.qw2["col_data"].view(E, H, F),
+                               self.qw2["col_scale"], self.ms, out=self.dh)
+        rec(8)
+        mxq.grouped_gemm_wgrad(self.rqd["col_data"], self.rqd["col_scale"], self.qh["col_data"], self.qh["col_scale"],
+                               self.ms, out=self.dw2)
+        rec(9)
+        mxq.swiglu_bwd(self.dh, self.y1, out=self.dy1)
+        rec(10)
+        mxq.group_quantize(self.dy1, self.ms, dbias=True, out=self.qdy1, workspace=self.ws)
+        rec(11)
+        mxq.grouped_gemm_dgrad(self.qdy1["row_data"], self.qdy1["row_scale"], self.qw1["col_data"].view(E, 2 * F, H),
+                               self.qw1["col_scale"], self.ms, out=self.dx)
+        rec(12)
+        mxq.grouped_gemm_wgrad(self.qdy1["col_data"], self.qdy1["col_scale"], self.rqx["col_data"],
+                               self.rqx["col_scale"], self.ms, out=self.dw1)
+        rec(13)
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+
+
+def time_mlp(dev, steps=10, warmup=3):
+    import torch
+
+    st = MLPStep(dev)
+    for _ in range(warmup):
+        st.flush()
+        st.run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(14)] for _ in range(steps)]
+    for i in range(steps):
+        st.flush()
+        st.run(evs[i])
+    torch.cuda.synchronize()
+    ms = statistics.mean(evs[i][0].elapsed_time(evs[i][13]) for i in range(steps))
+    per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+           for j, k in enumerate(MLP_STAGES)}
+    gemm_ms = sum(v for k, v in per.items() if "prop" in k or "grad" in k)
+    return {"workload": MLP_WORKLOAD, "steps": steps, "warmup": warmup, "ms_per_step": ms,
+            "tflops_step": st.flops() / (ms * 1e-3) / 1e12, "gemm_tflops": st.flops() / (gemm_ms * 1e-3) / 1e12,
+            "stage_ms": per, "gpu_launches": st.launches_per_step * steps,
+            "step": "fwd+bwd of FC1 (bias) -> SwiGLU -> FC2 (bias), X and dY2 rowwise-prequantized"}
 
 
 KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
@@ -414,6 +539,11 @@ def main():
         e2e = {"value": aggregate(step_flops, world, ms_e2e * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
 
+    mlp = None
+    if not args.no_mlp and rank == 0:
+        del st
+        torch.cuda.empty_cache()
+        mlp = time_mlp(dev)
     if rank != 0:
         return
     bf16_peak, hbm_peak, src = peaks()
@@ -450,12 +580,13 @@ def main():
                    "step": "requant X + quantize W (row+col) + quantize dY (row+col) + fprop + dgrad + wgrad (fp32 dW)",
                    "l2": "256 MiB buffer written before every timed step (outside the event brackets)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": st.launches_per_step * args.steps,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * args.steps,
         "clocks": clocks,
         "kernels_ms": per_kernel, "gemm_tflops": gemm_tflops,
         "group_quantize_gbs": quant_gbs, "hbm_peak_gbs": hbm_peak,
         "group_quantize_frac": {k: v / hbm_peak for k, v in quant_gbs.items()},
         "wall_s_timed_region": wall,
+        "mlp_step": mlp,
     }
     print(json.dumps(line), flush=True)
 
