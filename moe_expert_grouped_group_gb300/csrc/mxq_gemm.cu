@@ -280,47 +280,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int64_t i = 0;; ++i) {
                 const Tile T = S.get(S.pick(i, cta, ncta));
                 if (!T.valid) break;
+                // Per tile: first-block coordinates and scale-atom addresses; each
+                // 128-deep K block then advances them by fixed strides.
+                int ax, ay, bx, by, adx, ady, bdx, bdy;
+                const uint8_t *sfa, *sfb0, *sfb1;  // atoms of K block 0; +512 B per block
+                if (p.mode == kFprop) {
+                    const int64_t kbs = p.K / BK, wrow = (int64_t)T.e * p.N + T.b_col;
+                    ax = 0; ay = (int)T.a_row; adx = BK; ady = 0;
+                    bx = 0; by = (int)wrow; bdx = BK; bdy = 0;
+                    sfa = p.sfa + (T.a_row / 128) * kbs * 512;
+                    sfb0 = p.sfb + (wrow / 128) * kbs * 512;
+                    sfb1 = sfb0 + kbs * 512;
+                } else if (p.mode == kDgrad) {
+                    const int64_t kbs = p.N / BK;
+                    const uint8_t* wb = p.sfb + (int64_t)T.e * p.K * (p.N / 32);
+                    ax = 0; ay = (int)T.a_row; adx = BK; ady = 0;
+                    bx = (int)T.b_col; by = (int)((int64_t)T.e * p.N); bdx = 0; bdy = BK;
+                    sfa = p.sfa + (T.a_row / 128) * kbs * 512;
+                    sfb0 = wb + (T.b_col / 128) * kbs * 512;
+                    sfb1 = sfb0 + kbs * 512;
+                } else {
+                    const int64_t kbs = T.me / BK;
+                    const uint8_t* ab = p.sfa + p.N * T.off / 32;
+                    const uint8_t* bb = p.sfb + p.K * T.off / 32;
+                    ax = (int)T.a_row; ay = (int)T.off; adx = 0; ady = BK;
+                    bx = (int)T.b_col; by = (int)T.off; bdx = 0; bdy = BK;
+                    sfa = ab + (T.a_row / 128) * kbs * 512;
+                    sfb0 = bb + (T.b_col / 128) * kbs * 512;
+                    sfb1 = sfb0 + kbs * 512;
+                }
+                // the second B box: 128 rows further (K-major B) or 128 columns further (MN-major B)
+                const int b2x = (p.mode == kFprop) ? 0 : 128, b2y = (p.mode == kFprop) ? 128 : 0;
                 for (int kb = 0; kb < T.nk; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) goto done_producer;
                     const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, STAGE_TX);
-                    const uint8_t *sfa, *sfb0, *sfb1;
-                    if (p.mode == kFprop) {
-                        const int64_t kbs = p.K / BK;
-                        tma_load_2d(sb, &tmA, fb, kb * BK, (int)T.a_row);
-                        const int64_t wrow = (int64_t)T.e * p.N + T.b_col;
-                        tma_load_2d(sb + A_BYTES, &tmB, fb, kb * BK, (int)wrow);
-                        tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, kb * BK, (int)(wrow + 128));
-                        sfa = p.sfa + ((T.a_row / 128) * kbs + kb) * 512;
-                        sfb0 = p.sfb + ((wrow / 128) * kbs + kb) * 512;
-                        sfb1 = p.sfb + ((wrow / 128 + 1) * kbs + kb) * 512;
-                    } else if (p.mode == kDgrad) {
-                        const int64_t kbs = p.N / BK;
-                        tma_load_2d(sb, &tmA, fb, kb * BK, (int)T.a_row);
-                        const int64_t wrow = (int64_t)T.e * p.N + kb * BK;
-                        tma_load_2d(sb + A_BYTES, &tmB, fb, (int)T.b_col, (int)wrow);
-                        tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, (int)(T.b_col + 128), (int)wrow);
-                        sfa = p.sfa + ((T.a_row / 128) * kbs + kb) * 512;
-                        const uint8_t* wb = p.sfb + (int64_t)T.e * p.K * (p.N / 32);
-                        sfb0 = wb + ((T.b_col / 128) * kbs + kb) * 512;
-                        sfb1 = wb + ((T.b_col / 128 + 1) * kbs + kb) * 512;
-                    } else {
-                        const int64_t kbs = T.me / BK;
-                        const int64_t trow = T.off + (int64_t)kb * BK;
-                        tma_load_2d(sb, &tmA, fb, (int)T.a_row, (int)trow);
-                        tma_load_2d(sb + A_BYTES, &tmB, fb, (int)T.b_col, (int)trow);
-                        tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, (int)(T.b_col + 128), (int)trow);
-                        const uint8_t* ab = p.sfa + p.N * T.off / 32;
-                        const uint8_t* bb = p.sfb + p.K * T.off / 32;
-                        sfa = ab + ((T.a_row / 128) * kbs + kb) * 512;
-                        sfb0 = bb + ((T.b_col / 128) * kbs + kb) * 512;
-                        sfb1 = bb + ((T.b_col / 128 + 1) * kbs + kb) * 512;
-                    }
+                    tma_load_2d(sb, &tmA, fb, ax, ay);
+                    tma_load_2d(sb + A_BYTES, &tmB, fb, bx, by);
+                    tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, bx + b2x, by + b2y);
                     const uint32_t sfs = smem_u32(smem + SF_REGION + stage * SF_STAGE_BYTES);
                     bulk_load(sfs, sfa, 512, fb);
                     bulk_load(sfs + 512, sfb0, 512, fb);
                     bulk_load(sfs + 1024, sfb1, 512, fb);
+                    ax += adx; ay += ady; bx += bdx; by += bdy;
+                    sfa += 512; sfb0 += 512; sfb1 += 512;
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
@@ -331,8 +335,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, aphase = 0;
-            // per-k-step descriptor advance: K-major +32 B; MN-major +32 rows (4 KB)
-            const uint32_t a_step = a_mn ? 4096u : 32u, b_step = b_mn ? 4096u : 32u;
+            // Descriptors of stage 0 / k-step 0; every other (stage, k) differs only in
+            // the start-address field (bits 0..13, in 16-byte units), which never
+            // carries because shared memory addresses stay below 256 KB.
+            // K-major k-steps advance 32 bytes, MN-major k-steps 32 rows (4 KB).
+            const uint32_t base = smem_u32(smem);
+            const uint64_t a_desc0 = a_mn ? smem_desc(base, BK * 128, 1024, 2) : smem_desc(base, 16, 1024, 2);
+            const uint64_t b_desc0 =
+                b_mn ? smem_desc(base + A_BYTES, BK * 128, 1024, 2) : smem_desc(base + A_BYTES, 16, 1024, 2);
+            const uint64_t sf_desc0 = smem_desc(smem_u32(smem + SF_REGION), 0, 128, 0);
+            const uint32_t a_step16 = a_mn ? 4096u / 16 : 32u / 16, b_step16 = b_mn ? 4096u / 16 : 32u / 16;
+            uint32_t id[BK / UMMA_K];
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) id[k] = idesc(a_mn, b_mn, (uint32_t)k);
             for (int64_t i = 0;; ++i) {
                 const Tile T = S.get(S.pick(i, cta, ncta));
                 if (!T.valid) break;
@@ -344,20 +359,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int kb = 0; kb < T.nk; ++kb) {
                         if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) goto done_mma;
                         fence_after();
-                        const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
-                        const uint32_t sfs = smem_u32(smem + SF_REGION + stage * SF_STAGE_BYTES);
-                        tmem_cp_sf(tmem + TMEM_SFA, smem_desc(sfs, 0, 128, 0));
-                        tmem_cp_sf(tmem + TMEM_SFB, smem_desc(sfs + 512, 0, 128, 0));
-                        tmem_cp_sf(tmem + TMEM_SFB + 4, smem_desc(sfs + 1024, 0, 128, 0));
+                        const uint64_t sfd = sf_desc0 + (uint64_t)(stage * (SF_STAGE_BYTES / 16));
+                        tmem_cp_sf(tmem + TMEM_SFA, sfd);
+                        tmem_cp_sf(tmem + TMEM_SFB, sfd + 512 / 16);
+                        tmem_cp_sf(tmem + TMEM_SFB + 4, sfd + 1024 / 16);
+                        const uint64_t ad = a_desc0 + (uint64_t)(stage * (STAGE_BYTES / 16));
+                        const uint64_t bd = b_desc0 + (uint64_t)(stage * (STAGE_BYTES / 16));
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            const uint64_t ad = a_mn ? smem_desc(sb + k * a_step, BK * 128, 1024, 2)
-                                                     : smem_desc(sb + k * a_step, 16, 1024, 2);
-                            const uint64_t bd = b_mn ? smem_desc(sb + A_BYTES + k * b_step, BK * 128, 1024, 2)
-                                                     : smem_desc(sb + A_BYTES + k * b_step, 16, 1024, 2);
-                            mma_mxf8(tmem, ad, bd, idesc(a_mn, b_mn, (uint32_t)k), tmem + TMEM_SFA, tmem + TMEM_SFB,
-                                     (kb | k) != 0);
-                        }
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            mma_mxf8(tmem, ad + k * a_step16, bd + k * b_step16, id[k], tmem + TMEM_SFA,
+                                     tmem + TMEM_SFB, (kb | k) != 0);
                         mma_commit(empty0 + 8 * stage);
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
