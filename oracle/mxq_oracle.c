@@ -507,6 +507,77 @@ ORC_API void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* y, int64_t M, in
         }
 }
 
+/* ------------------------------------------- SwiGLU in kernel precision */
+
+/* The fused SwiGLU + quantize path rounds h (and dY1) to bf16 inside the
+ * kernel, in fp32; a quantized code can only be compared bit for bit if the
+ * oracle takes that rounding decision in the same precision. These
+ * functions define the fp32 computation step by step -- every operation is
+ * one IEEE fp32 rounding (this file is built with -ffp-contract=off) -- and
+ * the CUDA kernels implement the same steps independently.
+ *
+ * e^x: Cody & Waite argument reduction, x = n*ln2 + r with n = rint(x*log2 e)
+ * and ln2 split into 0.693359375 (exact) + -2.12194440e-4, then the degree-7
+ * Taylor polynomial of e^r (|r| <= ln2/2, truncation < 6e-9 relative) by
+ * Horner, scaled by 2^n. Outside [-87, 88] it returns 0 or +inf. */
+static float exp_f32(float x) {
+    if (x > 88.0f) return INFINITY;
+    if (x < -87.0f) return 0.0f;
+    const float t = x * 1.44269504f;
+    const float n = nearbyintf(t);
+    const float r1 = x - n * 0.693359375f;
+    const float r = r1 - n * -2.12194440e-4f;
+    float p = 1.0f / 5040.0f;
+    p = p * r + 1.0f / 720.0f;
+    p = p * r + 1.0f / 120.0f;
+    p = p * r + 1.0f / 24.0f;
+    p = p * r + 1.0f / 6.0f;
+    p = p * r + 0.5f;
+    p = p * r + 1.0f;
+    p = p * r + 1.0f;
+    return ldexpf(p, (int)n);
+}
+
+ORC_API float orc_exp_f32(float x) { return exp_f32(x); }
+
+static float sigmoid_f32(float g) { return 1.0f / (1.0f + exp_f32(-g)); }
+
+static uint16_t bf16_round_f32(float f) { return orc_bf16_round((double)f); }
+
+/* h = (g * sigmoid(g)) * u, fp32 steps as above, rounded once to bf16. */
+ORC_API void orc_swiglu_fwd_f32(const uint16_t* y, int64_t M, int64_t F, uint16_t* h) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t f = 0; f < F; ++f) {
+            const float g = (float)orc_bf16_value(y[m * 2 * F + f]);
+            const float u = (float)orc_bf16_value(y[m * 2 * F + F + f]);
+            const float sg = sigmoid_f32(g);
+            const float silu = g * sg;
+            h[m * F + f] = bf16_round_f32(silu * u);
+        }
+}
+
+/* dg = ((dh * u) * s) * (1 + g * (1 - s)), du = dh * (g * s), s = sigmoid(g);
+ * fp32 steps in that order, each result rounded once to bf16. */
+ORC_API void orc_swiglu_bwd_f32(const uint16_t* dh, const uint16_t* y, int64_t M, int64_t F, uint16_t* dy) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t f = 0; f < F; ++f) {
+            const float d = (float)orc_bf16_value(dh[m * F + f]);
+            const float g = (float)orc_bf16_value(y[m * 2 * F + f]);
+            const float u = (float)orc_bf16_value(y[m * 2 * F + F + f]);
+            const float sg = sigmoid_f32(g);
+            const float one_minus = 1.0f - sg;
+            const float gt = g * one_minus;
+            const float fac = 1.0f + gt;
+            const float a = d * u;
+            const float b = a * sg;
+            dy[m * 2 * F + f] = bf16_round_f32(b * fac);
+            const float silu = g * sg;
+            dy[m * 2 * F + F + f] = bf16_round_f32(d * silu);
+        }
+}
+
 ORC_API int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

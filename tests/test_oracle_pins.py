@@ -434,3 +434,34 @@ def test_swiglu_against_closed_forms(orc):
     for got, want in ((dg, dhf * u * dsilu), (du, dhf * g * expit(g))):
         ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 2.0 ** -120))) - 7)
         assert np.all(np.abs(got - want) <= ulp * 0.51 + 1e-8 * np.abs(dhf * u))
+
+
+# -------------------------------------------- SwiGLU in kernel precision
+def test_exp_f32_accuracy(orc):
+    xs = np.concatenate([np.linspace(-87, 88, 4001), np.linspace(-1, 1, 2001)])
+    got = np.array([orc.exp_f32(float(np.float32(x))) for x in xs], np.float64)
+    ref = np.exp(xs.astype(np.float32).astype(np.float64))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2 * ulp)
+    assert orc.exp_f32(0.0) == 1.0 and orc.exp_f32(89.0) == np.inf and orc.exp_f32(-88.0) == 0.0
+
+
+def test_swiglu_f32_against_fp64_definition(orc):
+    rng = np.random.default_rng(19)
+    M, F = 96, 128
+    y = bf16_bits_from_f32((4 * rng.standard_normal((M, 2 * F))).astype(np.float32))
+    dh = bf16_bits_from_f32(rng.standard_normal((M, F)).astype(np.float32))
+    # forward: at most one bf16 ulp from the fp64 definition
+    a = orc.swiglu_fwd_f32(y).astype(np.int32)
+    b = orc.swiglu_fwd(y).astype(np.int32)
+    assert np.all((np.abs(a - b) <= 1) | (((a & 0x7FFF) <= 1) & ((b & 0x7FFF) <= 1)))
+    assert np.mean(a == b) > 0.99
+    # backward: within one ulp, except where 1 + g(1 - s) cancels (fp32 error of that factor)
+    yf = f32_from_bf16_bits(y).astype(np.float64)
+    g = np.concatenate([yf[:, :F], yf[:, :F]], axis=1)
+    da = f32_from_bf16_bits(orc.swiglu_bwd_f32(dh, y)).astype(np.float64)
+    db = f32_from_bf16_bits(orc.swiglu_bwd(dh, y)).astype(np.float64)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(db), 2.0 ** -120))) - 7)
+    dhf = np.concatenate([f32_from_bf16_bits(dh)] * 2, axis=1).astype(np.float64)
+    slack = 2.0 ** -21 * np.abs(dhf) * (1 + np.abs(g)) * np.abs(yf).max()
+    assert np.all(np.abs(da - db) <= ulp + slack)
