@@ -185,9 +185,8 @@ class NativeStep:
 
 
 MLP_WORKLOAD = "e64_h3072_f1024_t84k_prequant"
-MLP_STAGES = ["requant_x", "quantize_w1_w2", "fc1_fprop", "swiglu_fwd", "quantize_h", "fc2_fprop",
-              "requant_dy2_dbias", "fc2_dgrad", "fc2_wgrad", "swiglu_bwd", "quantize_dy1_dbias", "fc1_dgrad",
-              "fc1_wgrad"]
+MLP_STAGES = ["requant_x", "quantize_w1_w2", "fc1_fprop", "swiglu_quantize_h", "fc2_fprop", "requant_dy2_dbias",
+              "fc2_dgrad", "fc2_wgrad", "swiglu_bwd_quantize_dy1_dbias", "fc1_dgrad", "fc1_wgrad"]
 
 
 class MLPStep:
@@ -232,13 +231,13 @@ class MLPStep:
         self.qh = q(M, F)
         self.qdy1 = q(M, 2 * F)
         self.qdy1["dbias"] = torch.empty((E, 2 * F), dtype=torch.float32, device=dev)
-        self.ws = u8(max(mxq.workspace_bytes(2, M, 0, H, E), mxq.workspace_bytes(1, M, 0, 2 * F, E)))
-        self.y1, self.h, self.y2 = bf(M, 2 * F), bf(M, F), bf(M, H)
-        self.dh, self.dy1, self.dx = bf(M, F), bf(M, 2 * F), bf(M, H)
+        self.ws = u8(max(mxq.workspace_bytes(2, M, 0, H, E), mxq.workspace_bytes(7, M, 0, F, E)))
+        self.y1, self.y2 = bf(M, 2 * F), bf(M, H)
+        self.dh, self.dx = bf(M, F), bf(M, H)
         self.dw1 = torch.empty((E, 2 * F, H), dtype=torch.float32, device=dev)
         self.dw2 = torch.empty((E, H, F), dtype=torch.float32, device=dev)
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        self.launches_per_step = 16
+        self.launches_per_step = 14
 
     def flops(self):
         return 6.0 * self.M * (2 * self.F * self.H + self.H * self.F)
@@ -255,31 +254,27 @@ class MLPStep:
         mxq.grouped_gemm_fprop(self.x_row, self.rqx["row_scale_swizzled"], self.qw1["row_data"].view(E, 2 * F, H),
                                self.qw1["row_scale"], self.ms, bias=self.b1, out=self.y1)
         rec(3)
-        mxq.swiglu_fwd(self.y1, out=self.h)
+        mxq.swiglu_quantize(self.y1, self.ms, out=self.qh)
         rec(4)
-        mxq.group_quantize(self.h, self.ms, out=self.qh)
-        rec(5)
         mxq.grouped_gemm_fprop(self.qh["row_data"], self.qh["row_scale"], self.qw2["row_data"].view(E, H, F),
                                self.qw2["row_scale"], self.ms, bias=self.b2, out=self.y2)
-        rec(6)
+        rec(5)
         mxq.requant_colwise(self.dy2_row, self.dy2_rs, self.ms, dbias=True, out=self.rqd, workspace=self.ws)
-        rec(7)
+        rec(6)
         mxq.grouped_gemm_dgrad(self.dy2_row, self.rqd["row_scale_swizzled"], self.qw2["col_data"].view(E, H, F),
                                self.qw2["col_scale"], self.ms, out=self.dh)
-        rec(8)
+        rec(7)
         mxq.grouped_gemm_wgrad(self.rqd["col_data"], self.rqd["col_scale"], self.qh["col_data"], self.qh["col_scale"],
                                self.ms, out=self.dw2)
+        rec(8)
+        mxq.swiglu_bwd_quantize(self.dh, self.y1, self.ms, dbias=True, out=self.qdy1, workspace=self.ws)
         rec(9)
-        mxq.swiglu_bwd(self.dh, self.y1, out=self.dy1)
-        rec(10)
-        mxq.group_quantize(self.dy1, self.ms, dbias=True, out=self.qdy1, workspace=self.ws)
-        rec(11)
         mxq.grouped_gemm_dgrad(self.qdy1["row_data"], self.qdy1["row_scale"], self.qw1["col_data"].view(E, 2 * F, H),
                                self.qw1["col_scale"], self.ms, out=self.dx)
-        rec(12)
+        rec(10)
         mxq.grouped_gemm_wgrad(self.qdy1["col_data"], self.qdy1["col_scale"], self.rqx["col_data"],
                                self.rqx["col_scale"], self.ms, out=self.dw1)
-        rec(13)
+        rec(11)
 
     def flush(self):
         self.flush_buf.fill_(1)
@@ -293,19 +288,21 @@ def time_mlp(dev, steps=10, warmup=3):
         st.flush()
         st.run()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(14)] for _ in range(steps)]
+    n = len(MLP_STAGES) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(steps)]
     for i in range(steps):
         st.flush()
         st.run(evs[i])
     torch.cuda.synchronize()
-    ms = statistics.mean(evs[i][0].elapsed_time(evs[i][13]) for i in range(steps))
+    ms = statistics.mean(evs[i][0].elapsed_time(evs[i][n - 1]) for i in range(steps))
     per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
            for j, k in enumerate(MLP_STAGES)}
     gemm_ms = sum(v for k, v in per.items() if "prop" in k or "grad" in k)
     return {"workload": MLP_WORKLOAD, "steps": steps, "warmup": warmup, "ms_per_step": ms,
             "tflops_step": st.flops() / (ms * 1e-3) / 1e12, "gemm_tflops": st.flops() / (gemm_ms * 1e-3) / 1e12,
             "stage_ms": per, "gpu_launches": st.launches_per_step * steps,
-            "step": "fwd+bwd of FC1 (bias) -> SwiGLU -> FC2 (bias), X and dY2 rowwise-prequantized"}
+            "step": "fwd+bwd of FC1 (bias) -> SwiGLU -> FC2 (bias), X and dY2 rowwise-prequantized; SwiGLU fused "
+                    "with the quantization of h (forward) and of dY1 with its dbias (backward)"}
 
 
 KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]

@@ -124,7 +124,8 @@ enum {
     MXQ_OP_GROUPED_DBIAS = 3,
     MXQ_OP_GEMM_FPROP = 4,
     MXQ_OP_GEMM_DGRAD = 5,
-    MXQ_OP_GEMM_WGRAD = 6
+    MXQ_OP_GEMM_WGRAD = 6,
+    MXQ_OP_SWIGLU_BWD_QUANTIZE = 7
 };
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -227,6 +228,32 @@ MXQ_API int mxq_grouped_dbias_noalloc(const void* dy_bf16, int64_t M, int64_t N,
 MXQ_API int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream);
 MXQ_API int mxq_swiglu_bwd(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F, void* dy_bf16,
                    mxq_stream_t stream);
+
+/* SwiGLU fused with group_quantize [FM][RQ][DI] (the fused grouped MLP's
+ * FC1 -> activation -> FC2, with the activation's output quantized where it
+ * is produced). y (M, 2F) bf16 is the FC1 output [gate | up]; h = silu(g)*u
+ * is computed in fp32 (fixed sequence of IEEE operations: the same steps as
+ * mxq_swiglu_fwd, so the results agree bit for bit), rounded to bf16 and
+ * quantized exactly as mxq_group_quantize would quantize that bf16 h.
+ * flags: MXQ_ROWWISE / MXQ_COLWISE / MXQ_SWIZZLE as for group_quantize;
+ * MXQ_DEQUANT_OUT also writes h in bf16 to h_bf16_out (M, F). Outputs are
+ * (M, F) tensors with their scale buffers. F % 128 == 0. */
+MXQ_API int mxq_swiglu_quantize(const void* y_bf16, int64_t M, int64_t F, int E, const int64_t* d_m_splits,
+                                int flags, void* row_data, void* row_scale, void* col_data, void* col_scale,
+                                void* h_bf16_out, const int32_t* d_noop, int32_t* d_status, mxq_stream_t stream);
+
+/* SwiGLU backward fused with group_quantize and dbias [FM][RQ]: from dh
+ * (M, F) and y (M, 2F), dY1 = [dg | du] (M, 2F) is computed in fp32 (the
+ * steps of mxq_swiglu_bwd), rounded to bf16 and quantized as
+ * mxq_group_quantize would quantize it; dbias_out (E, 2F) fp32 or NULL gets
+ * its per-expert column sums (needs ws of mxq_workspace_bytes(
+ * MXQ_OP_SWIGLU_BWD_QUANTIZE, M, 0, F, E, 0) bytes); MXQ_DEQUANT_OUT also
+ * writes dY1 in bf16 to dy_bf16_out. F % 128 == 0. */
+MXQ_API int mxq_swiglu_bwd_quantize(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F, int E,
+                                    const int64_t* d_m_splits, int flags, void* row_data, void* row_scale,
+                                    void* col_data, void* col_scale, float* dbias_out, void* dy_bf16_out,
+                                    const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes,
+                                    mxq_stream_t stream);
 
 /* Copy the device status word to *h_out after `stream` drains (the only
  * synchronizing call). */

@@ -17,7 +17,9 @@ from .mxq import (  # noqa: F401
     scale_bytes,
     status_read,
     swiglu_bwd,
+    swiglu_bwd_quantize,
     swiglu_fwd,
+    swiglu_quantize,
     workspace_bytes,
 )
 

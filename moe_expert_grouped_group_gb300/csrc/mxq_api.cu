@@ -78,6 +78,7 @@ size_t mxq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int f
         case MXQ_OP_GROUP_QUANTIZE:
         case MXQ_OP_REQUANT_COLWISE: return (size_t)(M / 128) * (size_t)K * sizeof(float);
         case MXQ_OP_GROUPED_DBIAS: return (size_t)(M / 128) * (size_t)N * sizeof(float);
+        case MXQ_OP_SWIGLU_BWD_QUANTIZE: return (size_t)(M / 128) * (size_t)(2 * K) * sizeof(float);
         default: return 0;
     }
 }
@@ -248,6 +249,61 @@ int mxq_swiglu_bwd(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F
     if (!aligned16(dh_bf16) || !aligned16(y_bf16) || !aligned16(dy_bf16)) return MXQ_ERR_ALIGN;
     cudaError_t e = mxq::run_swiglu_bwd(dh_bf16, y_bf16, M, F, dy_bf16, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+static int swiglu_quantize_common(int backward, const void* dh, const void* y, int64_t M, int64_t F, int E,
+                                  const int64_t* m_splits, int flags, void* row_data, void* row_scale,
+                                  void* col_data, void* col_scale, float* dbias_out, void* bf16_out,
+                                  const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes,
+                                  mxq_stream_t stream) {
+    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE | MXQ_DEQUANT_OUT)) return MXQ_ERR_FLAGS;
+    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE, deq = flags & MXQ_DEQUANT_OUT;
+    if (!row && !col && !deq && !dbias_out) return MXQ_ERR_FLAGS;
+    if (M != 0 && (!y || (backward && !dh) || (row && (!row_data || !row_scale)) ||
+                   (col && (!col_data || !col_scale)) || (deq && !bf16_out)))
+        return MXQ_ERR_NULL;
+    if (int r = check_common(M, F, E, m_splits, true)) return r;
+    if (!aligned16(y) || !aligned16(dh) || !aligned16(row_data) || !aligned16(row_scale) || !aligned16(col_data) ||
+        !aligned16(col_scale) || !aligned16(dbias_out) || !aligned16(bf16_out) || !aligned16(ws))
+        return MXQ_ERR_ALIGN;
+    if (dbias_out && M != 0 &&
+        (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_SWIGLU_BWD_QUANTIZE, M, 0, backward ? F : F / 2, E, 0)))
+        return MXQ_ERR_WORKSPACE;
+    mxq::SwigluQuantCall c{};
+    c.backward = backward;
+    c.y = y;
+    c.dh = dh;
+    c.M = M;
+    c.F = F;
+    c.E = E;
+    c.m_splits = m_splits;
+    c.row_q = row ? row_data : nullptr;
+    c.row_s = row ? row_scale : nullptr;
+    c.col_q = col ? col_data : nullptr;
+    c.col_s = col ? col_scale : nullptr;
+    c.dbias = dbias_out;
+    c.partials = dbias_out ? static_cast<float*>(ws) : nullptr;
+    c.bf16_out = deq ? bf16_out : nullptr;
+    c.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    c.noop = d_noop;
+    c.status = d_status;
+    cudaError_t e = mxq::run_swiglu_quantize(c, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_swiglu_quantize(const void* y_bf16, int64_t M, int64_t F, int E, const int64_t* d_m_splits, int flags,
+                        void* row_data, void* row_scale, void* col_data, void* col_scale, void* h_bf16_out,
+                        const int32_t* d_noop, int32_t* d_status, mxq_stream_t stream) {
+    return swiglu_quantize_common(0, nullptr, y_bf16, M, F, E, d_m_splits, flags, row_data, row_scale, col_data,
+                                  col_scale, nullptr, h_bf16_out, d_noop, d_status, nullptr, 0, stream);
+}
+
+int mxq_swiglu_bwd_quantize(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F, int E,
+                            const int64_t* d_m_splits, int flags, void* row_data, void* row_scale, void* col_data,
+                            void* col_scale, float* dbias_out, void* dy_bf16_out, const int32_t* d_noop,
+                            int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
+    return swiglu_quantize_common(1, dh_bf16, y_bf16, M, F, E, d_m_splits, flags, row_data, row_scale, col_data,
+                                  col_scale, dbias_out, dy_bf16_out, d_noop, d_status, ws, ws_bytes, stream);
 }
 
 int mxq_status_read(const int32_t* d_status, int32_t* h_out, mxq_stream_t stream) {

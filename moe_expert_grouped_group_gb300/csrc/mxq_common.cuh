@@ -116,6 +116,47 @@ __device__ __forceinline__ void report_status(int32_t* d_status, int bits) {
     if (d_status && bits && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(d_status, bits);
 }
 
+// ------------------------------------------------ SwiGLU in fp32 steps
+// SwiGLU between FC1 and FC2 of a fused grouped MoE MLP (TransformerEngine
+// PR #3545, "Fix distributed BF16 weights and trim NVFP4 saved state in the
+// fused grouped MLP": FC1 -> activation -> FC2; gate = first half of FC1's
+// output). Every step is one IEEE fp32 operation (__f*_rn: never contracted
+// into an FMA) so that the bf16 rounding of h, and the E4M3 codes chosen
+// from it, are reproducible exactly. e^x: Cody & Waite argument reduction
+// x = n*ln2 + r (n = rint(x*log2 e), ln2 = 0.693359375 + -2.12194440e-4),
+// the degree-7 Taylor polynomial of e^r by Horner, times 2^n; 0 below -87,
+// +inf above 88.
+__device__ __forceinline__ float exp_f32_steps(float x) {
+    if (x > 88.0f) return __int_as_float(0x7f800000);
+    if (x < -87.0f) return 0.0f;
+    const float n = rintf(__fmul_rn(x, 1.44269504f));
+    const float r1 = __fsub_rn(x, __fmul_rn(n, 0.693359375f));
+    const float r = __fsub_rn(r1, __fmul_rn(n, -2.12194440e-4f));
+    float p = __fdiv_rn(1.0f, 5040.0f);
+    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 720.0f));
+    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 120.0f));
+    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 24.0f));
+    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 6.0f));
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));  // n in [-126, 127]
+}
+__device__ __forceinline__ float sigmoid_f32_steps(float g) {
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_f32_steps(-g)));
+}
+// h = (g * s) * u
+__device__ __forceinline__ float swiglu_h(float g, float u) {
+    return __fmul_rn(__fmul_rn(g, sigmoid_f32_steps(g)), u);
+}
+// dg = ((dh * u) * s) * (1 + g * (1 - s)), du = dh * (g * s)
+__device__ __forceinline__ void swiglu_grads(float d, float g, float u, float& dg, float& du) {
+    const float s = sigmoid_f32_steps(g);
+    const float fac = __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s)));
+    dg = __fmul_rn(__fmul_rn(__fmul_rn(d, u), s), fac);
+    du = __fmul_rn(d, __fmul_rn(g, s));
+}
+
 // ------------------------------------------ mbarrier and TMA wrappers (PTX)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bound on any on-chip wait
 

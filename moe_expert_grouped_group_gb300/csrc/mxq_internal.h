@@ -36,6 +36,24 @@ struct RequantCall {
     int32_t* status;
 };
 
+// SwiGLU fused with group quantization: forward quantizes h (M, F); backward
+// quantizes dY1 = [dg | du] (M, 2F) and reduces its dbias.
+struct SwigluQuantCall {
+    int backward;
+    const void* y;   // FC1 output (M, 2F) bf16, [gate | up]
+    const void* dh;  // backward: gradient of h (M, F) bf16
+    int64_t M, F;
+    int E;
+    const int64_t* m_splits;
+    void *row_q, *row_s, *col_q, *col_s;
+    float* dbias;
+    float* partials;  // workspace, (M/128) * Kout fp32, when dbias != nullptr
+    void* bf16_out;   // optional h or dY1 in bf16
+    int swizzle;
+    const int32_t* noop;
+    int32_t* status;
+};
+
 enum GemmMode { kFprop = 0, kDgrad = 1, kWgrad = 2 };
 
 struct GemmCall {
@@ -61,6 +79,9 @@ cudaError_t run_requant(const RequantCall& c, cudaStream_t s);
 cudaError_t run_grouped_dbias(const void* dy, int64_t M, int64_t N, int E, const int64_t* m_splits, float* out,
                               float* partials, int32_t* status, cudaStream_t s);
 cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s);
+cudaError_t run_swiglu_quantize(const SwigluQuantCall& c, cudaStream_t s);
+cudaError_t run_dbias_finalize(const float* partials, int64_t M, int64_t K, int E, const int64_t* m_splits,
+                               float* out, const int32_t* noop, cudaStream_t s);
 cudaError_t run_swiglu_fwd(const void* y, int64_t M, int64_t F, void* h, cudaStream_t s);
 cudaError_t run_swiglu_bwd(const void* dh, const void* y, int64_t M, int64_t F, void* dy, cudaStream_t s);
 

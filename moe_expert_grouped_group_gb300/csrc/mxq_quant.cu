@@ -393,6 +393,11 @@ static cudaError_t launch_finalize(const float* partials, int64_t M, int64_t K, 
     return cudaGetLastError();
 }
 
+cudaError_t run_dbias_finalize(const float* partials, int64_t M, int64_t K, int E, const int64_t* m_splits,
+                               float* out, const int32_t* noop, cudaStream_t s) {
+    return launch_finalize(partials, M, K, E, m_splits, out, noop, s);
+}
+
 cudaError_t run_group_quantize(const QuantCall& c, cudaStream_t s) {
     TileArgs a{};
     a.src = c.x;

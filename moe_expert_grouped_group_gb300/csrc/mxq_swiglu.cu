@@ -3,16 +3,16 @@
 // saved state in the fused grouped MLP": FC1 -> activation -> FC2). The FC1
 // output row is [gate | up] (gate first); h = silu(gate) * up.
 // Elementwise and HBM-bound: each thread moves 8 bf16 of gate and of up with
-// 16-byte loads; fp32 math (IEEE expf and division), bf16 RNE outputs.
+// 16-byte loads; fp32 math in the explicit steps of mxq_common.cuh (the same
+// steps the fused SwiGLU + quantize kernels use), bf16 RNE outputs.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 
+#include "mxq_common.cuh"
 #include "mxq_internal.h"
 
 namespace mxq {
-
-__device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf(-g)); }
 
 __device__ __forceinline__ void unpack8(uint4 w, float* f) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const uint16_t* __restr
         unpack8(__ldg(reinterpret_cast<const uint4*>(y + m * 2 * F + f)), g);
         unpack8(__ldg(reinterpret_cast<const uint4*>(y + m * 2 * F + F + f)), u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = g[j] * sigmoidf_(g[j]) * u[j];
+        for (int j = 0; j < 8; ++j) o[j] = swiglu_h(g[j], u[j]);
         *reinterpret_cast<uint4*>(h + m * F + f) = pack8(o);
     }
 }
@@ -57,11 +57,7 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t* __restr
         unpack8(__ldg(reinterpret_cast<const uint4*>(y + m * 2 * F + f)), g);
         unpack8(__ldg(reinterpret_cast<const uint4*>(y + m * 2 * F + F + f)), u);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float s = sigmoidf_(g[j]);
-            dg[j] = d[j] * u[j] * s * (1.0f + g[j] * (1.0f - s));
-            du[j] = d[j] * g[j] * s;
-        }
+        for (int j = 0; j < 8; ++j) swiglu_grads(d[j], g[j], u[j], dg[j], du[j]);
         *reinterpret_cast<uint4*>(dy + m * 2 * F + f) = pack8(dg);
         *reinterpret_cast<uint4*>(dy + m * 2 * F + F + f) = pack8(du);
     }

@@ -1,0 +1,367 @@
+// mxq_swiglu_quant.cu -- SwiGLU fused with MXFP8 group quantization, for the
+// grouped MoE MLP FC1 -> SwiGLU -> FC2 (TransformerEngine PR #3545, "Fix
+// distributed BF16 weights and trim NVFP4 saved state in the fused grouped
+// MLP"; quantization as in PR #3244 / PR #3224, see mxq_quant.cu).
+//
+//   forward : y = FC1 output (M, 2F) bf16 = [gate | up] -> h = silu(g) * u,
+//             rounded to bf16, quantized rowwise (FC2 fprop) and colwise
+//             (FC2 wgrad). h itself is written only if asked for.
+//   backward: dh (M, F), y (M, 2F) -> dY1 = [dg | du] (M, 2F), rounded to
+//             bf16, quantized rowwise (FC1 dgrad) and colwise (FC1 wgrad),
+//             with the per-expert FC1 dbias reduced from the same bf16 values.
+//
+// Same structure as the standalone quantizer: persistent CTAs of 4 compute
+// warps + 1 TMA producer warp, 128x128 output tiles. A stage holds the 128x128
+// input tiles a tile needs (g and u; plus dh backward). Each compute warp
+// first turns its own 32 rows into bf16 h (or dg and du) in place in shared
+// memory -- fp32 steps of mxq_common.cuh, one bf16 rounding -- then runs the
+// two quantization passes over that bf16 tile exactly as the standalone
+// kernel would over the tensor read from memory, so the codes equal
+// "SwiGLU, then group_quantize" bit for bit while h (or dY1) never makes a
+// round trip through HBM.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "mxq_common.cuh"
+#include "mxq_internal.h"
+
+namespace mxq {
+namespace swq {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kTileBytes = kTile * kTile * 2;  // one 128x128 bf16 tile
+
+struct Args {
+    int64_t M, F, E;
+    const int64_t* m_splits;
+    uint8_t *row_q, *row_s, *col_q, *col_s;  // quantized output (M, Kout)
+    float* partials;                          // dbias partials (M/128, Kout)
+    __nv_bfloat16* bf16_out;                  // optional h / dY1 (M, Kout)
+    int swizzle;
+    const int32_t* noop;
+    int32_t* status;
+};
+
+__device__ __forceinline__ void bar_compute() {
+    asm volatile("bar.sync 2, %0;" ::"n"(kWarps * 32) : "memory");
+}
+__device__ __forceinline__ bool bar_compute_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 2, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "n"(kWarps * 32)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ uint32_t group8_max_u8x4(uint32_t v) {
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) v = __vmaxu4(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Quantize one 128x128 bf16 tile held in shared memory (row r at tile + r*256)
+// into output column tile `kt` of an (M, Kout) tensor; warp `rg` owns rows
+// 32rg..32rg+31, lane l columns 4l..4l+3. Same passes as mx_tile_kernel's
+// bf16 path: colwise exponent max + dbias sums, then rowwise exponent max
+// over 8 lanes and the E4M3 encode; scale atoms staged in shared memory.
+template <bool kRow, bool kCol, bool kBias, bool kDeq>
+__device__ __forceinline__ void quantize_tile(const uint8_t* tile, const Args& a, int64_t mt, int64_t kt, int64_t Kout,
+                                              const int64_t* s_off, uint8_t* s_rs, uint8_t* s_cs,
+                                              float (*s_red)[kTile], int rg, int lane) {
+    const int blk = lane >> 3;
+    const int64_t tilesK = Kout / kTile;
+    const int64_t r0 = mt * kTile + rg * 32;
+    const int64_t col = kt * kTile + lane * 4;
+    const uint32_t Ku = (uint32_t)Kout;
+    const uint8_t* src = tile + (rg * 32) * (kTile * 2) + lane * 8;
+    auto ld_row = [&](int r) -> uint2 { return *reinterpret_cast<const uint2*>(src + r * (kTile * 2)); };
+
+    uint32_t ccode[4] = {0, 0, 0, 0};
+    float cinv[4] = {1.f, 1.f, 1.f, 1.f};
+    if constexpr (kCol || kBias) {
+        uint32_t m0 = 0, m1 = 0;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r) {
+            const uint2 u = ld_row(r);
+            m0 = __vmaxu2(m0, u.x & 0x7FFF7FFFu);
+            m1 = __vmaxu2(m1, u.y & 0x7FFF7FFFu);
+            if constexpr (kBias) {
+                sum[0] += bf16lo(u.x);
+                sum[1] += bf16hi(u.x);
+                sum[2] += bf16lo(u.y);
+                sum[3] += bf16hi(u.y);
+            }
+        }
+        if constexpr (kCol) {
+            const uint32_t e[4] = {(m0 >> 7) & 0xFFu, (m0 >> 23) & 0xFFu, (m1 >> 7) & 0xFFu, (m1 >> 23) & 0xFFu};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                ccode[j] = (uint32_t)max((int)e[j] - 8, 0);
+                cinv[j] = inv_scale_from_code(ccode[j]);
+            }
+            if (a.swizzle) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) s_cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
+            } else {
+                *reinterpret_cast<uint32_t*>(a.col_s + (mt * 4 + rg) * Kout + col) =
+                    ccode[0] | (ccode[1] << 8) | (ccode[2] << 16) | (ccode[3] << 24);
+            }
+        }
+        if constexpr (kBias) *reinterpret_cast<float4*>(&s_red[rg][lane * 4]) = make_float4(sum[0], sum[1], sum[2], sum[3]);
+    }
+
+    if constexpr (kRow || kCol || kDeq) {
+        uint8_t* rq = kRow ? a.row_q + r0 * Kout + col : nullptr;
+        uint8_t* cq = kCol ? a.col_q + r0 * Kout + col : nullptr;
+        __nv_bfloat16* dq = kDeq ? a.bf16_out + r0 * Kout + col : nullptr;
+#pragma unroll 2
+        for (int r4 = 0; r4 < 32; r4 += 4) {
+            uint2 u[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) u[k] = ld_row(r4 + k);
+            uint32_t packed = 0;
+            if constexpr (kRow) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t w2 = __vmaxu2(u[k].x & 0x7FFF7FFFu, u[k].y & 0x7FFF7FFFu);
+                    packed |= (max(w2 & 0xFFFFu, w2 >> 16) >> 7) << (8 * k);
+                }
+                packed = group8_max_u8x4(packed);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int r = r4 + k;
+                const float v[4] = {bf16lo(u[k].x), bf16hi(u[k].x), bf16lo(u[k].y), bf16hi(u[k].y)};
+                if constexpr (kRow) {
+                    const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
+                    const float inv = inv_scale_from_code(code);
+                    *reinterpret_cast<uint32_t*>(rq + r * Ku) =
+                        cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+                    if ((lane & 7) == 0) {
+                        if (a.swizzle) s_rs[r * 16 + rg * 4 + blk] = (uint8_t)code;
+                        else a.row_s[(r0 + r) * (Kout / 32) + kt * 4 + blk] = (uint8_t)code;
+                    }
+                }
+                if constexpr (kCol) {
+                    *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) |
+                                                                (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
+                }
+                if constexpr (kDeq) *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = u[k];
+            }
+        }
+    }
+
+    bar_compute();
+    if constexpr (kBias) {
+        const int c = threadIdx.x;  // 0..127
+        a.partials[mt * Kout + kt * kTile + c] = ((s_red[0][c] + s_red[1][c]) + s_red[2][c]) + s_red[3][c];
+    }
+    if constexpr (kRow) {
+        if (a.swizzle && threadIdx.x < 32) {
+            uint4* dst = reinterpret_cast<uint4*>(a.row_s + (mt * tilesK + kt) * 512);
+            dst[threadIdx.x] = reinterpret_cast<const uint4*>(s_rs)[threadIdx.x];
+        }
+    }
+    if constexpr (kCol) {
+        if (a.swizzle && threadIdx.x >= 32 && threadIdx.x < 64) {
+            const int64_t rt0 = mt * kTile;
+            const int e = expert_of(s_off, (int)a.E, rt0);
+            const int64_t off = s_off[e], me = s_off[e + 1] - off;
+            const int64_t atom = kt * (me / kTile) + (rt0 - off) / kTile;
+            uint4* dst = reinterpret_cast<uint4*>(a.col_s + Kout * off / 32 + atom * 512);
+            dst[threadIdx.x - 32] = reinterpret_cast<const uint4*>(s_cs)[threadIdx.x - 32];
+        }
+    }
+    bar_compute();
+}
+
+template <bool kBwd, bool kRow, bool kCol, bool kBias, bool kDeq>
+__global__ void __launch_bounds__(kThreads)
+    swiglu_quant_kernel(const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_dh, Args a) {
+    constexpr int kIn = kBwd ? 3 : 2;  // stage: [g][u] or [g][u][dh]
+    constexpr uint32_t kStageTx = kIn * kTileBytes;
+    extern __shared__ uint8_t sq_raw[];
+    __shared__ __align__(16) uint8_t s_rs[512];
+    __shared__ __align__(16) uint8_t s_cs[512];
+    __shared__ __align__(16) float s_red[4][kTile];
+    __shared__ int s_abort;
+
+    uint8_t* stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sq_raw) + 127) & ~uintptr_t(127));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kIn * kTileBytes);
+    int64_t* s_off = reinterpret_cast<int64_t*>(bars + 2);
+
+    if (a.noop && *a.noop) return;
+    const int bad = load_offsets(a.m_splits, (int)a.E, a.M, s_off);
+    if (bad) {
+        report_status(a.status, bad);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tilesF = a.F / kTile;
+    const int64_t tiles = (a.M / kTile) * tilesF;
+    const uint32_t full = smem_u32(bars), empty = smem_u32(bars + 1);
+    volatile int* abort_flag = &s_abort;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(full, 1);
+        mbar_init(empty, kWarps);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            uint32_t phase = 0;
+            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+                if (!mbar_wait(empty, phase ^ 1, abort_flag)) break;
+                const int x = (int)((t % tilesF) * kTile), y = (int)((t / tilesF) * kTile);
+                mbar_expect_tx(full, kStageTx);
+                tma_load_2d(smem_u32(stage), &tm_y, full, x, y);                              // gate
+                tma_load_2d(smem_u32(stage + kTileBytes), &tm_y, full, x + (int)a.F, y);    // up
+                if constexpr (kBwd) tma_load_2d(smem_u32(stage + 2 * kTileBytes), &tm_dh, full, x, y);
+                phase ^= 1;
+            }
+        }
+        return;
+    }
+
+    const int rg = warp;
+    uint32_t phase = 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const int64_t mt = t / tilesF, ft = t % tilesF;
+        const bool ok = mbar_wait(full, phase, abort_flag);
+        if (bar_compute_any(!ok)) break;
+        phase ^= 1;
+
+        // SwiGLU on this warp's 32 rows, written back as bf16 in place
+        uint8_t* g_row = stage + (rg * 32) * (kTile * 2) + lane * 8;
+        uint8_t* u_row = g_row + kTileBytes;
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+            uint2* gp = reinterpret_cast<uint2*>(g_row + r * (kTile * 2));
+            uint2* up = reinterpret_cast<uint2*>(u_row + r * (kTile * 2));
+            const uint2 gw = *gp, uw = *up;
+            const float g[4] = {bf16lo(gw.x), bf16hi(gw.x), bf16lo(gw.y), bf16hi(gw.y)};
+            const float u[4] = {bf16lo(uw.x), bf16hi(uw.x), bf16lo(uw.y), bf16hi(uw.y)};
+            if constexpr (!kBwd) {
+                float h[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) h[j] = swiglu_h(g[j], u[j]);
+                *gp = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+            } else {
+                const uint2 dw = *reinterpret_cast<const uint2*>(g_row + 2 * kTileBytes + r * (kTile * 2));
+                const float d[4] = {bf16lo(dw.x), bf16hi(dw.x), bf16lo(dw.y), bf16hi(dw.y)};
+                float dg[4], du[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) swiglu_grads(d[j], g[j], u[j], dg[j], du[j]);
+                *gp = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
+                *up = make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
+            }
+        }
+        __syncwarp();
+
+        if constexpr (!kBwd) {
+            quantize_tile<kRow, kCol, kBias, kDeq>(stage, a, mt, ft, a.F, s_off, s_rs, s_cs, s_red, rg, lane);
+        } else {
+            quantize_tile<kRow, kCol, kBias, kDeq>(stage, a, mt, ft, 2 * a.F, s_off, s_rs, s_cs, s_red, rg, lane);
+            quantize_tile<kRow, kCol, kBias, kDeq>(stage + kTileBytes, a, mt, tilesF + ft, 2 * a.F, s_off, s_rs,
+                                                   s_cs, s_red, rg, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty);  // this warp is done with the stage
+    }
+    if (threadIdx.x == 0 && s_abort && a.status) atomicOr(a.status, MXQ_STATUS_WAIT_TIMEOUT);
+}
+
+static int num_sms() {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return v;
+}
+
+template <bool kBwd, bool kRow, bool kCol, bool kBias, bool kDeq>
+static cudaError_t launch(const Args& a, const void* y, const void* dh, cudaStream_t s) {
+    const int64_t tiles = (a.M / kTile) * (a.F / kTile);
+    if (tiles == 0) return cudaSuccess;
+    constexpr int kIn = kBwd ? 3 : 2;
+    const int smem = 128 + kIn * kTileBytes + 16 + (int)(a.E + 1) * 8;
+    auto kern = swiglu_quant_kernel<kBwd, kRow, kCol, kBias, kDeq>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    CUtensorMap ty, td;
+    if (!encode_tmap_2d(&ty, y, a.M, 2 * a.F, 2, kTile, kTile, false)) return cudaErrorInvalidValue;
+    if (kBwd) {
+        if (!encode_tmap_2d(&td, dh, a.M, a.F, 2, kTile, kTile, false)) return cudaErrorInvalidValue;
+    } else {
+        td = ty;  // unused
+    }
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms() * std::max(per_sm, 1));
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(ty, td, a);
+    return cudaGetLastError();
+}
+
+template <bool kBwd>
+static cudaError_t dispatch(const Args& a, bool row, bool col, bool bias, bool deq, const void* y, const void* dh,
+                            cudaStream_t s) {
+#define MXQ_SWQ(R, C, B, D) \
+    if (row == R && col == C && bias == B && deq == D) return launch<kBwd, R, C, B, D>(a, y, dh, s);
+    MXQ_SWQ(true, true, false, false)
+    MXQ_SWQ(true, true, true, false)
+    MXQ_SWQ(true, true, false, true)
+    MXQ_SWQ(true, true, true, true)
+    MXQ_SWQ(true, false, false, false)
+    MXQ_SWQ(true, false, true, false)
+    MXQ_SWQ(true, false, false, true)
+    MXQ_SWQ(true, false, true, true)
+    MXQ_SWQ(false, true, false, false)
+    MXQ_SWQ(false, true, true, false)
+    MXQ_SWQ(false, true, false, true)
+    MXQ_SWQ(false, true, true, true)
+    MXQ_SWQ(false, false, true, false)
+    MXQ_SWQ(false, false, false, true)
+    MXQ_SWQ(false, false, true, true)
+#undef MXQ_SWQ
+    return cudaSuccess;  // nothing requested
+}
+
+}  // namespace swq
+
+cudaError_t run_swiglu_quantize(const SwigluQuantCall& c, cudaStream_t s) {
+    swq::Args a{};
+    a.M = c.M;
+    a.F = c.F;
+    a.E = c.E;
+    a.m_splits = c.m_splits;
+    a.row_q = (uint8_t*)c.row_q;
+    a.row_s = (uint8_t*)c.row_s;
+    a.col_q = (uint8_t*)c.col_q;
+    a.col_s = (uint8_t*)c.col_s;
+    a.partials = c.partials;
+    a.bf16_out = (__nv_bfloat16*)c.bf16_out;
+    a.swizzle = c.swizzle;
+    a.noop = c.noop;
+    a.status = c.status;
+    const bool row = c.row_q != nullptr, col = c.col_q != nullptr, bias = c.partials != nullptr,
+               deq = c.bf16_out != nullptr;
+    cudaError_t e = c.backward ? swq::dispatch<true>(a, row, col, bias, deq, c.y, c.dh, s)
+                               : swq::dispatch<false>(a, row, col, bias, deq, c.y, nullptr, s);
+    if (e != cudaSuccess || !bias) return e;
+    return run_dbias_finalize(c.partials, c.M, c.backward ? 2 * c.F : c.F, c.E, c.m_splits, c.dbias, c.noop, s);
+}
+
+}  // namespace mxq

@@ -19,14 +19,14 @@ from .build import LIB
 
 ROWWISE, COLWISE, SWIZZLE, DEQUANT_OUT, ACCUMULATE, OUT_BF16 = 1, 2, 4, 8, 16, 32
 OP_GROUP_QUANTIZE, OP_REQUANT_COLWISE, OP_GROUPED_DBIAS = 1, 2, 3
-OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD = 4, 5, 6
+OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD, OP_SWIGLU_BWD_QUANTIZE = 4, 5, 6, 7
 STATUS_SPLIT_UNALIGNED, STATUS_SPLIT_NEGATIVE, STATUS_SPLIT_SUM, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
 
 SYMBOLS = [
     "mxq_version", "mxq_scale_bytes", "mxq_workspace_bytes", "mxq_group_quantize", "mxq_requant_colwise",
     "mxq_grouped_dbias", "mxq_grouped_gemm_fprop", "mxq_grouped_gemm_dgrad", "mxq_grouped_gemm_wgrad",
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
-    "mxq_grouped_dbias_noalloc",
+    "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize",
 ]
 
 
@@ -57,6 +57,9 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_grouped_dbias_noalloc.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P]
     L.mxq_grouped_dbias_noalloc.restype = _INT
     L.mxq_swiglu_fwd.argtypes = [_P, _I64, _I64, _P, _P]
+    L.mxq_swiglu_quantize.argtypes = [_P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P]
+    L.mxq_swiglu_bwd_quantize.argtypes = [_P, _P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          _SZ, _P]
     L.mxq_swiglu_bwd.argtypes = [_P, _P, _I64, _I64, _P, _P]
     L.mxq_status_read.argtypes = [_P, _P, _P]
     L.mxq_error_string.argtypes = [_INT]
@@ -253,3 +256,61 @@ def swiglu_bwd(dh, y, out=None):
     out = out if out is not None else torch.empty((M, F2), dtype=torch.bfloat16, device=y.device)
     _check(lib().mxq_swiglu_bwd(_ptr(dh), _ptr(y), M, F2 // 2, _ptr(out), _stream()), "mxq_swiglu_bwd")
     return out
+
+
+def _quant_outputs(o, M, K, rowwise, colwise, dev):
+    if rowwise:
+        o.setdefault("row_data", _u8((M, K), dev))
+        o.setdefault("row_scale", _u8(scale_bytes(M, K, False), dev))
+    if colwise:
+        o.setdefault("col_data", _u8((M, K), dev))
+        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+    return o
+
+
+def swiglu_quantize(y, m_splits, rowwise=True, colwise=True, swizzle=True, h_out=False, noop=None, status=None,
+                    out=None):
+    """SwiGLU forward fused with group_quantize: y (M, 2F) bf16 -> quantized h (M, F)
+    (dict row_data/row_scale/col_data/col_scale, plus "h" in bf16 if h_out)."""
+    M, F2 = y.shape
+    F = F2 // 2
+    m_splits = _splits(m_splits)
+    E = m_splits.numel()
+    dev = y.device
+    o = _quant_outputs(dict(out or {}), M, F, rowwise, colwise, dev)
+    if h_out:
+        o.setdefault("h", torch.empty((M, F), dtype=torch.bfloat16, device=dev))
+    flags = ((ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
+             | (DEQUANT_OUT if h_out else 0))
+    rc = lib().mxq_swiglu_quantize(_ptr(y), M, F, E, _ptr(m_splits), flags, _ptr(o.get("row_data")),
+                                   _ptr(o.get("row_scale")), _ptr(o.get("col_data")), _ptr(o.get("col_scale")),
+                                   _ptr(o.get("h")), _ptr(noop), _ptr(status), _stream())
+    _check(rc, "mxq_swiglu_quantize")
+    return o
+
+
+def swiglu_bwd_quantize(dh, y, m_splits, rowwise=True, colwise=True, swizzle=True, dbias=False, dy_out=False,
+                        noop=None, status=None, out=None, workspace=None):
+    """SwiGLU backward fused with group_quantize (+dbias): dh (M, F), y (M, 2F) ->
+    quantized dY1 (M, 2F), optional "dbias" (E, 2F) fp32 and "dy" in bf16."""
+    M, F2 = y.shape
+    F = F2 // 2
+    m_splits = _splits(m_splits)
+    E = m_splits.numel()
+    dev = y.device
+    o = _quant_outputs(dict(out or {}), M, F2, rowwise, colwise, dev)
+    if dy_out:
+        o.setdefault("dy", torch.empty((M, F2), dtype=torch.bfloat16, device=dev))
+    ws = None
+    if dbias:
+        o.setdefault("dbias", torch.empty((E, F2), dtype=torch.float32, device=dev))
+        ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SWIGLU_BWD_QUANTIZE, M, 0, F, E)),
+                                                         dev)
+    flags = ((ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
+             | (DEQUANT_OUT if dy_out else 0))
+    rc = lib().mxq_swiglu_bwd_quantize(_ptr(dh), _ptr(y), M, F, E, _ptr(m_splits), flags, _ptr(o.get("row_data")),
+                                       _ptr(o.get("row_scale")), _ptr(o.get("col_data")), _ptr(o.get("col_scale")),
+                                       _ptr(o.get("dbias")), _ptr(o.get("dy")), _ptr(noop), _ptr(status), _ptr(ws),
+                                       0 if ws is None else ws.numel() * ws.element_size(), _stream())
+    _check(rc, "mxq_swiglu_bwd_quantize")
+    return o
