@@ -28,7 +28,8 @@ def lib():
     global _lib
     if _lib is None:
         path = library_path()
-        if not os.path.exists(path):
+        src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "mxq_oracle.c")
+        if not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(src):
             build_oracle()
         _lib = ctypes.CDLL(path)
         _declare(_lib)

@@ -514,27 +514,29 @@ ORC_API void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* y, int64_t M, in
  * oracle takes that rounding decision in the same precision. These
  * functions define the fp32 computation step by step -- every operation is
  * one IEEE fp32 rounding (this file is built with -ffp-contract=off) -- and
- * the CUDA kernels implement the same steps independently.
+ * the CUDA kernels implement the same steps independently. fmaf is the
+ * IEEE fused multiply-add: one rounding of a*b+c.
  *
  * e^x: Cody & Waite argument reduction, x = n*ln2 + r with n = rint(x*log2 e)
- * and ln2 split into 0.693359375 (exact) + -2.12194440e-4, then the degree-7
- * Taylor polynomial of e^r (|r| <= ln2/2, truncation < 6e-9 relative) by
- * Horner, scaled by 2^n. Outside [-87, 88] it returns 0 or +inf. */
+ * and ln2 split into 0.693359375 (exact, so n*ln2hi is exact) +
+ * -2.12194440e-4, then the degree-7 Taylor polynomial of e^r (|r| <= ln2/2,
+ * truncation < 6e-9 relative) by Horner steps of one fmaf each, scaled by
+ * 2^n. The coefficients are 1/k! rounded to fp32, written out in hex.
+ * Outside [-87, 88] it returns 0 or +inf. */
 static float exp_f32(float x) {
     if (x > 88.0f) return INFINITY;
     if (x < -87.0f) return 0.0f;
-    const float t = x * 1.44269504f;
-    const float n = nearbyintf(t);
-    const float r1 = x - n * 0.693359375f;
-    const float r = r1 - n * -2.12194440e-4f;
-    float p = 1.0f / 5040.0f;
-    p = p * r + 1.0f / 720.0f;
-    p = p * r + 1.0f / 120.0f;
-    p = p * r + 1.0f / 24.0f;
-    p = p * r + 1.0f / 6.0f;
-    p = p * r + 0.5f;
-    p = p * r + 1.0f;
-    p = p * r + 1.0f;
+    const float n = nearbyintf(x * 1.44269504f);
+    float r = fmaf(-n, 0.693359375f, x);
+    r = fmaf(-n, -2.12194440e-4f, r);
+    float p = 0x1.a01a02p-13f;        /* 1/5040 */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);  /* 1/720 */
+    p = fmaf(p, r, 0x1.111112p-7f);   /* 1/120 */
+    p = fmaf(p, r, 0x1.555556p-5f);   /* 1/24 */
+    p = fmaf(p, r, 0x1.555556p-3f);   /* 1/6 */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
     return ldexpf(p, (int)n);
 }
 

@@ -47,6 +47,12 @@ MUTATIONS = [
     ("swiglu gate and up swapped", "double g = orc_bf16_value(y[m * 2 * F + f]);\n            double u = orc_bf16_value(y[m * 2 * F + F + f]);\n            double sg = 1.0 / (1.0 + exp(-g));\n            h[",
      "double u = orc_bf16_value(y[m * 2 * F + f]);\n            double g = orc_bf16_value(y[m * 2 * F + F + f]);\n            double sg = 1.0 / (1.0 + exp(-g));\n            h[",
      ["test_swiglu_against_closed_forms"]),
+    ("exp polynomial drops the 1/24 term", "p = fmaf(p, r, 0x1.555556p-5f);   /* 1/24 */",
+     "p = fmaf(p, r, 0.0f);", ["test_exp_f32_accuracy"]),
+    ("exp reduction drops the low part of ln2", "r = fmaf(-n, -2.12194440e-4f, r);", "r = r;",
+     ["test_exp_f32_accuracy"]),
+    ("fp32 swiglu backward uses (1 + s) for (1 - s)", "const float one_minus = 1.0f - sg;",
+     "const float one_minus = 1.0f + sg;", ["test_swiglu_f32_against_fp64_definition"]),
     ("colwise blocks cross rows wrongly", "for (int t = 0; t < 32; ++t) v[t] = x[(32 * i + t) * K + k];",
      "for (int t = 0; t < 32; ++t) v[t] = x[(32 * i + t) * K + (k ^ 1)];",
      ["test_group_quantize_equals_blockwise_definition"]),
