@@ -120,30 +120,47 @@ __device__ __forceinline__ void report_status(int32_t* d_status, int bits) {
 // SwiGLU between FC1 and FC2 of a fused grouped MoE MLP (TransformerEngine
 // PR #3545, "Fix distributed BF16 weights and trim NVFP4 saved state in the
 // fused grouped MLP": FC1 -> activation -> FC2; gate = first half of FC1's
-// output). Every step is one IEEE fp32 operation (__f*_rn: never contracted
-// into an FMA) so that the bf16 rounding of h, and the E4M3 codes chosen
-// from it, are reproducible exactly. e^x: Cody & Waite argument reduction
-// x = n*ln2 + r (n = rint(x*log2 e), ln2 = 0.693359375 + -2.12194440e-4),
-// the degree-7 Taylor polynomial of e^r by Horner, times 2^n; 0 below -87,
-// +inf above 88.
+// output). Every step is one IEEE fp32 operation with one rounding (__f*_rn
+// are never contracted; __fmaf_rn is an explicit fused multiply-add) so that
+// the bf16 rounding of h, and the E4M3 codes chosen from it, are
+// reproducible exactly. All of it is branch-free (range limits are selects)
+// so the unrolled element loops keep their instruction-level parallelism.
+// e^x: Cody & Waite argument reduction x = n*ln2 + r (n = rint(x*log2 e),
+// ln2 = 0.693359375 + -2.12194440e-4), the degree-7 Taylor polynomial of e^r
+// by fused Horner steps with coefficients 1/k! rounded to fp32, times 2^n;
+// 0 below -87, +inf above 88.
 __device__ __forceinline__ float exp_f32_steps(float x) {
-    if (x > 88.0f) return __int_as_float(0x7f800000);
-    if (x < -87.0f) return 0.0f;
     const float n = rintf(__fmul_rn(x, 1.44269504f));
-    const float r1 = __fsub_rn(x, __fmul_rn(n, 0.693359375f));
-    const float r = __fsub_rn(r1, __fmul_rn(n, -2.12194440e-4f));
-    float p = __fdiv_rn(1.0f, 5040.0f);
-    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 720.0f));
-    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 120.0f));
-    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 24.0f));
-    p = __fadd_rn(__fmul_rn(p, r), __fdiv_rn(1.0f, 6.0f));
-    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));  // n in [-126, 127]
+    float r = __fmaf_rn(-n, 0.693359375f, x);
+    r = __fmaf_rn(-n, -2.12194440e-4f, r);
+    float p = 0x1.a01a02p-13f;             // 1/5040
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/720
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/120
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/24
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/6
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    // 2^n as exponent bits; n lies in [-126, 127] wherever the value is kept
+    const float v = __fmul_rn(p, __uint_as_float(((uint32_t)__float2int_rz(n) + 127u) << 23));
+    return x > 88.0f ? __int_as_float(0x7f800000) : (x < -87.0f ? 0.0f : v);
 }
+// 1/d for d in [1, 2^126): Newton-Raphson y <- y + y*(1 - d*y), three steps
+// from the bit-pattern estimate as_float(0x7EF311C3 - bits(d)) (relative
+// error <= 5.1%, squared by each step to below 2^-24 after the third).
+__device__ __forceinline__ float recip_f32_steps(float d) {
+    float y = __uint_as_float(0x7EF311C3u - __float_as_uint(d));
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const float e = __fmaf_rn(-d, y, 1.0f);
+        y = __fmaf_rn(y, e, y);
+    }
+    return y;
+}
+// sigmoid(g) = 1/(1 + e^-g), 0 below g = -87 (true value under 2^-125)
 __device__ __forceinline__ float sigmoid_f32_steps(float g) {
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_f32_steps(-g)));
+    const float y = recip_f32_steps(__fadd_rn(1.0f, exp_f32_steps(-g)));
+    return g < -87.0f ? 0.0f : y;
 }
 // h = (g * s) * u
 __device__ __forceinline__ float swiglu_h(float g, float u) {

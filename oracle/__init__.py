@@ -77,6 +77,8 @@ def _declare(L):
     L.orc_swiglu_bwd.argtypes = [_P, _P, _I64, _I64, _P]
     L.orc_exp_f32.argtypes = [ctypes.c_float]
     L.orc_exp_f32.restype = ctypes.c_float
+    L.orc_recip_f32.argtypes = [ctypes.c_float]
+    L.orc_recip_f32.restype = ctypes.c_float
     L.orc_swiglu_fwd_f32.argtypes = [_P, _I64, _I64, _P]
     L.orc_swiglu_bwd_f32.argtypes = [_P, _P, _I64, _I64, _P]
     L.orc_num_threads.restype = _INT
@@ -334,6 +336,10 @@ def swiglu_bwd(dh_bits, y_bits):
 
 def exp_f32(x: float) -> float:
     return lib().orc_exp_f32(float(x))
+
+
+def recip_f32(d: float) -> float:
+    return lib().orc_recip_f32(float(d))
 
 
 def swiglu_fwd_f32(y_bits):

@@ -522,8 +522,9 @@ ORC_API void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* y, int64_t M, in
  * -2.12194440e-4, then the degree-7 Taylor polynomial of e^r (|r| <= ln2/2,
  * truncation < 6e-9 relative) by Horner steps of one fmaf each, scaled by
  * 2^n. The coefficients are 1/k! rounded to fp32, written out in hex.
- * Outside [-87, 88] it returns 0 or +inf. */
+ * Outside [-87, 88] it returns 0 or +inf; NaN stays NaN. */
 static float exp_f32(float x) {
+    if (x != x) return x;
     if (x > 88.0f) return INFINITY;
     if (x < -87.0f) return 0.0f;
     const float n = nearbyintf(x * 1.44269504f);
@@ -542,7 +543,32 @@ static float exp_f32(float x) {
 
 ORC_API float orc_exp_f32(float x) { return exp_f32(x); }
 
-static float sigmoid_f32(float g) { return 1.0f / (1.0f + exp_f32(-g)); }
+/* 1/d for d in [1, 2^126): Newton-Raphson iteration y <- y + y*(1 - d*y)
+ * (two fmaf per step) from the bit-pattern estimate y0 = as_float(0x7EF311C3
+ * - bits(d)), whose relative error is at most 5.1%; three steps square that
+ * to below 2^-24 (measured: within 0.5003 ulp of 1/d). Only fp32 adds,
+ * multiplies and an integer subtraction: no division. */
+static float recip_f32(float d) {
+    uint32_t b;
+    memcpy(&b, &d, sizeof b);
+    b = 0x7EF311C3u - b;
+    float y;
+    memcpy(&y, &b, sizeof y);
+    for (int i = 0; i < 3; ++i) {
+        const float e = fmaf(-d, y, 1.0f);
+        y = fmaf(y, e, y);
+    }
+    return y;
+}
+
+ORC_API float orc_recip_f32(float d) { return recip_f32(d); }
+
+/* sigmoid(g) = 1/(1 + e^-g); taken as 0 below g = -87, where the true value
+ * is under 2^-125 (this also keeps d = 1 + e^-g inside recip_f32's range). */
+static float sigmoid_f32(float g) {
+    if (g < -87.0f) return 0.0f;
+    return recip_f32(1.0f + exp_f32(-g));
+}
 
 static uint16_t bf16_round_f32(float f) { return orc_bf16_round((double)f); }
 

@@ -53,6 +53,10 @@ MUTATIONS = [
      ["test_exp_f32_accuracy"]),
     ("fp32 swiglu backward uses (1 + s) for (1 - s)", "const float one_minus = 1.0f - sg;",
      "const float one_minus = 1.0f + sg;", ["test_swiglu_f32_against_fp64_definition"]),
+    ("reciprocal stops after two Newton steps", "for (int i = 0; i < 3; ++i) {\n        const float e = fmaf(-d, y, 1.0f);",
+     "for (int i = 0; i < 2; ++i) {\n        const float e = fmaf(-d, y, 1.0f);", ["test_recip_f32_accuracy"]),
+    ("sigmoid uses 1 - e^-g", "return recip_f32(1.0f + exp_f32(-g));", "return recip_f32(1.0f - exp_f32(-g));",
+     ["test_swiglu_f32_against_fp64_definition"]),
     ("colwise blocks cross rows wrongly", "for (int t = 0; t < 32; ++t) v[t] = x[(32 * i + t) * K + k];",
      "for (int t = 0; t < 32; ++t) v[t] = x[(32 * i + t) * K + (k ^ 1)];",
      ["test_group_quantize_equals_blockwise_definition"]),

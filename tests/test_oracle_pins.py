@@ -446,6 +446,19 @@ def test_exp_f32_accuracy(orc):
     assert orc.exp_f32(0.0) == 1.0 and orc.exp_f32(89.0) == np.inf and orc.exp_f32(-88.0) == 0.0
 
 
+def test_recip_f32_accuracy(orc):
+    # within 0.5 ulp (plus the measured 3e-4 slack) of 1/d over [1, e^87],
+    # exact where 1/d is representable
+    rng = np.random.default_rng(23)
+    d = np.concatenate([1 + 3 * rng.random(3000), np.exp(rng.uniform(0, 87, 3000)), 2.0 ** np.arange(0, 126)])
+    d = d.astype(np.float32)
+    got = np.array([orc.recip_f32(float(v)) for v in d], np.float64)
+    exact = 1 / d.astype(np.float64)
+    ulp = np.spacing(exact.astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= 0.5004 * ulp)
+    assert orc.recip_f32(1.0) == 1.0 and orc.recip_f32(4.0) == 0.25 and orc.recip_f32(2.0 ** 100) == 2.0 ** -100
+
+
 def test_swiglu_f32_against_fp64_definition(orc):
     rng = np.random.default_rng(19)
     M, F = 96, 128
