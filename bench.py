@@ -54,6 +54,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
+    p.add_argument("--only", choices=["swiglu_quantize"],
+                   help="time only the fused SwiGLU->quantize kernels (forward and backward) on the MLP workload's "
+                        "shapes and print their line (a small footprint for profilers)")
     return p.parse_args()
 
 
@@ -298,11 +301,72 @@ def time_mlp(dev, steps=10, warmup=3):
     per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
            for j, k in enumerate(MLP_STAGES)}
     gemm_ms = sum(v for k, v in per.items() if "prop" in k or "grad" in k)
+    fb, bb = swiglu_quant_bytes(st.M, st.F)
+    swq_gbs = {"swiglu_quantize_h": fb / (per["swiglu_quantize_h"] * 1e-3) / 1e9,
+               "swiglu_bwd_quantize_dy1_dbias": bb / (per["swiglu_bwd_quantize_dy1_dbias"] * 1e-3) / 1e9}
     return {"workload": MLP_WORKLOAD, "steps": steps, "warmup": warmup, "ms_per_step": ms,
             "tflops_step": st.flops() / (ms * 1e-3) / 1e12, "gemm_tflops": st.flops() / (gemm_ms * 1e-3) / 1e12,
-            "stage_ms": per, "gpu_launches": st.launches_per_step * steps,
+            "stage_ms": per, "swiglu_quantize_gbs": swq_gbs, "gpu_launches": st.launches_per_step * steps,
             "step": "fwd+bwd of FC1 (bias) -> SwiGLU -> FC2 (bias), X and dY2 rowwise-prequantized; SwiGLU fused "
                     "with the quantization of h (forward) and of dY1 with its dbias (backward)"}
+
+
+def swiglu_quant_bytes(M, F):
+    """Algorithmic HBM bytes of the fused SwiGLU->quantize kernels (row+col
+    E4M3 codes and E8M0 scales written once, inputs read once; backward adds
+    the fp32 per-128-row dbias partials)."""
+    fwd = M * 2 * F * 2 + M * F * (2 + 2 / 32)
+    bwd = M * F * 2 + M * 2 * F * 2 + M * 2 * F * (2 + 2 / 32) + (M // 128) * 2 * F * 4
+    return fwd, bwd
+
+
+def time_swiglu_quantize(dev, steps, warmup):
+    """The fused SwiGLU->quantize kernels alone on the MLP workload's shapes:
+    y1 (M, 2F) and dh (M, F) bf16 ~N(0,1), forward with h's row+col codes,
+    backward with dY1's row+col codes and its dbias."""
+    import torch
+
+    import moe_expert_grouped_group_gb300 as mxq
+    from synth import WORKLOADS, bf16_normal, make_m_splits
+
+    w = WORKLOADS[MLP_WORKLOAD]
+    M, F, E = w.M, w.F, w.E
+    tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    ms = torch.from_numpy(make_m_splits(w, 0)).to(dev)
+    y1 = tb(bf16_normal((M, 2 * F), 1.0, (0, w.wid, 11)))
+    dh = tb(bf16_normal((M, F), 1.0, (0, w.wid, 12)))
+    u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+    sb = mxq.scale_bytes
+
+    def q(rows, cols):
+        return {"row_data": u8((rows, cols)), "row_scale": u8(sb(rows, cols, False)),
+                "col_data": u8((rows, cols)), "col_scale": u8(sb(rows, cols, True))}
+
+    qh, qdy1 = q(M, F), q(M, 2 * F)
+    qdy1["dbias"] = torch.empty((E, 2 * F), dtype=torch.float32, device=dev)
+    ws = u8(mxq.workspace_bytes(7, M, 0, F, E))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(warmup + steps):
+        flush.fill_(1)
+        e = ev[i - warmup] if i >= warmup else None
+        if e:
+            e[0].record()
+        mxq.swiglu_quantize(y1, ms, out=qh)
+        if e:
+            e[1].record()
+        mxq.swiglu_bwd_quantize(dh, y1, ms, dbias=True, out=qdy1, workspace=ws)
+        if e:
+            e[2].record()
+    torch.cuda.synchronize()
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    fb, bb = swiglu_quant_bytes(M, F)
+    return {"workload": MLP_WORKLOAD, "rows": M, "F": F, "steps": steps, "warmup": warmup,
+            "fwd_us": fwd_ms * 1e3, "bwd_us": bwd_ms * 1e3,
+            "fwd_gbs": fb / (fwd_ms * 1e-3) / 1e9, "bwd_gbs": bb / (bwd_ms * 1e-3) / 1e9,
+            "fwd_bytes": fb, "bwd_bytes": bb,
+            "l2": "256 MiB buffer written before every forward+backward pair"}
 
 
 KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
@@ -514,6 +578,14 @@ def main():
     from __graft_entry__ import build
 
     build()
+    if args.only == "swiglu_quantize":
+        r = time_swiglu_quantize(dev, max(1, args.steps), max(1, args.warmup))
+        _, hbm_peak, src = peaks()
+        r.update(fwd_frac=r["fwd_gbs"] / hbm_peak, bwd_frac=r["bwd_gbs"] / hbm_peak, hbm_peak_gbs=hbm_peak,
+                 peak_source=src)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
     w, d = make_host_workload()
     st = NativeStep(w, d, dev)
     flops, bytes_ = algorithmic(w)

@@ -125,12 +125,17 @@ __device__ __forceinline__ void report_status(int32_t* d_status, int bits) {
 // the bf16 rounding of h, and the E4M3 codes chosen from it, are
 // reproducible exactly. All of it is branch-free (range limits are selects)
 // so the unrolled element loops keep their instruction-level parallelism.
-// e^x: Cody & Waite argument reduction x = n*ln2 + r (n = rint(x*log2 e),
-// ln2 = 0.693359375 + -2.12194440e-4), the degree-7 Taylor polynomial of e^r
-// by fused Horner steps with coefficients 1/k! rounded to fp32, times 2^n;
-// 0 below -87, +inf above 88.
-__device__ __forceinline__ float exp_f32_steps(float x) {
-    const float n = rintf(__fmul_rn(x, 1.44269504f));
+// e^x for x in [-86, 88]: Cody & Waite argument reduction x = n*ln2 + r, n
+// the integer nearest to x*log2 e (one fused multiply-add onto 1.5*2^23
+// rounds the product to an integer, whose value then sits in the low
+// mantissa bits of j), ln2 = 0.693359375 + -2.12194440e-4; the degree-7
+// Taylor polynomial of e^r by fused Horner steps with coefficients 1/k!
+// rounded to fp32; then 2^n applied by adding n to p's exponent field
+// (exact: n >= -124 keeps the result normal). Outside [-86, 88] the value is
+// meaningless; callers clamp or select.
+__device__ __forceinline__ float exp_core_f32(float x) {
+    const float j = __fmaf_rn(x, 1.44269504f, 0x1.8p23f);
+    const float n = __fsub_rn(j, 0x1.8p23f);
     float r = __fmaf_rn(-n, 0.693359375f, x);
     r = __fmaf_rn(-n, -2.12194440e-4f, r);
     float p = 0x1.a01a02p-13f;             // 1/5040
@@ -141,9 +146,8 @@ __device__ __forceinline__ float exp_f32_steps(float x) {
     p = __fmaf_rn(p, r, 0.5f);
     p = __fmaf_rn(p, r, 1.0f);
     p = __fmaf_rn(p, r, 1.0f);
-    // 2^n as exponent bits; n lies in [-126, 127] wherever the value is kept
-    const float v = __fmul_rn(p, __uint_as_float(((uint32_t)__float2int_rz(n) + 127u) << 23));
-    return x > 88.0f ? __int_as_float(0x7f800000) : (x < -87.0f ? 0.0f : v);
+    // bits(j) = bits(1.5*2^23) + n, and bits(1.5*2^23) << 23 wraps to 0
+    return __uint_as_float(__float_as_uint(p) + (__float_as_uint(j) << 23));
 }
 // 1/d for d in [1, 2^126): Newton-Raphson y <- y + y*(1 - d*y), three steps
 // from the bit-pattern estimate as_float(0x7EF311C3 - bits(d)) (relative
@@ -157,10 +161,12 @@ __device__ __forceinline__ float recip_f32_steps(float d) {
     }
     return y;
 }
-// sigmoid(g) = 1/(1 + e^-g), 0 below g = -87 (true value under 2^-125)
+// sigmoid(g) = 1/(1 + e^-g), 0 below g = -86 (true value under 2^-124).
+// e^-g is taken at max(-g, -86): above g = 86 that is e^-86 instead of 0,
+// and 1 + e^-86 rounds to 1 exactly as 1 + 0 does.
 __device__ __forceinline__ float sigmoid_f32_steps(float g) {
-    const float y = recip_f32_steps(__fadd_rn(1.0f, exp_f32_steps(-g)));
-    return g < -87.0f ? 0.0f : y;
+    const float y = recip_f32_steps(__fadd_rn(1.0f, exp_core_f32(fmaxf(-g, -86.0f))));
+    return g < -86.0f ? 0.0f : y;
 }
 // h = (g * s) * u
 __device__ __forceinline__ float swiglu_h(float g, float u) {
@@ -179,6 +185,14 @@ constexpr unsigned long long kWaitNs = 2000000000ull;  // bound on any on-chip w
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
+}
+// First A-byte-aligned address at or after p, a pointer into dynamic shared
+// memory. Offsetting p itself (rather than casting an aligned integer back to
+// a pointer) lets the compiler keep the shared address space, so accesses
+// through the result are shared-memory loads and stores, not generic ones.
+template <uint32_t A>
+__device__ __forceinline__ uint8_t* smem_align(uint8_t* p) {
+    return p + ((A - (smem_u32(p) & (A - 1))) & (A - 1));
 }
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, Params p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = smem_align<1024>(smem_raw);
     int64_t* s_off = reinterpret_cast<int64_t*>(smem + TABLE_REGION);
     int16_t* s_order = reinterpret_cast<int16_t*>(s_off + p.E + 1);
     __shared__ uint32_t s_tmem;

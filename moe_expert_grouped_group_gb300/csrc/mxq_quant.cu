@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kTileThreads)
     __shared__ int s_abort;
 
     // dynamic shared memory: [input stages][full/empty barriers][expert offsets (E+1)]
-    uint8_t* q_smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q_smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t* q_smem = smem_align<128>(q_smem_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(q_smem + Sh::kStages * Sh::kStageBytes);
     int64_t* s_off = reinterpret_cast<int64_t*>(bars + 2 * Sh::kStages);
 

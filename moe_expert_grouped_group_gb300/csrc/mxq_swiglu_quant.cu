@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ __align__(16) float s_red[4][kTile];
     __shared__ int s_abort;
 
-    uint8_t* stage = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sq_raw) + 127) & ~uintptr_t(127));
+    uint8_t* stage = smem_align<128>(sq_raw);
     uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kIn * kTileBytes);
     int64_t* s_off = reinterpret_cast<int64_t*>(bars + 2);
 

@@ -517,17 +517,20 @@ ORC_API void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* y, int64_t M, in
  * the CUDA kernels implement the same steps independently. fmaf is the
  * IEEE fused multiply-add: one rounding of a*b+c.
  *
- * e^x: Cody & Waite argument reduction, x = n*ln2 + r with n = rint(x*log2 e)
- * and ln2 split into 0.693359375 (exact, so n*ln2hi is exact) +
- * -2.12194440e-4, then the degree-7 Taylor polynomial of e^r (|r| <= ln2/2,
- * truncation < 6e-9 relative) by Horner steps of one fmaf each, scaled by
- * 2^n. The coefficients are 1/k! rounded to fp32, written out in hex.
- * Outside [-87, 88] it returns 0 or +inf; NaN stays NaN. */
+ * e^x: Cody & Waite argument reduction, x = n*ln2 + r with n the integer
+ * nearest to x*log2 e (one fused multiply-add onto 1.5*2^23 rounds the product
+ * straight to an integer, ties to even; subtracting 1.5*2^23 is exact) and ln2
+ * split into 0.693359375 (exact, so n*ln2hi is exact) + -2.12194440e-4, then
+ * the degree-7 Taylor polynomial of e^r (|r| <= ln2/2, truncation < 6e-9
+ * relative) by Horner steps of one fmaf each, scaled by 2^n. The
+ * coefficients are 1/k! rounded to fp32, written out in hex. Outside
+ * [-86, 88] it returns 0 or +inf (so 2^n, n >= -124, keeps p*2^n normal and
+ * the scaling exact); NaN stays NaN. */
 static float exp_f32(float x) {
     if (x != x) return x;
     if (x > 88.0f) return INFINITY;
-    if (x < -87.0f) return 0.0f;
-    const float n = nearbyintf(x * 1.44269504f);
+    if (x < -86.0f) return 0.0f;
+    const float n = fmaf(x, 1.44269504f, 0x1.8p23f) - 0x1.8p23f;
     float r = fmaf(-n, 0.693359375f, x);
     r = fmaf(-n, -2.12194440e-4f, r);
     float p = 0x1.a01a02p-13f;        /* 1/5040 */
@@ -563,10 +566,10 @@ static float recip_f32(float d) {
 
 ORC_API float orc_recip_f32(float d) { return recip_f32(d); }
 
-/* sigmoid(g) = 1/(1 + e^-g); taken as 0 below g = -87, where the true value
- * is under 2^-125 (this also keeps d = 1 + e^-g inside recip_f32's range). */
+/* sigmoid(g) = 1/(1 + e^-g); taken as 0 below g = -86, where the true value
+ * is under 2^-124 (this also keeps d = 1 + e^-g inside recip_f32's range). */
 static float sigmoid_f32(float g) {
-    if (g < -87.0f) return 0.0f;
+    if (g < -86.0f) return 0.0f;
     return recip_f32(1.0f + exp_f32(-g));
 }
 

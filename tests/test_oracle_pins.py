@@ -438,12 +438,19 @@ def test_swiglu_against_closed_forms(orc):
 
 # -------------------------------------------- SwiGLU in kernel precision
 def test_exp_f32_accuracy(orc):
-    xs = np.concatenate([np.linspace(-87, 88, 4001), np.linspace(-1, 1, 2001)])
-    got = np.array([orc.exp_f32(float(np.float32(x))) for x in xs], np.float64)
-    ref = np.exp(xs.astype(np.float32).astype(np.float64))
+    # within 2 ulp of e^x over [-86, 88], including arguments next to the
+    # points where x*log2 e is a half-integer (n switches, |r| reaches ln2/2)
+    ties = ((np.arange(-124, 127) + 0.5) / np.log2(np.e)).astype(np.float32)
+    near = np.concatenate([ties, np.nextafter(ties, np.float32(np.inf)), np.nextafter(ties, np.float32(-np.inf))])
+    xs = np.concatenate([np.linspace(-86, 88, 4001).astype(np.float32), np.linspace(-1, 1, 2001).astype(np.float32),
+                         near])
+    xs = xs[(xs >= -86) & (xs <= 88)]
+    got = np.array([orc.exp_f32(float(x)) for x in xs], np.float64)
+    ref = np.exp(xs.astype(np.float64))
     ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
     assert np.all(np.abs(got - ref) <= 2 * ulp)
-    assert orc.exp_f32(0.0) == 1.0 and orc.exp_f32(89.0) == np.inf and orc.exp_f32(-88.0) == 0.0
+    assert orc.exp_f32(0.0) == 1.0 and orc.exp_f32(89.0) == np.inf and orc.exp_f32(-86.5) == 0.0
+    assert np.isnan(orc.exp_f32(float("nan")))
 
 
 def test_recip_f32_accuracy(orc):
