@@ -10,15 +10,15 @@
 //             bf16, quantized rowwise (FC1 dgrad) and colwise (FC1 wgrad),
 //             with the per-expert FC1 dbias reduced from the same bf16 values.
 //
-// Same structure as the standalone quantizer: persistent CTAs of 4 compute
-// warps + 1 TMA producer warp, 128x128 output tiles. A stage holds the 128x128
-// input tiles a tile needs (g and u; plus dh backward). Each compute warp
-// first turns its own 32 rows into bf16 h (or dg and du) in place in shared
-// memory -- fp32 steps of mxq_common.cuh, one bf16 rounding -- then runs the
-// two quantization passes over that bf16 tile exactly as the standalone
-// kernel would over the tensor read from memory, so the codes equal
-// "SwiGLU, then group_quantize" bit for bit while h (or dY1) never makes a
-// round trip through HBM.
+// Persistent CTAs of 8 compute warps + 1 TMA producer warp, 128x128 output
+// tiles. A stage holds the 128x128 input tiles a tile needs (g and u; plus
+// dh backward). Warp w turns rows 16w..16w+15 into bf16 h (or dg and du),
+// written back in place -- fp32 steps of mxq_common.cuh, one bf16 rounding
+// -- gathering each column's exponent maximum (and dbias sum) in registers
+// on the way. After one exchange of those 16-row statistics through shared
+// memory (a 32-row colwise block is two warps), every warp encodes its own
+// rows rowwise and colwise: the same codes as "SwiGLU, then group_quantize"
+// bit for bit, while h (or dY1) never makes a round trip through HBM.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -29,9 +29,11 @@
 namespace mxq {
 namespace swq {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kTileBytes = kTile * kTile * 2;  // one 128x128 bf16 tile
+constexpr int kWarps = 8;                       // compute warps
+constexpr int kThreads = (kWarps + 1) * 32;     // + 1 TMA producer warp
+constexpr int kTileBytes = kTile * kTile * 2;   // one 128x128 bf16 tile
+constexpr int kPreRows = kTile / kWarps;        // rows per warp
+constexpr int kComputeThreads = kWarps * 32;
 
 struct Args {
     int64_t M, F, E;
@@ -44,8 +46,18 @@ struct Args {
     int32_t* status;
 };
 
+// Per output tile: its two 512-byte scale atoms, each warp's colwise
+// exponent maxima over its 16 rows (four bytes per lane) and its 16-row
+// dbias sums.
+struct Scratch {
+    uint8_t rs[512];
+    uint8_t cs[512];
+    uint32_t xexp[kWarps][32];
+    float red[kWarps][kTile];
+};
+
 __device__ __forceinline__ void bar_compute() {
-    asm volatile("bar.sync 2, %0;" ::"n"(kWarps * 32) : "memory");
+    asm volatile("bar.sync 2, %0;" ::"n"(kComputeThreads) : "memory");
 }
 __device__ __forceinline__ bool bar_compute_any(bool pred) {
     uint32_t r;
@@ -55,146 +67,157 @@ __device__ __forceinline__ bool bar_compute_any(bool pred) {
         "bar.red.or.pred q, 2, %2, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)pred), "n"(kWarps * 32)
+        : "r"((uint32_t)pred), "n"(kComputeThreads)
         : "memory");
     return r != 0;
-}
-__device__ __forceinline__ uint32_t group8_max_u8x4(uint32_t v) {
-#pragma unroll
-    for (int o = 4; o >= 1; o >>= 1) v = __vmaxu4(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Quantize one 128x128 bf16 tile held in shared memory (row r at tile + r*256)
-// into output column tile `kt` of an (M, Kout) tensor; warp `rg` owns rows
-// 32rg..32rg+31, lane l columns 4l..4l+3. Same passes as mx_tile_kernel's
-// bf16 path: colwise exponent max + dbias sums, then rowwise exponent max
-// over 8 lanes and the E4M3 encode; scale atoms staged in shared memory.
-template <bool kRow, bool kCol, bool kBias, bool kDeq>
-__device__ __forceinline__ void quantize_tile(const uint8_t* tile, const Args& a, int64_t mt, int64_t kt, int64_t Kout,
-                                              const int64_t* s_off, uint8_t* s_rs, uint8_t* s_cs,
-                                              float (*s_red)[kTile], int rg, int lane) {
+// Colwise statistics of one output tile over a warp's 16 rows, gathered as
+// the bf16 results are produced: per column the largest |bits| (two
+// columns per word) and, for dbias, the fp32 sum.
+template <bool kBias>
+struct ColStats {
+    uint32_t m[2] = {0u, 0u};
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    __device__ __forceinline__ void add(uint2 w) {
+        m[0] = __vmaxu2(m[0], w.x & 0x7FFF7FFFu);
+        m[1] = __vmaxu2(m[1], w.y & 0x7FFF7FFFu);
+        if constexpr (kBias) {
+            sum[0] += bf16lo(w.x);
+            sum[1] += bf16hi(w.x);
+            sum[2] += bf16lo(w.y);
+            sum[3] += bf16hi(w.y);
+        }
+    }
+    // the four biased exponents, one byte per column
+    __device__ __forceinline__ uint32_t exps() const {
+        return ((m[0] >> 7) & 0xFFu) | (((m[0] >> 23) & 0xFFu) << 8) | (((m[1] >> 7) & 0xFFu) << 16) |
+               (((m[1] >> 23) & 0xFFu) << 24);
+    }
+};
+
+// Encode the 16 rows of one output tile that warp w produced (bf16 in shared
+// memory, row r at rows + r*256, lane l reading columns 4l..4l+3) into output
+// column tile `kt` of an (M, Kout) tensor. The colwise scale of each 32-row
+// block comes from the exponent maxima of warps w and w^1 (the two halves of
+// the block); the rowwise scale of each row from the 8 lanes of its
+// 32-column block. Swizzled scale bytes are staged in `sc` for flush_scratch.
+template <bool kRow, bool kCol, bool kDeq>
+__device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, int64_t mt, int64_t kt,
+                                            int64_t Kout, Scratch& sc, int w, int lane) {
+    auto o = [&](int r) { return *reinterpret_cast<const uint2*>(rows + r * (kTile * 2)); };
     const int blk = lane >> 3;
-    const int64_t tilesK = Kout / kTile;
-    const int64_t r0 = mt * kTile + rg * 32;
+    const int rg = w >> 1;                          // 32-row block of the tile
+    const int64_t r0 = mt * kTile + w * kPreRows;   // first row of this warp
     const int64_t col = kt * kTile + lane * 4;
     const uint32_t Ku = (uint32_t)Kout;
-    const uint8_t* src = tile + (rg * 32) * (kTile * 2) + lane * 8;
-    auto ld_row = [&](int r) -> uint2 { return *reinterpret_cast<const uint2*>(src + r * (kTile * 2)); };
 
     uint32_t ccode[4] = {0, 0, 0, 0};
     float cinv[4] = {1.f, 1.f, 1.f, 1.f};
-    if constexpr (kCol || kBias) {
-        uint32_t m0 = 0, m1 = 0;
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-        for (int r = 0; r < 32; ++r) {
-            const uint2 u = ld_row(r);
-            m0 = __vmaxu2(m0, u.x & 0x7FFF7FFFu);
-            m1 = __vmaxu2(m1, u.y & 0x7FFF7FFFu);
-            if constexpr (kBias) {
-                sum[0] += bf16lo(u.x);
-                sum[1] += bf16hi(u.x);
-                sum[2] += bf16lo(u.y);
-                sum[3] += bf16hi(u.y);
-            }
-        }
-        if constexpr (kCol) {
-            const uint32_t e[4] = {(m0 >> 7) & 0xFFu, (m0 >> 23) & 0xFFu, (m1 >> 7) & 0xFFu, (m1 >> 23) & 0xFFu};
+    if constexpr (kCol) {
+        const uint32_t e = __vmaxu4(sc.xexp[w][lane], sc.xexp[w ^ 1][lane]);
+        uint32_t packed = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                ccode[j] = (uint32_t)max((int)e[j] - 8, 0);
-                cinv[j] = inv_scale_from_code(ccode[j]);
-            }
+        for (int j = 0; j < 4; ++j) {
+            ccode[j] = (uint32_t)max((int)((e >> (8 * j)) & 0xFFu) - 8, 0);
+            cinv[j] = inv_scale_from_code(ccode[j]);
+            packed |= ccode[j] << (8 * j);
+        }
+        if ((w & 1) == 0) {
             if (a.swizzle) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) s_cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
+                for (int j = 0; j < 4; ++j) sc.cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
             } else {
-                *reinterpret_cast<uint32_t*>(a.col_s + (mt * 4 + rg) * Kout + col) =
-                    ccode[0] | (ccode[1] << 8) | (ccode[2] << 16) | (ccode[3] << 24);
+                *reinterpret_cast<uint32_t*>(a.col_s + (mt * 4 + rg) * Kout + col) = packed;
             }
         }
-        if constexpr (kBias) *reinterpret_cast<float4*>(&s_red[rg][lane * 4]) = make_float4(sum[0], sum[1], sum[2], sum[3]);
     }
-
-    if constexpr (kRow || kCol || kDeq) {
-        uint8_t* rq = kRow ? a.row_q + r0 * Kout + col : nullptr;
-        uint8_t* cq = kCol ? a.col_q + r0 * Kout + col : nullptr;
-        __nv_bfloat16* dq = kDeq ? a.bf16_out + r0 * Kout + col : nullptr;
+    uint8_t* rq = kRow ? a.row_q + r0 * Kout + col : nullptr;
+    uint8_t* cq = kCol ? a.col_q + r0 * Kout + col : nullptr;
+    __nv_bfloat16* dq = kDeq ? a.bf16_out + r0 * Kout + col : nullptr;
 #pragma unroll 2
-        for (int r4 = 0; r4 < 32; r4 += 4) {
-            uint2 u[4];
+    for (int r4 = 0; r4 < kPreRows; r4 += 4) {
+        uint2 ow[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) u[k] = ld_row(r4 + k);
-            uint32_t packed = 0;
-            if constexpr (kRow) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t w2 = __vmaxu2(u[k].x & 0x7FFF7FFFu, u[k].y & 0x7FFF7FFFu);
-                    packed |= (max(w2 & 0xFFFFu, w2 >> 16) >> 7) << (8 * k);
-                }
-                packed = group8_max_u8x4(packed);
-            }
+        for (int k = 0; k < 4; ++k) ow[k] = o(r4 + k);
+        uint32_t packed = 0;
+        if constexpr (kRow) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int r = r4 + k;
-                const float v[4] = {bf16lo(u[k].x), bf16hi(u[k].x), bf16lo(u[k].y), bf16hi(u[k].y)};
-                if constexpr (kRow) {
-                    const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
-                    const float inv = inv_scale_from_code(code);
-                    *reinterpret_cast<uint32_t*>(rq + r * Ku) =
-                        cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
-                    if ((lane & 7) == 0) {
-                        if (a.swizzle) s_rs[r * 16 + rg * 4 + blk] = (uint8_t)code;
-                        else a.row_s[(r0 + r) * (Kout / 32) + kt * 4 + blk] = (uint8_t)code;
-                    }
-                }
-                if constexpr (kCol) {
-                    *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) |
-                                                                (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
-                }
-                if constexpr (kDeq) *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = u[k];
+                const uint32_t m = __vmaxu2(ow[k].x & 0x7FFF7FFFu, ow[k].y & 0x7FFF7FFFu);
+                packed |= (max(m & 0xFFFFu, m >> 16) >> 7) << (8 * k);
             }
+#pragma unroll
+            for (int s = 4; s >= 1; s >>= 1) packed = __vmaxu4(packed, __shfl_xor_sync(0xffffffffu, packed, s));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = r4 + k;
+            const uint2 u = ow[k];
+            const float v[4] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y)};
+            if constexpr (kRow) {
+                const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
+                const float inv = inv_scale_from_code(code);
+                *reinterpret_cast<uint32_t*>(rq + r * Ku) =
+                    cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+                if ((lane & 7) == 0) {
+                    if (a.swizzle) sc.rs[((w & 1) * kPreRows + r) * 16 + rg * 4 + blk] = (uint8_t)code;
+                    else a.row_s[(r0 + r) * (Kout / 32) + kt * 4 + blk] = (uint8_t)code;
+                }
+            }
+            if constexpr (kCol) {
+                *reinterpret_cast<uint32_t*>(cq + r * Ku) =
+                    cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) | (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
+            }
+            if constexpr (kDeq) *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = u;
         }
     }
+}
 
-    bar_compute();
+// Write out one tile's scratch: the dbias partial of each of its 128 columns
+// (the eight 16-row sums added in warp order) and, for swizzled scales, its
+// rowwise atom and its colwise atom (the latter at the expert's base).
+// `t` is this thread's index among the 128 threads that flush the tile.
+template <bool kRow, bool kCol, bool kBias>
+__device__ __forceinline__ void flush_scratch(const Scratch& sc, const Args& a, int64_t mt, int64_t kt, int64_t Kout,
+                                              const int64_t* s_off, int t) {
     if constexpr (kBias) {
-        const int c = threadIdx.x;  // 0..127
-        a.partials[mt * Kout + kt * kTile + c] = ((s_red[0][c] + s_red[1][c]) + s_red[2][c]) + s_red[3][c];
+        float acc = sc.red[0][t];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) acc += sc.red[w][t];
+        a.partials[mt * Kout + kt * kTile + t] = acc;
     }
     if constexpr (kRow) {
-        if (a.swizzle && threadIdx.x < 32) {
-            uint4* dst = reinterpret_cast<uint4*>(a.row_s + (mt * tilesK + kt) * 512);
-            dst[threadIdx.x] = reinterpret_cast<const uint4*>(s_rs)[threadIdx.x];
+        if (a.swizzle && t < 32) {
+            uint4* dst = reinterpret_cast<uint4*>(a.row_s + (mt * (Kout / kTile) + kt) * 512);
+            dst[t] = reinterpret_cast<const uint4*>(sc.rs)[t];
         }
     }
     if constexpr (kCol) {
-        if (a.swizzle && threadIdx.x >= 32 && threadIdx.x < 64) {
+        if (a.swizzle && t >= 32 && t < 64) {
             const int64_t rt0 = mt * kTile;
             const int e = expert_of(s_off, (int)a.E, rt0);
             const int64_t off = s_off[e], me = s_off[e + 1] - off;
             const int64_t atom = kt * (me / kTile) + (rt0 - off) / kTile;
             uint4* dst = reinterpret_cast<uint4*>(a.col_s + Kout * off / 32 + atom * 512);
-            dst[threadIdx.x - 32] = reinterpret_cast<const uint4*>(s_cs)[threadIdx.x - 32];
+            dst[t - 32] = reinterpret_cast<const uint4*>(sc.cs)[t - 32];
         }
     }
-    bar_compute();
 }
 
+// Forward: 3 CTAs per SM (64 KB stage); backward: 2 (96 KB stage).
 template <bool kBwd, bool kRow, bool kCol, bool kBias, bool kDeq>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
     swiglu_quant_kernel(const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_dh, Args a) {
-    constexpr int kIn = kBwd ? 3 : 2;  // stage: [g][u] or [g][u][dh]
+    constexpr int kIn = kBwd ? 3 : 2;   // stage: [g][u] or [g][u][dh]
+    constexpr int kOut = kBwd ? 2 : 1;  // output tiles per stage: h, or dg and du
     constexpr uint32_t kStageTx = kIn * kTileBytes;
     extern __shared__ uint8_t sq_raw[];
-    __shared__ __align__(16) uint8_t s_rs[512];
-    __shared__ __align__(16) uint8_t s_cs[512];
-    __shared__ __align__(16) float s_red[4][kTile];
+    __shared__ __align__(16) Scratch s_sc[kOut];
     __shared__ int s_abort;
 
     uint8_t* stage = smem_align<128>(sq_raw);
@@ -237,7 +260,11 @@ __global__ void __launch_bounds__(kThreads)
         return;
     }
 
-    const int rg = warp;
+    // Warp w owns rows 16w..16w+15 of every output tile, lane l columns
+    // 4l..4l+3. Backward: the first 128 compute threads flush dg's scratch,
+    // the other 128 du's; forward: the first 128 flush h's.
+    const int fgrp = threadIdx.x >> 7;
+    const int ft_tid = threadIdx.x & 127;
     uint32_t phase = 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int64_t mt = t / tilesF, ft = t % tilesF;
@@ -245,11 +272,14 @@ __global__ void __launch_bounds__(kThreads)
         if (bar_compute_any(!ok)) break;
         phase ^= 1;
 
-        // SwiGLU on this warp's 32 rows, written back as bf16 in place
-        uint8_t* g_row = stage + (rg * 32) * (kTile * 2) + lane * 8;
+        // SwiGLU of this warp's 16 rows, rounded to bf16 and written back in
+        // place (h or dg over the gate tile, du over the up tile), with the
+        // colwise statistics of each output tile
+        ColStats<kBias> cs[kOut];
+        uint8_t* g_row = stage + (warp * kPreRows) * (kTile * 2) + lane * 8;
         uint8_t* u_row = g_row + kTileBytes;
 #pragma unroll 4
-        for (int r = 0; r < 32; ++r) {
+        for (int r = 0; r < kPreRows; ++r) {
             uint2* gp = reinterpret_cast<uint2*>(g_row + r * (kTile * 2));
             uint2* up = reinterpret_cast<uint2*>(u_row + r * (kTile * 2));
             const uint2 gw = *gp, uw = *up;
@@ -259,28 +289,46 @@ __global__ void __launch_bounds__(kThreads)
                 float h[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) h[j] = swiglu_h(g[j], u[j]);
-                *gp = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+                const uint2 hw = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
+                *gp = hw;
+                if (kCol || kBias) cs[0].add(hw);
             } else {
                 const uint2 dw = *reinterpret_cast<const uint2*>(g_row + 2 * kTileBytes + r * (kTile * 2));
                 const float d[4] = {bf16lo(dw.x), bf16hi(dw.x), bf16lo(dw.y), bf16hi(dw.y)};
                 float dg[4], du[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) swiglu_grads(d[j], g[j], u[j], dg[j], du[j]);
-                *gp = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
-                *up = make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
+                const uint2 gw2 = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
+                const uint2 uw2 = make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
+                *gp = gw2;
+                *up = uw2;
+                if (kCol || kBias) {
+                    cs[0].add(gw2);
+                    cs[kOut - 1].add(uw2);
+                }
             }
         }
-        __syncwarp();
-
-        if constexpr (!kBwd) {
-            quantize_tile<kRow, kCol, kBias, kDeq>(stage, a, mt, ft, a.F, s_off, s_rs, s_cs, s_red, rg, lane);
-        } else {
-            quantize_tile<kRow, kCol, kBias, kDeq>(stage, a, mt, ft, 2 * a.F, s_off, s_rs, s_cs, s_red, rg, lane);
-            quantize_tile<kRow, kCol, kBias, kDeq>(stage + kTileBytes, a, mt, tilesF + ft, 2 * a.F, s_off, s_rs,
-                                                   s_cs, s_red, rg, lane);
+#pragma unroll
+        for (int q = 0; q < kOut; ++q) {
+            if constexpr (kCol) s_sc[q].xexp[warp][lane] = cs[q].exps();
+            if constexpr (kBias)
+                *reinterpret_cast<float4*>(&s_sc[q].red[warp][lane * 4]) =
+                    make_float4(cs[q].sum[0], cs[q].sum[1], cs[q].sum[2], cs[q].sum[3]);
         }
+        bar_compute();  // every warp's colwise statistics are in
+
+        const int64_t Kout = kBwd ? 2 * a.F : a.F;
+#pragma unroll
+        for (int q = 0; q < kOut; ++q)
+            encode_rows<kRow, kCol, kDeq>(g_row + q * kTileBytes, a, mt, q ? tilesF + ft : ft, Kout, s_sc[q], warp,
+                                          lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty);  // this warp is done with the stage
+        bar_compute();                      // scratch complete
+        if (fgrp < kOut)
+            flush_scratch<kRow, kCol, kBias>(s_sc[fgrp], a, mt, fgrp ? tilesF + ft : ft, Kout, s_off, ft_tid);
+        // the next tile's first barrier orders these reads before any new
+        // write to the scratch
     }
     if (threadIdx.x == 0 && s_abort && a.status) atomicOr(a.status, MXQ_STATUS_WAIT_TIMEOUT);
 }
