@@ -224,7 +224,12 @@ MXQ_API int mxq_grouped_dbias_noalloc(const void* dy_bf16, int64_t M, int64_t N,
  * first F columns of the FC1 output are the gate):
  *   fwd: y (M, 2F) bf16 -> h (M, F) bf16, h = silu(g) * u;
  *   bwd: dh (M, F), y (M, 2F) -> dy (M, 2F) = [dh*u*silu'(g) | dh*silu(g)].
- * fp32 math, bf16 I/O. F % 8 == 0. */
+ * bf16 I/O; the math is a fixed sequence of fp32 IEEE operations, each
+ * rounded once: e^x by Cody-Waite reduction and the degree-7 Taylor
+ * polynomial (fused multiply-adds), sigmoid(g) = 1/(1 + e^-g) with the
+ * reciprocal by three Newton-Raphson steps, taken as 0 below g = -86;
+ * h = (g*s)*u, dg = ((dh*u)*s)*(1 + g*(1 - s)), du = dh*(g*s). The result
+ * is reproducible bit for bit on any IEEE fp32 machine. F % 8 == 0. */
 MXQ_API int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream);
 MXQ_API int mxq_swiglu_bwd(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F, void* dy_bf16,
                    mxq_stream_t stream);
