@@ -77,6 +77,8 @@ def _declare(L):
     L.orc_swiglu_bwd.argtypes = [_P, _P, _I64, _I64, _P]
     L.orc_exp_f32.argtypes = [ctypes.c_float]
     L.orc_exp_f32.restype = ctypes.c_float
+    L.orc_scaled_bias_grads.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P, _P]
+    L.orc_scaled_bias_grads.restype = _INT
     L.orc_recip_f32.argtypes = [ctypes.c_float]
     L.orc_recip_f32.restype = ctypes.c_float
     L.orc_swiglu_fwd_f32.argtypes = [_P, _I64, _I64, _P]
@@ -238,6 +240,22 @@ def grouped_dbias(dy_bits, m_splits):
     if lib().orc_grouped_dbias(_p(dy), M, N, len(ms), _p(ms), _p(out)) != 0:
         raise ValueError("orc_grouped_dbias rejected the input")
     return out
+
+
+def scaled_bias_grads(dy_values, m_splits, probs, bias_bits, dbias=True, dprobs=True):
+    """Scaled-bias and routing-scale gradients (see mxq_oracle.c): dy_values
+    (M, N) exact values in float64, probs (M,) float32, bias_bits (E, N) bf16
+    bits. Returns (db (E, N), ds (M,)) in float64 (None where not asked)."""
+    dy = _c(dy_values, np.float64)
+    M, N = dy.shape
+    ms = _c(m_splits, np.int64)
+    db = np.zeros((len(ms), N), np.float64) if dbias else None
+    ds = np.zeros(M, np.float64) if dprobs else None
+    rc = lib().orc_scaled_bias_grads(_p(dy), M, N, len(ms), _p(ms), _p(_c(probs, np.float32)),
+                                     _p(_c(bias_bits, np.uint16)), _p(db), _p(ds))
+    if rc != 0:
+        raise ValueError("orc_scaled_bias_grads rejected the input")
+    return db, ds
 
 
 # ------------------------------------------------------------------- GEMMs

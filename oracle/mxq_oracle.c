@@ -371,6 +371,42 @@ ORC_API int orc_grouped_dbias(const uint16_t* dy, int64_t M, int64_t N, int E, c
     return 0;
 }
 
+/* Scaled bias and routing-scale gradients [RQ: bias and routing-scale
+ * reductions are taken from the dequantized gradient]. Reading (the pages do
+ * not print the formula): expert e adds its bias scaled by the token's
+ * routing scale, y[m,:] = X[m,:] W_e^T + s_m * b_e, so for the gradient dY
+ *   db[e,n] = sum over expert e's rows m of s_m * dY[m,n]
+ *   ds[m]   = sum over n of dY[m,n] * b_e(m)[n]
+ * in fp64. dy holds the exact values (bf16 widened, or the dequantized
+ * rowwise wire format); bias is bf16 bits (E, N); probs fp32 (M). Either
+ * output may be NULL. An empty expert gives db = 0. */
+ORC_API int orc_scaled_bias_grads(const double* dy, int64_t M, int64_t N, int E, const int64_t* m_splits,
+                                  const float* probs, const uint16_t* bias, double* dbias, double* dprobs) {
+    if (orc_check_splits(m_splits, E, M)) return -1;
+    int64_t off = 0;
+    for (int e = 0; e < E; ++e) {
+        const int64_t end = off + m_splits[e];
+        if (dbias) {
+            #pragma omp parallel for schedule(static)
+            for (int64_t n = 0; n < N; ++n) {
+                double acc = 0.0;
+                for (int64_t m = off; m < end; ++m) acc += (double)probs[m] * dy[m * N + n];
+                dbias[e * N + n] = acc;
+            }
+        }
+        if (dprobs) {
+            #pragma omp parallel for schedule(static)
+            for (int64_t m = off; m < end; ++m) {
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) acc += dy[m * N + n] * orc_bf16_value(bias[e * N + n]);
+                dprobs[m] = acc;
+            }
+        }
+        off = end;
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------- GEMMs */
 
 /* Each GEMM entry is the textbook dot product of dequantized operands in

@@ -57,6 +57,15 @@ MUTATIONS = [
      "for (int i = 0; i < 2; ++i) {\n        const float e = fmaf(-d, y, 1.0f);", ["test_recip_f32_accuracy"]),
     ("sigmoid uses 1 - e^-g", "return recip_f32(1.0f + exp_f32(-g));", "return recip_f32(1.0f - exp_f32(-g));",
      ["test_swiglu_f32_against_fp64_definition"]),
+    ("scaled dbias drops the routing scale", "acc += (double)probs[m] * dy[m * N + n];", "acc += dy[m * N + n];",
+     ["test_scaled_bias_grads_are_gradients_of_the_scaled_bias_term"]),
+    ("routing-scale grad reads the next expert's bias", "acc += dy[m * N + n] * orc_bf16_value(bias[e * N + n]);",
+     "acc += dy[m * N + n] * orc_bf16_value(bias[((e + 1) % E) * N + n]);",
+     ["test_scaled_bias_grads_are_gradients_of_the_scaled_bias_term"]),
+    ("routing-scale grad skips the last column",
+     "for (int64_t n = 0; n < N; ++n) acc += dy[m * N + n] * orc_bf16_value(bias[e * N + n]);",
+     "for (int64_t n = 0; n < N - 1; ++n) acc += dy[m * N + n] * orc_bf16_value(bias[e * N + n]);",
+     ["test_scaled_bias_grads_are_gradients_of_the_scaled_bias_term"]),
     ("colwise blocks cross rows wrongly", "for (int t = 0; t < 32; ++t) v[t] = x[(32 * i + t) * K + k];",
      "for (int t = 0; t < 32; ++t) v[t] = x[(32 * i + t) * K + (k ^ 1)];",
      ["test_group_quantize_equals_blockwise_definition"]),

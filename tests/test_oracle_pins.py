@@ -485,3 +485,58 @@ def test_swiglu_f32_against_fp64_definition(orc):
     dhf = np.concatenate([f32_from_bf16_bits(dh)] * 2, axis=1).astype(np.float64)
     slack = 2.0 ** -21 * np.abs(dhf) * (1 + np.abs(g)) * np.abs(yf).max()
     assert np.all(np.abs(da - db) <= ulp + slack)
+
+
+# ------------------------------------------- scaled bias / routing scales
+def _scaled_bias_case(seed=31):
+    rng = np.random.default_rng(seed)
+    ms = np.array([128, 0, 256, 128], np.int64)  # one empty expert
+    M, N, E = int(ms.sum()), 256, len(ms)
+    dy_bits = bf16_bits_from_f32(rng.standard_normal((M, N)).astype(np.float32))
+    probs = rng.random(M).astype(np.float32)
+    bias = bf16_bits_from_f32((0.02 * rng.standard_normal((E, N))).astype(np.float32))
+    return dy_bits, ms, probs, bias
+
+
+def test_scaled_bias_grads_are_gradients_of_the_scaled_bias_term(orc):
+    # L(s, b) = sum_m sum_n dY[m,n] * s_m * b_e(m)[n], the part of <dY, y> that the
+    # scaled bias contributes, is linear in every s_m and b_e[n]: central differences
+    # of this forward definition give both gradients up to rounding
+    dy_bits, ms, probs, bias = _scaled_bias_case()
+    dy = f32_from_bf16_bits(dy_bits).astype(np.float64)
+    b = f32_from_bf16_bits(bias).astype(np.float64)
+    e_of = np.repeat(np.arange(len(ms)), ms)
+
+    def L(s, bb):
+        return float(np.sum(dy * (s[:, None] * bb[e_of])))
+
+    db, ds = orc.scaled_bias_grads(dy, ms, probs, bias)
+    s0, h = probs.astype(np.float64), 0.5
+    for m in [0, 127, 128, 300, 383, 384, 511]:
+        sp, sm = s0.copy(), s0.copy()
+        sp[m] += h
+        sm[m] -= h
+        fd = (L(sp, b) - L(sm, b)) / (2 * h)
+        assert abs(ds[m] - fd) <= 1e-9 * (1 + abs(fd)), m
+    for e, n in [(0, 0), (0, 255), (2, 17), (3, 128), (3, 255)]:
+        bp, bm = b.copy(), b.copy()
+        bp[e, n] += h
+        bm[e, n] -= h
+        fd = (L(s0, bp) - L(s0, bm)) / (2 * h)
+        assert abs(db[e, n] - fd) <= 1e-9 * (1 + abs(fd)), (e, n)
+    assert np.all(db[1] == 0)  # the empty expert
+    # both sides of <dY, s*b> agree: sum_m s_m ds_m == sum_e <b_e, db_e> == L(s, b)
+    tot = L(s0, b)
+    assert abs(float(s0 @ ds) - tot) <= 1e-9 * (1 + abs(tot))
+    assert abs(float(np.sum(b * db)) - tot) <= 1e-9 * (1 + abs(tot))
+
+
+def test_scaled_bias_with_unit_scales_is_the_plain_dbias(orc):
+    dy_bits, ms, _, bias = _scaled_bias_case(seed=32)
+    dy = f32_from_bf16_bits(dy_bits).astype(np.float64)
+    db, ds = orc.scaled_bias_grads(dy, ms, np.ones(len(dy), np.float32), bias, dprobs=False)
+    assert ds is None
+    assert np.array_equal(db, orc.grouped_dbias(dy_bits, ms))
+    zero = np.zeros_like(bias)
+    _, ds0 = orc.scaled_bias_grads(dy, ms, np.ones(len(dy), np.float32), zero, dbias=False)
+    assert np.all(ds0 == 0)
