@@ -125,7 +125,8 @@ enum {
     MXQ_OP_GEMM_FPROP = 4,
     MXQ_OP_GEMM_DGRAD = 5,
     MXQ_OP_GEMM_WGRAD = 6,
-    MXQ_OP_SWIGLU_BWD_QUANTIZE = 7
+    MXQ_OP_SWIGLU_BWD_QUANTIZE = 7,
+    MXQ_OP_SCALED_BIAS = 8
 };
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -175,6 +176,34 @@ MXQ_API int mxq_requant_colwise(const void* row_data, const void* row_scale_comp
  * (fixed-order tree per 128-row tile, fp64 across tiles); needs ws. */
 MXQ_API int mxq_grouped_dbias(const void* dy_bf16, int64_t M, int64_t N, int E, const int64_t* d_m_splits, float* dbias_out,
                       int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream);
+
+/* Scaled bias and routing-scale gradients [RQ: "bias and routing-scale
+ * reductions" are taken from the dequantized gradient] (reading: expert e
+ * adds its bias scaled by the token's routing scale, y[m,:] = X[m,:] W_e^T
+ * + s_m * b_e; the pages print no formula). From the gradient dY (M, K):
+ *   dbias_out[e, k] = sum over expert e's rows m of s_m * dY[m, k]  (E, K) fp32
+ *   dprobs_out[m]   = sum over k of dY[m, k] * b_e(m)[k]             (M)    fp32
+ * fused into the pass that quantizes (bf16 dY) or requantizes (rowwise E4M3
+ * wire format, reductions of the exact dequantized values) the gradient.
+ * probs: device fp32 (M), the routing scales s_m; bias_bf16: device (E, K).
+ * Either output may be NULL, not both; d_m_splits is required. Workspace:
+ * mxq_workspace_bytes(MXQ_OP_SCALED_BIAS, M, 0, K, E, 0) bytes. Sums are
+ * fp32 in a fixed order per 128x128 tile, then fp64 over tiles: identical
+ * run to run. Other arguments, flags and errors as mxq_group_quantize /
+ * mxq_requant_colwise; with flags == 0 (and MXQ_DEQUANT_OUT unset) only the
+ * two reductions run. */
+MXQ_API int mxq_group_quantize_scaled_bias(const void* x_bf16, int64_t M, int64_t K, int E,
+                                           const int64_t* d_m_splits, int flags, void* row_data, void* row_scale,
+                                           void* col_data, void* col_scale, const float* probs,
+                                           const void* bias_bf16, float* dbias_out, float* dprobs_out,
+                                           const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes,
+                                           mxq_stream_t stream);
+MXQ_API int mxq_requant_colwise_scaled_bias(const void* row_data, const void* row_scale_compact, int64_t M,
+                                            int64_t K, int E, const int64_t* d_m_splits, int flags, void* col_data,
+                                            void* col_scale, void* row_scale_swizzled_out, const float* probs,
+                                            const void* bias_bf16, float* dbias_out, float* dprobs_out,
+                                            void* dequant_bf16_out, const int32_t* d_noop, int32_t* d_status,
+                                            void* ws, size_t ws_bytes, mxq_stream_t stream);
 
 /* grouped fprop [RQ][DI]: Y[m, :] = X[m, :] . W[e(m)]^T (+ bias[e(m)]),
  * X rowwise (M,K) E4M3 + swizzled rowwise scales; W rowwise (E,N,K) E4M3

@@ -8,12 +8,14 @@ from . import mxq  # noqa: F401
 from .mxq import (  # noqa: F401
     MXQError,
     group_quantize,
+    group_quantize_scaled_bias,
     grouped_dbias,
     grouped_gemm_dgrad,
     grouped_gemm_fprop,
     grouped_gemm_wgrad,
     new_status,
     requant_colwise,
+    requant_colwise_scaled_bias,
     scale_bytes,
     status_read,
     swiglu_bwd,

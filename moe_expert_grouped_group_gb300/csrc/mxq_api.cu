@@ -79,6 +79,8 @@ size_t mxq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int f
         case MXQ_OP_REQUANT_COLWISE: return (size_t)(M / 128) * (size_t)K * sizeof(float);
         case MXQ_OP_GROUPED_DBIAS: return (size_t)(M / 128) * (size_t)N * sizeof(float);
         case MXQ_OP_SWIGLU_BWD_QUANTIZE: return (size_t)(M / 128) * (size_t)(2 * K) * sizeof(float);
+        case MXQ_OP_SCALED_BIAS:  // column-sum partials (M/128, K) + row-dot partials (M, K/128)
+            return 2 * (size_t)(M / 128) * (size_t)K * sizeof(float);
         default: return 0;
     }
 }
@@ -150,6 +152,104 @@ int mxq_requant_colwise(const void* row_data, const void* row_scale_compact, int
     c.swizzle = (flags & MXQ_SWIZZLE) != 0;
     c.noop = d_noop;
     c.status = d_status;
+    cudaError_t e = mxq::run_requant(c, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+// Checks shared by the two scaled-bias entry points; on success fills the
+// workspace split (column-sum partials first, then row-dot partials).
+static int scaled_bias_common(int64_t M, int64_t K, int E, const int64_t* d_m_splits, const float* probs,
+                              const void* bias, float* dbias_out, float* dprobs_out, void* ws, size_t ws_bytes,
+                              float** partials, float** dp_partials) {
+    if (!dbias_out && !dprobs_out) return MXQ_ERR_FLAGS;
+    if (!bias || (M != 0 && !probs)) return MXQ_ERR_NULL;
+    if (int r = check_common(M, K, E, d_m_splits, true)) return r;
+    if (!aligned16(probs) || !aligned16(bias) || !aligned16(dbias_out) || !aligned16(dprobs_out) || !aligned16(ws))
+        return MXQ_ERR_ALIGN;
+    if (M != 0 && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_SCALED_BIAS, M, 0, K, E, 0)))
+        return MXQ_ERR_WORKSPACE;
+    *partials = static_cast<float*>(ws);
+    *dp_partials = ws ? static_cast<float*>(ws) + (M / 128) * K : nullptr;
+    return MXQ_OK;
+}
+
+int mxq_group_quantize_scaled_bias(const void* x_bf16, int64_t M, int64_t K, int E, const int64_t* d_m_splits,
+                                   int flags, void* row_data, void* row_scale, void* col_data, void* col_scale,
+                                   const float* probs, const void* bias_bf16, float* dbias_out, float* dprobs_out,
+                                   const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes,
+                                   mxq_stream_t stream) {
+    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE)) return MXQ_ERR_FLAGS;
+    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE;
+    if (M != 0 && (!x_bf16 || (row && (!row_data || !row_scale)) || (col && (!col_data || !col_scale))))
+        return MXQ_ERR_NULL;
+    float *partials = nullptr, *dp = nullptr;
+    if (int r = scaled_bias_common(M, K, E, d_m_splits, probs, bias_bf16, dbias_out, dprobs_out, ws, ws_bytes,
+                                   &partials, &dp))
+        return r;
+    if (!aligned16(x_bf16) || !aligned16(row_data) || !aligned16(row_scale) || !aligned16(col_data) ||
+        !aligned16(col_scale))
+        return MXQ_ERR_ALIGN;
+    mxq::QuantCall c{};
+    c.x = x_bf16;
+    c.M = M;
+    c.K = K;
+    c.E = E;
+    c.m_splits = d_m_splits;
+    c.row_q = row ? row_data : nullptr;
+    c.row_s = row ? row_scale : nullptr;
+    c.col_q = col ? col_data : nullptr;
+    c.col_s = col ? col_scale : nullptr;
+    c.dbias = dbias_out;
+    c.partials = partials;
+    c.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    c.noop = d_noop;
+    c.status = d_status;
+    c.probs = probs;
+    c.bias = bias_bf16;
+    c.dprobs = dprobs_out;
+    c.dp_partials = dp;
+    cudaError_t e = mxq::run_group_quantize(c, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_requant_colwise_scaled_bias(const void* row_data, const void* row_scale_compact, int64_t M, int64_t K, int E,
+                                    const int64_t* d_m_splits, int flags, void* col_data, void* col_scale,
+                                    void* row_scale_swizzled_out, const float* probs, const void* bias_bf16,
+                                    float* dbias_out, float* dprobs_out, void* dequant_bf16_out,
+                                    const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes,
+                                    mxq_stream_t stream) {
+    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE | MXQ_DEQUANT_OUT)) return MXQ_ERR_FLAGS;
+    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE, deq = flags & MXQ_DEQUANT_OUT;
+    if (M != 0 && (!row_data || !row_scale_compact || (col && (!col_data || !col_scale)) ||
+                   (row && !row_scale_swizzled_out) || (deq && !dequant_bf16_out)))
+        return MXQ_ERR_NULL;
+    float *partials = nullptr, *dp = nullptr;
+    if (int r = scaled_bias_common(M, K, E, d_m_splits, probs, bias_bf16, dbias_out, dprobs_out, ws, ws_bytes,
+                                   &partials, &dp))
+        return r;
+    if (!aligned16(row_data) || !aligned16(row_scale_compact) || !aligned16(col_data) || !aligned16(col_scale) ||
+        !aligned16(row_scale_swizzled_out) || !aligned16(dequant_bf16_out))
+        return MXQ_ERR_ALIGN;
+    mxq::RequantCall c{};
+    c.row_q = row_data;
+    c.row_s_compact = row_scale_compact;
+    c.M = M;
+    c.K = K;
+    c.E = E;
+    c.m_splits = d_m_splits;
+    c.col_q = col ? col_data : nullptr;
+    c.col_s = col ? col_scale : nullptr;
+    c.row_s_swizzled = row ? row_scale_swizzled_out : nullptr;
+    c.dbias = dbias_out;
+    c.partials = partials;
+    c.deq_out = deq ? dequant_bf16_out : nullptr;
+    c.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    c.noop = d_noop;
+    c.status = d_status;
+    c.probs = probs;
+    c.bias = bias_bf16;
+    c.dprobs = dprobs_out;
+    c.dp_partials = dp;
     cudaError_t e = mxq::run_requant(c, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
 }

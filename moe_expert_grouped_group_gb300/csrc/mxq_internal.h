@@ -19,6 +19,13 @@ struct QuantCall {
     int swizzle;
     const int32_t* noop;
     int32_t* status;
+    // scaled bias (probs != nullptr): s_m (M), b_e (E, K) bf16; outputs
+    // dbias = sum s_m dY_m (uses partials) and dprobs (M) from dp_partials
+    // (M, K/128) fp32 of workspace
+    const float* probs;
+    const void* bias;
+    float* dprobs;
+    float* dp_partials;
 };
 
 struct RequantCall {
@@ -34,6 +41,11 @@ struct RequantCall {
     int swizzle;
     const int32_t* noop;
     int32_t* status;
+    // scaled bias, as in QuantCall
+    const float* probs;
+    const void* bias;
+    float* dprobs;
+    float* dp_partials;
 };
 
 // SwiGLU fused with group quantization: forward quantizes h (M, F); backward

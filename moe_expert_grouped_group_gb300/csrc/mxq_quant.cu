@@ -53,6 +53,9 @@ struct TileArgs {
     uint8_t* col_s;
     float* partials;           // (M/128, K) fp32 column sums per tile
     __nv_bfloat16* deq_out;    // requant: bf16 dequantized tensor
+    const float* probs;        // scaled bias: routing scale s_m per row (M)
+    const __nv_bfloat16* bias; // scaled bias: b_e (E, K)
+    float* dp_partials;        // scaled bias: (M, K/128) fp32 per-tile sums of dY[m,:] . b_e
     int swizzle;
     const int32_t* noop;
     int32_t* status;
@@ -113,9 +116,30 @@ __device__ __forceinline__ bool compute_bar_any(bool pred) {
     return r != 0;
 }
 
-template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq>
+// Sum of v[r] over the 32 lanes for every r, by five exchange-and-add rounds
+// that halve the rows each lane keeps: afterwards lane l holds row l's total
+// in v[0]. Fixed order, so the result is the same run to run.
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float send = up ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[0];
+}
+
+// kScaled (scaled bias, with kBias): the column sums weight row m by its
+// routing scale s_m, and each row's dot product with its expert's bias is
+// reduced per tile into dp_partials.
+template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq, bool kScaled = false>
 __global__ void __launch_bounds__(kTileThreads)
     mx_tile_kernel(const __grid_constant__ CUtensorMap tm_in, TileArgs a) {
+    static_assert(!kScaled || kBias, "the scaled-bias reductions ride on the dbias pass");
     using Sh = TileShape<kReq>;
     extern __shared__ uint8_t q_smem_raw[];
     __shared__ __align__(16) uint8_t s_rs[512];
@@ -181,6 +205,17 @@ __global__ void __launch_bounds__(kTileThreads)
         // requant: lane l reads the 4 compact rowwise scale codes of row r0 + l
         uint32_t sw = 0;
         if constexpr (kReq) sw = __ldg(reinterpret_cast<const unsigned int*>(a.src_scale + (r0 + lane) * (K / 32) + kt * 4));
+        // scaled bias: lane l reads s of row r0 + l and b_e of its 4 columns
+        float pw = 0.f, bv[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (kScaled) {
+            pw = __ldg(a.probs + r0 + lane);
+            const int e = expert_of(s_off, a.E, mt * kTile);
+            const uint2 b2 = __ldg(reinterpret_cast<const uint2*>(a.bias + (int64_t)e * K + col));
+            bv[0] = bf16lo(b2.x);
+            bv[1] = bf16hi(b2.x);
+            bv[2] = bf16lo(b2.y);
+            bv[3] = bf16hi(b2.y);
+        }
 
         const bool ok = mbar_wait(full0 + 8 * stage, phase, abort_flag);
         if (compute_bar_any(!ok)) break;
@@ -215,19 +250,36 @@ __global__ void __launch_bounds__(kTileThreads)
         if constexpr (kCol || kBias) {
             uint32_t m[4] = {0, 0, 0, 0};
             float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) {
-                const uint2 u = ld_row(r);
-                if constexpr (!kReq && !kBias) {
-                    m[0] = __vmaxu2(m[0], u.x & 0x7FFF7FFFu);
-                    m[1] = __vmaxu2(m[1], u.y & 0x7FFF7FFFu);
-                } else {
+            if constexpr (kScaled) {
+                float dp[32];  // this lane's 4-column share of each row's dot product with b_e
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
                     float v[4];
-                    vals(r, u, v);
+                    vals(r, ld_row(r), v);
+                    const float s_r = __shfl_sync(0xffffffffu, pw, r);
+                    dp[r] = v[0] * bv[0] + v[1] * bv[1] + v[2] * bv[2] + v[3] * bv[3];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
-                        sum[j] += v[j];
+                        sum[j] += s_r * v[j];
+                    }
+                }
+                a.dp_partials[(r0 + lane) * tilesK + kt] = transpose_reduce32(dp, lane);
+            } else {
+#pragma unroll 8
+                for (int r = 0; r < 32; ++r) {
+                    const uint2 u = ld_row(r);
+                    if constexpr (!kReq && !kBias) {
+                        m[0] = __vmaxu2(m[0], u.x & 0x7FFF7FFFu);
+                        m[1] = __vmaxu2(m[1], u.y & 0x7FFF7FFFu);
+                    } else {
+                        float v[4];
+                        vals(r, u, v);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
+                            sum[j] += v[j];
+                        }
                     }
                 }
             }
@@ -356,6 +408,21 @@ __global__ void __launch_bounds__(256) dbias_finalize_kernel(const float* __rest
     out[(int64_t)e * K + c] = (float)acc;
 }
 
+// Second stage of the routing-scale gradient: ds[m] = sum over the K/128
+// column tiles of row m's partial dot products, in tile order, in fp64.
+__global__ void __launch_bounds__(256) dprobs_finalize_kernel(const float* __restrict__ dp_partials, int64_t M,
+                                                              int64_t tilesK, int E, const int64_t* m_splits,
+                                                              float* __restrict__ out, const int32_t* noop) {
+    __shared__ int64_t s_off[MXQ_MAX_EXPERTS + 1];
+    if (noop && *noop) return;
+    if (load_offsets(m_splits, E, M, s_off)) return;  // reported by the tile kernel
+    const int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (m >= M) return;
+    double acc = 0.0;
+    for (int64_t t = 0; t < tilesK; ++t) acc += (double)dp_partials[m * tilesK + t];
+    out[m] = (float)acc;
+}
+
 static int num_sms() {
     static int n[64] = {0};
     int dev = 0;
@@ -367,22 +434,21 @@ static int num_sms() {
     return v;
 }
 
-template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq>
+template <bool kReq, bool kRow, bool kCol, bool kBias, bool kDeq, bool kScaled = false>
 static cudaError_t launch_tile(const TileArgs& a, cudaStream_t s) {
     using Sh = TileShape<kReq>;
+    auto kern = mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq, kScaled>;
     const int64_t tiles = (a.M / kTile) * (a.K / kTile);
     if (tiles == 0) return cudaSuccess;
     const int smem = Sh::kSmem + (a.E + 1) * 8;
-    const cudaError_t attr = cudaFuncSetAttribute(mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr != cudaSuccess) return attr;
     CUtensorMap tm;
     if (!encode_tmap_2d(&tm, a.src, a.M, a.K, Sh::kInBytes, kTile, kTile, false)) return cudaErrorInvalidValue;
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq>,
-                                                  kTileThreads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTileThreads, smem);
     const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms() * std::max(per_sm, 1));
-    mx_tile_kernel<kReq, kRow, kCol, kBias, kDeq><<<(unsigned)grid, kTileThreads, smem, s>>>(tm, a);
+    kern<<<(unsigned)grid, kTileThreads, smem, s>>>(tm, a);
     return cudaGetLastError();
 }
 
@@ -396,6 +462,24 @@ static cudaError_t launch_finalize(const float* partials, int64_t M, int64_t K, 
 cudaError_t run_dbias_finalize(const float* partials, int64_t M, int64_t K, int E, const int64_t* m_splits,
                                float* out, const int32_t* noop, cudaStream_t s) {
     return launch_finalize(partials, M, K, E, m_splits, out, noop, s);
+}
+
+// After a scaled-bias tile launch: the per-expert scaled column sums and the
+// per-row routing-scale gradients, each finalized only when asked for.
+static cudaError_t finish_scaled(const float* partials, const float* dp_partials, int64_t M, int64_t K, int E,
+                                 const int64_t* m_splits, float* dbias, float* dprobs, const int32_t* noop,
+                                 cudaError_t err, cudaStream_t s) {
+    if (err != cudaSuccess || M == 0) return err;
+    if (dbias) {
+        err = launch_finalize(partials, M, K, E, m_splits, dbias, noop, s);
+        if (err != cudaSuccess) return err;
+    }
+    if (dprobs) {
+        dprobs_finalize_kernel<<<(unsigned)((M + 255) / 256), 256, 0, s>>>(dp_partials, M, K / kTile, E, m_splits,
+                                                                          dprobs, noop);
+        err = cudaGetLastError();
+    }
+    return err;
 }
 
 cudaError_t run_group_quantize(const QuantCall& c, cudaStream_t s) {
@@ -415,6 +499,16 @@ cudaError_t run_group_quantize(const QuantCall& c, cudaStream_t s) {
     a.status = c.status;
     const bool r = c.row_q != nullptr, k = c.col_q != nullptr, b = c.partials != nullptr;
     cudaError_t err;
+    if (c.probs) {
+        a.probs = c.probs;
+        a.bias = static_cast<const __nv_bfloat16*>(c.bias);
+        a.dp_partials = c.dp_partials;
+        if (r && k) err = launch_tile<false, true, true, true, false, true>(a, s);
+        else if (r) err = launch_tile<false, true, false, true, false, true>(a, s);
+        else if (k) err = launch_tile<false, false, true, true, false, true>(a, s);
+        else err = launch_tile<false, false, false, true, false, true>(a, s);
+        return finish_scaled(c.partials, c.dp_partials, c.M, c.K, c.E, c.m_splits, c.dbias, c.dprobs, c.noop, err, s);
+    }
     if (r && k && b) err = launch_tile<false, true, true, true, false>(a, s);
     else if (r && k) err = launch_tile<false, true, true, false, false>(a, s);
     else if (r && b) err = launch_tile<false, true, false, true, false>(a, s);
@@ -446,6 +540,25 @@ cudaError_t run_requant(const RequantCall& c, cudaStream_t s) {
     const bool r = c.row_s_swizzled != nullptr, k = c.col_q != nullptr, b = c.partials != nullptr,
                d = c.deq_out != nullptr;
     cudaError_t err;
+    if (c.probs) {
+        a.probs = c.probs;
+        a.bias = static_cast<const __nv_bfloat16*>(c.bias);
+        a.dp_partials = c.dp_partials;
+#define MXQ_RQS(R, K_, D) \
+    else if (r == R && k == K_ && d == D) err = launch_tile<true, R, K_, true, D, true>(a, s);
+        if (false) err = cudaSuccess;
+        MXQ_RQS(true, true, false)
+        MXQ_RQS(false, true, false)
+        MXQ_RQS(true, false, false)
+        MXQ_RQS(false, false, false)
+        MXQ_RQS(true, true, true)
+        MXQ_RQS(false, true, true)
+        MXQ_RQS(true, false, true)
+        MXQ_RQS(false, false, true)
+#undef MXQ_RQS
+        else err = cudaErrorInvalidValue;
+        return finish_scaled(c.partials, c.dp_partials, c.M, c.K, c.E, c.m_splits, c.dbias, c.dprobs, c.noop, err, s);
+    }
     // The common dispatch shapes get their own instantiation; the rest share
     // the full variant with unused outputs masked by null checks below.
     if (r && k && !b && !d) err = launch_tile<true, true, true, false, false>(a, s);

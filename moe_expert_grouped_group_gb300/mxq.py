@@ -19,14 +19,15 @@ from .build import LIB
 
 ROWWISE, COLWISE, SWIZZLE, DEQUANT_OUT, ACCUMULATE, OUT_BF16 = 1, 2, 4, 8, 16, 32
 OP_GROUP_QUANTIZE, OP_REQUANT_COLWISE, OP_GROUPED_DBIAS = 1, 2, 3
-OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD, OP_SWIGLU_BWD_QUANTIZE = 4, 5, 6, 7
+OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD, OP_SWIGLU_BWD_QUANTIZE, OP_SCALED_BIAS = 4, 5, 6, 7, 8
 STATUS_SPLIT_UNALIGNED, STATUS_SPLIT_NEGATIVE, STATUS_SPLIT_SUM, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
 
 SYMBOLS = [
     "mxq_version", "mxq_scale_bytes", "mxq_workspace_bytes", "mxq_group_quantize", "mxq_requant_colwise",
     "mxq_grouped_dbias", "mxq_grouped_gemm_fprop", "mxq_grouped_gemm_dgrad", "mxq_grouped_gemm_wgrad",
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
-    "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize",
+    "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
+    "mxq_requant_colwise_scaled_bias",
 ]
 
 
@@ -61,6 +62,10 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_swiglu_bwd_quantize.argtypes = [_P, _P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                           _SZ, _P]
     L.mxq_swiglu_bwd.argtypes = [_P, _P, _I64, _I64, _P, _P]
+    L.mxq_group_quantize_scaled_bias.argtypes = [_P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                 _P, _P, _P, _SZ, _P]
+    L.mxq_requant_colwise_scaled_bias.argtypes = [_P, _P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P,
+                                                  _P, _P, _P, _P, _SZ, _P]
     L.mxq_status_read.argtypes = [_P, _P, _P]
     L.mxq_error_string.argtypes = [_INT]
     L.mxq_error_string.restype = ctypes.c_char_p
@@ -189,6 +194,68 @@ def requant_colwise(row_data, row_scale_compact, m_splits, colwise=True, swizzle
         _ptr(o.get("col_scale")), _ptr(o.get("row_scale_swizzled")), _ptr(o.get("dbias")), _ptr(o.get("dequant")),
         _ptr(noop), _ptr(status), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream())
     _check(rc, "mxq_requant_colwise")
+    return o
+
+
+def group_quantize_scaled_bias(x, m_splits, probs, bias, rowwise=True, colwise=True, swizzle=True, dbias=True,
+                               dprobs=True, noop=None, status=None, out=None, workspace=None):
+    """bf16 gradient x (M, K), routing scales probs (M,) fp32, expert biases bias (E, K) bf16 ->
+    dict(row_data, row_scale, col_data, col_scale, dbias = sum s_m x_m per expert, dprobs = x_m . b_e)."""
+    M, K = x.shape
+    m_splits = _splits(m_splits)
+    E = m_splits.numel()
+    dev = x.device
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
+    o = dict(out or {})
+    if rowwise:
+        o.setdefault("row_data", _u8((M, K), dev))
+        o.setdefault("row_scale", _u8(scale_bytes(M, K, False), dev))
+    if colwise:
+        o.setdefault("col_data", _u8((M, K), dev))
+        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+    if dbias:
+        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+    if dprobs:
+        o.setdefault("dprobs", torch.empty((M,), dtype=torch.float32, device=dev))
+    ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SCALED_BIAS, M, 0, K, E)), dev)
+    rc = lib().mxq_group_quantize_scaled_bias(
+        _ptr(x), M, K, E, _ptr(m_splits), flags, _ptr(o.get("row_data")), _ptr(o.get("row_scale")),
+        _ptr(o.get("col_data")), _ptr(o.get("col_scale")), _ptr(probs), _ptr(bias), _ptr(o.get("dbias")),
+        _ptr(o.get("dprobs")), _ptr(noop), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(), _stream())
+    _check(rc, "mxq_group_quantize_scaled_bias")
+    return o
+
+
+def requant_colwise_scaled_bias(row_data, row_scale_compact, m_splits, probs, bias, colwise=True, swizzle=True,
+                                row_scale_swizzled=True, dequant=False, dbias=True, dprobs=True, noop=None,
+                                status=None, out=None, workspace=None):
+    """Rowwise E4M3 gradient (M, K) + compact scales -> requant outputs as requant_colwise, plus the
+    scaled-bias reductions of the dequantized values (dbias, dprobs) as group_quantize_scaled_bias."""
+    M, K = row_data.shape
+    m_splits = _splits(m_splits)
+    E = m_splits.numel()
+    dev = row_data.device
+    flags = ((COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0) | (ROWWISE if row_scale_swizzled else 0)
+             | (DEQUANT_OUT if dequant else 0))
+    o = dict(out or {})
+    if colwise:
+        o.setdefault("col_data", _u8((M, K), dev))
+        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+    if row_scale_swizzled:
+        o.setdefault("row_scale_swizzled", _u8(scale_bytes(M, K, False), dev))
+    if dequant:
+        o.setdefault("dequant", torch.empty((M, K), dtype=torch.bfloat16, device=dev))
+    if dbias:
+        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+    if dprobs:
+        o.setdefault("dprobs", torch.empty((M,), dtype=torch.float32, device=dev))
+    ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SCALED_BIAS, M, 0, K, E)), dev)
+    rc = lib().mxq_requant_colwise_scaled_bias(
+        _ptr(row_data), _ptr(row_scale_compact), M, K, E, _ptr(m_splits), flags, _ptr(o.get("col_data")),
+        _ptr(o.get("col_scale")), _ptr(o.get("row_scale_swizzled")), _ptr(probs), _ptr(bias), _ptr(o.get("dbias")),
+        _ptr(o.get("dprobs")), _ptr(o.get("dequant")), _ptr(noop), _ptr(status), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream())
+    _check(rc, "mxq_requant_colwise_scaled_bias")
     return o
 
 
