@@ -54,9 +54,10 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
-    p.add_argument("--only", choices=["swiglu_quantize"],
-                   help="time only the fused SwiGLU->quantize kernels (forward and backward) on the MLP workload's "
-                        "shapes and print their line (a small footprint for profilers)")
+    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias"],
+                   help="time only one fused kernel family on the MLP workload's shapes and print its line (a "
+                        "small footprint for profilers): the SwiGLU->quantize kernels (forward and backward), or "
+                        "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions")
     return p.parse_args()
 
 
@@ -369,6 +370,58 @@ def time_swiglu_quantize(dev, steps, warmup):
             "l2": "256 MiB buffer written before every forward+backward pair"}
 
 
+def time_scaled_bias(dev, steps, warmup):
+    """Requant of the rowwise-quantized FC2 gradient (83968 x 3072, 64 experts):
+    with the plain fused dbias, and with the scaled-bias reductions (dbias
+    weighted by seeded routing scales, and each row's dot product with its
+    expert's bias)."""
+    import torch
+
+    import moe_expert_grouped_group_gb300 as mxq
+    from synth import WORKLOADS, make_inputs
+
+    w = WORKLOADS[MLP_WORKLOAD]
+    d = make_inputs(w, which=("dy2", "b2"))
+    M, K, E = w.M, w.K, w.E
+    tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    ms = torch.from_numpy(d["m_splits"]).to(dev)
+    wire = mxq.group_quantize(tb(d["dy2"]), ms, rowwise=True, colwise=False, swizzle=False)
+    probs = torch.from_numpy(np.random.default_rng([0, w.wid, 8]).random(M).astype(np.float32)).to(dev)
+    b2 = tb(d["b2"])
+    u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
+    sb = mxq.scale_bytes
+    out = {"col_data": u8((M, K)), "col_scale": u8(sb(M, K, True)), "row_scale_swizzled": u8(sb(M, K, False)),
+           "dbias": torch.empty((E, K), dtype=torch.float32, device=dev),
+           "dprobs": torch.empty((M,), dtype=torch.float32, device=dev)}
+    ws = u8(mxq.workspace_bytes(mxq.mxq.OP_SCALED_BIAS, M, 0, K, E))
+    plain_out = {k: v for k, v in out.items() if k != "dprobs"}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    runs = {
+        "requant_dbias": lambda: mxq.requant_colwise(wire["row_data"], wire["row_scale"], ms, dbias=True,
+                                                     out=plain_out, workspace=ws),
+        "requant_scaled_bias": lambda: mxq.requant_colwise_scaled_bias(wire["row_data"], wire["row_scale"], ms,
+                                                                       probs, b2, out=out, workspace=ws),
+    }
+    res = {"workload": MLP_WORKLOAD, "rows": M, "cols": K, "steps": steps, "warmup": warmup,
+           "l2": "256 MiB buffer written before every launch"}
+    base = M * K * (2 + 3 / 32)  # E4M3 in + colwise out + three scale sets
+    nbytes = {"requant_dbias": base, "requant_scaled_bias": base + M * 4 + E * K * 2}
+    for name, fn in runs.items():
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(warmup + steps):
+            flush.fill_(1)
+            if i >= warmup:
+                ev[i - warmup][0].record()
+            fn()
+            if i >= warmup:
+                ev[i - warmup][1].record()
+        torch.cuda.synchronize()
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+        res[name + "_us"] = us
+        res[name + "_gbs"] = nbytes[name] / (us * 1e-6) / 1e9
+    return res
+
+
 KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
 
 
@@ -583,6 +636,14 @@ def main():
         _, hbm_peak, src = peaks()
         r.update(fwd_frac=r["fwd_gbs"] / hbm_peak, bwd_frac=r["bwd_gbs"] / hbm_peak, hbm_peak_gbs=hbm_peak,
                  peak_source=src)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
+    if args.only == "scaled_bias":
+        r = time_scaled_bias(dev, max(1, args.steps), max(1, args.warmup))
+        _, hbm_peak, src = peaks()
+        r.update({k.replace("_gbs", "_frac"): v / hbm_peak for k, v in list(r.items()) if k.endswith("_gbs")})
+        r.update(hbm_peak_gbs=hbm_peak, peak_source=src)
         if rank == 0:
             print(json.dumps(r), flush=True)
         return

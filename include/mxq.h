@@ -214,6 +214,26 @@ MXQ_API int mxq_grouped_gemm_fprop(const void* x_data, const void* x_scale, cons
                            const int64_t* d_m_splits, void* y_bf16, int32_t* d_status, void* ws,
                            size_t ws_bytes, mxq_stream_t stream);
 
+/* grouped fprop of FC1 with SwiGLU and its quantization in the epilogue
+ * (the fused grouped MLP's FC1 -> activation [FM]; quantization as
+ * mxq_group_quantize [RQ][DI]). x_data (M, K) E4M3 rowwise with swizzled
+ * scales; w1_data (E, 2F, K) E4M3 rowwise (rows [0, F) of each expert are
+ * the gate, [F, 2F) the up projection) with swizzled scales; bias_bf16
+ * (E, 2F) or NULL. Writes:
+ *   y1_bf16 (M, 2F): the FC1 output, bit-identical to mxq_grouped_gemm_fprop
+ *     (saved for the SwiGLU backward);
+ *   h = silu(gate) * up from those bf16 values in the fp32 steps of
+ *     mxq_swiglu_fwd, quantized rowwise (h_row_data (M, F), h_row_scale) and
+ *     colwise (h_col_data (M, F), h_col_scale) exactly as mxq_swiglu_quantize
+ *     would quantize it (flags: MXQ_SWIZZLE selects swizzled scales, else
+ *     compact).
+ * F % 128 == 0, K % 128 == 0. ws may be NULL. */
+MXQ_API int mxq_grouped_gemm_fprop_swiglu(const void* x_data, const void* x_scale, const void* w1_data,
+                                          const void* w1_scale, const void* bias_bf16, int64_t M, int64_t K,
+                                          int64_t F, int E, const int64_t* d_m_splits, int flags, void* y1_bf16,
+                                          void* h_row_data, void* h_row_scale, void* h_col_data, void* h_col_scale,
+                                          int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream);
+
 /* grouped dgrad [RQ][FM]: dX[m, :] = dY[m, :] . W[e(m)], dY rowwise (M,N)
  * + swizzled rowwise scales; W colwise (E,N,K) E4M3 (W's byte order,
  * blocks along N) + per-expert swizzled colwise scales (expert e: logical

@@ -12,6 +12,7 @@ from .mxq import (  # noqa: F401
     grouped_dbias,
     grouped_gemm_dgrad,
     grouped_gemm_fprop,
+    grouped_gemm_fprop_swiglu,
     grouped_gemm_wgrad,
     new_status,
     requant_colwise,

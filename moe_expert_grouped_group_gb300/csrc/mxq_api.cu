@@ -267,7 +267,7 @@ int mxq_grouped_dbias(const void* dy_bf16, int64_t M, int64_t N, int E, const in
 
 static int gemm_common(int mode, const void* a, const void* as, const void* b, const void* bs, const void* bias,
                        int64_t M, int64_t N, int64_t K, int E, const int64_t* m_splits, void* out, int accumulate,
-                       int out_bf16, int32_t* d_status, mxq_stream_t stream) {
+                       int out_bf16, int32_t* d_status, mxq_stream_t stream, const mxq::GemmExtra* extra = nullptr) {
     // With M == 0 the token-major operands (and fprop/dgrad outputs) are empty.
     const bool a_empty_ok = (M == 0), b_empty_ok = (M == 0 && mode == mxq::kWgrad);
     const bool out_empty_ok = (M == 0 && mode != mxq::kWgrad);
@@ -277,8 +277,9 @@ static int gemm_common(int mode, const void* a, const void* as, const void* b, c
     if (int r = check_common(M, K, E, m_splits, true)) return r;
     if (N <= 0 || N % 128 || N > ((int64_t)1 << 31) / 128) return MXQ_ERR_SHAPE;
     if ((int64_t)E * N > ((int64_t)1 << 31) - 256) return MXQ_ERR_SHAPE;
-    if (mode == mxq::kFprop && N % 256) return MXQ_ERR_SHAPE;
-    if (mode != mxq::kFprop && K % 256) return MXQ_ERR_SHAPE;
+    const bool fwd = (mode == mxq::kFprop || mode == mxq::kFpropSwiglu);
+    if (fwd && N % 256) return MXQ_ERR_SHAPE;
+    if (!fwd && K % 256) return MXQ_ERR_SHAPE;
     if (!aligned16(a) || !aligned16(as) || !aligned16(b) || !aligned16(bs) || !aligned16(bias) || !aligned16(out))
         return MXQ_ERR_ALIGN;
     mxq::GemmCall c{};
@@ -297,8 +298,37 @@ static int gemm_common(int mode, const void* a, const void* as, const void* b, c
     c.accumulate = accumulate;
     c.out_bf16 = out_bf16;
     c.status = d_status;
+    if (extra) {
+        c.h_row = extra->h_row;
+        c.h_row_s = extra->h_row_s;
+        c.h_col = extra->h_col;
+        c.h_col_s = extra->h_col_s;
+        c.swizzle = extra->swizzle;
+    }
     cudaError_t e = mxq::run_grouped_gemm(c, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_grouped_gemm_fprop_swiglu(const void* x_data, const void* x_scale, const void* w1_data, const void* w1_scale,
+                                  const void* bias_bf16, int64_t M, int64_t K, int64_t F, int E,
+                                  const int64_t* d_m_splits, int flags, void* y1_bf16, void* h_row_data,
+                                  void* h_row_scale, void* h_col_data, void* h_col_scale, int32_t* d_status,
+                                  void* ws, size_t ws_bytes, mxq_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (flags & ~MXQ_SWIZZLE) return MXQ_ERR_FLAGS;
+    if (F <= 0 || F % 128 || F > ((int64_t)1 << 30)) return MXQ_ERR_SHAPE;
+    if (M != 0 && (!h_row_data || !h_row_scale || !h_col_data || !h_col_scale)) return MXQ_ERR_NULL;
+    if (!aligned16(h_row_data) || !aligned16(h_row_scale) || !aligned16(h_col_data) || !aligned16(h_col_scale))
+        return MXQ_ERR_ALIGN;
+    mxq::GemmExtra x{};
+    x.h_row = h_row_data;
+    x.h_row_s = h_row_scale;
+    x.h_col = h_col_data;
+    x.h_col_s = h_col_scale;
+    x.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    return gemm_common(mxq::kFpropSwiglu, x_data, x_scale, w1_data, w1_scale, bias_bf16, M, 2 * F, K, E, d_m_splits,
+                       y1_bf16, 0, 1, d_status, stream, &x);
 }
 
 int mxq_grouped_gemm_fprop(const void* x_data, const void* x_scale, const void* w_data, const void* w_scale,

@@ -89,6 +89,9 @@ struct Params {
     int accumulate, out_bf16;
     int tma_store;  // 1: outputs leave through TMA bulk-tensor stores of staged boxes
     int32_t* status;
+    // kFpropSwiglu: quantized h (M, N/2) and its scales
+    uint8_t *h_row, *h_row_s, *h_col, *h_col_s;
+    int swizzle;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -173,7 +176,7 @@ struct Sched {
     __device__ void init(int mode_, int64_t M_, int64_t N_, int64_t K_, int E_, const int64_t* off_,
                          const int16_t* order_) {
         mode = mode_; M = M_; N = N_; K = K_; E = E_; off = off_; order = order_;
-        if (mode == kFprop) { tiles_n = N / BN; total = (M / BM) * tiles_n; }
+        if (mode == kFprop || mode == kFpropSwiglu) { tiles_n = N / BN; total = (M / BM) * tiles_n; }
         else if (mode == kDgrad) { tiles_n = K / BN; total = (M / BM) * tiles_n; }
         else { tiles_n = (N / BM) * (K / BN); total = (int64_t)E * tiles_n; }
     }
@@ -189,11 +192,13 @@ struct Sched {
         if (mode != kWgrad) {
             const int64_t mt = t / tiles_n, nt = t % tiles_n;
             T.a_row = mt * BM;
-            T.b_col = nt * BN;
+            // kFpropSwiglu: tile nt covers gate columns [128 nt, +128) and the
+            // matching up columns [N/2 + 128 nt, +128)
+            T.b_col = nt * (mode == kFpropSwiglu ? BN / 2 : BN);
             T.e = expert_of(off, E, T.a_row);
             T.off = off[T.e];
             T.me = off[T.e + 1] - T.off;
-            T.nk = (int)((mode == kFprop ? K : N) / BK);
+            T.nk = (int)((mode == kDgrad ? N : K) / BK);
         } else {
             const int64_t ei = t / tiles_n, r = t % tiles_n;
             const int64_t kt = K / BN;
@@ -208,6 +213,169 @@ struct Sched {
     }
 };
 
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b2);
+}
+
+// Epilogue of the SwiGLU-fused FC1 fprop (kFpropSwiglu) for one tile: the
+// accumulator holds gate columns [T.b_col, +128) in TMEM columns 0..127 and
+// the matching up columns in 128..255. Warp (q, half) takes rows 32q..32q+31
+// (lane = row) and the 64 columns T.b_col + 64 half + [0, 64) of both halves.
+// It writes y1 = bf16(acc + bias) as the plain fprop epilogue does (the
+// saved FC1 output), then h = silu(g) * u from those bf16 values in the fp32
+// steps of mxq_common.cuh, and quantizes h as group_quantize does: rowwise
+// over the lane's two 32-column blocks, colwise over the warp's 32 rows (a
+// byte-wise max of exponents across the lanes), E4M3 by the same cast.
+__device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile& T, uint32_t tmem, int q, int half,
+                                                     int lane, uint8_t* epi_buf, uint32_t acc_empty,
+                                                     const CUtensorMap* tmOut) {
+    const int64_t F = p.N / 2;
+    uint32_t r[BN / 2];
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + 64 * half;
+    TMEM_LD32(tq + 0, (r + 0));     // gate
+    TMEM_LD32(tq + 32, (r + 32));
+    TMEM_LD32(tq + 128, (r + 64));  // up
+    TMEM_LD32(tq + 160, (r + 96));
+    tmem_wait_ld();
+    fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(acc_empty);  // the MMA warp may start the next tile
+
+    const int64_t f0 = T.b_col + 64 * half;  // first gate (and h) column of this warp
+    const int64_t row = T.a_row + q * 32 + lane;
+
+    // y1 = bf16(acc + bias): y[0, 32) gate pairs, y[32, 64) up pairs
+    uint32_t y[64];
+#pragma unroll
+    for (int hp = 0; hp < 2; ++hp) {
+        const __nv_bfloat16* bias = p.bias ? p.bias + (int64_t)T.e * p.N + hp * F + f0 : nullptr;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[64 * hp + 8 * v + j]);
+            if (bias) {
+                const uint4 bw = __ldg(reinterpret_cast<const uint4*>(bias) + v);
+                const uint32_t ws[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    f[2 * j] += __uint_as_float(ws[j] << 16);
+                    f[2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) y[32 * hp + 4 * v + j] = bf16x2_bits(f[2 * j], f[2 * j + 1]);
+        }
+    }
+    // y1 through four staged 32x32 boxes: gate f0, f0+32; up F+f0, F+f0+32
+    const int out_row0 = (int)(T.a_row + q * 32);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(epi_buf + lane * 64);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            dst[v] = make_uint4(y[16 * b + 4 * v], y[16 * b + 4 * v + 1], y[16 * b + 4 * v + 2], y[16 * b + 4 * v + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+            const int col = (int)(b < 2 ? f0 + 32 * b : F + f0 + 32 * (b - 2));
+            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                             (uint64_t)tmOut),
+                         "r"(col), "r"(out_row0), "r"(smem_u32(epi_buf))
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+    }
+
+    // h = silu(g) * u, rounded to bf16
+    uint32_t hw[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        hw[i] = bf16x2_bits(swiglu_h(bf16lo(y[i]), bf16lo(y[32 + i])), swiglu_h(bf16hi(y[i]), bf16hi(y[32 + i])));
+
+    // rowwise: two 32-column blocks per lane
+    uint8_t* hrow = p.h_row + row * F + f0;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = __vmaxu2(m, hw[16 * b + i] & 0x7FFF7FFFu);
+        const uint32_t code = (uint32_t)max((int)(max(m & 0xFFFFu, m >> 16) >> 7) - 8, 0);
+        const float inv = inv_scale_from_code(code);
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t w0 = hw[16 * b + 2 * k], w1 = hw[16 * b + 2 * k + 1];
+            o[k] = cvt_e4m3x2(bf16lo(w0) * inv, bf16hi(w0) * inv) | (cvt_e4m3x2(bf16lo(w1) * inv, bf16hi(w1) * inv) << 16);
+        }
+        uint4* d = reinterpret_cast<uint4*>(hrow + 32 * b);
+        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        const int64_t c = (f0 + 32 * b) / 32;  // 32-column block index of h
+        if (p.swizzle)
+            p.h_row_s[((row / 128) * (F / 128) + c / 4) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + c % 4] =
+                (uint8_t)code;
+        else
+            p.h_row_s[row * (F / 32) + c] = (uint8_t)code;
+    }
+
+    // colwise: per column the largest exponent over the warp's 32 rows
+    uint32_t e4[16];  // four columns per word, one byte each
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t a = hw[2 * i], b2 = hw[2 * i + 1];
+        e4[i] = ((a >> 7) & 0xFFu) | (((a >> 23) & 0xFFu) << 8) | (((b2 >> 7) & 0xFFu) << 16) |
+                (((b2 >> 23) & 0xFFu) << 24);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) e4[i] = __vmaxu4(e4[i], __shfl_xor_sync(0xffffffffu, e4[i], off));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) e4[i] = __vsub4(__vmaxu4(e4[i], 0x08080808u), 0x08080808u);  // max(e - 8, 0)
+    uint8_t* hcol = p.h_col + row * F + f0;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t cw = e4[4 * v + k];
+            const uint32_t w0 = hw[8 * v + 2 * k], w1 = hw[8 * v + 2 * k + 1];
+            o[k] = cvt_e4m3x2(bf16lo(w0) * inv_scale_from_code(cw & 0xFFu),
+                              bf16hi(w0) * inv_scale_from_code((cw >> 8) & 0xFFu)) |
+                   (cvt_e4m3x2(bf16lo(w1) * inv_scale_from_code((cw >> 16) & 0xFFu),
+                               bf16hi(w1) * inv_scale_from_code(cw >> 24))
+                    << 16);
+        }
+        *reinterpret_cast<uint4*>(hcol + 16 * v) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    // colwise scale bytes of this 32-row block: lane l < 16 writes columns f0 + 4l .. +3
+    uint32_t mine = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mine = (lane == i) ? e4[i] : mine;
+    if (lane < 16) {
+        const int64_t k0 = f0 + 4 * lane;
+        const int64_t rb0 = T.a_row + 32 * q;  // first row of the block
+        if (p.swizzle) {
+            // per expert: logical (F, m_e/32) at byte F * off_e / 32
+            const int64_t i = (rb0 - T.off) / 32, C4 = T.me / 128;
+            uint8_t* base = p.h_col_s + F * T.off / 32;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t k = k0 + j;
+                base[((k / 128) * C4 + i / 4) * 512 + (k % 32) * 16 + ((k % 128) / 32) * 4 + i % 4] =
+                    (uint8_t)(mine >> (8 * j));
+            }
+        } else {
+            *reinterpret_cast<uint32_t*>(p.h_col_s + (rb0 / 32) * F + k0) = mine;
+        }
+    }
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, Params p) {
@@ -224,7 +392,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         report_status(p.status, bad);
         return;
     }
-    if (p.mode == kWgrad) {
+    if (kMode == kWgrad) {
         // rank experts by token count, heaviest first (ties: lower index first)
         for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
             const int64_t me = s_off[e + 1] - s_off[e];
@@ -267,10 +435,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = s_tmem;
 
     Sched S;
-    S.init(p.mode, p.M, p.N, p.K, p.E, s_off, s_order);
+    S.init(kMode, p.M, p.N, p.K, p.E, s_off, s_order);
     const int ncta = gridDim.x, cta = blockIdx.x;
-    const uint32_t a_mn = (p.mode == kWgrad) ? 1u : 0u;
-    const uint32_t b_mn = (p.mode == kFprop) ? 0u : 1u;
+    constexpr bool kFwd = (kMode == kFprop || kMode == kFpropSwiglu);
+    const uint32_t a_mn = (kMode == kWgrad) ? 1u : 0u;
+    const uint32_t b_mn = kFwd ? 0u : 1u;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -284,14 +453,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // 128-deep K block then advances them by fixed strides.
                 int ax, ay, bx, by, adx, ady, bdx, bdy;
                 const uint8_t *sfa, *sfb0, *sfb1;  // atoms of K block 0; +512 B per block
-                if (p.mode == kFprop) {
+                if (kFwd) {
                     const int64_t kbs = p.K / BK, wrow = (int64_t)T.e * p.N + T.b_col;
                     ax = 0; ay = (int)T.a_row; adx = BK; ady = 0;
                     bx = 0; by = (int)wrow; bdx = BK; bdy = 0;
                     sfa = p.sfa + (T.a_row / 128) * kbs * 512;
                     sfb0 = p.sfb + (wrow / 128) * kbs * 512;
-                    sfb1 = sfb0 + kbs * 512;
-                } else if (p.mode == kDgrad) {
+                    // second B box: the next 128 rows, or (SwiGLU) the up rows F further
+                    sfb1 = sfb0 + (kMode == kFpropSwiglu ? (p.N / 2) / 128 : 1) * kbs * 512;
+                } else if (kMode == kDgrad) {
                     const int64_t kbs = p.N / BK;
                     const uint8_t* wb = p.sfb + (int64_t)T.e * p.K * (p.N / 32);
                     ax = 0; ay = (int)T.a_row; adx = BK; ady = 0;
@@ -310,7 +480,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     sfb1 = sfb0 + kbs * 512;
                 }
                 // the second B box: 128 rows further (K-major B) or 128 columns further (MN-major B)
-                const int b2x = (p.mode == kFprop) ? 0 : 128, b2y = (p.mode == kFprop) ? 128 : 0;
+                const int b2x = kFwd ? 0 : 128, b2y = kFwd ? (kMode == kFpropSwiglu ? (int)(p.N / 2) : 128) : 0;
                 for (int kb = 0; kb < T.nk; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) goto done_producer;
                     const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES);
@@ -395,10 +565,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (!ok || *abort_flag) break;
             fence_after();
+            if constexpr (kMode == kFpropSwiglu) {
+                swiglu_tile_epilogue(p, T, tmem, q, half, lane, epi_buf, acc_empty, &tmOut);
+                aphase ^= 1;
+                continue;
+            }
             // Pull this warp's 32 x 128 slice of the accumulator into registers,
             // then hand the accumulator back to the MMA warp before storing.
             uint32_t r[BN / 2];
-            const bool zero = (p.mode == kWgrad && T.nk == 0);
+            const bool zero = (kMode == kWgrad && T.nk == 0);
             if (!zero) {
                 const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + col0;
                 TMEM_LD32(tbase + 0, (r + 0));
@@ -418,11 +593,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (p.tma_store) {
                 // Stage 32-row boxes in this warp's buffer and write each with one
                 // TMA store: a box is 32 columns (bf16) or 16 columns (fp32).
-                const bool f32 = (p.mode == kWgrad && !p.out_bf16);
+                const bool f32 = (kMode == kWgrad && !p.out_bf16);
                 const int box_cols = f32 ? 16 : 32;
-                const int out_row0 = (int)((p.mode == kWgrad ? (int64_t)T.e * p.N : 0) + T.a_row + q * 32);
+                const int out_row0 = (int)((kMode == kWgrad ? (int64_t)T.e * p.N : 0) + T.a_row + q * 32);
                 const __nv_bfloat16* bias =
-                    (p.mode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col + col0 : nullptr;
+                    (kMode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col + col0 : nullptr;
 #pragma unroll
                 for (int c = 0; c < BN / 2; c += 16) {
                     if (!f32 && (c & 31)) continue;
@@ -470,11 +645,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     (void)box_cols;
                 }
-            } else if (p.mode != kWgrad) {
-                const int64_t ldo = (p.mode == kFprop) ? p.N : p.K;
+            } else if (kMode != kWgrad) {
+                const int64_t ldo = (kMode == kFprop) ? p.N : p.K;
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + row * ldo + T.b_col + col0;
                 const __nv_bfloat16* bias =
-                    (p.mode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col + col0 : nullptr;
+                    (kMode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.b_col + col0 : nullptr;
 #pragma unroll
                 for (int c = 0; c < BN / 2; c += 8) {
                     float f[8];
@@ -612,12 +787,23 @@ static int sm_count() {
 
 cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     using namespace gemm;
-    const cudaError_t attr_err =
-        cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MXQ_MAX_EXPERTS));
+    cudaError_t attr_err;
+    if (c.mode == kFpropSwiglu)
+        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kFpropSwiglu>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MXQ_MAX_EXPERTS));
+    else if (c.mode == kFprop)
+        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kFprop>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes(MXQ_MAX_EXPERTS));
+    else if (c.mode == kDgrad)
+        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kDgrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes(MXQ_MAX_EXPERTS));
+    else
+        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kWgrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes(MXQ_MAX_EXPERTS));
     if (attr_err != cudaSuccess) return attr_err;
 
     int64_t tiles;
-    if (c.mode == kFprop) tiles = (c.M / BM) * (c.N / BN);
+    if (c.mode == kFprop || c.mode == kFpropSwiglu) tiles = (c.M / BM) * (c.N / BN);
     else if (c.mode == kDgrad) tiles = (c.M / BM) * (c.K / BN);
     else tiles = (int64_t)c.E * (c.N / BM) * (c.K / BN);
     if (tiles == 0) return cudaSuccess;
@@ -629,7 +815,7 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
 
     CUtensorMap ta, tb;
     bool ok;
-    if (c.mode == kFprop) {
+    if (c.mode == kFprop || c.mode == kFpropSwiglu) {
         ok = make_map(&ta, c.a_data, c.M, c.K) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
     } else if (c.mode == kDgrad) {
         ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
@@ -643,7 +829,7 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     memset(&to, 0, sizeof(to));
     const int tma_store = !c.accumulate;
     if (tma_store) {
-        if (c.mode == kFprop) ok = encode_tmap_2d(&to, c.out, c.M, c.N, 2, 32, 32, false);
+        if (c.mode == kFprop || c.mode == kFpropSwiglu) ok = encode_tmap_2d(&to, c.out, c.M, c.N, 2, 32, 32, false);
         else if (c.mode == kDgrad) ok = encode_tmap_2d(&to, c.out, c.M, c.K, 2, 32, 32, false);
         else if (c.out_bf16) ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 2, 32, 32, false);
         else ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 4, 16, 32, false);
@@ -665,9 +851,18 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     p.out_bf16 = c.out_bf16;
     p.tma_store = tma_store;
     p.status = c.status;
+    p.h_row = static_cast<uint8_t*>(c.h_row);
+    p.h_row_s = static_cast<uint8_t*>(c.h_row_s);
+    p.h_col = static_cast<uint8_t*>(c.h_col);
+    p.h_col_s = static_cast<uint8_t*>(c.h_col_s);
+    p.swizzle = c.swizzle;
 
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
-    grouped_gemm_kernel<<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
+    if (c.mode == kFpropSwiglu)
+        grouped_gemm_kernel<kFpropSwiglu><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
+    else if (c.mode == kFprop) grouped_gemm_kernel<kFprop><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
+    else if (c.mode == kDgrad) grouped_gemm_kernel<kDgrad><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
+    else grouped_gemm_kernel<kWgrad><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
     return cudaGetLastError();
 }
 

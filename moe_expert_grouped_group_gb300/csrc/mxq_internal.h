@@ -66,7 +66,9 @@ struct SwigluQuantCall {
     int32_t* status;
 };
 
-enum GemmMode { kFprop = 0, kDgrad = 1, kWgrad = 2 };
+// kFpropSwiglu: FC1 fprop of a SwiGLU MLP (N = 2F) whose epilogue also
+// applies SwiGLU to the bf16 output and quantizes h (rowwise + colwise).
+enum GemmMode { kFprop = 0, kDgrad = 1, kWgrad = 2, kFpropSwiglu = 3 };
 
 struct GemmCall {
     int mode;
@@ -78,6 +80,15 @@ struct GemmCall {
     void* out;
     int accumulate, out_bf16;  // wgrad only
     int32_t* status;
+    // kFpropSwiglu: h = silu(gate) * up quantized to (M, N/2) codes and scales
+    void *h_row, *h_row_s, *h_col, *h_col_s;
+    int swizzle;
+};
+
+// The extra outputs of kFpropSwiglu, as passed through the C ABI.
+struct GemmExtra {
+    void *h_row, *h_row_s, *h_col, *h_col_s;
+    int swizzle;
 };
 
 // Encodes a 2-D row-major tensor map (rows x cols elements of elem_bytes)

@@ -27,7 +27,7 @@ SYMBOLS = [
     "mxq_grouped_dbias", "mxq_grouped_gemm_fprop", "mxq_grouped_gemm_dgrad", "mxq_grouped_gemm_wgrad",
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
-    "mxq_requant_colwise_scaled_bias",
+    "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu",
 ]
 
 
@@ -53,6 +53,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_requant_colwise.argtypes = [_P, _P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_dbias.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_fprop.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_gemm_fprop_swiglu.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P,
+                                                _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_wgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_dbias_noalloc.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P]
@@ -281,6 +283,30 @@ def grouped_gemm_fprop(x_data, x_scale, w_data, w_scale, m_splits, bias=None, st
                                       E, _ptr(m_splits), _ptr(out), _ptr(status), None, 0, _stream())
     _check(rc, "mxq_grouped_gemm_fprop")
     return out
+
+
+def grouped_gemm_fprop_swiglu(x_data, x_scale, w1_data, w1_scale, m_splits, bias=None, swizzle=True, status=None,
+                              out=None):
+    """FC1 of a SwiGLU MLP with the activation and its quantization in the GEMM epilogue.
+    x_data (M, K) u8, w1_data (E, 2F, K) u8 ([gate | up] rows), swizzled scales ->
+    dict(y1 (M, 2F) bf16, row_data, row_scale, col_data, col_scale of h (M, F))."""
+    M, K = x_data.shape
+    E, N2, _ = w1_data.shape
+    F = N2 // 2
+    m_splits = _splits(m_splits)
+    dev = x_data.device
+    o = dict(out or {})
+    o.setdefault("y1", torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev))
+    o.setdefault("row_data", _u8((M, F), dev))
+    o.setdefault("row_scale", _u8(scale_bytes(M, F, False), dev))
+    o.setdefault("col_data", _u8((M, F), dev))
+    o.setdefault("col_scale", _u8(scale_bytes(M, F, True), dev))
+    rc = lib().mxq_grouped_gemm_fprop_swiglu(
+        _ptr(x_data), _ptr(x_scale), _ptr(w1_data), _ptr(w1_scale), _ptr(bias), M, K, F, E, _ptr(m_splits),
+        SWIZZLE if swizzle else 0, _ptr(o["y1"]), _ptr(o["row_data"]), _ptr(o["row_scale"]), _ptr(o["col_data"]),
+        _ptr(o["col_scale"]), _ptr(status), None, 0, _stream())
+    _check(rc, "mxq_grouped_gemm_fprop_swiglu")
+    return o
 
 
 def grouped_gemm_dgrad(dy_data, dy_scale, w_col_data, w_col_scale, m_splits, status=None, out=None):
