@@ -126,7 +126,8 @@ enum {
     MXQ_OP_GEMM_DGRAD = 5,
     MXQ_OP_GEMM_WGRAD = 6,
     MXQ_OP_SWIGLU_BWD_QUANTIZE = 7,
-    MXQ_OP_SCALED_BIAS = 8
+    MXQ_OP_SCALED_BIAS = 8,
+    MXQ_OP_GEMM_DGRAD_SWIGLU = 9
 };
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -242,6 +243,27 @@ MXQ_API int mxq_grouped_gemm_dgrad(const void* dy_data, const void* dy_scale, co
                            const void* w_col_scale, int64_t M, int64_t N, int64_t K, int E,
                            const int64_t* d_m_splits, void* dx_bf16, int32_t* d_status, void* ws,
                            size_t ws_bytes, mxq_stream_t stream);
+
+/* grouped dgrad of FC2 with the SwiGLU backward and the quantization of its
+ * result in the epilogue (the fused grouped MLP's activation backward [FM];
+ * quantization and dbias as mxq_group_quantize [RQ][DI]). dh = dY2 . W2_e
+ * (dy_data (M, N) rowwise with swizzled scales, w_col_data (E, N, F)
+ * colwise) never leaves the chip: it is rounded to bf16 as
+ * mxq_grouped_gemm_dgrad would write it and, with the saved FC1 output
+ * y1_bf16 (M, 2F) = [g | u], turned into dY1 = [dg | du] (M, 2F) in the fp32
+ * steps of mxq_swiglu_bwd, rounded to bf16 and quantized rowwise
+ * (dy1_row_*) and colwise (dy1_col_*) exactly as mxq_swiglu_bwd_quantize
+ * would quantize it (flags: MXQ_SWIZZLE, else compact scales).
+ * dbias_out (E, 2F) fp32 or NULL: per-expert column sums of dY1 (fp32 per 32
+ * rows in a fixed order, fp64 over blocks; needs ws of
+ * mxq_workspace_bytes(MXQ_OP_GEMM_DGRAD_SWIGLU, M, N, F, E, 0) bytes).
+ * F % 256 == 0, N % 128 == 0. */
+MXQ_API int mxq_grouped_gemm_dgrad_swiglu(const void* dy_data, const void* dy_scale, const void* w_col_data,
+                                          const void* w_col_scale, const void* y1_bf16, int64_t M, int64_t N,
+                                          int64_t F, int E, const int64_t* d_m_splits, int flags,
+                                          void* dy1_row_data, void* dy1_row_scale, void* dy1_col_data,
+                                          void* dy1_col_scale, float* dbias_out, int32_t* d_status, void* ws,
+                                          size_t ws_bytes, mxq_stream_t stream);
 
 /* grouped wgrad [RQ][FM]: dW[e] = dY_e^T . X_e over expert e's tokens,
  * from the colwise copies only: dY colwise (M,N) + per-expert swizzled

@@ -11,6 +11,7 @@ from .mxq import (  # noqa: F401
     group_quantize_scaled_bias,
     grouped_dbias,
     grouped_gemm_dgrad,
+    grouped_gemm_dgrad_swiglu,
     grouped_gemm_fprop,
     grouped_gemm_fprop_swiglu,
     grouped_gemm_wgrad,

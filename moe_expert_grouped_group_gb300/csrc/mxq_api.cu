@@ -81,6 +81,8 @@ size_t mxq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int f
         case MXQ_OP_SWIGLU_BWD_QUANTIZE: return (size_t)(M / 128) * (size_t)(2 * K) * sizeof(float);
         case MXQ_OP_SCALED_BIAS:  // column-sum partials (M/128, K) + row-dot partials (M, K/128)
             return 2 * (size_t)(M / 128) * (size_t)K * sizeof(float);
+        case MXQ_OP_GEMM_DGRAD_SWIGLU:  // dY1 column sums per 32 rows: (M/32, 2K)
+            return (size_t)(M / 32) * (size_t)(2 * K) * sizeof(float);
         default: return 0;
     }
 }
@@ -270,7 +272,7 @@ static int gemm_common(int mode, const void* a, const void* as, const void* b, c
                        int out_bf16, int32_t* d_status, mxq_stream_t stream, const mxq::GemmExtra* extra = nullptr) {
     // With M == 0 the token-major operands (and fprop/dgrad outputs) are empty.
     const bool a_empty_ok = (M == 0), b_empty_ok = (M == 0 && mode == mxq::kWgrad);
-    const bool out_empty_ok = (M == 0 && mode != mxq::kWgrad);
+    const bool out_empty_ok = (M == 0 && mode != mxq::kWgrad) || mode == mxq::kDgradSwiglu;
     if ((!a && !a_empty_ok) || (!as && !a_empty_ok) || (!b && !b_empty_ok) || (!bs && !b_empty_ok) ||
         (!out && !out_empty_ok))
         return MXQ_ERR_NULL;
@@ -299,11 +301,13 @@ static int gemm_common(int mode, const void* a, const void* as, const void* b, c
     c.out_bf16 = out_bf16;
     c.status = d_status;
     if (extra) {
-        c.h_row = extra->h_row;
-        c.h_row_s = extra->h_row_s;
-        c.h_col = extra->h_col;
-        c.h_col_s = extra->h_col_s;
+        c.q_row = extra->q_row;
+        c.q_row_s = extra->q_row_s;
+        c.q_col = extra->q_col;
+        c.q_col_s = extra->q_col_s;
         c.swizzle = extra->swizzle;
+        c.y1 = extra->y1;
+        c.dbias_part = extra->dbias_part;
     }
     cudaError_t e = mxq::run_grouped_gemm(c, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
@@ -322,13 +326,44 @@ int mxq_grouped_gemm_fprop_swiglu(const void* x_data, const void* x_scale, const
     if (!aligned16(h_row_data) || !aligned16(h_row_scale) || !aligned16(h_col_data) || !aligned16(h_col_scale))
         return MXQ_ERR_ALIGN;
     mxq::GemmExtra x{};
-    x.h_row = h_row_data;
-    x.h_row_s = h_row_scale;
-    x.h_col = h_col_data;
-    x.h_col_s = h_col_scale;
+    x.q_row = h_row_data;
+    x.q_row_s = h_row_scale;
+    x.q_col = h_col_data;
+    x.q_col_s = h_col_scale;
     x.swizzle = (flags & MXQ_SWIZZLE) != 0;
     return gemm_common(mxq::kFpropSwiglu, x_data, x_scale, w1_data, w1_scale, bias_bf16, M, 2 * F, K, E, d_m_splits,
                        y1_bf16, 0, 1, d_status, stream, &x);
+}
+
+int mxq_grouped_gemm_dgrad_swiglu(const void* dy_data, const void* dy_scale, const void* w_col_data,
+                                  const void* w_col_scale, const void* y1_bf16, int64_t M, int64_t N, int64_t F,
+                                  int E, const int64_t* d_m_splits, int flags, void* dy1_row_data,
+                                  void* dy1_row_scale, void* dy1_col_data, void* dy1_col_scale, float* dbias_out,
+                                  int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
+    if (flags & ~MXQ_SWIZZLE) return MXQ_ERR_FLAGS;
+    if (F <= 0 || F % 256) return MXQ_ERR_SHAPE;
+    if (M != 0 && (!y1_bf16 || !dy1_row_data || !dy1_row_scale || !dy1_col_data || !dy1_col_scale))
+        return MXQ_ERR_NULL;
+    if (!aligned16(y1_bf16) || !aligned16(dy1_row_data) || !aligned16(dy1_row_scale) || !aligned16(dy1_col_data) ||
+        !aligned16(dy1_col_scale) || !aligned16(dbias_out) || !aligned16(ws))
+        return MXQ_ERR_ALIGN;
+    if (dbias_out && M != 0 && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GEMM_DGRAD_SWIGLU, M, N, F, E, 0)))
+        return MXQ_ERR_WORKSPACE;
+    mxq::GemmExtra x{};
+    x.q_row = dy1_row_data;
+    x.q_row_s = dy1_row_scale;
+    x.q_col = dy1_col_data;
+    x.q_col_s = dy1_col_scale;
+    x.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    x.y1 = y1_bf16;
+    x.dbias_part = dbias_out ? static_cast<float*>(ws) : nullptr;
+    const int r = gemm_common(mxq::kDgradSwiglu, dy_data, dy_scale, w_col_data, w_col_scale, nullptr, M, N, F, E,
+                              d_m_splits, nullptr, 0, 1, d_status, stream, &x);
+    if (r != MXQ_OK || !dbias_out) return r;
+    cudaError_t e = M == 0 ? cudaMemsetAsync(dbias_out, 0, (size_t)E * 2 * F * sizeof(float), (cudaStream_t)stream)
+                           : mxq::run_dbias_finalize(static_cast<float*>(ws), M, 2 * F, E, d_m_splits, dbias_out,
+                                                     nullptr, (cudaStream_t)stream, 32);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
 }
 
 int mxq_grouped_gemm_fprop(const void* x_data, const void* x_scale, const void* w_data, const void* w_scale,

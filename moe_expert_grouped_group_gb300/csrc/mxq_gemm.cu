@@ -89,9 +89,11 @@ struct Params {
     int accumulate, out_bf16;
     int tma_store;  // 1: outputs leave through TMA bulk-tensor stores of staged boxes
     int32_t* status;
-    // kFpropSwiglu: quantized h (M, N/2) and its scales
-    uint8_t *h_row, *h_row_s, *h_col, *h_col_s;
+    // kFpropSwiglu: quantized h (M, N/2); kDgradSwiglu: quantized dY1 (M, 2K)
+    uint8_t *q_row, *q_row_s, *q_col, *q_col_s;
     int swizzle;
+    const __nv_bfloat16* y1;  // kDgradSwiglu: saved FC1 output (M, 2K)
+    float* dbias_part;        // kDgradSwiglu: (M/32, 2K) per-32-row column sums, or null
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -177,7 +179,7 @@ struct Sched {
                          const int16_t* order_) {
         mode = mode_; M = M_; N = N_; K = K_; E = E_; off = off_; order = order_;
         if (mode == kFprop || mode == kFpropSwiglu) { tiles_n = N / BN; total = (M / BM) * tiles_n; }
-        else if (mode == kDgrad) { tiles_n = K / BN; total = (M / BM) * tiles_n; }
+        else if (mode == kDgrad || mode == kDgradSwiglu) { tiles_n = K / BN; total = (M / BM) * tiles_n; }
         else { tiles_n = (N / BM) * (K / BN); total = (int64_t)E * tiles_n; }
     }
     // i-th tile of CTA `cta` among `ncta` (serpentine deal over the ordered list)
@@ -198,7 +200,7 @@ struct Sched {
             T.e = expert_of(off, E, T.a_row);
             T.off = off[T.e];
             T.me = off[T.e + 1] - T.off;
-            T.nk = (int)((mode == kDgrad ? N : K) / BK);
+            T.nk = (int)((mode == kDgrad || mode == kDgradSwiglu ? N : K) / BK);
         } else {
             const int64_t ei = t / tiles_n, r = t % tiles_n;
             const int64_t kt = K / BN;
@@ -216,6 +218,167 @@ struct Sched {
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&b2);
+}
+
+// Sum of v[i] over the 32 lanes for every i: five exchange-and-add rounds
+// halve the values each lane keeps; afterwards lane l holds i = l in v[0].
+// Fixed order, so the sums are the same run to run.
+__device__ __forceinline__ float lane_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float send = up ? v[i] : v[i + n / 2];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[0];
+}
+
+// MXFP8-quantize one 32-column block of a warp's 32 rows of an (M, W) bf16
+// tensor, as group_quantize does: w holds this lane's row (lane = row
+// rb0 + lane) at columns col0 .. col0+31 as bf16 pairs. Rowwise: one block
+// per lane. Colwise: per column the largest exponent across the lanes (the
+// 32-row block rb0 .. rb0+31, inside expert T.e). Codes go to p.q_row /
+// p.q_col, E8M0 scales to p.q_row_s / p.q_col_s (swizzled per p.swizzle).
+// With p.dbias_part, the block's 32 column sums go to row rb0/32 of it.
+__device__ __forceinline__ void quant_block32(const uint32_t (&w)[16], const Params& p, const Tile& T, int64_t W,
+                                              int64_t rb0, int64_t col0, int lane) {
+    const int64_t row = rb0 + lane;
+    // rowwise
+    {
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+        const uint32_t code = (uint32_t)max((int)(max(m & 0xFFFFu, m >> 16) >> 7) - 8, 0);
+        const float inv = inv_scale_from_code(code);
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t w0 = w[2 * k], w1 = w[2 * k + 1];
+            o[k] = cvt_e4m3x2(bf16lo(w0) * inv, bf16hi(w0) * inv) | (cvt_e4m3x2(bf16lo(w1) * inv, bf16hi(w1) * inv) << 16);
+        }
+        uint4* d = reinterpret_cast<uint4*>(p.q_row + row * W + col0);
+        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        const int64_t c = col0 / 32;
+        if (p.swizzle)
+            p.q_row_s[((row / 128) * (W / 128) + c / 4) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + c % 4] =
+                (uint8_t)code;
+        else
+            p.q_row_s[row * (W / 32) + c] = (uint8_t)code;
+    }
+    // colwise
+    uint32_t e4[8];  // four columns per word, one exponent byte each
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t a = w[2 * i], b = w[2 * i + 1];
+        e4[i] = ((a >> 7) & 0xFFu) | (((a >> 23) & 0xFFu) << 8) | (((b >> 7) & 0xFFu) << 16) | (((b >> 23) & 0xFFu) << 24);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e4[i] = __vmaxu4(e4[i], __shfl_xor_sync(0xffffffffu, e4[i], off));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e4[i] = __vsub4(__vmaxu4(e4[i], 0x08080808u), 0x08080808u);  // max(e - 8, 0)
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t cw = e4[4 * v + k];
+            const uint32_t w0 = w[8 * v + 2 * k], w1 = w[8 * v + 2 * k + 1];
+            o[k] = cvt_e4m3x2(bf16lo(w0) * inv_scale_from_code(cw & 0xFFu),
+                              bf16hi(w0) * inv_scale_from_code((cw >> 8) & 0xFFu)) |
+                   (cvt_e4m3x2(bf16lo(w1) * inv_scale_from_code((cw >> 16) & 0xFFu),
+                               bf16hi(w1) * inv_scale_from_code(cw >> 24))
+                    << 16);
+        }
+        *reinterpret_cast<uint4*>(p.q_col + row * W + col0 + 16 * v) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    uint32_t mine = 0;  // lane l < 8 writes the scales of columns col0 + 4l .. +3
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mine = (lane == i) ? e4[i] : mine;
+    if (lane < 8) {
+        const int64_t k0 = col0 + 4 * lane;
+        if (p.swizzle) {
+            // per expert: logical (W, m_e/32) at byte W * off_e / 32
+            const int64_t i = (rb0 - T.off) / 32, C4 = T.me / 128;
+            uint8_t* base = p.q_col_s + W * T.off / 32;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t k = k0 + j;
+                base[((k / 128) * C4 + i / 4) * 512 + (k % 32) * 16 + ((k % 128) / 32) * 4 + i % 4] =
+                    (uint8_t)(mine >> (8 * j));
+            }
+        } else {
+            *reinterpret_cast<uint32_t*>(p.q_col_s + (rb0 / 32) * W + k0) = mine;
+        }
+    }
+    if (p.dbias_part) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            v[2 * j] = bf16lo(w[j]);
+            v[2 * j + 1] = bf16hi(w[j]);
+        }
+        p.dbias_part[(rb0 / 32) * W + col0 + lane] = lane_transpose_sum32(v, lane);
+    }
+}
+
+// Epilogue of the SwiGLU-fused FC2 dgrad (kDgradSwiglu) for one tile: the
+// accumulator holds dh for 128 rows x 256 columns of F. Warp (q, half) takes
+// rows 32q..32q+31 (lane = row) and columns T.b_col + 128 half + [0, 128),
+// in four 32-column chunks: dh rounded to bf16 as the plain dgrad writes
+// it, g and u from the saved FC1 output, dg and du in the fp32 steps of
+// mxq_common.cuh, each rounded to bf16 and quantized into dY1 (columns f and
+// F + f) with its dbias partials.
+__device__ __forceinline__ void swiglu_bwd_tile_epilogue(const Params& p, const Tile& T, uint32_t tmem, int q,
+                                                         int half, int lane, uint32_t acc_empty) {
+    const int64_t F = p.K, W = 2 * p.K;
+    uint32_t r[BN / 2];
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + 128 * half;
+    TMEM_LD32(tbase + 0, (r + 0));
+    TMEM_LD32(tbase + 32, (r + 32));
+    TMEM_LD32(tbase + 64, (r + 64));
+    TMEM_LD32(tbase + 96, (r + 96));
+    tmem_wait_ld();
+    fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(acc_empty);  // the MMA warp may start the next tile
+    uint32_t dh2[BN / 4];  // dh rounded to bf16 as the plain dgrad writes it, as pairs
+#pragma unroll
+    for (int j = 0; j < BN / 4; ++j) dh2[j] = bf16x2_bits(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+
+    const int64_t f0 = T.b_col + 128 * half;
+    const int64_t rb0 = T.a_row + 32 * q;
+    const __nv_bfloat16* yr = p.y1 + (rb0 + lane) * W;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int64_t fc = f0 + 32 * c;
+        uint32_t gw[16], uw[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 g4 = __ldg(reinterpret_cast<const uint4*>(yr + fc) + v);
+            const uint4 u4 = __ldg(reinterpret_cast<const uint4*>(yr + F + fc) + v);
+            gw[4 * v] = g4.x; gw[4 * v + 1] = g4.y; gw[4 * v + 2] = g4.z; gw[4 * v + 3] = g4.w;
+            uw[4 * v] = u4.x; uw[4 * v + 1] = u4.y; uw[4 * v + 2] = u4.z; uw[4 * v + 3] = u4.w;
+        }
+        uint32_t dgw[16], duw[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t dw = dh2[16 * c + j];
+            float dg0, du0, dg1, du1;
+            swiglu_grads(bf16lo(dw), bf16lo(gw[j]), bf16lo(uw[j]), dg0, du0);
+            swiglu_grads(bf16hi(dw), bf16hi(gw[j]), bf16hi(uw[j]), dg1, du1);
+            dgw[j] = bf16x2_bits(dg0, dg1);
+            duw[j] = bf16x2_bits(du0, du1);
+        }
+        quant_block32(dgw, p, T, W, rb0, fc, lane);
+        quant_block32(duw, p, T, W, rb0, F + fc, lane);
+    }
 }
 
 // Epilogue of the SwiGLU-fused FC1 fprop (kFpropSwiglu) for one tile: the
@@ -296,83 +459,15 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
     for (int i = 0; i < 32; ++i)
         hw[i] = bf16x2_bits(swiglu_h(bf16lo(y[i]), bf16lo(y[32 + i])), swiglu_h(bf16hi(y[i]), bf16hi(y[32 + i])));
 
-    // rowwise: two 32-column blocks per lane
-    uint8_t* hrow = p.h_row + row * F + f0;
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = __vmaxu2(m, hw[16 * b + i] & 0x7FFF7FFFu);
-        const uint32_t code = (uint32_t)max((int)(max(m & 0xFFFFu, m >> 16) >> 7) - 8, 0);
-        const float inv = inv_scale_from_code(code);
-        uint32_t o[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t w0 = hw[16 * b + 2 * k], w1 = hw[16 * b + 2 * k + 1];
-            o[k] = cvt_e4m3x2(bf16lo(w0) * inv, bf16hi(w0) * inv) | (cvt_e4m3x2(bf16lo(w1) * inv, bf16hi(w1) * inv) << 16);
-        }
-        uint4* d = reinterpret_cast<uint4*>(hrow + 32 * b);
-        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        const int64_t c = (f0 + 32 * b) / 32;  // 32-column block index of h
-        if (p.swizzle)
-            p.h_row_s[((row / 128) * (F / 128) + c / 4) * 512 + (row % 32) * 16 + ((row % 128) / 32) * 4 + c % 4] =
-                (uint8_t)code;
-        else
-            p.h_row_s[row * (F / 32) + c] = (uint8_t)code;
-    }
-
-    // colwise: per column the largest exponent over the warp's 32 rows
-    uint32_t e4[16];  // four columns per word, one byte each
+    // rowwise and colwise codes of h, two 32-column blocks
+    uint32_t w0[16], w1[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-        const uint32_t a = hw[2 * i], b2 = hw[2 * i + 1];
-        e4[i] = ((a >> 7) & 0xFFu) | (((a >> 23) & 0xFFu) << 8) | (((b2 >> 7) & 0xFFu) << 16) |
-                (((b2 >> 23) & 0xFFu) << 24);
+        w0[i] = hw[i];
+        w1[i] = hw[16 + i];
     }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) e4[i] = __vmaxu4(e4[i], __shfl_xor_sync(0xffffffffu, e4[i], off));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) e4[i] = __vsub4(__vmaxu4(e4[i], 0x08080808u), 0x08080808u);  // max(e - 8, 0)
-    uint8_t* hcol = p.h_col + row * F + f0;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t cw = e4[4 * v + k];
-            const uint32_t w0 = hw[8 * v + 2 * k], w1 = hw[8 * v + 2 * k + 1];
-            o[k] = cvt_e4m3x2(bf16lo(w0) * inv_scale_from_code(cw & 0xFFu),
-                              bf16hi(w0) * inv_scale_from_code((cw >> 8) & 0xFFu)) |
-                   (cvt_e4m3x2(bf16lo(w1) * inv_scale_from_code((cw >> 16) & 0xFFu),
-                               bf16hi(w1) * inv_scale_from_code(cw >> 24))
-                    << 16);
-        }
-        *reinterpret_cast<uint4*>(hcol + 16 * v) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    // colwise scale bytes of this 32-row block: lane l < 16 writes columns f0 + 4l .. +3
-    uint32_t mine = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) mine = (lane == i) ? e4[i] : mine;
-    if (lane < 16) {
-        const int64_t k0 = f0 + 4 * lane;
-        const int64_t rb0 = T.a_row + 32 * q;  // first row of the block
-        if (p.swizzle) {
-            // per expert: logical (F, m_e/32) at byte F * off_e / 32
-            const int64_t i = (rb0 - T.off) / 32, C4 = T.me / 128;
-            uint8_t* base = p.h_col_s + F * T.off / 32;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t k = k0 + j;
-                base[((k / 128) * C4 + i / 4) * 512 + (k % 32) * 16 + ((k % 128) / 32) * 4 + i % 4] =
-                    (uint8_t)(mine >> (8 * j));
-            }
-        } else {
-            *reinterpret_cast<uint32_t*>(p.h_col_s + (rb0 / 32) * F + k0) = mine;
-        }
-    }
+    quant_block32(w0, p, T, F, T.a_row + q * 32, f0, lane);
+    quant_block32(w1, p, T, F, T.a_row + q * 32, f0 + 32, lane);
 }
 
 template <int kMode>
@@ -461,7 +556,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     sfb0 = p.sfb + (wrow / 128) * kbs * 512;
                     // second B box: the next 128 rows, or (SwiGLU) the up rows F further
                     sfb1 = sfb0 + (kMode == kFpropSwiglu ? (p.N / 2) / 128 : 1) * kbs * 512;
-                } else if (kMode == kDgrad) {
+                } else if (kMode == kDgrad || kMode == kDgradSwiglu) {
                     const int64_t kbs = p.N / BK;
                     const uint8_t* wb = p.sfb + (int64_t)T.e * p.K * (p.N / 32);
                     ax = 0; ay = (int)T.a_row; adx = BK; ady = 0;
@@ -567,6 +662,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_after();
             if constexpr (kMode == kFpropSwiglu) {
                 swiglu_tile_epilogue(p, T, tmem, q, half, lane, epi_buf, acc_empty, &tmOut);
+                aphase ^= 1;
+                continue;
+            }
+            if constexpr (kMode == kDgradSwiglu) {
+                swiglu_bwd_tile_epilogue(p, T, tmem, q, half, lane, acc_empty);
                 aphase ^= 1;
                 continue;
             }
@@ -791,6 +891,9 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     if (c.mode == kFpropSwiglu)
         attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kFpropSwiglu>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MXQ_MAX_EXPERTS));
+    else if (c.mode == kDgradSwiglu)
+        attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kDgradSwiglu>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(MXQ_MAX_EXPERTS));
     else if (c.mode == kFprop)
         attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kFprop>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem_bytes(MXQ_MAX_EXPERTS));
@@ -804,7 +907,7 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
 
     int64_t tiles;
     if (c.mode == kFprop || c.mode == kFpropSwiglu) tiles = (c.M / BM) * (c.N / BN);
-    else if (c.mode == kDgrad) tiles = (c.M / BM) * (c.K / BN);
+    else if (c.mode == kDgrad || c.mode == kDgradSwiglu) tiles = (c.M / BM) * (c.K / BN);
     else tiles = (int64_t)c.E * (c.N / BM) * (c.K / BN);
     if (tiles == 0) return cudaSuccess;
     if (c.mode == kWgrad && c.M == 0) {
@@ -817,7 +920,7 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     bool ok;
     if (c.mode == kFprop || c.mode == kFpropSwiglu) {
         ok = make_map(&ta, c.a_data, c.M, c.K) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
-    } else if (c.mode == kDgrad) {
+    } else if (c.mode == kDgrad || c.mode == kDgradSwiglu) {
         ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
     } else {
         ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, c.M, c.K);
@@ -827,7 +930,7 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     // Output boxes for the TMA-store epilogue (not used when accumulating).
     CUtensorMap to;
     memset(&to, 0, sizeof(to));
-    const int tma_store = !c.accumulate;
+    const int tma_store = !c.accumulate && c.mode != kDgradSwiglu;  // dh never leaves the chip there
     if (tma_store) {
         if (c.mode == kFprop || c.mode == kFpropSwiglu) ok = encode_tmap_2d(&to, c.out, c.M, c.N, 2, 32, 32, false);
         else if (c.mode == kDgrad) ok = encode_tmap_2d(&to, c.out, c.M, c.K, 2, 32, 32, false);
@@ -851,15 +954,19 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     p.out_bf16 = c.out_bf16;
     p.tma_store = tma_store;
     p.status = c.status;
-    p.h_row = static_cast<uint8_t*>(c.h_row);
-    p.h_row_s = static_cast<uint8_t*>(c.h_row_s);
-    p.h_col = static_cast<uint8_t*>(c.h_col);
-    p.h_col_s = static_cast<uint8_t*>(c.h_col_s);
+    p.q_row = static_cast<uint8_t*>(c.q_row);
+    p.q_row_s = static_cast<uint8_t*>(c.q_row_s);
+    p.q_col = static_cast<uint8_t*>(c.q_col);
+    p.q_col_s = static_cast<uint8_t*>(c.q_col_s);
     p.swizzle = c.swizzle;
+    p.y1 = static_cast<const __nv_bfloat16*>(c.y1);
+    p.dbias_part = c.dbias_part;
 
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
     if (c.mode == kFpropSwiglu)
         grouped_gemm_kernel<kFpropSwiglu><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
+    else if (c.mode == kDgradSwiglu)
+        grouped_gemm_kernel<kDgradSwiglu><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
     else if (c.mode == kFprop) grouped_gemm_kernel<kFprop><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
     else if (c.mode == kDgrad) grouped_gemm_kernel<kDgrad><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
     else grouped_gemm_kernel<kWgrad><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);

@@ -68,7 +68,10 @@ struct SwigluQuantCall {
 
 // kFpropSwiglu: FC1 fprop of a SwiGLU MLP (N = 2F) whose epilogue also
 // applies SwiGLU to the bf16 output and quantizes h (rowwise + colwise).
-enum GemmMode { kFprop = 0, kDgrad = 1, kWgrad = 2, kFpropSwiglu = 3 };
+// kDgradSwiglu: FC2 dgrad (output dh, K = F) whose epilogue applies the
+// SwiGLU backward with the saved FC1 output and quantizes dY1 = [dg | du]
+// (rowwise + colwise) and reduces its dbias partials.
+enum GemmMode { kFprop = 0, kDgrad = 1, kWgrad = 2, kFpropSwiglu = 3, kDgradSwiglu = 4 };
 
 struct GemmCall {
     int mode;
@@ -80,15 +83,19 @@ struct GemmCall {
     void* out;
     int accumulate, out_bf16;  // wgrad only
     int32_t* status;
-    // kFpropSwiglu: h = silu(gate) * up quantized to (M, N/2) codes and scales
-    void *h_row, *h_row_s, *h_col, *h_col_s;
+    // kFpropSwiglu: h (M, N/2); kDgradSwiglu: dY1 (M, 2K) -- codes and scales
+    void *q_row, *q_row_s, *q_col, *q_col_s;
     int swizzle;
+    const void* y1;      // kDgradSwiglu: saved FC1 output (M, 2K) bf16
+    float* dbias_part;   // kDgradSwiglu: (M/32, 2K) fp32 column sums per 32 rows, or null
 };
 
-// The extra outputs of kFpropSwiglu, as passed through the C ABI.
+// The extra operands of the SwiGLU-fused modes, as passed through the C ABI.
 struct GemmExtra {
-    void *h_row, *h_row_s, *h_col, *h_col_s;
+    void *q_row, *q_row_s, *q_col, *q_col_s;
     int swizzle;
+    const void* y1;
+    float* dbias_part;
 };
 
 // Encodes a 2-D row-major tensor map (rows x cols elements of elem_bytes)
@@ -103,8 +110,10 @@ cudaError_t run_grouped_dbias(const void* dy, int64_t M, int64_t N, int E, const
                               float* partials, int32_t* status, cudaStream_t s);
 cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s);
 cudaError_t run_swiglu_quantize(const SwigluQuantCall& c, cudaStream_t s);
+// out[e, :] = fp64 sum, in order, of expert e's partial rows; each partial row
+// covers rows_per_partial consecutive token rows.
 cudaError_t run_dbias_finalize(const float* partials, int64_t M, int64_t K, int E, const int64_t* m_splits,
-                               float* out, const int32_t* noop, cudaStream_t s);
+                               float* out, const int32_t* noop, cudaStream_t s, int64_t rows_per_partial = 128);
 cudaError_t run_swiglu_fwd(const void* y, int64_t M, int64_t F, void* h, cudaStream_t s);
 cudaError_t run_swiglu_bwd(const void* dh, const void* y, int64_t M, int64_t F, void* dy, cudaStream_t s);
 

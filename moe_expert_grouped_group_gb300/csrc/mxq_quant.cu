@@ -391,18 +391,20 @@ __global__ void __launch_bounds__(kTileThreads)
     if (threadIdx.x == 0 && s_abort && a.status) atomicOr(a.status, MXQ_STATUS_WAIT_TIMEOUT);
 }
 
-// Second dbias stage: out[e, c] = sum over expert e's 128-row tiles of the
-// tile partials, in tile order, accumulated in fp64.
+// Second dbias stage: out[e, c] = sum over expert e's row blocks of the block
+// partials (one per `rpp` rows: 128 for the tile kernels, 32 where a warp's
+// rows are reduced on their own), in block order, accumulated in fp64.
 __global__ void __launch_bounds__(256) dbias_finalize_kernel(const float* __restrict__ partials, int64_t M,
                                                              int64_t K, int E, const int64_t* m_splits,
-                                                             float* __restrict__ out, const int32_t* noop) {
+                                                             float* __restrict__ out, const int32_t* noop,
+                                                             int64_t rpp) {
     __shared__ int64_t s_off[MXQ_MAX_EXPERTS + 1];
     if (noop && *noop) return;
     if (load_offsets(m_splits, E, M, s_off)) return;  // reported by the tile kernel
     const int e = blockIdx.y;
     const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= K) return;
-    const int64_t t0 = s_off[e] / kTile, t1 = s_off[e + 1] / kTile;
+    const int64_t t0 = s_off[e] / rpp, t1 = s_off[e + 1] / rpp;
     double acc = 0.0;
     for (int64_t t = t0; t < t1; ++t) acc += (double)partials[t * K + c];
     out[(int64_t)e * K + c] = (float)acc;
@@ -453,15 +455,15 @@ static cudaError_t launch_tile(const TileArgs& a, cudaStream_t s) {
 }
 
 static cudaError_t launch_finalize(const float* partials, int64_t M, int64_t K, int E, const int64_t* m_splits,
-                                   float* out, const int32_t* noop, cudaStream_t s) {
+                                   float* out, const int32_t* noop, cudaStream_t s, int64_t rpp = kTile) {
     dim3 grid((unsigned)((K + 255) / 256), (unsigned)E);
-    dbias_finalize_kernel<<<grid, 256, 0, s>>>(partials, M, K, E, m_splits, out, noop);
+    dbias_finalize_kernel<<<grid, 256, 0, s>>>(partials, M, K, E, m_splits, out, noop, rpp);
     return cudaGetLastError();
 }
 
 cudaError_t run_dbias_finalize(const float* partials, int64_t M, int64_t K, int E, const int64_t* m_splits,
-                               float* out, const int32_t* noop, cudaStream_t s) {
-    return launch_finalize(partials, M, K, E, m_splits, out, noop, s);
+                               float* out, const int32_t* noop, cudaStream_t s, int64_t rows_per_partial) {
+    return launch_finalize(partials, M, K, E, m_splits, out, noop, s, rows_per_partial);
 }
 
 // After a scaled-bias tile launch: the per-expert scaled column sums and the

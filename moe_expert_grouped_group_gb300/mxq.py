@@ -20,6 +20,7 @@ from .build import LIB
 ROWWISE, COLWISE, SWIZZLE, DEQUANT_OUT, ACCUMULATE, OUT_BF16 = 1, 2, 4, 8, 16, 32
 OP_GROUP_QUANTIZE, OP_REQUANT_COLWISE, OP_GROUPED_DBIAS = 1, 2, 3
 OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD, OP_SWIGLU_BWD_QUANTIZE, OP_SCALED_BIAS = 4, 5, 6, 7, 8
+OP_GEMM_DGRAD_SWIGLU = 9
 STATUS_SPLIT_UNALIGNED, STATUS_SPLIT_NEGATIVE, STATUS_SPLIT_SUM, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
 
 SYMBOLS = [
@@ -27,7 +28,7 @@ SYMBOLS = [
     "mxq_grouped_dbias", "mxq_grouped_gemm_fprop", "mxq_grouped_gemm_dgrad", "mxq_grouped_gemm_wgrad",
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
-    "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu",
+    "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu", "mxq_grouped_gemm_dgrad_swiglu",
 ]
 
 
@@ -54,6 +55,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_grouped_dbias.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_fprop.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_fprop_swiglu.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P,
+                                                _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_gemm_dgrad_swiglu.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P,
                                                 _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_wgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
@@ -319,6 +322,34 @@ def grouped_gemm_dgrad(dy_data, dy_scale, w_col_data, w_col_scale, m_splits, sta
                                       E, _ptr(m_splits), _ptr(out), _ptr(status), None, 0, _stream())
     _check(rc, "mxq_grouped_gemm_dgrad")
     return out
+
+
+def grouped_gemm_dgrad_swiglu(dy_data, dy_scale, w_col_data, w_col_scale, y1, m_splits, swizzle=True, dbias=True,
+                              status=None, out=None, workspace=None):
+    """FC2 dgrad with the SwiGLU backward and the quantization of dY1 in the GEMM epilogue.
+    dy_data (M, N) rowwise, w_col_data (E, N, F) colwise, y1 (M, 2F) bf16 saved FC1 output ->
+    dict(row_data, row_scale, col_data, col_scale of dY1 (M, 2F), dbias (E, 2F))."""
+    M, N = dy_data.shape
+    E, _, F = w_col_data.shape
+    m_splits = _splits(m_splits)
+    dev = dy_data.device
+    o = dict(out or {})
+    o.setdefault("row_data", _u8((M, 2 * F), dev))
+    o.setdefault("row_scale", _u8(scale_bytes(M, 2 * F, False), dev))
+    o.setdefault("col_data", _u8((M, 2 * F), dev))
+    o.setdefault("col_scale", _u8(scale_bytes(M, 2 * F, True), dev))
+    ws = None
+    if dbias:
+        o.setdefault("dbias", torch.empty((E, 2 * F), dtype=torch.float32, device=dev))
+        ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_GEMM_DGRAD_SWIGLU, M, N, F, E)),
+                                                         dev)
+    rc = lib().mxq_grouped_gemm_dgrad_swiglu(
+        _ptr(dy_data), _ptr(dy_scale), _ptr(w_col_data), _ptr(w_col_scale), _ptr(y1), M, N, F, E, _ptr(m_splits),
+        SWIZZLE if swizzle else 0, _ptr(o["row_data"]), _ptr(o["row_scale"]), _ptr(o["col_data"]),
+        _ptr(o["col_scale"]), _ptr(o.get("dbias")), _ptr(status), _ptr(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _stream())
+    _check(rc, "mxq_grouped_gemm_dgrad_swiglu")
+    return o
 
 
 def grouped_gemm_wgrad(dy_col_data, dy_col_scale, x_col_data, x_col_scale, m_splits, accumulate=False,

@@ -102,3 +102,73 @@ def test_full_size_fprop_swiglu(mxq):
     assert np.array_equal(host(fused["y1"]), host(plain))
     del plain
     _check_h(mxq, fused, ms, True)
+
+
+# ------------------------------------------------ FC2 dgrad + SwiGLU backward
+def _bwd_operands(ms, F, H, seed):
+    rng = np.random.default_rng(seed)
+    ms = np.asarray(ms, np.int64)
+    M, E = int(ms.sum()), len(ms)
+    dy2 = bf16_bits_from_f32(rng.standard_normal((M, H)).astype(np.float32))
+    w2 = bf16_bits_from_f32((0.05 * rng.standard_normal((E, H, F))).astype(np.float32))
+    y1 = bf16_bits_from_f32((2.0 * rng.standard_normal((M, 2 * F))).astype(np.float32))
+    return dy2, w2, y1, ms
+
+
+def _run_bwd(mxq, dy2, w2, y1, ms, swizzle):
+    E, H, F = w2.shape
+    sdy = orc.group_quantize(dy2, ms, rowwise=True, colwise=False, swizzled=True)
+    sw = orc.quantize_weights(w2, swizzled=True)
+    args = (dev_u8(sdy["row_q"]), dev_u8(sdy["row_s"]), dev_u8(sw["col_q"]).view(E, H, F), dev_u8(sw["col_s"]))
+    y1d = dev_bf16(y1)
+    fused = mxq.grouped_gemm_dgrad_swiglu(*args, y1d, dev_i64(ms), swizzle=swizzle)
+    dh = mxq.grouped_gemm_dgrad(*args, dev_i64(ms))
+    ref = mxq.swiglu_bwd_quantize(dh, y1d, dev_i64(ms), swizzle=swizzle, dbias=True, dy_out=True)
+    return fused, dh, ref
+
+
+def _check_bwd(fused, dh, ref, y1, ms, swizzle):
+    # the codes: oracle's fp32 SwiGLU backward of (plain dgrad's dh, y1), then its group_quantize
+    dy1 = orc.swiglu_bwd_f32(host(dh), y1)
+    assert np.array_equal(dy1, host(ref["dy"]))
+    o = orc.group_quantize(dy1, ms, swizzled=swizzle)
+    for dk, ok in (("row_data", "row_q"), ("row_scale", "row_s"), ("col_data", "col_q"), ("col_scale", "col_s")):
+        got = host(fused[dk]).reshape(o[ok].shape)
+        assert np.array_equal(got, o[ok]), (dk, first_diff(got, o[ok]))
+        assert np.array_equal(host(fused[dk]), host(ref[dk])), dk
+    # dbias: a different fixed summation order than the standalone kernel, so within the tolerance
+    db = orc.grouped_dbias(dy1, ms)
+    a = np.abs((dy1.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+    off = np.concatenate([[0], np.cumsum(ms)])
+    got = host(fused["dbias"]).astype(np.float64)
+    for e in range(len(ms)):
+        tol = 1e-5 * a[off[e]:off[e + 1]].sum(axis=0) + 1e-30
+        assert np.all(np.abs(got[e] - db[e]) <= tol), e
+
+
+BWD_CASES = [
+    ([128, 256, 0, 128], 256, 512),
+    ([384], 512, 256),
+    ([128] * 4, 256, 384),
+]
+
+
+@pytest.mark.parametrize("swizzle", [True, False])
+@pytest.mark.parametrize("case", BWD_CASES, ids=[f"E{len(s)}_F{f}_H{h}" for s, f, h in BWD_CASES])
+def test_dgrad_swiglu_stagewise(mxq, case, swizzle):
+    splits, F, H = case
+    dy2, w2, y1, ms = _bwd_operands(splits, F, H, 63)
+    fused, dh, ref = _run_bwd(mxq, dy2, w2, y1, ms, swizzle)
+    _check_bwd(fused, dh, ref, y1, ms, swizzle)
+
+
+def test_full_size_dgrad_swiglu(mxq):
+    """64 experts, 83968 routed rows: FC2 dgrad (hidden 3072 -> F = 1024) with the SwiGLU
+    backward of a synthetic saved FC1 output."""
+    w = WORKLOADS["e64_h3072_f1024_t84k_prequant"]
+    d = make_inputs(w, which=("dy2", "w2"))
+    ms = d["m_splits"]
+    y1 = bf16_bits_from_f32((2.0 * np.random.default_rng([0, w.wid, 9]).standard_normal((w.M, 2 * w.F)))
+                            .astype(np.float32))
+    fused, dh, ref = _run_bwd(mxq, d["dy2"], d["w2"], y1, ms, True)
+    _check_bwd(fused, dh, ref, y1, ms, True)
