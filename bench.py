@@ -54,10 +54,11 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
-    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias"],
+    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp"],
                    help="time only one fused kernel family on the MLP workload's shapes and print its line (a "
-                        "small footprint for profilers): the SwiGLU->quantize kernels (forward and backward), or "
-                        "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions")
+                        "small footprint for profilers): the SwiGLU->quantize kernels (forward and backward), "
+                        "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions, or the "
+                        "SwiGLU-fused FC1 fprop and FC2 dgrad vs their unfused pairs")
     return p.parse_args()
 
 
@@ -235,7 +236,8 @@ class MLPStep:
         self.qh = q(M, F)
         self.qdy1 = q(M, 2 * F)
         self.qdy1["dbias"] = torch.empty((E, 2 * F), dtype=torch.float32, device=dev)
-        self.ws = u8(max(mxq.workspace_bytes(2, M, 0, H, E), mxq.workspace_bytes(7, M, 0, F, E)))
+        self.ws = u8(max(mxq.workspace_bytes(mxq.mxq.OP_REQUANT_COLWISE, M, 0, H, E),
+                         mxq.workspace_bytes(mxq.mxq.OP_SWIGLU_BWD_QUANTIZE, M, 0, F, E)))
         self.y1, self.y2 = bf(M, 2 * F), bf(M, H)
         self.fc1_out = dict(self.qh, y1=self.y1)  # FC1 output saved bf16 + h quantized in its epilogue
         self.dh, self.dx = bf(M, F), bf(M, H)
@@ -302,14 +304,13 @@ def time_mlp(dev, steps=10, warmup=3):
     per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
            for j, k in enumerate(MLP_STAGES)}
     gemm_ms = sum(v for k, v in per.items() if "prop" in k or "grad" in k)
-    _, bb = swiglu_quant_bytes(st.M, st.F)
-    swq_gbs = {"swiglu_bwd_quantize_dy1_dbias": bb / (per["swiglu_bwd_quantize_dy1_dbias"] * 1e-3) / 1e9}
+
     return {"workload": MLP_WORKLOAD, "steps": steps, "warmup": warmup, "ms_per_step": ms,
             "tflops_step": st.flops() / (ms * 1e-3) / 1e12, "gemm_tflops": st.flops() / (gemm_ms * 1e-3) / 1e12,
-            "stage_ms": per, "swiglu_quantize_gbs": swq_gbs, "gpu_launches": st.launches_per_step * steps,
+            "stage_ms": per, "gpu_launches": st.launches_per_step * steps,
             "step": "fwd+bwd of FC1 (bias) -> SwiGLU -> FC2 (bias), X and dY2 rowwise-prequantized; SwiGLU and "
-                    "the quantization of h in FC1's GEMM epilogue (forward), SwiGLU fused with the quantization "
-                    "of dY1 and its dbias (backward)",
+                    "the quantization of h in FC1's GEMM epilogue (forward); SwiGLU backward fused with the "
+                    "quantization of dY1 and its dbias (backward)",
             "gemm_note": "gemm_tflops counts the FC1 stage whole (its epilogue also runs SwiGLU and quantizes h)"}
 
 
@@ -420,6 +421,69 @@ def time_scaled_bias(dev, steps, warmup):
         us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
         res[name + "_us"] = us
         res[name + "_gbs"] = nbytes[name] / (us * 1e-6) / 1e9
+    return res
+
+
+def time_fused_mlp(dev, steps, warmup):
+    """The two SwiGLU-fused GEMMs of the MLP workload (64 experts, 83968 rows,
+    hidden 3072, F 1024) against their unfused pairs: FC1 fprop + SwiGLU and
+    quantization of h, and FC2 dgrad + SwiGLU backward and quantization of dY1
+    with its dbias. Operands are quantized on the device."""
+    import torch
+
+    import moe_expert_grouped_group_gb300 as mxq
+    from synth import WORKLOADS, make_inputs
+
+    w = WORKLOADS[MLP_WORKLOAD]
+    d = make_inputs(w, which=("x", "w", "w2", "dy2", "b1"))
+    E, H, F, M = w.E, w.K, w.F, w.M
+    tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    ms = torch.from_numpy(d["m_splits"]).to(dev)
+    qx = mxq.group_quantize(tb(d["x"]), ms, rowwise=True, colwise=False)
+    qd = mxq.group_quantize(tb(d["dy2"]), ms, rowwise=True, colwise=False)
+    qw1 = mxq.group_quantize(tb(d["w"]).view(E * 2 * F, H), None, E=E, colwise=False)
+    qw2 = mxq.group_quantize(tb(d["w2"]).view(E * H, F), None, E=E, rowwise=False)
+    del d
+    b1 = tb(make_inputs(w, which=("b1",))["b1"])
+    w1v, w2v = qw1["row_data"].view(E, 2 * F, H), qw2["col_data"].view(E, H, F)
+    fc1_out = mxq.grouped_gemm_fprop_swiglu(qx["row_data"], qx["row_scale"], w1v, qw1["row_scale"], ms, bias=b1)
+    y1 = fc1_out["y1"]
+    ws = torch.empty(mxq.workspace_bytes(mxq.mxq.OP_GEMM_DGRAD_SWIGLU, M, H, F, E), dtype=torch.uint8, device=dev)
+    dy1 = mxq.grouped_gemm_dgrad_swiglu(qd["row_data"], qd["row_scale"], w2v, qw2["col_scale"], y1, ms,
+                                        workspace=ws)
+    dh = torch.empty((M, F), dtype=torch.bfloat16, device=dev)
+    qh = {k: torch.empty_like(v) for k, v in fc1_out.items() if k != "y1"}
+    qdy1 = {k: torch.empty_like(v) for k, v in dy1.items()}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    runs = {
+        "fc1_fused": [lambda: mxq.grouped_gemm_fprop_swiglu(qx["row_data"], qx["row_scale"], w1v, qw1["row_scale"],
+                                                            ms, bias=b1, out=fc1_out)],
+        "fc1_unfused": [lambda: mxq.grouped_gemm_fprop(qx["row_data"], qx["row_scale"], w1v, qw1["row_scale"], ms,
+                                                       bias=b1, out=y1),
+                        lambda: mxq.swiglu_quantize(y1, ms, out=qh)],
+        "fc2_dgrad_fused": [lambda: mxq.grouped_gemm_dgrad_swiglu(qd["row_data"], qd["row_scale"], w2v,
+                                                                  qw2["col_scale"], y1, ms, out=dy1, workspace=ws)],
+        "fc2_dgrad_unfused": [lambda: mxq.grouped_gemm_dgrad(qd["row_data"], qd["row_scale"], w2v, qw2["col_scale"],
+                                                             ms, out=dh),
+                              lambda: mxq.swiglu_bwd_quantize(dh, y1, ms, dbias=True, out=qdy1, workspace=ws)],
+    }
+    res = {"workload": MLP_WORKLOAD, "steps": steps, "warmup": warmup,
+           "l2": "256 MiB buffer written before every launch sequence"}
+    for name, fns in runs.items():
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(warmup + steps):
+            flush.fill_(1)
+            if i >= warmup:
+                ev[i - warmup][0].record()
+            for fn in fns:
+                fn()
+            if i >= warmup:
+                ev[i - warmup][1].record()
+        torch.cuda.synchronize()
+        res[name + "_us"] = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    fl = 2.0 * M * 2 * F * H  # one GEMM of either linear: 2 M (2F) H = 2 M H F * 2
+    res["fc1_fused_tflops"] = fl / (res["fc1_fused_us"] * 1e-6) / 1e12
+    res["fc2_dgrad_fused_tflops"] = (2.0 * M * H * F) / (res["fc2_dgrad_fused_us"] * 1e-6) / 1e12
     return res
 
 
@@ -637,6 +701,11 @@ def main():
         _, hbm_peak, src = peaks()
         r.update(fwd_frac=r["fwd_gbs"] / hbm_peak, bwd_frac=r["bwd_gbs"] / hbm_peak, hbm_peak_gbs=hbm_peak,
                  peak_source=src)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
+    if args.only == "fused_mlp":
+        r = time_fused_mlp(dev, max(1, args.steps), max(1, args.warmup))
         if rank == 0:
             print(json.dumps(r), flush=True)
         return

@@ -334,7 +334,10 @@ __device__ __forceinline__ void quant_block32(const uint32_t (&w)[16], const Par
 // in four 32-column chunks: dh rounded to bf16 as the plain dgrad writes
 // it, g and u from the saved FC1 output, dg and du in the fp32 steps of
 // mxq_common.cuh, each rounded to bf16 and quantized into dY1 (columns f and
-// F + f) with its dbias partials.
+// F + f) with its dbias partials. This epilogue does about twice the
+// arithmetic of the forward one on the same 8 warps per SM, so on the
+// 64-expert workload it outlasts the dgrad mainloop (736 us against 440 us
+// for dgrad followed by the standalone 16-warp-per-SM swiglu_bwd_quantize).
 __device__ __forceinline__ void swiglu_bwd_tile_epilogue(const Params& p, const Tile& T, uint32_t tmem, int q,
                                                          int half, int lane, uint32_t acc_empty) {
     const int64_t F = p.K, W = 2 * p.K;
@@ -355,7 +358,10 @@ __device__ __forceinline__ void swiglu_bwd_tile_epilogue(const Params& p, const 
     const int64_t f0 = T.b_col + 128 * half;
     const int64_t rb0 = T.a_row + 32 * q;
     const __nv_bfloat16* yr = p.y1 + (rb0 + lane) * W;
-#pragma unroll
+    // The chunk loop stays rolled (an unrolled body would not fit the
+    // instruction cache); dh2 is shifted down one chunk per pass so that the
+    // body only ever reads dh2[0..15] and the array stays in registers.
+#pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         const int64_t fc = f0 + 32 * c;
         uint32_t gw[16], uw[16];
@@ -369,7 +375,7 @@ __device__ __forceinline__ void swiglu_bwd_tile_epilogue(const Params& p, const 
         uint32_t dgw[16], duw[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-            const uint32_t dw = dh2[16 * c + j];
+            const uint32_t dw = dh2[j];
             float dg0, du0, dg1, du1;
             swiglu_grads(bf16lo(dw), bf16lo(gw[j]), bf16lo(uw[j]), dg0, du0);
             swiglu_grads(bf16hi(dw), bf16hi(gw[j]), bf16hi(uw[j]), dg1, du1);
@@ -378,6 +384,8 @@ __device__ __forceinline__ void swiglu_bwd_tile_epilogue(const Params& p, const 
         }
         quant_block32(dgw, p, T, W, rb0, fc, lane);
         quant_block32(duw, p, T, W, rb0, F + fc, lane);
+#pragma unroll
+        for (int j = 0; j < BN / 4 - 16; ++j) dh2[j] = dh2[j + 16];
     }
 }
 
