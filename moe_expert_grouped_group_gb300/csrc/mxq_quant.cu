@@ -406,7 +406,8 @@ __global__ void __launch_bounds__(256) dbias_finalize_kernel(const float* __rest
     if (c >= K) return;
     const int64_t t0 = s_off[e] / rpp, t1 = s_off[e + 1] / rpp;
     double acc = 0.0;
-    for (int64_t t = t0; t < t1; ++t) acc += (double)partials[t * K + c];
+#pragma unroll 8
+    for (int64_t t = t0; t < t1; ++t) acc += (double)partials[t * K + c];  // loads run ahead of the adds
     out[(int64_t)e * K + c] = (float)acc;
 }
 
@@ -421,6 +422,7 @@ __global__ void __launch_bounds__(256) dprobs_finalize_kernel(const float* __res
     const int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (m >= M) return;
     double acc = 0.0;
+#pragma unroll 8
     for (int64_t t = 0; t < tilesK; ++t) acc += (double)dp_partials[m * tilesK + t];
     out[m] = (float)acc;
 }
