@@ -232,6 +232,93 @@ def requant_colwise(row_q, row_s_compact, m_splits, swizzled=True, dbias=False, 
     return {"col_q": col_q, "col_s": col_s, "row_s_swizzled": row_sw, "dbias": db, "deq": deq}
 
 
+# ------------------------------------------- experts not aligned to 128 rows
+# TransformerEngine PR #3244's review notes that swizzling a grouped
+# activation as one dense tensor is valid only when every expert's token count
+# is padded to a multiple of 128, and that a grouped swizzle handles variable
+# per-expert dims. Reading: each expert is padded with zero rows up to a
+# multiple of 128 and quantized by the aligned rules. Zero rows never raise a block's
+# amax, so a partial 32-row colwise block is scaled by its real rows only.
+# The E4M3 codes keep the dense (M, K) layout and the compact rowwise scales
+# stay dense (rowwise blocks do not depend on the grouping); swizzled scales
+# and colwise compact scales live in the padded row space of
+# R = sum_e round_up(m_e, 128) rows, expert e's rows starting at
+# P_e = sum_{e' < e} round_up(m_e', 128); pad bytes are 0.
+
+def padded_offsets(m_splits):
+    """(P, mp): padded row offsets P[0..E] and padded counts round_up(m_e, 128)."""
+    ms = np.asarray(m_splits, np.int64)
+    mp = (ms + 127) // 128 * 128
+    return np.concatenate([[0], np.cumsum(mp)]).astype(np.int64), mp
+
+
+def pad_rows(a, m_splits):
+    """Rows of a (M, ...) placed at their padded positions; pad rows are zero."""
+    ms = np.asarray(m_splits, np.int64)
+    P, _ = padded_offsets(ms)
+    off = np.concatenate([[0], np.cumsum(ms)])
+    out = np.zeros((int(P[-1]),) + a.shape[1:], a.dtype)
+    for e in range(len(ms)):
+        out[P[e]:P[e] + ms[e]] = a[off[e]:off[e + 1]]
+    return out
+
+
+def unpad_rows(a, m_splits):
+    """Inverse of pad_rows: the real rows of a padded (R, ...) array, dense."""
+    ms = np.asarray(m_splits, np.int64)
+    P, _ = padded_offsets(ms)
+    return np.concatenate([a[P[e]:P[e] + ms[e]] for e in range(len(ms))], axis=0)
+
+
+def group_quantize_padded(x_bits, m_splits, rowwise=True, colwise=True, swizzled=False):
+    """Grouped quantization with any expert counts (see above). Returns row_q, col_q (M, K);
+    row_s: compact (round_up(M,128), K/32 padded to 4) dense, or swizzled over R rows;
+    col_s: compact (R/32, K) or swizzled per expert at byte K*P_e/32."""
+    x = _c(x_bits, np.uint16)
+    M, K = x.shape
+    ms = _c(m_splits, np.int64)
+    _, mp = padded_offsets(ms)
+    o = group_quantize(pad_rows(x, ms), mp, rowwise, colwise, swizzled)
+    out = {"row_q": None, "row_s": o["row_s"], "col_q": None, "col_s": o["col_s"]}
+    if rowwise:
+        out["row_q"] = unpad_rows(o["row_q"], ms)
+        if not swizzled:
+            rr, rc = compact_shape(M, K, False)
+            dense = np.zeros((rr, rc), np.uint8)
+            dense[:M] = unpad_rows(o["row_s"], ms)
+            out["row_s"] = dense
+    if colwise:
+        out["col_q"] = unpad_rows(o["col_q"], ms)
+    return out
+
+
+def requant_colwise_padded(row_q, row_s_compact, m_splits, swizzled=True, dbias=False, dequant=False):
+    """Requant with any expert counts: the dense wire format (codes + dense compact rowwise
+    scales) is padded with zero rows (code 0 scales), requantized by the aligned rules, and the
+    codes and dequantized rows are taken back to the dense layout; col_s and row_s_swizzled
+    stay in the padded row space."""
+    q = _c(row_q, np.uint8)
+    M, K = q.shape
+    ms = _c(m_splits, np.int64)
+    P, mp = padded_offsets(ms)
+    R = int(P[-1])
+    rr, rc = compact_shape(R, K, False)
+    s_p = np.zeros((rr, rc), np.uint8)
+    s_p[:R] = pad_rows(np.asarray(row_s_compact).reshape(-1, rc)[:M], ms)
+    o = requant_colwise(pad_rows(q, ms), s_p, mp, swizzled=swizzled, dbias=dbias, dequant=dequant)
+    o["col_q"] = unpad_rows(o["col_q"], ms)
+    if dequant:
+        o["deq"] = unpad_rows(o["deq"], ms)
+    return o
+
+
+def grouped_dbias_padded(dy_bits, m_splits):
+    """Per-expert column sums for any expert counts (pad rows are zero)."""
+    ms = _c(m_splits, np.int64)
+    _, mp = padded_offsets(ms)
+    return grouped_dbias(pad_rows(_c(dy_bits, np.uint16), ms), mp)
+
+
 def grouped_dbias(dy_bits, m_splits):
     dy = _c(dy_bits, np.uint16)
     M, N = dy.shape

@@ -9,6 +9,7 @@ import ctypes
 import os
 import subprocess
 
+import numpy as np
 import pytest
 
 import oracle
@@ -109,3 +110,15 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new, tests):
     finally:
         oracle._lib = saved
     assert failed, f"no pin caught the planted mistake: {name}"
+
+
+def test_pins_catch_padding_to_32_rows(monkeypatch):
+    """Planted mistake in the oracle's Python layer: experts padded to 32 rows instead of 128."""
+    def wrong(m_splits):
+        ms = np.asarray(m_splits, np.int64)
+        mp = (ms + 31) // 32 * 32
+        return np.concatenate([[0], np.cumsum(mp)]).astype(np.int64), mp
+
+    monkeypatch.setattr(oracle, "padded_offsets", wrong)
+    with pytest.raises((AssertionError, ValueError)):
+        pins.test_padded_partial_colwise_block_by_brute_force(oracle)

@@ -540,3 +540,83 @@ def test_scaled_bias_with_unit_scales_is_the_plain_dbias(orc):
     zero = np.zeros_like(bias)
     _, ds0 = orc.scaled_bias_grads(dy, ms, np.ones(len(dy), np.float32), zero, dbias=False)
     assert np.all(ds0 == 0)
+
+
+# ------------------------------------------- experts not aligned to 128 rows
+def test_padded_grouping_reduces_to_the_aligned_one(orc):
+    rng = np.random.default_rng(71)
+    ms = np.array([128, 0, 256, 128], np.int64)
+    x = bf16_bits_from_f32(rng.standard_normal((512, 256)).astype(np.float32))
+    for sw in (False, True):
+        a = orc.group_quantize(x, ms, swizzled=sw)
+        b = orc.group_quantize_padded(x, ms, swizzled=sw)
+        for k in a:
+            assert np.array_equal(a[k], b[k]), (sw, k)
+    wire = orc.group_quantize(x, ms, rowwise=True, colwise=False)
+    a = orc.requant_colwise(wire["row_q"], wire["row_s"], ms, dbias=True, dequant=True)
+    b = orc.requant_colwise_padded(wire["row_q"], wire["row_s"], ms, dbias=True, dequant=True)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_padded_partial_colwise_block_by_brute_force(orc):
+    # expert 0 has 40 rows: one full 32-row block and a partial block of 8 real rows;
+    # expert 1 has 3 rows. Each partial block's scale and codes come from its real rows
+    # alone, through the pinned block quantizer
+    rng = np.random.default_rng(72)
+    ms = np.array([40, 3], np.int64)
+    M, K = 43, 128
+    x = bf16_bits_from_f32((rng.standard_normal((M, K)) * np.exp2(rng.integers(-3, 3, (M, 1)))).astype(np.float32))
+    o = orc.group_quantize_padded(x, ms, rowwise=False, colwise=True, swizzled=False)
+    xv = f32_from_bf16_bits(x).astype(np.float64)
+    P, _ = orc.padded_offsets(ms)
+    assert o["col_s"].shape == (int(P[-1]) // 32, K)
+    blocks = [(0, 0, 32, 0), (0, 32, 40, 1), (1, 40, 43, P[1] // 32)]  # (expert, first row, end, scale row)
+    for _, r0, r1, srow in blocks:
+        for k in range(K):
+            codes = np.zeros(r1 - r0, np.uint8)
+            code = np.zeros(1, np.uint8)
+            orc.lib().orc_quantize_block(orc._p(np.ascontiguousarray(xv[r0:r1, k])), r1 - r0, orc._p(codes),
+                                         orc._p(code))
+            assert o["col_s"][srow, k] == code[0], (r0, k)
+            assert np.array_equal(o["col_q"][r0:r1, k], codes), (r0, k)
+    # pad scale rows are zero: rows 2..3 of expert 0 (block rows 2, 3) and 5..7 of expert 1
+    used = {0, 1, P[1] // 32}
+    for r in range(o["col_s"].shape[0]):
+        if r not in used:
+            assert np.all(o["col_s"][r] == 0), r
+
+
+def test_padded_swizzled_layouts_hold_every_scale_once(orc):
+    rng = np.random.default_rng(73)
+    ms = np.array([200, 0, 57, 128], np.int64)
+    M, K = int(ms.sum()), 256
+    x = bf16_bits_from_f32(rng.standard_normal((M, K)).astype(np.float32))
+    c = orc.group_quantize_padded(x, ms, swizzled=False)
+    s = orc.group_quantize_padded(x, ms, swizzled=True)
+    P, mp = orc.padded_offsets(ms)
+    R = int(P[-1])
+    # rowwise: the swizzle of the padded (R, K/32) matrix whose real rows are the dense compact scales
+    Sp = orc.pad_rows(c["row_s"][:M, :K // 32], ms)
+    assert np.array_equal(s["row_s"], orc.swizzle(Sp))
+    # colwise: expert e's (K, mp_e/32) matrix at byte K * P_e / 32
+    for e in range(len(ms)):
+        if mp[e] == 0:
+            continue
+        Se = c["col_s"][P[e] // 32:(P[e] + mp[e]) // 32].T
+        base = K * P[e] // 32
+        assert np.array_equal(s["col_s"][base:base + Se.size], orc.swizzle(Se)), e
+    assert s["col_s"].size == K * R // 32 and s["row_s"].size == R * K // 32
+    # and the codes are the padded ones gathered back
+    assert np.array_equal(s["row_q"], c["row_q"]) and np.array_equal(s["col_q"], c["col_q"])
+
+
+def test_padded_dbias_is_the_plain_column_sum(orc):
+    rng = np.random.default_rng(74)
+    ms = np.array([33, 0, 95], np.int64)
+    dy = bf16_bits_from_f32(rng.standard_normal((128, 256)).astype(np.float32))
+    db = orc.grouped_dbias_padded(dy, ms)
+    v = f32_from_bf16_bits(dy).astype(np.float64)
+    assert np.allclose(db[0], v[:33].sum(axis=0), rtol=0, atol=1e-12)
+    assert np.all(db[1] == 0)
+    assert np.allclose(db[2], v[33:].sum(axis=0), rtol=0, atol=1e-12)
