@@ -114,7 +114,9 @@ enum {
     MXQ_SWIZZLE = 4,      /* scales in the swizzled GEMM layout (else compact) */
     MXQ_DEQUANT_OUT = 8,  /* requant: also write the dequantized bf16 tensor */
     MXQ_ACCUMULATE = 16,  /* wgrad: dW += product (else dW = product) */
-    MXQ_OUT_BF16 = 32     /* wgrad: dW in bf16 (else fp32) */
+    MXQ_OUT_BF16 = 32,    /* wgrad: dW in bf16 (else fp32) */
+    MXQ_PAD_EXPERTS = 64  /* group_quantize / requant: expert counts need not be
+                             multiples of 128; see "Padded grouping" below */
 };
 
 /* operation ids for mxq_workspace_bytes */
@@ -137,6 +139,28 @@ MXQ_API int mxq_version(void);
  * shape of [RQ]; for rows % 128 == 0 and cols % 128 == 0 the swizzled
  * layout has the same size. colwise != 0 selects the colwise shape. */
 MXQ_API size_t mxq_scale_bytes(int64_t rows, int64_t cols, int colwise);
+
+/* Padded grouping (flag MXQ_PAD_EXPERTS on mxq_group_quantize and
+ * mxq_requant_colwise) [RQ: the review of the grouped swizzle -- a dense
+ * swizzle is valid only when each expert's tokens are padded to a multiple
+ * of 128; a grouped swizzle handles variable per-expert dims]. Each m_e may
+ * be any count >= 0 (M any, d_m_splits required). Every expert is padded,
+ * in the scale row space only, to round_up(m_e, 128) rows: expert e's scale
+ * rows start at poff_e = sum_{e'<e} round_up(m_e', 128), R = poff_E.
+ *   - E4M3 codes (row and col), the compact rowwise scales and the bf16
+ *     dequant output keep the dense (M, K) layouts;
+ *   - swizzled rowwise scales: the swizzle of the (R, K/32) matrix whose row
+ *     poff_e + i holds token row off_e + i (pad rows 0);
+ *   - colwise blocks are 32 rows of one expert starting at off_e; the last
+ *     block of an expert may hold fewer rows and is scaled by them (as if
+ *     the padding were zero rows). Compact colwise scales: (R/32, K), block
+ *     i of expert e at row poff_e/32 + i; swizzled: expert e's logical
+ *     (K, round_up(m_e,128)/32) matrix at byte K * poff_e / 32; pads 0;
+ *   - dbias as usual (workspace: mxq_workspace_bytes with the flag).
+ * With 128-aligned counts every output equals the unflagged call's.
+ * mxq_scale_bytes_grouped(rows = M, cols = K, E, colwise) is a size that
+ * holds the padded scale buffers for any split of M rows into E experts. */
+MXQ_API size_t mxq_scale_bytes_grouped(int64_t rows, int64_t cols, int E, int colwise);
 
 /* Workspace bytes `op` needs for these sizes and flags (0 if none). For
  * group_quantize / requant it is nonzero only when dbias is requested:

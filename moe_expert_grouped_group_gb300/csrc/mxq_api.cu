@@ -44,9 +44,10 @@ bool device_pointer(const void* p) {
     return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
-int check_common(int64_t M, int64_t K, int E, const int64_t* m_splits, bool splits_required) {
+int check_common(int64_t M, int64_t K, int E, const int64_t* m_splits, bool splits_required, bool padded = false) {
     if (!arch_ok()) return MXQ_ERR_ARCH;
-    if (M < 0 || K <= 0 || M % 128 || K % 128) return MXQ_ERR_SHAPE;
+    if (M < 0 || K <= 0 || (!padded && M % 128) || K % 128) return MXQ_ERR_SHAPE;
+    if (padded && !m_splits) return MXQ_ERR_NULL;
     if (E < 1 || E > MXQ_MAX_EXPERTS) return MXQ_ERR_SHAPE;
     if (M > ((int64_t)1 << 31) - 128 || K > ((int64_t)1 << 31) - 128) return MXQ_ERR_SHAPE;
     if (m_splits == nullptr) {
@@ -71,12 +72,20 @@ size_t mxq_scale_bytes(int64_t rows, int64_t cols, int colwise) {
     return (size_t)(up(rows / 32, 4) * up(cols, 128));
 }
 
+// Rows of the padded scale row space of E experts with M rows in total, at
+// most: sum round_up(m_e, 128) <= round_up(M, 128) + 128 E.
+static int64_t padded_rows_bound(int64_t M, int E) { return (M + 127) / 128 * 128 + (int64_t)128 * E; }
+
+size_t mxq_scale_bytes_grouped(int64_t rows, int64_t cols, int E, int colwise) {
+    if (rows < 0 || cols < 0 || E < 1) return 0;
+    return mxq_scale_bytes(padded_rows_bound(rows, E), cols, colwise);
+}
+
 size_t mxq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int flags) {
-    (void)E;
-    (void)flags;
+    const int64_t Mt = (flags & MXQ_PAD_EXPERTS) ? padded_rows_bound(M, E) : M;
     switch (op) {
         case MXQ_OP_GROUP_QUANTIZE:
-        case MXQ_OP_REQUANT_COLWISE: return (size_t)(M / 128) * (size_t)K * sizeof(float);
+        case MXQ_OP_REQUANT_COLWISE: return (size_t)(Mt / 128) * (size_t)K * sizeof(float);
         case MXQ_OP_GROUPED_DBIAS: return (size_t)(M / 128) * (size_t)N * sizeof(float);
         case MXQ_OP_SWIGLU_BWD_QUANTIZE: return (size_t)(M / 128) * (size_t)(2 * K) * sizeof(float);
         case MXQ_OP_SCALED_BIAS:  // column-sum partials (M/128, K) + row-dot partials (M, K/128)
@@ -90,13 +99,13 @@ size_t mxq_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int f
 int mxq_group_quantize(const void* x_bf16, int64_t M, int64_t K, int E, const int64_t* d_m_splits, int flags,
                        void* row_data, void* row_scale, void* col_data, void* col_scale, float* dbias_out,
                        const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
-    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE)) return MXQ_ERR_FLAGS;
-    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE;
+    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE | MXQ_PAD_EXPERTS)) return MXQ_ERR_FLAGS;
+    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE, pad = flags & MXQ_PAD_EXPERTS;
     if (!row && !col && !dbias_out) return MXQ_ERR_FLAGS;
     // With M == 0 every data buffer is empty (and may be NULL).
     if (M != 0 && (!x_bf16 || (row && (!row_data || !row_scale)) || (col && (!col_data || !col_scale))))
         return MXQ_ERR_NULL;
-    if (int r = check_common(M, K, E, d_m_splits, false)) return r;
+    if (int r = check_common(M, K, E, d_m_splits, false, pad)) return r;
     if (!aligned16(x_bf16) || !aligned16(row_data) || !aligned16(row_scale) || !aligned16(col_data) ||
         !aligned16(col_scale) || !aligned16(dbias_out) || !aligned16(ws))
         return MXQ_ERR_ALIGN;
@@ -117,7 +126,8 @@ int mxq_group_quantize(const void* x_bf16, int64_t M, int64_t K, int E, const in
     c.swizzle = (flags & MXQ_SWIZZLE) != 0;
     c.noop = d_noop;
     c.status = d_status;
-    cudaError_t e = mxq::run_group_quantize(c, (cudaStream_t)stream);
+    cudaError_t e = pad ? mxq::run_group_quantize_padded(c, (cudaStream_t)stream)
+                        : mxq::run_group_quantize(c, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
 }
 
@@ -125,13 +135,14 @@ int mxq_requant_colwise(const void* row_data, const void* row_scale_compact, int
                         const int64_t* d_m_splits, int flags, void* col_data, void* col_scale,
                         void* row_scale_swizzled_out, float* dbias_out, void* dequant_bf16_out,
                         const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
-    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE | MXQ_DEQUANT_OUT)) return MXQ_ERR_FLAGS;
-    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE, deq = flags & MXQ_DEQUANT_OUT;
+    if (flags & ~(MXQ_ROWWISE | MXQ_COLWISE | MXQ_SWIZZLE | MXQ_DEQUANT_OUT | MXQ_PAD_EXPERTS)) return MXQ_ERR_FLAGS;
+    const bool row = flags & MXQ_ROWWISE, col = flags & MXQ_COLWISE, deq = flags & MXQ_DEQUANT_OUT,
+               pad = flags & MXQ_PAD_EXPERTS;
     if (!row && !col && !deq && !dbias_out) return MXQ_ERR_FLAGS;
     if (M != 0 && (!row_data || !row_scale_compact || (col && (!col_data || !col_scale)) ||
                    (row && !row_scale_swizzled_out) || (deq && !dequant_bf16_out)))
         return MXQ_ERR_NULL;
-    if (int r = check_common(M, K, E, d_m_splits, false)) return r;
+    if (int r = check_common(M, K, E, d_m_splits, false, pad)) return r;
     if (!aligned16(row_data) || !aligned16(row_scale_compact) || !aligned16(col_data) || !aligned16(col_scale) ||
         !aligned16(row_scale_swizzled_out) || !aligned16(dbias_out) || !aligned16(dequant_bf16_out) ||
         !aligned16(ws))
@@ -154,7 +165,7 @@ int mxq_requant_colwise(const void* row_data, const void* row_scale_compact, int
     c.swizzle = (flags & MXQ_SWIZZLE) != 0;
     c.noop = d_noop;
     c.status = d_status;
-    cudaError_t e = mxq::run_requant(c, (cudaStream_t)stream);
+    cudaError_t e = pad ? mxq::run_requant_padded(c, (cudaStream_t)stream) : mxq::run_requant(c, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
 }
 

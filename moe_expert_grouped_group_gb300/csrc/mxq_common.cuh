@@ -101,6 +101,58 @@ __device__ __forceinline__ int load_offsets(const int64_t* __restrict__ d_m_spli
     return s_bad;
 }
 
+// The same view for expert counts that need not be multiples of 128: token
+// offsets off[0..E] and padded offsets poff[0..E] (each expert rounded up to
+// 128 rows, the row space of per-expert padded scale layouts). Validates
+// m_e >= 0 and sum == M. Must be called by all threads of the block.
+__device__ __forceinline__ int load_offsets_padded(const int64_t* __restrict__ d_m_splits, int E, int64_t M,
+                                                   int64_t* s_off, int64_t* s_poff) {
+    __shared__ int s_bad;
+    const int tid = threadIdx.x;
+    if (tid < 32) {
+        const int lane = tid;
+        const int per = (E + 31) / 32;
+        const int lo = min(E, lane * per), hi = min(E, lo + per);
+        int64_t local = 0, plocal = 0;
+        int bad = 0;
+        for (int e = lo; e < hi; ++e) {
+            const int64_t v = d_m_splits[e];
+            if (v < 0) bad |= MXQ_STATUS_SPLIT_NEGATIVE;
+            local += v;
+            plocal += (v + 127) / 128 * 128;
+        }
+        int64_t incl = local, pincl = plocal;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            const int64_t pt = __shfl_up_sync(0xffffffffu, pincl, o);
+            if (lane >= o) {
+                incl += t;
+                pincl += pt;
+            }
+        }
+        int64_t run = incl - local, prun = pincl - plocal;
+        for (int e = lo; e < hi; ++e) {
+            const int64_t v = d_m_splits[e];
+            s_off[e] = run;
+            s_poff[e] = prun;
+            run += v;
+            prun += (v + 127) / 128 * 128;
+        }
+        const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+        const int64_t ptotal = __shfl_sync(0xffffffffu, pincl, 31);
+        bad = __reduce_or_sync(0xffffffffu, bad);
+        if (lane == 0) {
+            s_off[E] = total;
+            s_poff[E] = ptotal;
+            if (total != M) bad |= MXQ_STATUS_SPLIT_SUM;
+            s_bad = bad;
+        }
+    }
+    __syncthreads();
+    return s_bad;
+}
+
 // Expert owning row `row` (0 <= row < M): the e with off[e] <= row < off[e+1].
 __device__ __forceinline__ int expert_of(const int64_t* s_off, int E, int64_t row) {
     int lo = 0, hi = E - 1;

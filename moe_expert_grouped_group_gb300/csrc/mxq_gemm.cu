@@ -414,7 +414,6 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
     if (lane == 0) mbar_arrive(acc_empty);  // the MMA warp may start the next tile
 
     const int64_t f0 = T.b_col + 64 * half;  // first gate (and h) column of this warp
-    const int64_t row = T.a_row + q * 32 + lane;
 
     // y1 = bf16(acc + bias): y[0, 32) gate pairs, y[32, 64) up pairs
     uint32_t y[64];

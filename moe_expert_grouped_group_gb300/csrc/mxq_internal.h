@@ -109,6 +109,9 @@ cudaError_t run_requant(const RequantCall& c, cudaStream_t s);
 cudaError_t run_grouped_dbias(const void* dy, int64_t M, int64_t N, int E, const int64_t* m_splits, float* out,
                               float* partials, int32_t* status, cudaStream_t s);
 cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s);
+// Expert counts that need not be multiples of 128 (per-expert padded scales).
+cudaError_t run_group_quantize_padded(const QuantCall& c, cudaStream_t s);
+cudaError_t run_requant_padded(const RequantCall& c, cudaStream_t s);
 cudaError_t run_swiglu_quantize(const SwigluQuantCall& c, cudaStream_t s);
 // out[e, :] = fp64 sum, in order, of expert e's partial rows; each partial row
 // covers rows_per_partial consecutive token rows.

@@ -17,7 +17,7 @@ import torch
 
 from .build import LIB
 
-ROWWISE, COLWISE, SWIZZLE, DEQUANT_OUT, ACCUMULATE, OUT_BF16 = 1, 2, 4, 8, 16, 32
+ROWWISE, COLWISE, SWIZZLE, DEQUANT_OUT, ACCUMULATE, OUT_BF16, PAD_EXPERTS = 1, 2, 4, 8, 16, 32, 64
 OP_GROUP_QUANTIZE, OP_REQUANT_COLWISE, OP_GROUPED_DBIAS = 1, 2, 3
 OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD, OP_SWIGLU_BWD_QUANTIZE, OP_SCALED_BIAS = 4, 5, 6, 7, 8
 OP_GEMM_DGRAD_SWIGLU = 9
@@ -29,6 +29,7 @@ SYMBOLS = [
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
     "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu", "mxq_grouped_gemm_dgrad_swiglu",
+    "mxq_scale_bytes_grouped",
 ]
 
 
@@ -48,6 +49,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_version.restype = _INT
     L.mxq_scale_bytes.argtypes = [_I64, _I64, _INT]
     L.mxq_scale_bytes.restype = _SZ
+    L.mxq_scale_bytes_grouped.argtypes = [_I64, _I64, _INT, _INT]
+    L.mxq_scale_bytes_grouped.restype = _SZ
     L.mxq_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64, _INT, _INT]
     L.mxq_workspace_bytes.restype = _SZ
     L.mxq_group_quantize.argtypes = [_P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]
@@ -125,6 +128,11 @@ def scale_bytes(rows: int, cols: int, colwise: bool) -> int:
     return int(lib().mxq_scale_bytes(rows, cols, int(colwise)))
 
 
+def scale_bytes_grouped(rows: int, cols: int, E: int, colwise: bool) -> int:
+    """A scale-buffer size that holds the per-expert padded layout for any split of `rows`."""
+    return int(lib().mxq_scale_bytes_grouped(rows, cols, E, int(colwise)))
+
+
 def workspace_bytes(op: int, M: int, N: int, K: int, E: int, flags: int = 0) -> int:
     return int(lib().mxq_workspace_bytes(op, M, N, K, E, flags))
 
@@ -144,8 +152,9 @@ def _u8(n, dev):
 
 
 def group_quantize(x, m_splits=None, E=None, rowwise=True, colwise=True, swizzle=True, dbias=False,
-                   noop=None, status=None, out=None, workspace=None):
-    """bf16 x (M, K) -> dict(row_data, row_scale, col_data, col_scale, dbias)."""
+                   noop=None, status=None, out=None, workspace=None, pad_experts=False):
+    """bf16 x (M, K) -> dict(row_data, row_scale, col_data, col_scale, dbias).
+    pad_experts: expert counts need not be multiples of 128 (per-expert padded scale layouts)."""
     M, K = x.shape
     m_splits = _splits(m_splits)
     if E is None:
@@ -153,18 +162,22 @@ def group_quantize(x, m_splits=None, E=None, rowwise=True, colwise=True, swizzle
             raise MXQError("E is required for uniform members")
         E = m_splits.numel()
     dev = x.device
-    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
+    flags = ((ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
+             | (PAD_EXPERTS if pad_experts else 0))
     o = dict(out or {})
     if rowwise:
         o.setdefault("row_data", _u8((M, K), dev))
-        o.setdefault("row_scale", _u8(scale_bytes(M, K, False), dev))
+        rs = scale_bytes_grouped(M, K, E, False) if (pad_experts and swizzle) else scale_bytes(M, K, False)
+        o.setdefault("row_scale", _u8(rs, dev))
     if colwise:
         o.setdefault("col_data", _u8((M, K), dev))
-        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+        o.setdefault("col_scale", _u8(scale_bytes_grouped(M, K, E, True) if pad_experts else scale_bytes(M, K, True),
+                                      dev))
     ws = None
     if dbias:
         o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
-        ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_GROUP_QUANTIZE, M, 0, K, E)), dev)
+        ws = workspace if workspace is not None else _u8(
+            max(16, workspace_bytes(OP_GROUP_QUANTIZE, M, 0, K, E, flags)), dev)
     rc = lib().mxq_group_quantize(
         _ptr(x), M, K, E, _ptr(m_splits), flags, _ptr(o.get("row_data")), _ptr(o.get("row_scale")),
         _ptr(o.get("col_data")), _ptr(o.get("col_scale")), _ptr(o.get("dbias")), _ptr(noop), _ptr(status),
@@ -174,26 +187,29 @@ def group_quantize(x, m_splits=None, E=None, rowwise=True, colwise=True, swizzle
 
 
 def requant_colwise(row_data, row_scale_compact, m_splits, colwise=True, swizzle=True, row_scale_swizzled=True,
-                    dbias=False, dequant=False, noop=None, status=None, out=None, workspace=None):
-    """Rowwise E4M3 (M, K) + compact scales -> dict(col_data, col_scale, row_scale_swizzled, dbias, dequant)."""
+                    dbias=False, dequant=False, noop=None, status=None, out=None, workspace=None, pad_experts=False):
+    """Rowwise E4M3 (M, K) + compact scales -> dict(col_data, col_scale, row_scale_swizzled, dbias, dequant).
+    pad_experts: expert counts need not be multiples of 128 (per-expert padded scale layouts)."""
     M, K = row_data.shape
     m_splits = _splits(m_splits)
     E = m_splits.numel()
     dev = row_data.device
     flags = ((COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0) | (ROWWISE if row_scale_swizzled else 0)
-             | (DEQUANT_OUT if dequant else 0))
+             | (DEQUANT_OUT if dequant else 0) | (PAD_EXPERTS if pad_experts else 0))
+    sb = (lambda r, c, cw: scale_bytes_grouped(r, c, E, cw)) if pad_experts else scale_bytes
     o = dict(out or {})
     if colwise:
         o.setdefault("col_data", _u8((M, K), dev))
-        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+        o.setdefault("col_scale", _u8(sb(M, K, True), dev))
     if row_scale_swizzled:
-        o.setdefault("row_scale_swizzled", _u8(scale_bytes(M, K, False), dev))
+        o.setdefault("row_scale_swizzled", _u8(sb(M, K, False), dev))
     if dequant:
         o.setdefault("dequant", torch.empty((M, K), dtype=torch.bfloat16, device=dev))
     ws = None
     if dbias:
         o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
-        ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_REQUANT_COLWISE, M, 0, K, E)), dev)
+        ws = workspace if workspace is not None else _u8(
+            max(16, workspace_bytes(OP_REQUANT_COLWISE, M, 0, K, E, flags)), dev)
     rc = lib().mxq_requant_colwise(
         _ptr(row_data), _ptr(row_scale_compact), M, K, E, _ptr(m_splits), flags, _ptr(o.get("col_data")),
         _ptr(o.get("col_scale")), _ptr(o.get("row_scale_swizzled")), _ptr(o.get("dbias")), _ptr(o.get("dequant")),

@@ -1,0 +1,153 @@
+"""GPU parity: grouped quantization, requant and dbias with expert counts
+that are not multiples of 128 (flag MXQ_PAD_EXPERTS: per-expert padded scale
+layouts, after TransformerEngine PR #3244's review of the grouped swizzle),
+against the oracle's padded grouping, through the C ABI. Codes and scales
+bit-exact (scale buffers are compared over the padded row space the splits
+actually use); dbias within 1e-5 * sum|x| per column."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from synth import WORKLOADS, bf16_bits_from_f32, make_inputs
+from tests._gpu import bf16_to_f64, dev_bf16, dev_i64, dev_u8, first_diff, host, lib, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mxq():
+    require_gpu()
+    return lib()
+
+
+SPLITS = [
+    [40, 3],                      # M = 43: partial blocks, M not a multiple of 128
+    [128, 256, 0, 128],           # aligned (must equal the unflagged call)
+    [200, 0, 57, 128, 1],         # empty and one-row experts
+    [96, 160, 32, 224],           # multiples of 32, not of 128
+    [0, 0, 300],
+    [17] * 11,                    # many small experts inside one 128-row slice
+]
+
+
+def _x(M, K, seed):
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((M, K)) * np.exp2(rng.integers(-4, 4, (M, 1)))).astype(np.float32)
+    x[rng.random((M, K)) < 0.001] *= 1000.0
+    return bf16_bits_from_f32(x)
+
+
+def _cmp_scales(got, ref, what):
+    ref = np.asarray(ref).reshape(-1)
+    got = host(got).reshape(-1)[:ref.size]
+    assert np.array_equal(got, ref), (what, first_diff(got, ref))
+
+
+@pytest.mark.parametrize("swz", [True, False])
+@pytest.mark.parametrize("splits", SPLITS, ids=["_".join(map(str, s[:5])) for s in SPLITS])
+def test_padded_group_quantize(mxq, splits, swz):
+    ms = np.array(splits, np.int64)
+    M, K = int(ms.sum()), 384
+    x = _x(M, K, 81)
+    q = mxq.group_quantize(dev_bf16(x), dev_i64(ms), swizzle=swz, dbias=True, pad_experts=True)
+    o = orc.group_quantize_padded(x, ms, swizzled=swz)
+    assert np.array_equal(host(q["row_data"]), o["row_q"])
+    assert np.array_equal(host(q["col_data"]), o["col_q"])
+    if swz:
+        _cmp_scales(q["row_scale"], o["row_s"], "row_s")
+    else:  # dense compact rowwise scales: the rows the tensor has
+        got = host(q["row_scale"]).reshape(o["row_s"].shape)[:M]
+        assert np.array_equal(got, o["row_s"][:M])
+    _cmp_scales(q["col_scale"], o["col_s"], "col_s")
+    db = orc.grouped_dbias_padded(x, ms)
+    a = np.abs(bf16_to_f64(x))
+    off = np.concatenate([[0], np.cumsum(ms)])
+    got = host(q["dbias"]).astype(np.float64)
+    for e in range(len(ms)):
+        tol = 1e-5 * a[off[e]:off[e + 1]].sum(axis=0) + 1e-30
+        assert np.all(np.abs(got[e] - db[e]) <= tol), e
+
+
+def test_padded_flag_with_aligned_splits_changes_nothing(mxq):
+    ms = np.array([256, 0, 128, 384], np.int64)
+    M, K = int(ms.sum()), 512
+    x = dev_bf16(_x(M, K, 82))
+    for swz in (True, False):
+        a = mxq.group_quantize(x, dev_i64(ms), swizzle=swz, dbias=True)
+        b = mxq.group_quantize(x, dev_i64(ms), swizzle=swz, dbias=True, pad_experts=True)
+        for k in a:
+            assert torch.equal(a[k], b[k].view(-1)[:a[k].numel()].view(a[k].shape)), (swz, k)
+
+
+@pytest.mark.parametrize("swz", [True, False])
+@pytest.mark.parametrize("splits", SPLITS[2:5], ids=["_".join(map(str, s[:5])) for s in SPLITS[2:5]])
+def test_padded_requant(mxq, splits, swz):
+    ms = np.array(splits, np.int64)
+    M, K = int(ms.sum()), 256
+    x = _x(M, K, 83)
+    # the wire format: dense rowwise codes and dense compact scales (rowwise blocks ignore the grouping)
+    wire = orc.group_quantize_padded(x, ms, rowwise=True, colwise=False, swizzled=False)
+    r = mxq.requant_colwise(dev_u8(wire["row_q"]), dev_u8(wire["row_s"]), dev_i64(ms), swizzle=swz, dbias=True,
+                            dequant=True, pad_experts=True)
+    o = orc.requant_colwise_padded(wire["row_q"], wire["row_s"], ms, swizzled=swz, dbias=True, dequant=True)
+    assert np.array_equal(host(r["col_data"]), o["col_q"])
+    _cmp_scales(r["col_scale"], o["col_s"], "col_s")
+    _cmp_scales(r["row_scale_swizzled"], o["row_s_swizzled"], "row_s_swizzled")
+    assert np.array_equal(host(r["dequant"]), o["deq"])
+    deq = orc.dequant_rowwise(wire["row_q"], wire["row_s"])
+    off = np.concatenate([[0], np.cumsum(ms)])
+    got = host(r["dbias"]).astype(np.float64)
+    for e in range(len(ms)):
+        tol = 1e-5 * np.abs(deq[off[e]:off[e + 1]]).sum(axis=0) + 1e-30
+        assert np.all(np.abs(got[e] - o["dbias"][e]) <= tol), e
+
+
+def test_padded_status_bits(mxq):
+    M, K = 300, 128
+    x = dev_bf16(_x(M, K, 84))
+    for bad, bit in (([100, -50, 250], 2), ([100, 150], 4)):
+        status = mxq.new_status()
+        out = {"row_data": torch.full((M, K), 7, dtype=torch.uint8, device="cuda")}
+        mxq.group_quantize(x, dev_i64(bad), colwise=False, status=status, out=out, pad_experts=True)
+        assert mxq.status_read(status) & bit
+        assert torch.all(out["row_data"] == 7)
+    status = mxq.new_status()
+    mxq.group_quantize(x, dev_i64([100, 200]), status=status, pad_experts=True)
+    assert mxq.status_read(status) == 0  # unaligned counts are valid with the flag
+
+
+def test_full_size_padded_unaligned_routing(mxq):
+    """The 64-expert workload's 83968 routed rows with counts NOT rounded to 128: seeded
+    moves of rows between experts (sum kept), quantize with dbias and requant of the
+    same rows as a wire format."""
+    w = WORKLOADS["e64_h3072_f1024_t84k_prequant"]
+    d = make_inputs(w, which=("dy2",))
+    rng = np.random.default_rng([0, w.wid, 10])
+    ms = d["m_splits"].copy()
+    for _ in range(256):
+        a, b = rng.integers(0, w.E, 2)
+        mv = int(min(ms[a], rng.integers(1, 200)))
+        ms[a] -= mv
+        ms[b] += mv
+    assert ms.sum() == w.M and np.any(ms % 128)
+    x = d["dy2"]
+    q = mxq.group_quantize(dev_bf16(x), dev_i64(ms), dbias=True, pad_experts=True)
+    o = orc.group_quantize_padded(x, ms, swizzled=True)
+    assert np.array_equal(host(q["row_data"]), o["row_q"])
+    assert np.array_equal(host(q["col_data"]), o["col_q"])
+    _cmp_scales(q["row_scale"], o["row_s"], "row_s")
+    _cmp_scales(q["col_scale"], o["col_s"], "col_s")
+    db = orc.grouped_dbias_padded(x, ms)
+    a = np.abs(bf16_to_f64(x))
+    off = np.concatenate([[0], np.cumsum(ms)])
+    got = host(q["dbias"]).astype(np.float64)
+    for e in range(w.E):
+        assert np.all(np.abs(got[e] - db[e]) <= 1e-5 * a[off[e]:off[e + 1]].sum(axis=0) + 1e-30), e
+    del q, o, a
+    wire = orc.group_quantize_padded(x, ms, rowwise=True, colwise=False, swizzled=False)
+    r = mxq.requant_colwise(dev_u8(wire["row_q"]), dev_u8(wire["row_s"]), dev_i64(ms), pad_experts=True)
+    o = orc.requant_colwise_padded(wire["row_q"], wire["row_s"], ms, swizzled=True)
+    assert np.array_equal(host(r["col_data"]), o["col_q"])
+    _cmp_scales(r["col_scale"], o["col_s"], "col_s")
+    _cmp_scales(r["row_scale_swizzled"], o["row_s_swizzled"], "row_s_swizzled")
