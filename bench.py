@@ -54,11 +54,12 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
-    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp"],
+    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp", "padded"],
                    help="time only one fused kernel family on the MLP workload's shapes and print its line (a "
                         "small footprint for profilers): the SwiGLU->quantize kernels (forward and backward), "
-                        "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions, or the "
-                        "SwiGLU-fused FC1 fprop and FC2 dgrad vs their unfused pairs")
+                        "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions, the "
+                        "SwiGLU-fused FC1 fprop and FC2 dgrad vs their unfused pairs, or group_quantize with "
+                        "expert counts that are not multiples of 128")
     return p.parse_args()
 
 
@@ -487,6 +488,61 @@ def time_fused_mlp(dev, steps, warmup):
     return res
 
 
+def unaligned_splits(w, ms):
+    """The workload's routed rows with counts NOT rounded to 128: seeded moves of rows
+    between experts, the total kept."""
+    rng = np.random.default_rng([0, w.wid, 10])
+    ms = ms.copy()
+    for _ in range(256):
+        a, b = rng.integers(0, w.E, 2)
+        mv = int(min(ms[a], rng.integers(1, 200)))
+        ms[a] -= mv
+        ms[b] += mv
+    return ms
+
+
+def time_padded(dev, steps, warmup):
+    """group_quantize (row + col + dbias, swizzled) of the 83968 x 3072 FC2 gradient: aligned
+    counts, aligned counts through the padded-grouping path, and unaligned counts."""
+    import torch
+
+    import moe_expert_grouped_group_gb300 as mxq
+    from synth import WORKLOADS, make_inputs
+
+    w = WORKLOADS[MLP_WORKLOAD]
+    d = make_inputs(w, which=("dy2",))
+    M, K, E = w.M, w.K, w.E
+    x = torch.from_numpy(np.ascontiguousarray(d["dy2"]).view(np.int16)).to(dev).view(torch.bfloat16)
+    ms_a = torch.from_numpy(d["m_splits"]).to(dev)
+    ms_u = torch.from_numpy(unaligned_splits(w, d["m_splits"])).to(dev)
+    outs = {k: mxq.group_quantize(x, ms_a, dbias=True, pad_experts=(k != "aligned"))
+            for k in ("aligned", "aligned_padded_path", "unaligned")}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    runs = {"aligned": lambda: mxq.group_quantize(x, ms_a, dbias=True, out=outs["aligned"]),
+            "aligned_padded_path": lambda: mxq.group_quantize(x, ms_a, dbias=True, pad_experts=True,
+                                                              out=outs["aligned_padded_path"]),
+            "unaligned": lambda: mxq.group_quantize(x, ms_u, dbias=True, pad_experts=True, out=outs["unaligned"])}
+    res = {"workload": MLP_WORKLOAD, "rows": M, "cols": K, "steps": steps, "warmup": warmup,
+           "unaligned_experts": int((unaligned_splits(w, d["m_splits"]) % 128 != 0).sum()),
+           "l2": "256 MiB buffer written before every launch"}
+    nbytes = M * K * (2 + 2 + 2 / 32)
+    _, hbm, _ = peaks()
+    for name, fn in runs.items():
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(warmup + steps):
+            flush.fill_(1)
+            if i >= warmup:
+                ev[i - warmup][0].record()
+            fn()
+            if i >= warmup:
+                ev[i - warmup][1].record()
+        torch.cuda.synchronize()
+        us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+        res[name + "_us"] = us
+        res[name + "_frac"] = nbytes / (us * 1e-6) / 1e9 / hbm
+    return res
+
+
 KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
 
 
@@ -701,6 +757,11 @@ def main():
         _, hbm_peak, src = peaks()
         r.update(fwd_frac=r["fwd_gbs"] / hbm_peak, bwd_frac=r["bwd_gbs"] / hbm_peak, hbm_peak_gbs=hbm_peak,
                  peak_source=src)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
+    if args.only == "padded":
+        r = time_padded(dev, max(1, args.steps), max(1, args.warmup))
         if rank == 0:
             print(json.dumps(r), flush=True)
         return

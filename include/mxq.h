@@ -239,6 +239,21 @@ MXQ_API int mxq_grouped_gemm_fprop(const void* x_data, const void* x_scale, cons
                            const int64_t* d_m_splits, void* y_bf16, int32_t* d_status, void* ws,
                            size_t ws_bytes, mxq_stream_t stream);
 
+/* mxq_grouped_gemm_fprop / _dgrad with flags. MXQ_PAD_EXPERTS: expert
+ * counts need not be multiples of 128 (M any, E <= 512); the activation's
+ * (X's, or dY's) rowwise scales are in the padded swizzled layout that
+ * mxq_group_quantize / mxq_requant_colwise produce with the same flag;
+ * rows are processed per expert in 128-row slices and only the expert's
+ * rows of the output are written. Without flags these are the plain calls. */
+MXQ_API int mxq_grouped_gemm_fprop_ex(const void* x_data, const void* x_scale, const void* w_data,
+                                      const void* w_scale, const void* bias_bf16, int64_t M, int64_t N, int64_t K,
+                                      int E, const int64_t* d_m_splits, int flags, void* y_bf16, int32_t* d_status,
+                                      void* ws, size_t ws_bytes, mxq_stream_t stream);
+MXQ_API int mxq_grouped_gemm_dgrad_ex(const void* dy_data, const void* dy_scale, const void* w_col_data,
+                                      const void* w_col_scale, int64_t M, int64_t N, int64_t K, int E,
+                                      const int64_t* d_m_splits, int flags, void* dx_bf16, int32_t* d_status,
+                                      void* ws, size_t ws_bytes, mxq_stream_t stream);
+
 /* grouped fprop of FC1 with SwiGLU and its quantization in the epilogue
  * (the fused grouped MLP's FC1 -> activation [FM]; quantization as
  * mxq_group_quantize [RQ][DI]). x_data (M, K) E4M3 rowwise with swizzled
@@ -294,7 +309,10 @@ MXQ_API int mxq_grouped_gemm_dgrad_swiglu(const void* dy_data, const void* dy_sc
  * colwise scales, X colwise (M,K) + per-expert swizzled colwise scales.
  * dW (E,N,K) fp32 (bf16 with MXQ_OUT_BF16); MXQ_ACCUMULATE adds into dW.
  * An empty expert gets dW[e] = 0 (unchanged with MXQ_ACCUMULATE).
- * K % 256 == 0. */
+ * MXQ_PAD_EXPERTS: expert counts need not be multiples of 128 (M any,
+ * E <= 512), both colwise scale sets in the padded layout; the tokens past
+ * an expert in its last 128-token block are cleared on chip before the
+ * MMAs. K % 256 == 0. */
 MXQ_API int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_scale, const void* x_col_data,
                            const void* x_col_scale, int64_t M, int64_t N, int64_t K, int E,
                            const int64_t* d_m_splits, int flags, void* dw, int32_t* d_status, void* ws,

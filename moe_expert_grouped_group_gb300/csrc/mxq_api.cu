@@ -280,14 +280,16 @@ int mxq_grouped_dbias(const void* dy_bf16, int64_t M, int64_t N, int E, const in
 
 static int gemm_common(int mode, const void* a, const void* as, const void* b, const void* bs, const void* bias,
                        int64_t M, int64_t N, int64_t K, int E, const int64_t* m_splits, void* out, int accumulate,
-                       int out_bf16, int32_t* d_status, mxq_stream_t stream, const mxq::GemmExtra* extra = nullptr) {
+                       int out_bf16, int32_t* d_status, mxq_stream_t stream, const mxq::GemmExtra* extra = nullptr,
+                       bool pad = false) {
     // With M == 0 the token-major operands (and fprop/dgrad outputs) are empty.
     const bool a_empty_ok = (M == 0), b_empty_ok = (M == 0 && mode == mxq::kWgrad);
     const bool out_empty_ok = (M == 0 && mode != mxq::kWgrad) || mode == mxq::kDgradSwiglu;
     if ((!a && !a_empty_ok) || (!as && !a_empty_ok) || (!b && !b_empty_ok) || (!bs && !b_empty_ok) ||
         (!out && !out_empty_ok))
         return MXQ_ERR_NULL;
-    if (int r = check_common(M, K, E, m_splits, true)) return r;
+    if (int r = check_common(M, K, E, m_splits, true, pad)) return r;
+    if (pad && E > 512) return MXQ_ERR_SHAPE;  // the padded offset table's shared-memory budget
     if (N <= 0 || N % 128 || N > ((int64_t)1 << 31) / 128) return MXQ_ERR_SHAPE;
     if ((int64_t)E * N > ((int64_t)1 << 31) - 256) return MXQ_ERR_SHAPE;
     const bool fwd = (mode == mxq::kFprop || mode == mxq::kFpropSwiglu);
@@ -311,6 +313,7 @@ static int gemm_common(int mode, const void* a, const void* as, const void* b, c
     c.accumulate = accumulate;
     c.out_bf16 = out_bf16;
     c.status = d_status;
+    c.pad = pad;
     if (extra) {
         c.q_row = extra->q_row;
         c.q_row_s = extra->q_row_s;
@@ -377,24 +380,42 @@ int mxq_grouped_gemm_dgrad_swiglu(const void* dy_data, const void* dy_scale, con
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
 }
 
+int mxq_grouped_gemm_fprop_ex(const void* x_data, const void* x_scale, const void* w_data, const void* w_scale,
+                              const void* bias_bf16, int64_t M, int64_t N, int64_t K, int E,
+                              const int64_t* d_m_splits, int flags, void* y_bf16, int32_t* d_status, void* ws,
+                              size_t ws_bytes, mxq_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (flags & ~MXQ_PAD_EXPERTS) return MXQ_ERR_FLAGS;
+    return gemm_common(mxq::kFprop, x_data, x_scale, w_data, w_scale, bias_bf16, M, N, K, E, d_m_splits, y_bf16, 0, 1,
+                       d_status, stream, nullptr, (flags & MXQ_PAD_EXPERTS) != 0);
+}
+
 int mxq_grouped_gemm_fprop(const void* x_data, const void* x_scale, const void* w_data, const void* w_scale,
                            const void* bias_bf16, int64_t M, int64_t N, int64_t K, int E,
                            const int64_t* d_m_splits, void* y_bf16, int32_t* d_status, void* ws,
                            size_t ws_bytes, mxq_stream_t stream) {
+    return mxq_grouped_gemm_fprop_ex(x_data, x_scale, w_data, w_scale, bias_bf16, M, N, K, E, d_m_splits, 0, y_bf16,
+                                     d_status, ws, ws_bytes, stream);
+}
+
+int mxq_grouped_gemm_dgrad_ex(const void* dy_data, const void* dy_scale, const void* w_col_data,
+                              const void* w_col_scale, int64_t M, int64_t N, int64_t K, int E,
+                              const int64_t* d_m_splits, int flags, void* dx_bf16, int32_t* d_status, void* ws,
+                              size_t ws_bytes, mxq_stream_t stream) {
     (void)ws;
     (void)ws_bytes;
-    return gemm_common(mxq::kFprop, x_data, x_scale, w_data, w_scale, bias_bf16, M, N, K, E, d_m_splits, y_bf16, 0, 1,
-                       d_status, stream);
+    if (flags & ~MXQ_PAD_EXPERTS) return MXQ_ERR_FLAGS;
+    return gemm_common(mxq::kDgrad, dy_data, dy_scale, w_col_data, w_col_scale, nullptr, M, N, K, E, d_m_splits,
+                       dx_bf16, 0, 1, d_status, stream, nullptr, (flags & MXQ_PAD_EXPERTS) != 0);
 }
 
 int mxq_grouped_gemm_dgrad(const void* dy_data, const void* dy_scale, const void* w_col_data,
                            const void* w_col_scale, int64_t M, int64_t N, int64_t K, int E,
                            const int64_t* d_m_splits, void* dx_bf16, int32_t* d_status, void* ws,
                            size_t ws_bytes, mxq_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
-    return gemm_common(mxq::kDgrad, dy_data, dy_scale, w_col_data, w_col_scale, nullptr, M, N, K, E, d_m_splits,
-                       dx_bf16, 0, 1, d_status, stream);
+    return mxq_grouped_gemm_dgrad_ex(dy_data, dy_scale, w_col_data, w_col_scale, M, N, K, E, d_m_splits, 0, dx_bf16,
+                                     d_status, ws, ws_bytes, stream);
 }
 
 int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_scale, const void* x_col_data,
@@ -403,9 +424,10 @@ int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_scale, co
                            size_t ws_bytes, mxq_stream_t stream) {
     (void)ws;
     (void)ws_bytes;
-    if (flags & ~(MXQ_ACCUMULATE | MXQ_OUT_BF16)) return MXQ_ERR_FLAGS;
+    if (flags & ~(MXQ_ACCUMULATE | MXQ_OUT_BF16 | MXQ_PAD_EXPERTS)) return MXQ_ERR_FLAGS;
     return gemm_common(mxq::kWgrad, dy_col_data, dy_col_scale, x_col_data, x_col_scale, nullptr, M, N, K, E,
-                       d_m_splits, dw, (flags & MXQ_ACCUMULATE) != 0, (flags & MXQ_OUT_BF16) != 0, d_status, stream);
+                       d_m_splits, dw, (flags & MXQ_ACCUMULATE) != 0, (flags & MXQ_OUT_BF16) != 0, d_status, stream,
+                       nullptr, (flags & MXQ_PAD_EXPERTS) != 0);
 }
 
 int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream) {

@@ -76,6 +76,9 @@ constexpr int BAR_REGION = SF_REGION + STAGES * SF_STAGE_BYTES;
 constexpr int EPI_REGION = BAR_REGION + 256;
 constexpr int TABLE_REGION = EPI_REGION + EPI_WARPS * EPI_STAGE_BYTES;
 __host__ __device__ constexpr int smem_bytes(int E) { return 1024 + TABLE_REGION + 8 * (E + 1) + 2 * E; }
+// padded grouping keeps a second (E+1)-entry offset table
+__host__ __device__ constexpr int smem_bytes_padded(int E) { return smem_bytes(E) + 8 * (E + 1); }
+constexpr int MAX_EXPERTS_PADDED = 512;  // smem_bytes_padded(512) fits the 227 KB per-block limit
 
 struct Params {
     int mode;
@@ -164,6 +167,11 @@ struct Tile {
     int64_t off, me; // expert token offset / count
     int nk;          // number of 128-deep K blocks
     bool valid;
+    // padded grouping (expert counts not multiples of 128; the aligned values otherwise)
+    int64_t pa_row;  // fprop/dgrad: the tile's first row in the padded scale row space
+    int vr;          // fprop/dgrad: rows of the tile inside its expert
+    int64_t poff, mp;// the expert's padded first row / padded row count
+    int vk;          // wgrad: tokens of the expert in its last 128-deep K block
 };
 
 struct Sched {
@@ -172,14 +180,17 @@ struct Sched {
     int E;
     const int64_t* off;     // shared: exclusive offsets
     const int16_t* order;   // shared (wgrad): experts sorted by load, heaviest first
+    const int64_t* poff;    // shared (padded grouping): padded offsets, each expert rounded up to 128 rows
+    bool pad;
     int64_t tiles_n;        // fprop/dgrad: output col tiles; wgrad: tiles per expert
     int64_t total;
 
     __device__ void init(int mode_, int64_t M_, int64_t N_, int64_t K_, int E_, const int64_t* off_,
-                         const int16_t* order_) {
-        mode = mode_; M = M_; N = N_; K = K_; E = E_; off = off_; order = order_;
-        if (mode == kFprop || mode == kFpropSwiglu) { tiles_n = N / BN; total = (M / BM) * tiles_n; }
-        else if (mode == kDgrad || mode == kDgradSwiglu) { tiles_n = K / BN; total = (M / BM) * tiles_n; }
+                         const int16_t* order_, const int64_t* poff_ = nullptr, bool pad_ = false) {
+        mode = mode_; M = M_; N = N_; K = K_; E = E_; off = off_; order = order_; poff = poff_; pad = pad_;
+        const int64_t row_tiles = (pad ? poff[E] : M) / BM;  // padded grouping: each expert's 128-row slices
+        if (mode == kFprop || mode == kFpropSwiglu) { tiles_n = N / BN; total = row_tiles * tiles_n; }
+        else if (mode == kDgrad || mode == kDgradSwiglu) { tiles_n = K / BN; total = row_tiles * tiles_n; }
         else { tiles_n = (N / BM) * (K / BN); total = (int64_t)E * tiles_n; }
     }
     // i-th tile of CTA `cta` among `ncta` (serpentine deal over the ordered list)
@@ -193,23 +204,43 @@ struct Sched {
         if (!T.valid) return T;
         if (mode != kWgrad) {
             const int64_t mt = t / tiles_n, nt = t % tiles_n;
-            T.a_row = mt * BM;
             // kFpropSwiglu: tile nt covers gate columns [128 nt, +128) and the
             // matching up columns [N/2 + 128 nt, +128)
             T.b_col = nt * (mode == kFpropSwiglu ? BN / 2 : BN);
-            T.e = expert_of(off, E, T.a_row);
-            T.off = off[T.e];
-            T.me = off[T.e + 1] - T.off;
+            if (!pad) {
+                T.a_row = T.pa_row = mt * BM;
+                T.e = expert_of(off, E, T.a_row);
+                T.off = T.poff = off[T.e];
+                T.me = T.mp = off[T.e + 1] - T.off;
+                T.vr = BM;
+            } else {
+                // slice j of expert e: token rows off_e + 128 j .., scale rows poff_e + 128 j ..
+                T.e = expert_of(poff, E, mt * BM);
+                const int64_t j = mt - poff[T.e] / BM;
+                T.off = off[T.e];
+                T.me = off[T.e + 1] - T.off;
+                T.poff = poff[T.e];
+                T.mp = poff[T.e + 1] - T.poff;
+                T.a_row = T.off + j * BM;
+                T.pa_row = T.poff + j * BM;
+                const int64_t left = T.me - j * BM;
+                T.vr = (int)(left < BM ? left : BM);
+            }
             T.nk = (int)((mode == kDgrad || mode == kDgradSwiglu ? N : K) / BK);
+            T.vk = BK;
         } else {
             const int64_t ei = t / tiles_n, r = t % tiles_n;
             const int64_t kt = K / BN;
             T.e = order[ei];
-            T.a_row = (r / kt) * BM;
+            T.a_row = T.pa_row = (r / kt) * BM;
             T.b_col = (r % kt) * BN;
             T.off = off[T.e];
             T.me = off[T.e + 1] - T.off;
-            T.nk = (int)(T.me / BK);
+            T.poff = pad ? poff[T.e] : T.off;
+            T.mp = pad ? poff[T.e + 1] - T.poff : T.me;
+            T.nk = (int)(T.mp / BK);  // padded grouping: the last block may hold fewer tokens
+            T.vk = (int)(T.me - (int64_t)(T.nk > 0 ? T.nk - 1 : 0) * BK);
+            T.vr = BM;
         }
         return T;
     }
@@ -477,19 +508,24 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
     quant_block32(w1, p, T, F, T.a_row + q * 32, f0 + 32, lane);
 }
 
-template <int kMode>
+// kPad: padded grouping (expert counts need not be multiples of 128; A's
+// rowwise scales, or wgrad's colwise scales, in the per-expert padded layout).
+template <int kMode, bool kPad = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align<1024>(smem_raw);
+    // tables: offsets (E+1) [kPad: padded offsets (E+1)] expert order (E)
     int64_t* s_off = reinterpret_cast<int64_t*>(smem + TABLE_REGION);
-    int16_t* s_order = reinterpret_cast<int16_t*>(s_off + p.E + 1);
+    int64_t* s_poff = s_off + p.E + 1;
+    int16_t* s_order = reinterpret_cast<int16_t*>(kPad ? s_poff + p.E + 1 : s_off + p.E + 1);
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bad = load_offsets(p.m_splits, p.E, p.M, s_off);
+    const int bad = kPad ? load_offsets_padded(p.m_splits, p.E, p.M, s_off, s_poff)
+                         : load_offsets(p.m_splits, p.E, p.M, s_off);
     if (bad) {
         report_status(p.status, bad);
         return;
@@ -537,7 +573,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = s_tmem;
 
     Sched S;
-    S.init(kMode, p.M, p.N, p.K, p.E, s_off, s_order);
+    S.init(kMode, p.M, p.N, p.K, p.E, s_off, s_order, s_poff, kPad);
     const int ncta = gridDim.x, cta = blockIdx.x;
     constexpr bool kFwd = (kMode == kFprop || kMode == kFpropSwiglu);
     const uint32_t a_mn = (kMode == kWgrad) ? 1u : 0u;
@@ -559,7 +595,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int64_t kbs = p.K / BK, wrow = (int64_t)T.e * p.N + T.b_col;
                     ax = 0; ay = (int)T.a_row; adx = BK; ady = 0;
                     bx = 0; by = (int)wrow; bdx = BK; bdy = 0;
-                    sfa = p.sfa + (T.a_row / 128) * kbs * 512;
+                    sfa = p.sfa + (T.pa_row / 128) * kbs * 512;
                     sfb0 = p.sfb + (wrow / 128) * kbs * 512;
                     // second B box: the next 128 rows, or (SwiGLU) the up rows F further
                     sfb1 = sfb0 + (kMode == kFpropSwiglu ? (p.N / 2) / 128 : 1) * kbs * 512;
@@ -568,13 +604,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint8_t* wb = p.sfb + (int64_t)T.e * p.K * (p.N / 32);
                     ax = 0; ay = (int)T.a_row; adx = BK; ady = 0;
                     bx = (int)T.b_col; by = (int)((int64_t)T.e * p.N); bdx = 0; bdy = BK;
-                    sfa = p.sfa + (T.a_row / 128) * kbs * 512;
+                    sfa = p.sfa + (T.pa_row / 128) * kbs * 512;
                     sfb0 = wb + (T.b_col / 128) * kbs * 512;
                     sfb1 = sfb0 + kbs * 512;
                 } else {
-                    const int64_t kbs = T.me / BK;
-                    const uint8_t* ab = p.sfa + p.N * T.off / 32;
-                    const uint8_t* bb = p.sfb + p.K * T.off / 32;
+                    const int64_t kbs = T.mp / BK;
+                    const uint8_t* ab = p.sfa + p.N * T.poff / 32;
+                    const uint8_t* bb = p.sfb + p.K * T.poff / 32;
                     ax = (int)T.a_row; ay = (int)T.off; adx = 0; ady = BK;
                     bx = (int)T.b_col; by = (int)T.off; bdx = 0; bdy = BK;
                     sfa = ab + (T.a_row / 128) * kbs * 512;
@@ -604,7 +640,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // Padded wgrad: the expert's last 128-token block may hold fewer
+        // tokens; the rows past them (the next expert's tokens, or zeros past
+        // M) are cleared in the A tile and both B boxes by the whole warp
+        // before the MMAs read the stage. Elsewhere one lane runs the loop.
+        constexpr bool kClear = kPad && kMode == kWgrad;
+        if (kClear || lane == 0) {
+            const bool leader = (lane == 0);
             int stage = 0;
             uint32_t phase = 0, aphase = 0;
             // Descriptors of stage 0 / k-step 0; every other (stage, k) differs only in
@@ -626,25 +668,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait(acc_empty, aphase ^ 1, abort_flag)) break;
                 fence_after();
                 if (T.nk == 0) {
-                    mbar_arrive(acc_full);
+                    if (leader) mbar_arrive(acc_full);
                 } else {
                     for (int kb = 0; kb < T.nk; ++kb) {
                         if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) goto done_mma;
                         fence_after();
-                        const uint64_t sfd = sf_desc0 + (uint64_t)(stage * (SF_STAGE_BYTES / 16));
-                        tmem_cp_sf(tmem + TMEM_SFA, sfd);
-                        tmem_cp_sf(tmem + TMEM_SFB, sfd + 512 / 16);
-                        tmem_cp_sf(tmem + TMEM_SFB + 4, sfd + 1024 / 16);
-                        const uint64_t ad = a_desc0 + (uint64_t)(stage * (STAGE_BYTES / 16));
-                        const uint64_t bd = b_desc0 + (uint64_t)(stage * (STAGE_BYTES / 16));
+                        if constexpr (kClear) {
+                            if (kb == T.nk - 1 && T.vk < BK) {
+                                // token r of each 16 KB tile is its 128-byte row r (the swizzle stays inside a row)
+                                uint8_t* st = smem + stage * STAGE_BYTES;
+                                const int n16 = (BK - T.vk) * 128 / 16;
+                                for (int t3 = 0; t3 < 3; ++t3) {
+                                    uint4* z = reinterpret_cast<uint4*>(st + t3 * 16384 + T.vk * 128);
+                                    for (int j = lane; j < n16; j += 32) z[j] = make_uint4(0u, 0u, 0u, 0u);
+                                }
+                                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            }
+                            __syncwarp();
+                        }
+                        if (leader) {
+                            const uint64_t sfd = sf_desc0 + (uint64_t)(stage * (SF_STAGE_BYTES / 16));
+                            tmem_cp_sf(tmem + TMEM_SFA, sfd);
+                            tmem_cp_sf(tmem + TMEM_SFB, sfd + 512 / 16);
+                            tmem_cp_sf(tmem + TMEM_SFB + 4, sfd + 1024 / 16);
+                            const uint64_t ad = a_desc0 + (uint64_t)(stage * (STAGE_BYTES / 16));
+                            const uint64_t bd = b_desc0 + (uint64_t)(stage * (STAGE_BYTES / 16));
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            mma_mxf8(tmem, ad + k * a_step16, bd + k * b_step16, id[k], tmem + TMEM_SFA,
-                                     tmem + TMEM_SFB, (kb | k) != 0);
-                        mma_commit(empty0 + 8 * stage);
+                            for (int k = 0; k < BK / UMMA_K; ++k)
+                                mma_mxf8(tmem, ad + k * a_step16, bd + k * b_step16, id[k], tmem + TMEM_SFA,
+                                         tmem + TMEM_SFB, (kb | k) != 0);
+                            mma_commit(empty0 + 8 * stage);
+                        }
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
-                    mma_commit(acc_full);
+                    if (leader) mma_commit(acc_full);
                 }
                 aphase ^= 1;
             }
@@ -697,7 +754,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) mbar_arrive(acc_empty);
 
             const int64_t row = T.a_row + row_in_tile;
-            if (p.tma_store) {
+            // padded grouping: a 32-row box that reaches past the expert is written row by row
+            const bool box_full = !kPad || kMode == kWgrad || T.vr >= q * 32 + 32;
+            if (p.tma_store && box_full) {
                 // Stage 32-row boxes in this warp's buffer and write each with one
                 // TMA store: a box is 32 columns (bf16) or 16 columns (fp32).
                 const bool f32 = (kMode == kWgrad && !p.out_bf16);
@@ -753,6 +812,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     (void)box_cols;
                 }
             } else if (kMode != kWgrad) {
+                if (kPad && row_in_tile >= T.vr) {
+                    aphase ^= 1;
+                    continue;  // past the expert: nothing to write
+                }
                 const int64_t ldo = (kMode == kFprop) ? p.N : p.K;
                 __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + row * ldo + T.b_col + col0;
                 const __nv_bfloat16* bias =
@@ -911,10 +974,23 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
         attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<kWgrad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem_bytes(MXQ_MAX_EXPERTS));
     if (attr_err != cudaSuccess) return attr_err;
+    if (c.pad) {
+        const int sm = smem_bytes_padded(MAX_EXPERTS_PADDED);
+        attr_err = c.mode == kFprop   ? cudaFuncSetAttribute(grouped_gemm_kernel<kFprop, true>,
+                                                             cudaFuncAttributeMaxDynamicSharedMemorySize, sm)
+                   : c.mode == kDgrad ? cudaFuncSetAttribute(grouped_gemm_kernel<kDgrad, true>,
+                                                             cudaFuncAttributeMaxDynamicSharedMemorySize, sm)
+                                      : cudaFuncSetAttribute(grouped_gemm_kernel<kWgrad, true>,
+                                                             cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+        if (attr_err != cudaSuccess) return attr_err;
+    }
 
+    // padded grouping: the row-tile count is known on the device only; the
+    // grid is sized for its bound round_up(M, 128) / 128 + E
+    const int64_t row_tiles = c.pad ? (c.M + BM - 1) / BM + c.E : c.M / BM;
     int64_t tiles;
-    if (c.mode == kFprop || c.mode == kFpropSwiglu) tiles = (c.M / BM) * (c.N / BN);
-    else if (c.mode == kDgrad || c.mode == kDgradSwiglu) tiles = (c.M / BM) * (c.K / BN);
+    if (c.mode == kFprop || c.mode == kFpropSwiglu) tiles = (c.M == 0 ? 0 : row_tiles) * (c.N / BN);
+    else if (c.mode == kDgrad || c.mode == kDgradSwiglu) tiles = (c.M == 0 ? 0 : row_tiles) * (c.K / BN);
     else tiles = (int64_t)c.E * (c.N / BM) * (c.K / BN);
     if (tiles == 0) return cudaSuccess;
     if (c.mode == kWgrad && c.M == 0) {
@@ -970,7 +1046,12 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     p.dbias_part = c.dbias_part;
 
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
-    if (c.mode == kFpropSwiglu)
+    if (c.pad) {
+        const int sm = smem_bytes_padded(c.E);
+        if (c.mode == kFprop) grouped_gemm_kernel<kFprop, true><<<grid, NUM_THREADS, sm, s>>>(ta, tb, to, p);
+        else if (c.mode == kDgrad) grouped_gemm_kernel<kDgrad, true><<<grid, NUM_THREADS, sm, s>>>(ta, tb, to, p);
+        else grouped_gemm_kernel<kWgrad, true><<<grid, NUM_THREADS, sm, s>>>(ta, tb, to, p);
+    } else if (c.mode == kFpropSwiglu)
         grouped_gemm_kernel<kFpropSwiglu><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);
     else if (c.mode == kDgradSwiglu)
         grouped_gemm_kernel<kDgradSwiglu><<<grid, NUM_THREADS, smem_bytes(c.E), s>>>(ta, tb, to, p);

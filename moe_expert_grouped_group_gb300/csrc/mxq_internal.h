@@ -88,6 +88,7 @@ struct GemmCall {
     int swizzle;
     const void* y1;      // kDgradSwiglu: saved FC1 output (M, 2K) bf16
     float* dbias_part;   // kDgradSwiglu: (M/32, 2K) fp32 column sums per 32 rows, or null
+    int pad;             // fprop/dgrad/wgrad: padded grouping (expert counts not multiples of 128)
 };
 
 // The extra operands of the SwiGLU-fused modes, as passed through the C ABI.

@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "mxq_common.cuh"
 #include "mxq_internal.h"
@@ -264,127 +265,138 @@ __global__ void __launch_bounds__(kTileThreads)
         // ------------------------------------ pass 1: colwise amax, dbias
         uint32_t ccode[4] = {0, 0, 0, 0};
         float cinv[4] = {1.f, 1.f, 1.f, 1.f};
-        if constexpr (kCol || kBias) {
-            uint32_t m[4] = {0, 0, 0, 0};
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (kScaled) {
-                float dp[32];  // this lane's 4-column share of each row's dot product with b_e
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    float v[4];
-                    vals(r, ld_row(r), v);
-                    const float s_r = __shfl_sync(0xffffffffu, pw, r);
-                    if (kPad && r >= vb) {
-                        dp[r] = 0.f;
-                        continue;
-                    }
-                    dp[r] = v[0] * bv[0] + v[1] * bv[1] + v[2] * bv[2] + v[3] * bv[3];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
-                        sum[j] += s_r * v[j];
-                    }
-                }
-                const float dsum = transpose_reduce32(dp, lane);
-                if (!kPad || lane < vb) a.dp_partials[(r0 + lane) * tilesK + kt] = dsum;
-            } else {
-#pragma unroll 8
-                for (int r = 0; r < 32; ++r) {
-                    if (kPad && r >= vb) continue;
-                    const uint2 u = ld_row(r);
-                    if constexpr (!kReq && !kBias) {
-                        m[0] = __vmaxu2(m[0], u.x & 0x7FFF7FFFu);
-                        m[1] = __vmaxu2(m[1], u.y & 0x7FFF7FFFu);
-                    } else {
+        // Both passes; kMask (padded grouping, a warp whose 32 rows reach past its
+        // expert) skips the rows past the expert. Whole warps choose one form.
+        auto passes = [&](auto mask_t) {
+            constexpr bool kMask = decltype(mask_t)::value;
+            if constexpr (kCol || kBias) {
+                uint32_t m[4] = {0, 0, 0, 0};
+                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (kScaled) {
+                    float dp[32];  // this lane's 4-column share of each row's dot product with b_e
+    #pragma unroll
+                    for (int r = 0; r < 32; ++r) {
                         float v[4];
-                        vals(r, u, v);
-#pragma unroll
+                        vals(r, ld_row(r), v);
+                        const float s_r = __shfl_sync(0xffffffffu, pw, r);
+                        if (kMask && r >= vb) {
+                            dp[r] = 0.f;
+                            continue;
+                        }
+                        dp[r] = v[0] * bv[0] + v[1] * bv[1] + v[2] * bv[2] + v[3] * bv[3];
+    #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
-                            sum[j] += v[j];
+                            sum[j] += s_r * v[j];
+                        }
+                    }
+                    const float dsum = transpose_reduce32(dp, lane);
+                    if (!kMask || lane < vb) a.dp_partials[(r0 + lane) * tilesK + kt] = dsum;
+                } else {
+    #pragma unroll 8
+                    for (int r = 0; r < 32; ++r) {
+                        if (kMask && r >= vb) continue;
+                        const uint2 u = ld_row(r);
+                        if constexpr (!kReq && !kBias) {
+                            m[0] = __vmaxu2(m[0], u.x & 0x7FFF7FFFu);
+                            m[1] = __vmaxu2(m[1], u.y & 0x7FFF7FFFu);
+                        } else {
+                            float v[4];
+                            vals(r, u, v);
+    #pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
+                                sum[j] += v[j];
+                            }
                         }
                     }
                 }
+                if constexpr (kCol) {
+                    uint32_t e[4];
+                    if constexpr (!kReq && !kBias) {
+                        e[0] = (m[0] >> 7) & 0xFFu;
+                        e[1] = (m[0] >> 23) & 0xFFu;
+                        e[2] = (m[1] >> 7) & 0xFFu;
+                        e[3] = (m[1] >> 23) & 0xFFu;
+                    } else {
+    #pragma unroll
+                        for (int j = 0; j < 4; ++j) e[j] = m[j] >> 23;
+                    }
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        ccode[j] = (uint32_t)max((int)e[j] - 8, 0);
+                        cinv[j] = inv_scale_from_code(ccode[j]);
+                    }
+                    if (a.swizzle) {
+    #pragma unroll
+                        for (int j = 0; j < 4; ++j) s_cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
+                    } else {
+                        *reinterpret_cast<uint32_t*>(a.col_s + (g.prow0 / 32 + rg) * K + col) =
+                            ccode[0] | (ccode[1] << 8) | (ccode[2] << 16) | (ccode[3] << 24);
+                    }
+                }
+                if constexpr (kBias) *reinterpret_cast<float4*>(&s_red[rg][lane * 4]) = make_float4(sum[0], sum[1], sum[2], sum[3]);
             }
-            if constexpr (kCol) {
-                uint32_t e[4];
-                if constexpr (!kReq && !kBias) {
-                    e[0] = (m[0] >> 7) & 0xFFu;
-                    e[1] = (m[0] >> 23) & 0xFFu;
-                    e[2] = (m[1] >> 7) & 0xFFu;
-                    e[3] = (m[1] >> 23) & 0xFFu;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) e[j] = m[j] >> 23;
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    ccode[j] = (uint32_t)max((int)e[j] - 8, 0);
-                    cinv[j] = inv_scale_from_code(ccode[j]);
-                }
-                if (a.swizzle) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) s_cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
-                } else {
-                    *reinterpret_cast<uint32_t*>(a.col_s + (g.prow0 / 32 + rg) * K + col) =
-                        ccode[0] | (ccode[1] << 8) | (ccode[2] << 16) | (ccode[3] << 24);
-                }
-            }
-            if constexpr (kBias) *reinterpret_cast<float4*>(&s_red[rg][lane * 4]) = make_float4(sum[0], sum[1], sum[2], sum[3]);
-        }
-        if constexpr (kReq && kRow) *reinterpret_cast<uint32_t*>(&s_rs[lane * 16 + rg * 4]) = sw;
+            if constexpr (kReq && kRow) *reinterpret_cast<uint32_t*>(&s_rs[lane * 16 + rg * 4]) = sw;
 
-        // ------------------------------------------------- pass 2: encode
-        if constexpr ((kRow && !kReq) || kCol || kDeq) {
-            uint8_t* rq = kRow && !kReq ? a.row_q + r0 * K + col : nullptr;
-            uint8_t* cq = kCol ? a.col_q + r0 * K + col : nullptr;
-            __nv_bfloat16* dq = kDeq ? a.deq_out + r0 * K + col : nullptr;
-#pragma unroll 2
-            for (int r4 = 0; r4 < 32; r4 += 4) {
-                uint2 u[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) u[k] = ld_row(r4 + k);
-                uint32_t packed = 0;
-                if constexpr (kRow && !kReq) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t w2 = __vmaxu2(u[k].x & 0x7FFF7FFFu, u[k].y & 0x7FFF7FFFu);
-                        packed |= (max(w2 & 0xFFFFu, w2 >> 16) >> 7) << (8 * k);  // bf16 exponent field
-                    }
-                    packed = group8_max_u8x4(packed);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = r4 + k;
-                    const bool valid = !kPad || r < vb;  // kPad: rows past the expert are not written
-                    float v[4];
-                    vals(r, u[k], v);
+            // ------------------------------------------------- pass 2: encode
+            if constexpr ((kRow && !kReq) || kCol || kDeq) {
+                uint8_t* rq = kRow && !kReq ? a.row_q + r0 * K + col : nullptr;
+                uint8_t* cq = kCol ? a.col_q + r0 * K + col : nullptr;
+                __nv_bfloat16* dq = kDeq ? a.deq_out + r0 * K + col : nullptr;
+    #pragma unroll 2
+                for (int r4 = 0; r4 < 32; r4 += 4) {
+                    uint2 u[4];
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) u[k] = ld_row(r4 + k);
+                    uint32_t packed = 0;
                     if constexpr (kRow && !kReq) {
-                        const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
-                        const float inv = inv_scale_from_code(code);
-                        if (valid)
-                            *reinterpret_cast<uint32_t*>(rq + r * Ku) =
-                                cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
-                        if ((lane & 7) == 0) {
-                            if (a.swizzle) s_rs[r * 16 + rg * 4 + blk] = valid ? (uint8_t)code : (uint8_t)0;
-                            else if (valid) a.row_s[(r0 + r) * (K / 32) + kt * 4 + blk] = (uint8_t)code;
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t w2 = __vmaxu2(u[k].x & 0x7FFF7FFFu, u[k].y & 0x7FFF7FFFu);
+                            packed |= (max(w2 & 0xFFFFu, w2 >> 16) >> 7) << (8 * k);  // bf16 exponent field
                         }
+                        packed = group8_max_u8x4(packed);
                     }
-                    if (!valid) continue;
-                    if constexpr (kCol) {
-                        *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) |
-                                                                    (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
-                    }
-                    if constexpr (kDeq) {
-                        __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]);
-                        __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2], v[3]);
-                        uint2 o;
-                        o.x = *reinterpret_cast<uint32_t*>(&b0);
-                        o.y = *reinterpret_cast<uint32_t*>(&b1);
-                        *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = o;
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = r4 + k;
+                        const bool valid = !kMask || r < vb;  // kPad: rows past the expert are not written
+                        float v[4];
+                        vals(r, u[k], v);
+                        if constexpr (kRow && !kReq) {
+                            const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
+                            const float inv = inv_scale_from_code(code);
+                            if (valid)
+                                *reinterpret_cast<uint32_t*>(rq + r * Ku) =
+                                    cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+                            if ((lane & 7) == 0) {
+                                if (a.swizzle) s_rs[r * 16 + rg * 4 + blk] = valid ? (uint8_t)code : (uint8_t)0;
+                                else if (valid) a.row_s[(r0 + r) * (K / 32) + kt * 4 + blk] = (uint8_t)code;
+                            }
+                        }
+                        if (!valid) continue;
+                        if constexpr (kCol) {
+                            *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) |
+                                                                        (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
+                        }
+                        if constexpr (kDeq) {
+                            __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]);
+                            __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2], v[3]);
+                            uint2 o;
+                            o.x = *reinterpret_cast<uint32_t*>(&b0);
+                            o.y = *reinterpret_cast<uint32_t*>(&b1);
+                            *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = o;
+                        }
                     }
                 }
             }
+        };
+        if constexpr (kPad) {
+            if (vb < 32) passes(std::true_type{});
+            else passes(std::false_type{});
+        } else {
+            passes(std::false_type{});
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);  // this warp is done with the stage

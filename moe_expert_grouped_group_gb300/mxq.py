@@ -29,7 +29,7 @@ SYMBOLS = [
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
     "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu", "mxq_grouped_gemm_dgrad_swiglu",
-    "mxq_scale_bytes_grouped",
+    "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex",
 ]
 
 
@@ -61,6 +61,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
                                                 _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad_swiglu.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P,
                                                 _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_gemm_fprop_ex.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
+    L.mxq_grouped_gemm_dgrad_ex.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_wgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_dbias_noalloc.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P]
@@ -292,15 +294,18 @@ def grouped_dbias(dy, m_splits, status=None, out=None, workspace=None):
     return out
 
 
-def grouped_gemm_fprop(x_data, x_scale, w_data, w_scale, m_splits, bias=None, status=None, out=None):
-    """Y = X W_e^T (+ b_e). x_data (M,K) u8, w_data (E,N,K) u8, swizzled scales."""
+def grouped_gemm_fprop(x_data, x_scale, w_data, w_scale, m_splits, bias=None, status=None, out=None,
+                       pad_experts=False):
+    """Y = X W_e^T (+ b_e). x_data (M,K) u8, w_data (E,N,K) u8, swizzled scales.
+    pad_experts: expert counts need not be multiples of 128 (x_scale in the padded layout)."""
     M, K = x_data.shape
     E, N, _ = w_data.shape
     m_splits = _splits(m_splits)
     out = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x_data.device)
-    rc = lib().mxq_grouped_gemm_fprop(_ptr(x_data), _ptr(x_scale), _ptr(w_data), _ptr(w_scale), _ptr(bias), M, N, K,
-                                      E, _ptr(m_splits), _ptr(out), _ptr(status), None, 0, _stream())
-    _check(rc, "mxq_grouped_gemm_fprop")
+    rc = lib().mxq_grouped_gemm_fprop_ex(_ptr(x_data), _ptr(x_scale), _ptr(w_data), _ptr(w_scale), _ptr(bias), M, N,
+                                         K, E, _ptr(m_splits), PAD_EXPERTS if pad_experts else 0, _ptr(out),
+                                         _ptr(status), None, 0, _stream())
+    _check(rc, "mxq_grouped_gemm_fprop_ex")
     return out
 
 
@@ -328,15 +333,18 @@ def grouped_gemm_fprop_swiglu(x_data, x_scale, w1_data, w1_scale, m_splits, bias
     return o
 
 
-def grouped_gemm_dgrad(dy_data, dy_scale, w_col_data, w_col_scale, m_splits, status=None, out=None):
-    """dX = dY W_e. dy_data (M,N) rowwise, w_col_data (E,N,K) colwise."""
+def grouped_gemm_dgrad(dy_data, dy_scale, w_col_data, w_col_scale, m_splits, status=None, out=None,
+                       pad_experts=False):
+    """dX = dY W_e. dy_data (M,N) rowwise, w_col_data (E,N,K) colwise.
+    pad_experts: expert counts need not be multiples of 128 (dy_scale in the padded layout)."""
     M, N = dy_data.shape
     E, _, K = w_col_data.shape
     m_splits = _splits(m_splits)
     out = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dy_data.device)
-    rc = lib().mxq_grouped_gemm_dgrad(_ptr(dy_data), _ptr(dy_scale), _ptr(w_col_data), _ptr(w_col_scale), M, N, K,
-                                      E, _ptr(m_splits), _ptr(out), _ptr(status), None, 0, _stream())
-    _check(rc, "mxq_grouped_gemm_dgrad")
+    rc = lib().mxq_grouped_gemm_dgrad_ex(_ptr(dy_data), _ptr(dy_scale), _ptr(w_col_data), _ptr(w_col_scale), M, N,
+                                         K, E, _ptr(m_splits), PAD_EXPERTS if pad_experts else 0, _ptr(out),
+                                         _ptr(status), None, 0, _stream())
+    _check(rc, "mxq_grouped_gemm_dgrad_ex")
     return out
 
 
@@ -369,15 +377,16 @@ def grouped_gemm_dgrad_swiglu(dy_data, dy_scale, w_col_data, w_col_scale, y1, m_
 
 
 def grouped_gemm_wgrad(dy_col_data, dy_col_scale, x_col_data, x_col_scale, m_splits, accumulate=False,
-                       out_bf16=False, status=None, out=None):
-    """dW_e = dY_e^T X_e from the colwise copies; out (E, N, K) fp32 (or bf16)."""
+                       out_bf16=False, status=None, out=None, pad_experts=False):
+    """dW_e = dY_e^T X_e from the colwise copies; out (E, N, K) fp32 (or bf16).
+    pad_experts: expert counts need not be multiples of 128 (colwise scales in the padded layout)."""
     M, N = dy_col_data.shape
     K = x_col_data.shape[1]
     m_splits = _splits(m_splits)
     E = m_splits.numel()
     if out is None:
         out = torch.empty((E, N, K), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dy_col_data.device)
-    flags = (ACCUMULATE if accumulate else 0) | (OUT_BF16 if out_bf16 else 0)
+    flags = (ACCUMULATE if accumulate else 0) | (OUT_BF16 if out_bf16 else 0) | (PAD_EXPERTS if pad_experts else 0)
     rc = lib().mxq_grouped_gemm_wgrad(_ptr(dy_col_data), _ptr(dy_col_scale), _ptr(x_col_data), _ptr(x_col_scale), M,
                                       N, K, E, _ptr(m_splits), flags, _ptr(out), _ptr(status), None, 0, _stream())
     _check(rc, "mxq_grouped_gemm_wgrad")

@@ -151,3 +151,108 @@ def test_full_size_padded_unaligned_routing(mxq):
     assert np.array_equal(host(r["col_data"]), o["col_q"])
     _cmp_scales(r["col_scale"], o["col_s"], "col_s")
     _cmp_scales(r["row_scale_swizzled"], o["row_s_swizzled"], "row_s_swizzled")
+
+
+# ------------------------------------------------ GEMMs on padded layouts
+from tests._gpu import scaled_error  # noqa: E402
+
+TOL_BF16, TOL_F32 = 8e-3, 1e-3
+
+
+class PaddedOps:
+    """Operands of one grouped linear with any expert counts: GPU inputs from the oracle's
+    padded grouping (dense codes, padded swizzled scales); references from the aligned oracle
+    applied to the zero-padded rows (pad rows add nothing to any product)."""
+
+    def __init__(self, ms, N, K, seed):
+        rng = np.random.default_rng(seed)
+        self.ms = np.asarray(ms, np.int64)
+        self.M, self.N, self.K, self.E = int(self.ms.sum()), N, K, len(ms)
+        x = bf16_bits_from_f32(rng.standard_normal((self.M, K)).astype(np.float32))
+        w = bf16_bits_from_f32((0.02 * rng.standard_normal((self.E, N, K))).astype(np.float32))
+        dy = bf16_bits_from_f32(rng.standard_normal((self.M, N)).astype(np.float32))
+        self.sx = orc.group_quantize_padded(x, self.ms, swizzled=True)
+        self.sdy = orc.group_quantize_padded(dy, self.ms, swizzled=True)
+        self.sw = orc.quantize_weights(w, swizzled=True)
+        self.P, self.mp = orc.padded_offsets(self.ms)
+        self.cx = orc.group_quantize(orc.pad_rows(x, self.ms), self.mp)
+        self.cdy = orc.group_quantize(orc.pad_rows(dy, self.ms), self.mp)
+        self.cw = orc.quantize_weights(w)
+        off = np.concatenate([[0], np.cumsum(self.ms)])
+        self.prow = np.concatenate([self.P[e] + np.arange(self.ms[e]) for e in range(self.E)]).astype(np.int64)
+        assert self.prow.size == self.M and off[-1] == self.M
+
+    def gpu(self, mxq):
+        E, N, K = self.E, self.N, self.K
+        ms = dev_i64(self.ms)
+        y = mxq.grouped_gemm_fprop(dev_u8(self.sx["row_q"]), dev_u8(self.sx["row_s"]),
+                                   dev_u8(self.sw["row_q"]).view(E, N, K), dev_u8(self.sw["row_s"]), ms,
+                                   pad_experts=True)
+        dx = mxq.grouped_gemm_dgrad(dev_u8(self.sdy["row_q"]), dev_u8(self.sdy["row_s"]),
+                                    dev_u8(self.sw["col_q"]).view(E, N, K), dev_u8(self.sw["col_s"]), ms,
+                                    pad_experts=True)
+        dw = mxq.grouped_gemm_wgrad(dev_u8(self.sdy["col_q"]), dev_u8(self.sdy["col_s"]), dev_u8(self.sx["col_q"]),
+                                    dev_u8(self.sx["col_s"]), ms, pad_experts=True)
+        return y, dx, dw
+
+
+def _f64(t):
+    a = host(t)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _check_padded_gemms(mxq, op, rows=None, nk_samples=None):
+    E, N, K = op.E, op.N, op.K
+    y, dx, dw = op.gpu(mxq)
+    rows = np.arange(op.M) if rows is None else rows
+    r, c = np.meshgrid(rows, np.arange(N), indexing="ij")
+    ref, mag = orc.fprop_entries(op.cx["row_q"], op.cx["row_s"], op.cw["row_q"].reshape(E, N, K), op.cw["row_s"],
+                                 op.mp, op.prow[r.ravel()], c.ravel())
+    assert scaled_error(_f64(y)[r.ravel(), c.ravel()], ref, mag) <= TOL_BF16
+    r, c = np.meshgrid(rows, np.arange(K), indexing="ij")
+    ref, mag = orc.dgrad_entries(op.cdy["row_q"], op.cdy["row_s"], op.cw["col_q"].reshape(E, N, K), op.cw["col_s"],
+                                 op.mp, op.prow[r.ravel()], c.ravel())
+    assert scaled_error(_f64(dx)[r.ravel(), c.ravel()], ref, mag) <= TOL_BF16
+    if nk_samples is None:
+        e, n, k = (a.ravel() for a in np.meshgrid(np.arange(E), np.arange(N), np.arange(K), indexing="ij"))
+    else:
+        rng = np.random.default_rng(91)
+        e, n, k = rng.integers(0, E, nk_samples), rng.integers(0, N, nk_samples), rng.integers(0, K, nk_samples)
+    ref, mag = orc.wgrad_entries(op.cdy["col_q"], op.cdy["col_s"], op.cx["col_q"], op.cx["col_s"], op.mp, e, n, k)
+    assert scaled_error(_f64(dw)[e, n, k], ref, mag) <= TOL_F32
+    for ee in range(E):  # empty experts: dW = 0 exactly
+        if op.ms[ee] == 0:
+            assert np.all(host(dw)[ee] == 0)
+
+
+@pytest.mark.parametrize("splits", [[40, 3, 0, 200, 57], [1, 127, 129, 0], [300]],
+                         ids=["mixed", "edges", "one_expert"])
+def test_padded_gemms_every_entry(mxq, splits):
+    _check_padded_gemms(mxq, PaddedOps(splits, 256, 256, 92))
+
+
+def test_padded_gemms_sampled(mxq):
+    rng = np.random.default_rng(93)
+    ms = rng.integers(0, 700, 12)
+    ms[3] = 0
+    op = PaddedOps(ms, 512, 768, 94)
+    rows = np.unique(np.concatenate([np.cumsum(ms)[:-1], np.cumsum(ms) - 1, rng.integers(0, op.M, 200)]))
+    rows = rows[(rows >= 0) & (rows < op.M)]
+    _check_padded_gemms(mxq, op, rows=rows, nk_samples=20000)
+
+
+def test_padded_gemms_with_aligned_splits_match_the_plain_calls(mxq):
+    ms = [256, 0, 128, 384]
+    op = PaddedOps(ms, 256, 512, 95)
+    y, dx, dw = op.gpu(mxq)
+    E, N, K = op.E, op.N, op.K
+    d = dev_i64(np.asarray(ms, np.int64))
+    y0 = mxq.grouped_gemm_fprop(dev_u8(op.sx["row_q"]), dev_u8(op.sx["row_s"]), dev_u8(op.sw["row_q"]).view(E, N, K),
+                                dev_u8(op.sw["row_s"]), d)
+    dx0 = mxq.grouped_gemm_dgrad(dev_u8(op.sdy["row_q"]), dev_u8(op.sdy["row_s"]),
+                                 dev_u8(op.sw["col_q"]).view(E, N, K), dev_u8(op.sw["col_s"]), d)
+    dw0 = mxq.grouped_gemm_wgrad(dev_u8(op.sdy["col_q"]), dev_u8(op.sdy["col_s"]), dev_u8(op.sx["col_q"]),
+                                 dev_u8(op.sx["col_s"]), d)
+    assert torch.equal(y, y0) and torch.equal(dx, dx0) and torch.equal(dw, dw0)
