@@ -54,12 +54,13 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
-    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp", "padded"],
+    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp", "padded", "configs"],
                    help="time only one fused kernel family on the MLP workload's shapes and print its line (a "
                         "small footprint for profilers): the SwiGLU->quantize kernels (forward and backward), "
                         "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions, the "
-                        "SwiGLU-fused FC1 fprop and FC2 dgrad vs their unfused pairs, or group_quantize with "
-                        "expert counts that are not multiples of 128")
+                        "SwiGLU-fused FC1 fprop and FC2 dgrad vs their unfused pairs, group_quantize with "
+                        "expert counts that are not multiples of 128, or one grouped-linear step on every "
+                        "synthetic workload")
     return p.parse_args()
 
 
@@ -543,6 +544,80 @@ def time_padded(dev, steps, warmup):
     return res
 
 
+def time_configs(dev, steps, warmup):
+    """One grouped-linear step (the first linear: FC1 for the SwiGLU MLPs) on every synthetic
+    workload: X quantized row+col (or, prequantized, requantized colwise), W and dY quantized
+    row+col, fprop, dgrad, wgrad (fp32 dW); per-kernel CUDA-event times, GEMM TFLOP/s and
+    quantize GB/s with their roofline fractions."""
+    import torch
+
+    import moe_expert_grouped_group_gb300 as mxq
+    from synth import WORKLOADS, make_inputs
+
+    bf16_peak, hbm, _ = peaks()
+    mx_peak = bf16_peak * MXFP8_OVER_BF16
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    out = {}
+    for name, w in WORKLOADS.items():
+        d = make_inputs(w, which=("x", "w", "dy"))
+        E, N, K, M = w.E, w.N, w.K, w.M
+        ms = torch.from_numpy(d["m_splits"]).to(dev)
+        x, wt, dy = tb(d["x"]), tb(d["w"]).view(E * N, K), tb(d["dy"])
+        del d
+        if w.prequant_x:
+            wire = mxq.group_quantize(x, ms, rowwise=True, colwise=False, swizzle=False)
+            qx = mxq.requant_colwise(wire["row_data"], wire["row_scale"], ms)
+            qx["row_data"], qx["row_scale"] = wire["row_data"], qx["row_scale_swizzled"]
+        else:
+            qx = mxq.group_quantize(x, ms)
+        qw = mxq.group_quantize(wt, None, E=E)
+        qd = mxq.group_quantize(dy, ms)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((E, N, K), dtype=torch.float32, device=dev)
+        if w.prequant_x:
+            xq = lambda: mxq.requant_colwise(wire["row_data"], wire["row_scale"], ms, out={
+                "col_data": qx["col_data"], "col_scale": qx["col_scale"], "row_scale_swizzled": qx["row_scale"]})
+            xbytes = M * K * (2 + 3 / 32)
+        else:
+            xq = lambda: mxq.group_quantize(x, ms, out=qx)
+            xbytes = M * K * (4 + 2 / 32)
+        calls = [("x", xq), ("w", lambda: mxq.group_quantize(wt, None, E=E, out=qw)),
+                 ("dy", lambda: mxq.group_quantize(dy, ms, out=qd)),
+                 ("fprop", lambda: mxq.grouped_gemm_fprop(qx["row_data"], qx["row_scale"], qw["row_data"].view(E, N, K),
+                                                          qw["row_scale"], ms, out=y)),
+                 ("dgrad", lambda: mxq.grouped_gemm_dgrad(qd["row_data"], qd["row_scale"], qw["col_data"].view(E, N, K),
+                                                          qw["col_scale"], ms, out=dx)),
+                 ("wgrad", lambda: mxq.grouped_gemm_wgrad(qd["col_data"], qd["col_scale"], qx["col_data"],
+                                                          qx["col_scale"], ms, out=dw))]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
+        for i in range(warmup + steps):
+            flush.fill_(1)
+            for j, (_, fn) in enumerate(calls):
+                if i >= warmup:
+                    ev[i - warmup][j].record()
+                fn()
+            if i >= warmup:
+                ev[i - warmup][len(calls)].record()
+        torch.cuda.synchronize()
+        us = {k: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) * 1e3 for j, (k, _) in enumerate(calls)}
+        flops = 6.0 * M * N * K
+        gemm_us = us["fprop"] + us["dgrad"] + us["wgrad"]
+        qb = {"x": xbytes, "w": E * N * K * (4 + 2 / 32), "dy": M * N * (4 + 2 / 32)}
+        out[name] = {"us": {k: round(v, 1) for k, v in us.items()},
+                     "gemm_tflops": flops / (gemm_us * 1e-6) / 1e12,
+                     "gemm_frac": flops / (gemm_us * 1e-6) / 1e12 / mx_peak,
+                     "quant_frac": {k: qb[k] / (us[k] * 1e-6) / 1e9 / hbm for k in qb},
+                     "x_path": "requant" if w.prequant_x else "quantize"}
+        del x, wt, dy, qx, qw, qd, y, dx, dw
+        if w.prequant_x:
+            del wire
+        torch.cuda.empty_cache()
+    return {"steps": steps, "warmup": warmup, "l2": "256 MiB buffer written before every step",
+            "peak_tflops": mx_peak, "peak_gbs": hbm, "configs": out}
+
+
 KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
 
 
@@ -757,6 +832,11 @@ def main():
         _, hbm_peak, src = peaks()
         r.update(fwd_frac=r["fwd_gbs"] / hbm_peak, bwd_frac=r["bwd_gbs"] / hbm_peak, hbm_peak_gbs=hbm_peak,
                  peak_source=src)
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
+    if args.only == "configs":
+        r = time_configs(dev, max(1, args.steps), max(1, args.warmup))
         if rank == 0:
             print(json.dumps(r), flush=True)
         return
