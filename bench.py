@@ -602,12 +602,24 @@ def time_configs(dev, steps, warmup):
                 ev[i - warmup][len(calls)].record()
         torch.cuda.synchronize()
         us = {k: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) * 1e3 for j, (k, _) in enumerate(calls)}
+        wev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for i in range(steps):  # the three quantize calls again, no L2 flush in between
+            for j in range(3):
+                wev[i][j].record()
+                calls[j][1]()
+            wev[i][3].record()
+        torch.cuda.synchronize()
+        us_warm = {calls[j][0]: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in wev) * 1e3 for j in range(3)}
+        bound = gemm_bound_us(ms.cpu().numpy(), N, K, mx_peak, hbm)
         flops = 6.0 * M * N * K
         gemm_us = us["fprop"] + us["dgrad"] + us["wgrad"]
         qb = {"x": xbytes, "w": E * N * K * (4 + 2 / 32), "dy": M * N * (4 + 2 / 32)}
         out[name] = {"us": {k: round(v, 1) for k, v in us.items()},
                      "gemm_tflops": flops / (gemm_us * 1e-6) / 1e12,
                      "gemm_frac": flops / (gemm_us * 1e-6) / 1e12 / mx_peak,
+                     "gemm_per_expert_bound_us": {k: round(v, 1) for k, v in bound.items()},
+                     "gemm_frac_of_per_expert_bound": sum(bound.values()) / gemm_us,
+                     "us_no_l2_flush": {k: round(v, 1) for k, v in us_warm.items()},
                      "quant_frac": {k: qb[k] / (us[k] * 1e-6) / 1e9 / hbm for k in qb},
                      "x_path": "requant" if w.prequant_x else "quantize"}
         del x, wt, dy, qx, qw, qd, y, dx, dw
@@ -626,6 +638,39 @@ def algorithmic(w):
     flops = {"fprop": 2.0 * M * N * K, "dgrad": 2.0 * M * N * K, "wgrad": 2.0 * M * N * K}
     bytes_ = {"requant_x": 2.09375 * M * K, "quantize_w": 4.0625 * E * N * K, "quantize_dy": 4.0625 * M * N}
     return flops, bytes_
+
+
+def gemm_bound_us(m_splits, N, K, mx_peak_tflops, hbm_gbs):
+    """Per-expert roofline of the three grouped GEMMs: sum over experts of
+    max(flops_e / tensor peak, bytes_e / HBM bandwidth), bytes_e being the
+    algorithmic operand and output bytes of expert e (E4M3 codes + E8M0 scales
+    in, bf16 Y / dX and fp32 dW out; an empty expert still writes its dW
+    zeros). Equal to the dense bound when every expert is compute-bound."""
+    q = 1 + 1 / 32  # one E4M3 byte + its share of an E8M0 scale
+    tot = {"fprop": 0.0, "dgrad": 0.0, "wgrad": 0.0}
+    for m in (int(v) for v in m_splits):
+        f = 2.0 * m * N * K / (mx_peak_tflops * 1e12)
+        b = {"fprop": m * K * q + N * K * q + m * N * 2, "dgrad": m * N * q + N * K * q + m * K * 2,
+             "wgrad": m * N * q + m * K * q + N * K * 4}
+        for k in tot:
+            if m == 0 and k != "wgrad":
+                continue
+            tot[k] += max(f, b[k] / (hbm_gbs * 1e9))
+    return {k: v * 1e6 for k, v in tot.items()}
+
+
+def time_warm(st, steps):
+    """Per-kernel times of the step with no L2 flush between steps (inputs
+    that fit in the 129 MB L2 may then be served from it)."""
+    torch = st.torch
+    for _ in range(3):
+        st.run()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for i in range(steps):
+        st.run(evs[i])
+    torch.cuda.synchronize()
+    return {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+            for j, k in enumerate(KERNELS)}
 
 
 def time_native(st, steps, warmup, sampler):
@@ -655,40 +700,80 @@ def time_native(st, steps, warmup, sampler):
 
 
 def time_e2e(st, steps, warmup, d):
-    """Through the public API from pinned host memory: H2D of the step's
-    inputs (wire-format X, its scales, W, dY, m_splits), the step, D2H of its
-    results (Y, dX, dW)."""
+    """Through the public API from pinned host memory: every step copies its
+    inputs (wire-format X, its scales, W, dY, m_splits) host -> device, runs
+    the six calls and copies its results (Y, dX, dW) device -> host.
+
+    Pipelined: the copies run on their own streams, so step i+1's inputs go
+    up and step i-1's results come down while step i's kernels run; inputs
+    and outputs are double-buffered (two slots), the quantized intermediates
+    are shared (the kernels of consecutive steps are ordered on one stream).
+    Also returns the per-step time of the same work issued serially on one
+    stream."""
+    import copy
+
     torch = st.torch
-    host_in = {
-        "x_row": st.x_row.cpu().pin_memory(), "x_row_scale": st.x_row_scale.cpu().pin_memory(),
-        "wt": st.wt.cpu().pin_memory(), "dy": st.dy.cpu().pin_memory(), "ms": st.ms.cpu().pin_memory(),
-    }
-    host_out = {"y": torch.empty_like(st.y, device="cpu").pin_memory(),
-                "dx": torch.empty_like(st.dx, device="cpu").pin_memory(),
-                "dw": torch.empty_like(st.dw, device="cpu").pin_memory()}
-    dev_in = {"x_row": st.x_row, "x_row_scale": st.x_row_scale, "wt": st.wt, "dy": st.dy, "ms": st.ms}
+    names_in, names_out = ("x_row", "x_row_scale", "wt", "dy", "ms"), ("y", "dx", "dw")
+    host_in = {k: getattr(st, k).cpu().pin_memory() for k in names_in}
+    host_out = {k: torch.empty_like(getattr(st, k), device="cpu").pin_memory() for k in names_out}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    st2 = copy.copy(st)
+    for k in names_in + names_out:
+        setattr(st2, k, torch.empty_like(getattr(st, k)))
+    slots = [st, st2]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in slots]    # the slot's inputs have landed
+    ev_used = [torch.cuda.Event() for _ in slots]  # the slot's step has run
+    ev_out = [torch.cuda.Event() for _ in slots]   # the slot's results are on the host
 
-    def one():
-        for k, t in host_in.items():
-            dev_in[k].copy_(t, non_blocking=True)
+    def serial():
+        for k in names_in:
+            getattr(st, k).copy_(host_in[k], non_blocking=True)
         st.run()
-        host_out["y"].copy_(st.y, non_blocking=True)
-        host_out["dx"].copy_(st.dx, non_blocking=True)
-        host_out["dw"].copy_(st.dw, non_blocking=True)
+        for k in names_out:
+            host_out[k].copy_(getattr(st, k), non_blocking=True)
+
+    def pipelined(i):
+        j = i % 2
+        s = slots[j]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_used[j])  # step i-2 has finished reading this slot's inputs
+            for k in names_in:
+                getattr(s, k).copy_(host_in[k], non_blocking=True)
+            ev_in[j].record(s_in)
+        comp.wait_event(ev_in[j])
+        comp.wait_event(ev_out[j])  # step i-2's results have left this slot
+        s.run()
+        ev_used[j].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_used[j])
+            for k in names_out:
+                host_out[k].copy_(getattr(s, k), non_blocking=True)
+            ev_out[j].record(s_out)
+
+    def timed(body):
+        torch.cuda.synchronize()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(comp)
+        s_in.wait_stream(comp)
+        for i in range(steps):
+            body(i)
+        comp.wait_stream(s_in)
+        comp.wait_stream(s_out)
+        b.record(comp)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
 
     for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
-    barrier()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
-    torch.cuda.synchronize()
-    return a.elapsed_time(b) / steps, h2d, d2h
+        serial()
+    ms_serial = timed(lambda i: serial())
+    for i in range(warmup):
+        pipelined(i)
+    ms_pipe = timed(pipelined)
+    return ms_pipe, ms_serial, h2d, d2h
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -872,13 +957,19 @@ def main():
     gemm_ms = per_kernel["fprop"] + per_kernel["dgrad"] + per_kernel["wgrad"]
     gemm_tflops = step_flops / (gemm_ms * 1e-3) / 1e12
     quant_gbs = {k: bytes_[k] / (per_kernel[k] * 1e-3) / 1e9 for k in bytes_}
+    warm = time_warm(st, max(5, args.steps // 5))
 
     e2e = None
     if not args.no_e2e:
-        ms_e2e, h2d, d2h = time_e2e(st, max(5, args.steps // 5), 2, d)
-        ms_e2e = max_over_ranks(ms_e2e)
+        e2e_steps = max(10, args.steps // 2)
+        ms_e2e, ms_serial, h2d, d2h = time_e2e(st, e2e_steps, max(3, args.warmup), d)
+        ms_e2e, ms_serial = max_over_ranks(ms_e2e), max_over_ranks(ms_serial)
         e2e = {"value": aggregate(step_flops, world, ms_e2e * 1e-3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e, "steps": e2e_steps,
+               "issue": "copies on their own streams, overlapping the neighbouring steps' kernels; inputs and "
+                        "outputs double-buffered",
+               "serial_ms_per_step": ms_serial,
+               "serial_value": aggregate(step_flops, world, ms_serial * 1e-3) / 1e12}
 
     mlp = None
     if not args.no_mlp and rank == 0:
@@ -902,6 +993,9 @@ def main():
                 "frac": gemm_tflops / mx_peak, "traffic": traffic,
                 "kernel": "grouped_gemm_kernel (fprop+dgrad+wgrad launches of one step)",
                 "peak_source": f"{src} bf16 burst {bf16_peak} TFLOP/s x {MXFP8_OVER_BF16} (nominal MXFP8/BF16)"}
+    bound = gemm_bound_us(d["m_splits"], w.N, w.K, mx_peak, hbm_peak)
+    roofline["per_expert_bound_us"] = bound
+    roofline["frac_of_per_expert_bound"] = sum(bound.values()) / (gemm_ms * 1e3)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         t0 = time.perf_counter()
@@ -926,6 +1020,7 @@ def main():
         "kernels_ms": per_kernel, "gemm_tflops": gemm_tflops,
         "group_quantize_gbs": quant_gbs, "hbm_peak_gbs": hbm_peak,
         "group_quantize_frac": {k: v / hbm_peak for k, v in quant_gbs.items()},
+        "kernels_ms_no_l2_flush": warm,
         "wall_s_timed_region": wall,
         "mlp_step": mlp,
     }

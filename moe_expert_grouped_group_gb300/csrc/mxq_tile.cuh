@@ -52,12 +52,13 @@ __device__ __forceinline__ uint32_t group8_max_u8x4(uint32_t v) {
 // packed bytes (the E8M0 code depends only on the block's largest exponent).
 // Ring depth per CTA. The kernel is bound by issue and latency of its compute
 // warps, so more resident CTAs (shallower rings) beat deeper prefetch: on the
-// 16k-token workload 1 stage ran 51 us, 2 stages 64 us, 3 stages 79 us.
+// 16k-token workload quantize ran 51 us with 1 stage, 64 us with 2, 79 us
+// with 3; requant (E4M3 in) 27.8 / 29.8 / 31.7 us with 1 / 2 / 3 stages.
 #ifndef MXQ_QUANT_STAGES_BF16
-#define MXQ_QUANT_STAGES_BF16 1  // 32 KB bf16 tiles in flight per CTA
+#define MXQ_QUANT_STAGES_BF16 1  // 32 KB bf16 tile in flight per CTA
 #endif
 #ifndef MXQ_QUANT_STAGES_E4M3
-#define MXQ_QUANT_STAGES_E4M3 3  // 16 KB E4M3 tiles in flight per CTA
+#define MXQ_QUANT_STAGES_E4M3 1  // 16 KB E4M3 tile in flight per CTA
 #endif
 
 template <bool kReq>

@@ -1,0 +1,26 @@
+"""Host-side arithmetic of bench.py: the per-expert GEMM roofline."""
+import pytest
+
+import bench
+
+
+def test_per_expert_bound_equals_the_dense_bound_when_every_expert_is_compute_bound():
+    N, K, peak, bw = 4096, 2048, 3845.4, 6665.6
+    ms = [2048] * 8
+    b = bench.gemm_bound_us(ms, N, K, peak, bw)
+    dense = 2.0 * sum(ms) * N * K / (peak * 1e12) * 1e6
+    for k in ("fprop", "dgrad", "wgrad"):
+        assert b[k] == pytest.approx(dense, rel=1e-12)
+
+
+def test_small_and_empty_experts_are_bound_by_their_bytes():
+    N, K, peak, bw = 2048, 7168, 3845.4, 6665.6
+    q = 1 + 1 / 32
+    b = bench.gemm_bound_us([0, 128], N, K, peak, bw)
+    # expert 1 (128 rows) streams its weight: W bytes dominate its 2*128*N*K flops
+    fprop = (128 * K * q + N * K * q + 128 * N * 2) / (bw * 1e9) * 1e6
+    assert b["fprop"] == pytest.approx(fprop, rel=1e-12)
+    # the empty expert still writes its fp32 dW zeros; expert 1 writes its fp32 dW
+    wgrad = N * K * 4 / (bw * 1e9) * 1e6 + (128 * N * q + 128 * K * q + N * K * 4) / (bw * 1e9) * 1e6
+    assert b["wgrad"] == pytest.approx(wgrad, rel=1e-12)
+    assert b["dgrad"] == pytest.approx((128 * N * q + N * K * q + 128 * K * 2) / (bw * 1e9) * 1e6, rel=1e-12)
