@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(kTileThreads)
 
     const int rg = warp;         // 32-row group of the tile
     const int blk = lane >> 3;   // 32-column block of the tile holding this lane's 4 columns
+    const uint32_t sel_blk = 0x4440u | (uint32_t)blk;  // byte_perm selector: byte blk, zero-extended
     const uint32_t Ku = (uint32_t)K;
     int stage = 0;
     uint32_t phase = 0;
@@ -253,7 +254,10 @@ __global__ void __launch_bounds__(kTileThreads)
                 v[2] = bf16lo(u.y);
                 v[3] = bf16hi(u.y);
             } else {
-                const float sc = scale_from_code((__shfl_sync(0xffffffffu, sw, r) >> (8 * blk)) & 0xFFu);
+                // byte blk of row r's four codes; 2^(code - 127) from the code placed in
+                // the exponent field, code 0 -> 2^-127 (the subnormal 0x00400000)
+                const uint32_t code = __byte_perm(__shfl_sync(0xffffffffu, sw, r), 0u, sel_blk);
+                const float sc = __uint_as_float(max(code << 23, 0x00400000u));
                 const float2 lo = e4m3x2_to_f32((uint16_t)(u.x & 0xFFFFu));
                 const float2 hi = e4m3x2_to_f32((uint16_t)(u.x >> 16));
                 v[0] = lo.x * sc;
@@ -269,10 +273,11 @@ __global__ void __launch_bounds__(kTileThreads)
         // Both passes; kMask (padded grouping, a warp whose 32 rows reach past its
         // expert) skips the rows past the expert. Whole warps choose one form.
         auto passes = [&](auto mask_t) {
-            constexpr bool kMask = decltype(mask_t)::value;
+            [[maybe_unused]] constexpr bool kMask = decltype(mask_t)::value;
             if constexpr (kCol || kBias) {
-                uint32_t m[4] = {0, 0, 0, 0};
-                float sum[4] = {0.f, 0.f, 0.f, 0.f};
+                [[maybe_unused]] uint32_t m[4] = {0, 0, 0, 0};  // packed bf16 |x| bits (bf16 input, no dbias)
+                [[maybe_unused]] float mf[4] = {0.f, 0.f, 0.f, 0.f};  // |v| maxima (every other case)
+                [[maybe_unused]] float sum[4] = {0.f, 0.f, 0.f, 0.f};
                 if constexpr (kScaled) {
                     float dp[32];  // this lane's 4-column share of each row's dot product with b_e
     #pragma unroll
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(kTileThreads)
                         dp[r] = v[0] * bv[0] + v[1] * bv[1] + v[2] * bv[2] + v[3] * bv[3];
     #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
+                            mf[j] = fmaxf(mf[j], fabsf(v[j]));
                             sum[j] += s_r * v[j];
                         }
                     }
@@ -306,8 +311,8 @@ __global__ void __launch_bounds__(kTileThreads)
                             vals(r, u, v);
     #pragma unroll
                             for (int j = 0; j < 4; ++j) {
-                                m[j] = max(m[j], __float_as_uint(v[j]) & 0x7FFFFFFFu);
-                                sum[j] += v[j];
+                                mf[j] = fmaxf(mf[j], fabsf(v[j]));
+                                if constexpr (kBias) sum[j] += v[j];
                             }
                         }
                     }
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kTileThreads)
                         e[3] = (m[1] >> 23) & 0xFFu;
                     } else {
     #pragma unroll
-                        for (int j = 0; j < 4; ++j) e[j] = m[j] >> 23;
+                        for (int j = 0; j < 4; ++j) e[j] = __float_as_uint(mf[j]) >> 23;
                     }
     #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -342,15 +347,15 @@ __global__ void __launch_bounds__(kTileThreads)
 
             // ------------------------------------------------- pass 2: encode
             if constexpr ((kRow && !kReq) || kCol || kDeq) {
-                uint8_t* rq = kRow && !kReq ? a.row_q + r0 * K + col : nullptr;
-                uint8_t* cq = kCol ? a.col_q + r0 * K + col : nullptr;
-                __nv_bfloat16* dq = kDeq ? a.deq_out + r0 * K + col : nullptr;
+                [[maybe_unused]] uint8_t* rq = kRow && !kReq ? a.row_q + r0 * K + col : nullptr;
+                [[maybe_unused]] uint8_t* cq = kCol ? a.col_q + r0 * K + col : nullptr;
+                [[maybe_unused]] __nv_bfloat16* dq = kDeq ? a.deq_out + r0 * K + col : nullptr;
     #pragma unroll 2
                 for (int r4 = 0; r4 < 32; r4 += 4) {
                     uint2 u[4];
     #pragma unroll
                     for (int k = 0; k < 4; ++k) u[k] = ld_row(r4 + k);
-                    uint32_t packed = 0;
+                    [[maybe_unused]] uint32_t packed = 0;
                     if constexpr (kRow && !kReq) {
     #pragma unroll
                         for (int k = 0; k < 4; ++k) {
