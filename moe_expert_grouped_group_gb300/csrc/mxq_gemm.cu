@@ -73,12 +73,15 @@ constexpr int EPI_STAGE_BYTES = 2048;           // per epilogue warp: one 32-row
 // dynamic shared memory: [A/B stages][scale atoms][barriers][epilogue staging][expert tables]
 constexpr int SF_REGION = STAGES * STAGE_BYTES;
 constexpr int BAR_REGION = SF_REGION + STAGES * SF_STAGE_BYTES;
-constexpr int EPI_REGION = BAR_REGION + 256;
+constexpr int EPI_REGION = (BAR_REGION + 256 + 511) / 512 * 512;  // 512-aligned: the 64-byte swizzle's period
 constexpr int TABLE_REGION = EPI_REGION + EPI_WARPS * EPI_STAGE_BYTES;
 __host__ __device__ constexpr int smem_bytes(int E) { return 1024 + TABLE_REGION + 8 * (E + 1) + 2 * E; }
 // padded grouping keeps a second (E+1)-entry offset table
 __host__ __device__ constexpr int smem_bytes_padded(int E) { return smem_bytes(E) + 8 * (E + 1); }
 constexpr int MAX_EXPERTS_PADDED = 512;  // smem_bytes_padded(512) fits the 227 KB per-block limit
+static_assert(smem_bytes(MXQ_MAX_EXPERTS) <= 232448, "shared memory over the per-block limit");
+static_assert(smem_bytes_padded(MAX_EXPERTS_PADDED) <= 232448, "shared memory over the per-block limit");
+static_assert(EPI_REGION % 512 == 0, "the 64-byte swizzle of the staging boxes repeats every 512 bytes");
 
 struct Params {
     int mode;
@@ -478,7 +481,8 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
         uint4* dst = reinterpret_cast<uint4*>(epi_buf + lane * 64);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(y[16 * b + 4 * v], y[16 * b + 4 * v + 1], y[16 * b + 4 * v + 2], y[16 * b + 4 * v + 3]);
+            dst[v ^ ((lane >> 1) & 3)] =
+                make_uint4(y[16 * b + 4 * v], y[16 * b + 4 * v + 1], y[16 * b + 4 * v + 2], y[16 * b + 4 * v + 3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
@@ -796,9 +800,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // the previous box of this buffer must have been read out
                     if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                     __syncwarp();
+                    // row `lane` of the box; 16-byte chunk v sits at v ^ (row bits 1..2) (64-byte swizzle)
                     uint4* dst = reinterpret_cast<uint4*>(epi_buf + lane * 64);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+                    for (int v = 0; v < 4; ++v)
+                        dst[v ^ ((lane >> 1) & 3)] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
@@ -905,7 +911,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ------------------------------------------------------------------ host side
 // 2-D uint8 tensor (outer rows x inner cols, row-major), box 128 x 128, 128B swizzle.
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
-    return encode_tmap_2d(m, base, rows, cols, 1, 128, 128, true);
+    return encode_tmap_2d(m, base, rows, cols, 1, 128, 128, 128);
 }
 
 }  // namespace gemm
@@ -929,9 +935,14 @@ static EncodeTiledFn get_encode() {
 }
 
 bool encode_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int elem_bytes, int box_cols,
-                    int box_rows, bool swizzle128) {
+                    int box_rows, int swizzle_bytes) {
     EncodeTiledFn enc = get_encode();
     if (!enc || !base) return false;
+    if (swizzle_bytes != 0 && swizzle_bytes != 64 && swizzle_bytes != 128) return false;
+    if (swizzle_bytes && box_cols * elem_bytes != swizzle_bytes) return false;
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
     const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                    : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT32;
@@ -940,7 +951,7 @@ bool encode_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               sw,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1015,10 +1026,11 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     memset(&to, 0, sizeof(to));
     const int tma_store = !c.accumulate && c.mode != kDgradSwiglu;  // dh never leaves the chip there
     if (tma_store) {
-        if (c.mode == kFprop || c.mode == kFpropSwiglu) ok = encode_tmap_2d(&to, c.out, c.M, c.N, 2, 32, 32, false);
-        else if (c.mode == kDgrad) ok = encode_tmap_2d(&to, c.out, c.M, c.K, 2, 32, 32, false);
-        else if (c.out_bf16) ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 2, 32, 32, false);
-        else ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 4, 16, 32, false);
+        // 64-byte boxes rows, 64-byte swizzle: the epilogue's staging writes are bank-conflict free
+        if (c.mode == kFprop || c.mode == kFpropSwiglu) ok = encode_tmap_2d(&to, c.out, c.M, c.N, 2, 32, 32, 64);
+        else if (c.mode == kDgrad) ok = encode_tmap_2d(&to, c.out, c.M, c.K, 2, 32, 32, 64);
+        else if (c.out_bf16) ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 2, 32, 32, 64);
+        else ok = encode_tmap_2d(&to, c.out, (int64_t)c.E * c.N, c.K, 4, 16, 32, 64);
         if (!ok) return cudaErrorInvalidValue;
     }
 

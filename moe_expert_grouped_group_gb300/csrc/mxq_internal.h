@@ -100,10 +100,11 @@ struct GemmExtra {
 };
 
 // Encodes a 2-D row-major tensor map (rows x cols elements of elem_bytes)
-// with a box of box_rows x box_cols; swizzle128 selects the 128-byte
-// swizzle (box_cols * elem_bytes must then be 128). False on failure.
+// with a box of box_rows x box_cols. swizzle_bytes: 0 (none), 64 or 128 (the
+// 64- or 128-byte shared-memory swizzle; box_cols * elem_bytes must then
+// equal it). False on failure.
 bool encode_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int elem_bytes, int box_cols,
-                    int box_rows, bool swizzle128);
+                    int box_rows, int swizzle_bytes);
 
 cudaError_t run_group_quantize(const QuantCall& c, cudaStream_t s);
 cudaError_t run_requant(const RequantCall& c, cudaStream_t s);

@@ -350,9 +350,9 @@ static cudaError_t launch(const Args& a, const void* y, const void* dh, cudaStre
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     CUtensorMap ty, td;
-    if (!encode_tmap_2d(&ty, y, a.M, 2 * a.F, 2, kTile, kTile, false)) return cudaErrorInvalidValue;
+    if (!encode_tmap_2d(&ty, y, a.M, 2 * a.F, 2, kTile, kTile, 0)) return cudaErrorInvalidValue;
     if (kBwd) {
-        if (!encode_tmap_2d(&td, dh, a.M, a.F, 2, kTile, kTile, false)) return cudaErrorInvalidValue;
+        if (!encode_tmap_2d(&td, dh, a.M, a.F, 2, kTile, kTile, 0)) return cudaErrorInvalidValue;
     } else {
         td = ty;  // unused
     }

@@ -469,7 +469,7 @@ static cudaError_t launch_tile(const TileArgs& a, cudaStream_t s) {
     const cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (attr != cudaSuccess) return attr;
     CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, a.src, a.M, a.K, Sh::kInBytes, kTile, kTile, false)) return cudaErrorInvalidValue;
+    if (!encode_tmap_2d(&tm, a.src, a.M, a.K, Sh::kInBytes, kTile, kTile, 0)) return cudaErrorInvalidValue;
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTileThreads, smem);
     const int64_t grid = std::min<int64_t>(tiles, (int64_t)num_sms() * std::max(per_sm, 1));
