@@ -54,13 +54,13 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
-    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp", "padded", "configs"],
+    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp", "padded", "configs", "mma_peak"],
                    help="time only one fused kernel family on the MLP workload's shapes and print its line (a "
                         "small footprint for profilers): the SwiGLU->quantize kernels (forward and backward), "
                         "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions, the "
                         "SwiGLU-fused FC1 fprop and FC2 dgrad vs their unfused pairs, group_quantize with "
-                        "expert counts that are not multiples of 128, or one grouped-linear step on every "
-                        "synthetic workload")
+                        "expert counts that are not multiples of 128, one grouped-linear step on every "
+                        "synthetic workload, or the tensor-pipe ceiling probe (back-to-back block-scaled MMAs)")
     return p.parse_args()
 
 
@@ -640,6 +640,26 @@ def algorithmic(w):
     return flops, bytes_
 
 
+def time_mma_stream(mmas_per_sm=8192, reps=5):
+    """TFLOP/s of the tensor-pipe ceiling probe (back-to-back block-scaled 128x256x32 MMAs on
+    every SM from resident shared memory): the most the grouped GEMMs' instructions can reach."""
+    import torch
+
+    import moe_expert_grouped_group_gb300 as mxq
+
+    status = mxq.new_status()
+    for _ in range(2):
+        mxq.probe_mma_stream(mmas_per_sm, status=status)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    flops = sum(mxq.probe_mma_stream(mmas_per_sm, status=status) for _ in range(reps))
+    b.record()
+    torch.cuda.synchronize()
+    assert mxq.status_read(status) == 0, "the ceiling probe's wait timed out"
+    return flops / (a.elapsed_time(b) * 1e-3) / 1e12
+
+
 def gemm_bound_us(m_splits, N, K, mx_peak_tflops, hbm_gbs):
     """Per-expert roofline of the three grouped GEMMs: sum over experts of
     max(flops_e / tensor peak, bytes_e / HBM bandwidth), bytes_e being the
@@ -930,6 +950,15 @@ def main():
         if rank == 0:
             print(json.dumps(r), flush=True)
         return
+    if args.only == "mma_peak":
+        bf16_peak, _, src = peaks()
+        t = time_mma_stream()
+        r = {"metric": "block-scaled MXFP8 tcgen05 MMA stream (128x256x32, one CTA per SM, resident operands)",
+             "tflops": t, "unit": "TFLOP/s", "roofline_peak": bf16_peak * MXFP8_OVER_BF16,
+             "ratio_to_roofline_peak": t / (bf16_peak * MXFP8_OVER_BF16), "peak_source": src}
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
     if args.only == "fused_mlp":
         r = time_fused_mlp(dev, max(1, args.steps), max(1, args.warmup))
         if rank == 0:
@@ -993,6 +1022,9 @@ def main():
                 "frac": gemm_tflops / mx_peak, "traffic": traffic,
                 "kernel": "grouped_gemm_kernel (fprop+dgrad+wgrad launches of one step)",
                 "peak_source": f"{src} bf16 burst {bf16_peak} TFLOP/s x {MXFP8_OVER_BF16} (nominal MXFP8/BF16)"}
+    stream_tflops = time_mma_stream()
+    roofline["mma_stream_tflops"] = stream_tflops
+    roofline["frac_of_mma_stream"] = gemm_tflops / stream_tflops
     bound = gemm_bound_us(d["m_splits"], w.N, w.K, mx_peak, hbm_peak)
     roofline["per_expert_bound_us"] = bound
     roofline["frac_of_per_expert_bound"] = sum(bound.values()) / (gemm_ms * 1e3)

@@ -373,6 +373,18 @@ MXQ_API int mxq_swiglu_bwd_quantize(const void* dh_bf16, const void* y_bf16, int
                                     const int32_t* d_noop, int32_t* d_status, void* ws, size_t ws_bytes,
                                     mxq_stream_t stream);
 
+/* Measurement utility beside the MXFP8 path: the tensor-pipe ceiling that
+ * bounds the grouped GEMMs on this GPU. Launches one CTA per SM on `stream`;
+ * each issues mmas_per_sm block-scaled 128x256x32 tcgen05 MMAs (E4M3 x E4M3,
+ * E8M0 scales, fp32 accumulation in TMEM) back to back from operands resident
+ * in shared memory, with the scale copies and commit of the grouped GEMM's
+ * 128-deep K block but no loads, waits between K blocks, tile boundaries or
+ * epilogue. Timed on the stream, 2*128*256*32*mmas_per_sm*SMs / time is the
+ * most a kernel built from these instructions can reach. Reads and writes no
+ * global memory except *d_status (MXQ_STATUS_WAIT_TIMEOUT; may be NULL).
+ * mmas_per_sm in [0, 2^31); MXQ_ERR_SHAPE otherwise. */
+MXQ_API int mxq_probe_mma_stream(int64_t mmas_per_sm, int32_t* d_status, mxq_stream_t stream);
+
 /* Copy the device status word to *h_out after `stream` drains (the only
  * synchronizing call). */
 MXQ_API int mxq_status_read(const int32_t* d_status, int32_t* h_out, mxq_stream_t stream);

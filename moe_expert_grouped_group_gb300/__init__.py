@@ -16,6 +16,7 @@ from .mxq import (  # noqa: F401
     grouped_gemm_fprop_swiglu,
     grouped_gemm_wgrad,
     new_status,
+    probe_mma_stream,
     requant_colwise,
     requant_colwise_scaled_bias,
     scale_bytes,

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmxq.so")
 SOURCES = ["mxq_api.cu", "mxq_quant.cu", "mxq_quant_pad.cu", "mxq_gemm.cu", "mxq_swiglu.cu", "mxq_noalloc.cu",
-           "mxq_swiglu_quant.cu"]
+           "mxq_swiglu_quant.cu", "mxq_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-I", os.path.join(ROOT, "include")]

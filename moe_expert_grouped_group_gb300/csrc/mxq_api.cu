@@ -7,6 +7,7 @@
 
 #include "../../include/mxq.h"
 #include "mxq_internal.h"
+#include "mxq_peak.h"
 
 namespace {
 
@@ -428,6 +429,13 @@ int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_scale, co
     return gemm_common(mxq::kWgrad, dy_col_data, dy_col_scale, x_col_data, x_col_scale, nullptr, M, N, K, E,
                        d_m_splits, dw, (flags & MXQ_ACCUMULATE) != 0, (flags & MXQ_OUT_BF16) != 0, d_status, stream,
                        nullptr, (flags & MXQ_PAD_EXPERTS) != 0);
+}
+
+int mxq_probe_mma_stream(int64_t mmas_per_sm, int32_t* d_status, mxq_stream_t stream) {
+    if (!arch_ok()) return MXQ_ERR_ARCH;
+    if (mmas_per_sm < 0 || mmas_per_sm >= ((int64_t)1 << 31)) return MXQ_ERR_SHAPE;
+    cudaError_t e = mxq::run_mma_stream(mmas_per_sm, d_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
 }
 
 int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream) {

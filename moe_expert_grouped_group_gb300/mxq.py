@@ -29,7 +29,7 @@ SYMBOLS = [
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
     "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu", "mxq_grouped_gemm_dgrad_swiglu",
-    "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex",
+    "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex", "mxq_probe_mma_stream",
 ]
 
 
@@ -77,6 +77,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_requant_colwise_scaled_bias.argtypes = [_P, _P, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P, _P, _P, _P,
                                                   _P, _P, _P, _P, _SZ, _P]
     L.mxq_status_read.argtypes = [_P, _P, _P]
+    L.mxq_probe_mma_stream.argtypes = [_I64, _P, _P]
+    L.mxq_probe_mma_stream.restype = _INT
     L.mxq_error_string.argtypes = [_INT]
     L.mxq_error_string.restype = ctypes.c_char_p
     L.mxq_last_cuda_error.restype = _INT
@@ -391,6 +393,15 @@ def grouped_gemm_wgrad(dy_col_data, dy_col_scale, x_col_data, x_col_scale, m_spl
                                       N, K, E, _ptr(m_splits), flags, _ptr(out), _ptr(status), None, 0, _stream())
     _check(rc, "mxq_grouped_gemm_wgrad")
     return out
+
+
+def probe_mma_stream(mmas_per_sm=8192, status=None):
+    """Launch the tensor-pipe ceiling probe (not part of the MXFP8 path): one CTA per SM issues
+    mmas_per_sm block-scaled 128x256x32 MMAs from resident shared memory. Returns its FLOPs
+    (2*128*256*32*mmas_per_sm*SMs); time it with CUDA events on the current stream."""
+    _check(lib().mxq_probe_mma_stream(int(mmas_per_sm), _ptr(status), _stream()), "mxq_probe_mma_stream")
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 2.0 * 128 * 256 * 32 * mmas_per_sm * sms
 
 
 def swiglu_fwd(y, out=None):
