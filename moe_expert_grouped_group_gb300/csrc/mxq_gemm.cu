@@ -629,8 +629,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t fb = full0 + 8 * stage;
                     mbar_expect_tx(fb, STAGE_TX);
                     tma_load_2d(sb, &tmA, fb, ax, ay);
-                    tma_load_2d(sb + A_BYTES, &tmB, fb, bx, by);
-                    tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, bx + b2x, by + b2y);
+                    tma_load_2d(sb + A_BYTES, &tmB, fb, bx, by);  // kFprop: all 256 rows
+                    if (kMode != kFprop) tma_load_2d(sb + A_BYTES + 16384, &tmB, fb, bx + b2x, by + b2y);
                     const uint32_t sfs = smem_u32(smem + SF_REGION + stage * SF_STAGE_BYTES);
                     bulk_load(sfs, sfa, 512, fb);
                     bulk_load(sfs + 512, sfb0, 512, fb);
@@ -1013,7 +1013,11 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     CUtensorMap ta, tb;
     bool ok;
     if (c.mode == kFprop || c.mode == kFpropSwiglu) {
-        ok = make_map(&ta, c.a_data, c.M, c.K) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
+        // fprop: B's 256 K-major rows in one box (one TMA operation per stage fewer); the SwiGLU
+        // variant loads its gate and up rows as two 128-row boxes
+        ok = make_map(&ta, c.a_data, c.M, c.K) &&
+             (c.mode == kFprop ? encode_tmap_2d(&tb, c.b_data, (int64_t)c.E * c.N, c.K, 1, 128, 256, 128)
+                               : make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K));
     } else if (c.mode == kDgrad || c.mode == kDgradSwiglu) {
         ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K);
     } else {
