@@ -385,6 +385,13 @@ MXQ_API int mxq_swiglu_bwd_quantize(const void* dh_bf16, const void* y_bf16, int
  * mmas_per_sm in [0, 2^31); MXQ_ERR_SHAPE otherwise. */
 MXQ_API int mxq_probe_mma_stream(int64_t mmas_per_sm, int32_t* d_status, mxq_stream_t stream);
 
+/* Self-test of the failure path every kernel shares: one CTA waits, limit_ns
+ * long, on an mbarrier that nothing arrives on, with the kernels' bounded wait;
+ * the wait expires, the CTA's other waiter is released through the abort flag,
+ * MXQ_STATUS_WAIT_TIMEOUT is set in *d_status (required) and the kernel returns,
+ * leaving the context usable. limit_ns in [1e3, 1e10]; MXQ_ERR_SHAPE otherwise. */
+MXQ_API int mxq_selftest_wait_timeout(int64_t limit_ns, int32_t* d_status, mxq_stream_t stream);
+
 /* Copy the device status word to *h_out after `stream` drains (the only
  * synchronizing call). */
 MXQ_API int mxq_status_read(const int32_t* d_status, int32_t* h_out, mxq_stream_t stream);

@@ -20,6 +20,7 @@ from .mxq import (  # noqa: F401
     requant_colwise,
     requant_colwise_scaled_bias,
     scale_bytes,
+    selftest_wait_timeout,
     status_read,
     swiglu_bwd,
     swiglu_bwd_quantize,

@@ -438,6 +438,15 @@ int mxq_probe_mma_stream(int64_t mmas_per_sm, int32_t* d_status, mxq_stream_t st
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
 }
 
+int mxq_selftest_wait_timeout(int64_t limit_ns, int32_t* d_status, mxq_stream_t stream) {
+    if (!d_status) return MXQ_ERR_NULL;
+    if (!arch_ok()) return MXQ_ERR_ARCH;
+    if (limit_ns < 1000 || limit_ns > 10000000000LL) return MXQ_ERR_SHAPE;
+    if (!device_pointer(d_status)) return MXQ_ERR_HOST_POINTER;
+    cudaError_t e = mxq::run_wait_timeout(limit_ns, d_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
 int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream) {
     if (!y_bf16 || !h_bf16) return MXQ_ERR_NULL;
     if (!arch_ok()) return MXQ_ERR_ARCH;

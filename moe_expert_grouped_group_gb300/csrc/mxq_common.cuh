@@ -272,20 +272,25 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 // Bounded wait: true when the phase with `parity` completed; false after
-// about 2 s (sets *abort_flag) or once another role has set *abort_flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// limit_ns (sets *abort_flag) or once another role has set *abort_flag.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned long long limit_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 0;; ++i) {
         if (mbar_try(bar, parity)) return true;
         if ((i & 63) == 63) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 return false;
             }
         }
     }
+}
+// The kernels' wait: bounded by kWaitNs (about 2 s).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait_for(bar, parity, abort_flag, kWaitNs);
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
     asm volatile(

@@ -1,5 +1,6 @@
-// mxq_peak.cu -- the MXFP8 tensor-pipe ceiling of this GPU, a yardstick for
-// the grouped GEMMs' roofline (it is not part of the MXFP8 path).
+// mxq_peak.cu -- utilities beside the MXFP8 path: the tensor-pipe ceiling
+// of this GPU (a yardstick for the grouped GEMMs' roofline) and a self-test
+// of the bounded on-chip wait every kernel uses.
 //
 // One CTA per SM streams block-scaled 128x256x32 tcgen05 MMAs (E4M3 x E4M3,
 // E8M0 scales, fp32 accumulation in TMEM) from operands that stay resident
@@ -94,7 +95,34 @@ __global__ void __launch_bounds__(kPeakThreads) mma_stream_kernel(int64_t mmas, 
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
 }
 
+// Self-test of the bounded on-chip wait: lane 0 of warp 0 waits, limit_ns
+// long, on an mbarrier that nothing arrives on; lane 0 of warp 1 waits on the
+// same barrier with the kernels' own bound. The first wait expires and sets
+// the CTA's abort flag, which ends the second; the kernel then reports
+// MXQ_STATUS_WAIT_TIMEOUT and returns (no trap, no fault).
+__global__ void __launch_bounds__(64) wait_timeout_kernel(unsigned long long limit_ns, int32_t* status) {
+    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ int s_abort;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        mbar_init(smem_u32(&s_bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+        if (threadIdx.x == 0) (void)mbar_wait_for(smem_u32(&s_bar), 0, &s_abort, limit_ns);
+        else (void)mbar_wait(smem_u32(&s_bar), 0, &s_abort);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && s_abort) report_status(status, MXQ_STATUS_WAIT_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t run_wait_timeout(int64_t limit_ns, int32_t* status, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 64, 0, s>>>((unsigned long long)limit_ns, status);
+    return cudaGetLastError();
+}
 
 cudaError_t run_mma_stream(int64_t mmas_per_sm, int32_t* status, cudaStream_t s) {
     int dev = 0, sms = 0;

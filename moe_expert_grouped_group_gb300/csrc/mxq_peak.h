@@ -1,5 +1,6 @@
-// The MXFP8 tensor-pipe ceiling probe (mxq_peak.cu): a measurement utility
-// beside the MXFP8 path, exported as mxq_probe_mma_stream.
+// Utilities beside the MXFP8 path (mxq_peak.cu): the tensor-pipe ceiling
+// probe (mxq_probe_mma_stream) and the bounded-wait self-test
+// (mxq_selftest_wait_timeout).
 #pragma once
 #include <cuda_runtime.h>
 
@@ -9,4 +10,7 @@ namespace mxq {
 // One CTA per SM issues mmas_per_sm block-scaled 128x256x32 MMAs from
 // resident shared memory; a bounded-wait timeout sets MXQ_STATUS_WAIT_TIMEOUT.
 cudaError_t run_mma_stream(int64_t mmas_per_sm, int32_t* status, cudaStream_t s);
+// One CTA waits limit_ns on an mbarrier nothing arrives on, then reports
+// MXQ_STATUS_WAIT_TIMEOUT in *status.
+cudaError_t run_wait_timeout(int64_t limit_ns, int32_t* status, cudaStream_t s);
 }  // namespace mxq

@@ -30,6 +30,7 @@ SYMBOLS = [
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
     "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu", "mxq_grouped_gemm_dgrad_swiglu",
     "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex", "mxq_probe_mma_stream",
+    "mxq_selftest_wait_timeout",
 ]
 
 
@@ -79,6 +80,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_status_read.argtypes = [_P, _P, _P]
     L.mxq_probe_mma_stream.argtypes = [_I64, _P, _P]
     L.mxq_probe_mma_stream.restype = _INT
+    L.mxq_selftest_wait_timeout.argtypes = [_I64, _P, _P]
+    L.mxq_selftest_wait_timeout.restype = _INT
     L.mxq_error_string.argtypes = [_INT]
     L.mxq_error_string.restype = ctypes.c_char_p
     L.mxq_last_cuda_error.restype = _INT
@@ -402,6 +405,12 @@ def probe_mma_stream(mmas_per_sm=8192, status=None):
     _check(lib().mxq_probe_mma_stream(int(mmas_per_sm), _ptr(status), _stream()), "mxq_probe_mma_stream")
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return 2.0 * 128 * 256 * 32 * mmas_per_sm * sms
+
+
+def selftest_wait_timeout(status, limit_ns=20_000_000):
+    """Make one bounded on-chip wait expire on purpose (an mbarrier nothing arrives on): sets
+    STATUS_WAIT_TIMEOUT in `status` and returns, leaving the context usable."""
+    _check(lib().mxq_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream()), "mxq_selftest_wait_timeout")
 
 
 def swiglu_fwd(y, out=None):
