@@ -5,6 +5,8 @@
 // here allocates.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "../../include/mxq.h"
 #include "mxq_internal.h"
 #include "mxq_peak.h"
@@ -20,17 +22,21 @@ int fail_cuda(cudaError_t e) {
 
 bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Device attribute cache: 1 = sm_103 (GB300), -1 = other, 0 = unknown.
+// Device attribute cache: 1 = sm_103 (GB300), -1 = other, 0 = unknown (atomic: calls may come from
+// several host threads).
 int arch_ok() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev < 64 && cache[dev]) return cache[dev] > 0;
+    if (dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c) return c > 0;
+    }
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     const int ok = (major == 10 && minor == 3) ? 1 : -1;
-    if (dev < 64) cache[dev] = ok;
+    if (dev < 64) cache[dev].store(ok, std::memory_order_relaxed);
     return ok > 0;
 }
 

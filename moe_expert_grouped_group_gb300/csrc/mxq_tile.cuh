@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "mxq_common.cuh"
@@ -445,14 +446,18 @@ __global__ void __launch_bounds__(kTileThreads)
     if (threadIdx.x == 0 && s_abort && a.status) atomicOr(a.status, MXQ_STATUS_WAIT_TIMEOUT);
 }
 
+// SM count per device, cached (atomic: launches may come from several host threads).
 static int num_sms() {
-    static int n[64] = {0};
+    static std::atomic<int> n[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && n[dev]) return n[dev];
+    if (dev < 64) {
+        const int c = n[dev].load(std::memory_order_relaxed);
+        if (c) return c;
+    }
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    if (dev < 64) n[dev] = v;
+    if (dev < 64) n[dev].store(v, std::memory_order_relaxed);
     return v;
 }
 
