@@ -1040,7 +1040,8 @@ def main():
                "wall_s": time.perf_counter() - t0}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step_max, "ms_per_step_median": statistics.median(per_step),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8_e4m3 (fp32 accumulate)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
                    "m_splits": [int(v) for v in d["m_splits"]],
