@@ -115,6 +115,35 @@ def _stream():
     return torch.cuda.current_stream().cuda_stream
 
 
+_BF16 = (torch.bfloat16,)
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+_BYTE = tuple(d for d in (torch.uint8, torch.int8, getattr(torch, "float8_e4m3fn", None),
+                          getattr(torch, "float8_e8m0fnu", None)) if d is not None)
+
+
+def _need(t, name, nbytes, dtypes):
+    """The library takes raw pointers: check that a tensor the kernel reads or writes has the
+    element type it expects and at least the bytes it touches (an undersized output would be
+    written past its end). Outputs in the padded layouts are checked against the allocation bound
+    (scale_bytes_grouped); padded inputs against the dense size, a lower bound of their exact size,
+    which follows the device-resident expert counts."""
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise MXQError(f"{name}: dtype {t.dtype}, expected one of {[str(d) for d in dtypes]}")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise MXQError(f"{name}: {have} bytes, the call touches {int(nbytes)}")
+
+
+def _need_flags(noop, status):
+    _need(noop, "noop", 4, _I32)
+    _need(status, "status", 4, _I32)
+
+
 def _check(rc: int, what: str):
     if rc != 0:
         L = lib()
@@ -185,6 +214,14 @@ def group_quantize(x, m_splits=None, E=None, rowwise=True, colwise=True, swizzle
         o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
         ws = workspace if workspace is not None else _u8(
             max(16, workspace_bytes(OP_GROUP_QUANTIZE, M, 0, K, E, flags)), dev)
+    _need(x, "x", M * K * 2, _BF16)
+    _need(o.get("row_data"), "row_data", M * K, _BYTE)
+    _need(o.get("row_scale"), "row_scale", rs if rowwise else 0, _BYTE)
+    _need(o.get("col_data"), "col_data", M * K, _BYTE)
+    _need(o.get("col_scale"), "col_scale",
+          (scale_bytes_grouped(M, K, E, True) if pad_experts else scale_bytes(M, K, True)) if colwise else 0, _BYTE)
+    _need(o.get("dbias"), "dbias", E * K * 4, _F32)
+    _need_flags(noop, status)
     rc = lib().mxq_group_quantize(
         _ptr(x), M, K, E, _ptr(m_splits), flags, _ptr(o.get("row_data")), _ptr(o.get("row_scale")),
         _ptr(o.get("col_data")), _ptr(o.get("col_scale")), _ptr(o.get("dbias")), _ptr(noop), _ptr(status),
@@ -217,6 +254,14 @@ def requant_colwise(row_data, row_scale_compact, m_splits, colwise=True, swizzle
         o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
         ws = workspace if workspace is not None else _u8(
             max(16, workspace_bytes(OP_REQUANT_COLWISE, M, 0, K, E, flags)), dev)
+    _need(row_data, "row_data", M * K, _BYTE)
+    _need(row_scale_compact, "row_scale_compact", M * (K // 32), _BYTE)
+    _need(o.get("col_data"), "col_data", M * K, _BYTE)
+    _need(o.get("col_scale"), "col_scale", sb(M, K, True) if colwise else 0, _BYTE)
+    _need(o.get("row_scale_swizzled"), "row_scale_swizzled", sb(M, K, False) if row_scale_swizzled else 0, _BYTE)
+    _need(o.get("dequant"), "dequant", M * K * 2, _BF16)
+    _need(o.get("dbias"), "dbias", E * K * 4, _F32)
+    _need_flags(noop, status)
     rc = lib().mxq_requant_colwise(
         _ptr(row_data), _ptr(row_scale_compact), M, K, E, _ptr(m_splits), flags, _ptr(o.get("col_data")),
         _ptr(o.get("col_scale")), _ptr(o.get("row_scale_swizzled")), _ptr(o.get("dbias")), _ptr(o.get("dequant")),
@@ -246,6 +291,15 @@ def group_quantize_scaled_bias(x, m_splits, probs, bias, rowwise=True, colwise=T
     if dprobs:
         o.setdefault("dprobs", torch.empty((M,), dtype=torch.float32, device=dev))
     ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SCALED_BIAS, M, 0, K, E)), dev)
+    _need(x, "x", M * K * 2, _BF16)
+    _need(probs, "probs", M * 4, _F32)
+    _need(bias, "bias", E * K * 2, _BF16)
+    for k, n in (("row_data", M * K), ("row_scale", scale_bytes(M, K, False)), ("col_data", M * K),
+                 ("col_scale", scale_bytes(M, K, True))):
+        _need(o.get(k), k, n, _BYTE)
+    _need(o.get("dbias"), "dbias", E * K * 4, _F32)
+    _need(o.get("dprobs"), "dprobs", M * 4, _F32)
+    _need_flags(noop, status)
     rc = lib().mxq_group_quantize_scaled_bias(
         _ptr(x), M, K, E, _ptr(m_splits), flags, _ptr(o.get("row_data")), _ptr(o.get("row_scale")),
         _ptr(o.get("col_data")), _ptr(o.get("col_scale")), _ptr(probs), _ptr(bias), _ptr(o.get("dbias")),
@@ -278,6 +332,17 @@ def requant_colwise_scaled_bias(row_data, row_scale_compact, m_splits, probs, bi
     if dprobs:
         o.setdefault("dprobs", torch.empty((M,), dtype=torch.float32, device=dev))
     ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SCALED_BIAS, M, 0, K, E)), dev)
+    _need(row_data, "row_data", M * K, _BYTE)
+    _need(row_scale_compact, "row_scale_compact", M * (K // 32), _BYTE)
+    _need(probs, "probs", M * 4, _F32)
+    _need(bias, "bias", E * K * 2, _BF16)
+    for k, n in (("col_data", M * K), ("col_scale", scale_bytes(M, K, True)),
+                 ("row_scale_swizzled", scale_bytes(M, K, False))):
+        _need(o.get(k), k, n, _BYTE)
+    _need(o.get("dequant"), "dequant", M * K * 2, _BF16)
+    _need(o.get("dbias"), "dbias", E * K * 4, _F32)
+    _need(o.get("dprobs"), "dprobs", M * 4, _F32)
+    _need_flags(noop, status)
     rc = lib().mxq_requant_colwise_scaled_bias(
         _ptr(row_data), _ptr(row_scale_compact), M, K, E, _ptr(m_splits), flags, _ptr(o.get("col_data")),
         _ptr(o.get("col_scale")), _ptr(o.get("row_scale_swizzled")), _ptr(probs), _ptr(bias), _ptr(o.get("dbias")),
@@ -293,6 +358,9 @@ def grouped_dbias(dy, m_splits, status=None, out=None, workspace=None):
     E = m_splits.numel()
     out = out if out is not None else torch.empty((E, N), dtype=torch.float32, device=dy.device)
     ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_GROUPED_DBIAS, M, N, 0, E)), dy.device)
+    _need(dy, "dy", M * N * 2, _BF16)
+    _need(out, "out", E * N * 4, _F32)
+    _need_flags(None, status)
     rc = lib().mxq_grouped_dbias(_ptr(dy), M, N, E, _ptr(m_splits), _ptr(out), _ptr(status), _ptr(ws),
                                  ws.numel(), _stream())
     _check(rc, "mxq_grouped_dbias")
@@ -307,6 +375,14 @@ def grouped_gemm_fprop(x_data, x_scale, w_data, w_scale, m_splits, bias=None, st
     E, N, _ = w_data.shape
     m_splits = _splits(m_splits)
     out = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x_data.device)
+    _need(x_data, "x_data", M * K, _BYTE)
+    # padded inputs: the exact size follows the device-resident counts; the dense size is a lower bound
+    _need(x_scale, "x_scale", scale_bytes(M, K, False), _BYTE)
+    _need(w_data, "w_data", E * N * K, _BYTE)
+    _need(w_scale, "w_scale", scale_bytes(E * N, K, False), _BYTE)
+    _need(bias, "bias", E * N * 2, _BF16)
+    _need(out, "out", M * N * 2, _BF16)
+    _need_flags(None, status)
     rc = lib().mxq_grouped_gemm_fprop_ex(_ptr(x_data), _ptr(x_scale), _ptr(w_data), _ptr(w_scale), _ptr(bias), M, N,
                                          K, E, _ptr(m_splits), PAD_EXPERTS if pad_experts else 0, _ptr(out),
                                          _ptr(status), None, 0, _stream())
@@ -330,6 +406,16 @@ def grouped_gemm_fprop_swiglu(x_data, x_scale, w1_data, w1_scale, m_splits, bias
     o.setdefault("row_scale", _u8(scale_bytes(M, F, False), dev))
     o.setdefault("col_data", _u8((M, F), dev))
     o.setdefault("col_scale", _u8(scale_bytes(M, F, True), dev))
+    _need(x_data, "x_data", M * K, _BYTE)
+    _need(x_scale, "x_scale", scale_bytes(M, K, False), _BYTE)
+    _need(w1_data, "w1_data", E * 2 * F * K, _BYTE)
+    _need(w1_scale, "w1_scale", scale_bytes(E * 2 * F, K, False), _BYTE)
+    _need(bias, "bias", E * 2 * F * 2, _BF16)
+    _need(o["y1"], "y1", M * 2 * F * 2, _BF16)
+    for k, n in (("row_data", M * F), ("row_scale", scale_bytes(M, F, False)), ("col_data", M * F),
+                 ("col_scale", scale_bytes(M, F, True))):
+        _need(o[k], k, n, _BYTE)
+    _need_flags(None, status)
     rc = lib().mxq_grouped_gemm_fprop_swiglu(
         _ptr(x_data), _ptr(x_scale), _ptr(w1_data), _ptr(w1_scale), _ptr(bias), M, K, F, E, _ptr(m_splits),
         SWIZZLE if swizzle else 0, _ptr(o["y1"]), _ptr(o["row_data"]), _ptr(o["row_scale"]), _ptr(o["col_data"]),
@@ -346,6 +432,12 @@ def grouped_gemm_dgrad(dy_data, dy_scale, w_col_data, w_col_scale, m_splits, sta
     E, _, K = w_col_data.shape
     m_splits = _splits(m_splits)
     out = out if out is not None else torch.empty((M, K), dtype=torch.bfloat16, device=dy_data.device)
+    _need(dy_data, "dy_data", M * N, _BYTE)
+    _need(dy_scale, "dy_scale", scale_bytes(M, N, False), _BYTE)  # padded: a lower bound, as in fprop
+    _need(w_col_data, "w_col_data", E * N * K, _BYTE)
+    _need(w_col_scale, "w_col_scale", scale_bytes(E * N, K, True), _BYTE)
+    _need(out, "out", M * K * 2, _BF16)
+    _need_flags(None, status)
     rc = lib().mxq_grouped_gemm_dgrad_ex(_ptr(dy_data), _ptr(dy_scale), _ptr(w_col_data), _ptr(w_col_scale), M, N,
                                          K, E, _ptr(m_splits), PAD_EXPERTS if pad_experts else 0, _ptr(out),
                                          _ptr(status), None, 0, _stream())
@@ -372,6 +464,16 @@ def grouped_gemm_dgrad_swiglu(dy_data, dy_scale, w_col_data, w_col_scale, y1, m_
         o.setdefault("dbias", torch.empty((E, 2 * F), dtype=torch.float32, device=dev))
         ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_GEMM_DGRAD_SWIGLU, M, N, F, E)),
                                                          dev)
+    _need(dy_data, "dy_data", M * N, _BYTE)
+    _need(dy_scale, "dy_scale", scale_bytes(M, N, False), _BYTE)
+    _need(w_col_data, "w_col_data", E * N * F, _BYTE)
+    _need(w_col_scale, "w_col_scale", scale_bytes(E * N, F, True), _BYTE)
+    _need(y1, "y1", M * 2 * F * 2, _BF16)
+    for k, n in (("row_data", M * 2 * F), ("row_scale", scale_bytes(M, 2 * F, False)), ("col_data", M * 2 * F),
+                 ("col_scale", scale_bytes(M, 2 * F, True))):
+        _need(o[k], k, n, _BYTE)
+    _need(o.get("dbias"), "dbias", E * 2 * F * 4, _F32)
+    _need_flags(None, status)
     rc = lib().mxq_grouped_gemm_dgrad_swiglu(
         _ptr(dy_data), _ptr(dy_scale), _ptr(w_col_data), _ptr(w_col_scale), _ptr(y1), M, N, F, E, _ptr(m_splits),
         SWIZZLE if swizzle else 0, _ptr(o["row_data"]), _ptr(o["row_scale"]), _ptr(o["col_data"]),
@@ -392,6 +494,12 @@ def grouped_gemm_wgrad(dy_col_data, dy_col_scale, x_col_data, x_col_scale, m_spl
     if out is None:
         out = torch.empty((E, N, K), dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dy_col_data.device)
     flags = (ACCUMULATE if accumulate else 0) | (OUT_BF16 if out_bf16 else 0) | (PAD_EXPERTS if pad_experts else 0)
+    _need(dy_col_data, "dy_col_data", M * N, _BYTE)
+    _need(dy_col_scale, "dy_col_scale", scale_bytes(M, N, True), _BYTE)  # padded: a lower bound, as in fprop
+    _need(x_col_data, "x_col_data", M * K, _BYTE)
+    _need(x_col_scale, "x_col_scale", scale_bytes(M, K, True), _BYTE)
+    _need(out, "out", E * N * K * (2 if out_bf16 else 4), _BF16 if out_bf16 else _F32)
+    _need_flags(None, status)
     rc = lib().mxq_grouped_gemm_wgrad(_ptr(dy_col_data), _ptr(dy_col_scale), _ptr(x_col_data), _ptr(x_col_scale), M,
                                       N, K, E, _ptr(m_splits), flags, _ptr(out), _ptr(status), None, 0, _stream())
     _check(rc, "mxq_grouped_gemm_wgrad")
@@ -402,6 +510,7 @@ def probe_mma_stream(mmas_per_sm=8192, status=None):
     """Launch the tensor-pipe ceiling probe (not part of the MXFP8 path): one CTA per SM issues
     mmas_per_sm block-scaled 128x256x32 MMAs from resident shared memory. Returns its FLOPs
     (2*128*256*32*mmas_per_sm*SMs); time it with CUDA events on the current stream."""
+    _need_flags(None, status)
     _check(lib().mxq_probe_mma_stream(int(mmas_per_sm), _ptr(status), _stream()), "mxq_probe_mma_stream")
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return 2.0 * 128 * 256 * 32 * mmas_per_sm * sms
@@ -410,12 +519,15 @@ def probe_mma_stream(mmas_per_sm=8192, status=None):
 def selftest_wait_timeout(status, limit_ns=20_000_000):
     """Make one bounded on-chip wait expire on purpose (an mbarrier nothing arrives on): sets
     STATUS_WAIT_TIMEOUT in `status` and returns, leaving the context usable."""
+    _need_flags(None, status)
     _check(lib().mxq_selftest_wait_timeout(int(limit_ns), _ptr(status), _stream()), "mxq_selftest_wait_timeout")
 
 
 def swiglu_fwd(y, out=None):
     M, F2 = y.shape
     out = out if out is not None else torch.empty((M, F2 // 2), dtype=torch.bfloat16, device=y.device)
+    _need(y, "y", M * F2 * 2, _BF16)
+    _need(out, "out", M * (F2 // 2) * 2, _BF16)
     _check(lib().mxq_swiglu_fwd(_ptr(y), M, F2 // 2, _ptr(out), _stream()), "mxq_swiglu_fwd")
     return out
 
@@ -423,6 +535,9 @@ def swiglu_fwd(y, out=None):
 def swiglu_bwd(dh, y, out=None):
     M, F2 = y.shape
     out = out if out is not None else torch.empty((M, F2), dtype=torch.bfloat16, device=y.device)
+    _need(dh, "dh", M * (F2 // 2) * 2, _BF16)
+    _need(y, "y", M * F2 * 2, _BF16)
+    _need(out, "out", M * F2 * 2, _BF16)
     _check(lib().mxq_swiglu_bwd(_ptr(dh), _ptr(y), M, F2 // 2, _ptr(out), _stream()), "mxq_swiglu_bwd")
     return out
 
@@ -451,6 +566,12 @@ def swiglu_quantize(y, m_splits, rowwise=True, colwise=True, swizzle=True, h_out
         o.setdefault("h", torch.empty((M, F), dtype=torch.bfloat16, device=dev))
     flags = ((ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
              | (DEQUANT_OUT if h_out else 0))
+    _need(y, "y", M * F2 * 2, _BF16)
+    for k, n in (("row_data", M * F), ("row_scale", scale_bytes(M, F, False)), ("col_data", M * F),
+                 ("col_scale", scale_bytes(M, F, True))):
+        _need(o.get(k), k, n, _BYTE)
+    _need(o.get("h"), "h", M * F * 2, _BF16)
+    _need_flags(noop, status)
     rc = lib().mxq_swiglu_quantize(_ptr(y), M, F, E, _ptr(m_splits), flags, _ptr(o.get("row_data")),
                                    _ptr(o.get("row_scale")), _ptr(o.get("col_data")), _ptr(o.get("col_scale")),
                                    _ptr(o.get("h")), _ptr(noop), _ptr(status), _stream())
@@ -477,6 +598,14 @@ def swiglu_bwd_quantize(dh, y, m_splits, rowwise=True, colwise=True, swizzle=Tru
                                                          dev)
     flags = ((ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
              | (DEQUANT_OUT if dy_out else 0))
+    _need(dh, "dh", M * F * 2, _BF16)
+    _need(y, "y", M * F2 * 2, _BF16)
+    for k, n in (("row_data", M * F2), ("row_scale", scale_bytes(M, F2, False)), ("col_data", M * F2),
+                 ("col_scale", scale_bytes(M, F2, True))):
+        _need(o.get(k), k, n, _BYTE)
+    _need(o.get("dbias"), "dbias", E * F2 * 4, _F32)
+    _need(o.get("dy"), "dy", M * F2 * 2, _BF16)
+    _need_flags(noop, status)
     rc = lib().mxq_swiglu_bwd_quantize(_ptr(dh), _ptr(y), M, F, E, _ptr(m_splits), flags, _ptr(o.get("row_data")),
                                        _ptr(o.get("row_scale")), _ptr(o.get("col_data")), _ptr(o.get("col_scale")),
                                        _ptr(o.get("dbias")), _ptr(o.get("dy")), _ptr(noop), _ptr(status), _ptr(ws),
