@@ -257,3 +257,38 @@ def test_padded_gemms_with_aligned_splits_match_the_plain_calls(mxq):
     dw0 = mxq.grouped_gemm_wgrad(dev_u8(op.sdy["col_q"]), dev_u8(op.sdy["col_s"]), dev_u8(op.sx["col_q"]),
                                  dev_u8(op.sx["col_s"]), d)
     assert torch.equal(y, y0) and torch.equal(dx, dx0) and torch.equal(dw, dw0)
+
+
+def test_padded_fprop_with_bias(mxq):
+    """The bias on padded operands: full 32-row boxes leave through TMA stores, the rows of a box that
+    reaches past its expert row by row; both add b_e in fp32 before the bf16 rounding."""
+    ms = [40, 3, 0, 200, 57]
+    op = PaddedOps(ms, 256, 256, 96)
+    E, N, K = op.E, op.N, op.K
+    bias = bf16_bits_from_f32((0.5 * np.random.default_rng(97).standard_normal((E, N))).astype(np.float32))
+    y = mxq.grouped_gemm_fprop(dev_u8(op.sx["row_q"]), dev_u8(op.sx["row_s"]), dev_u8(op.sw["row_q"]).view(E, N, K),
+                               dev_u8(op.sw["row_s"]), dev_i64(op.ms), bias=dev_bf16(bias), pad_experts=True)
+    r, c = np.meshgrid(np.arange(op.M), np.arange(N), indexing="ij")
+    ref, mag = orc.fprop_entries(op.cx["row_q"], op.cx["row_s"], op.cw["row_q"].reshape(E, N, K), op.cw["row_s"],
+                                 op.mp, op.prow[r.ravel()], c.ravel(), bias=bias)
+    assert scaled_error(_f64(y)[r.ravel(), c.ravel()], ref, mag) <= TOL_BF16
+
+
+def test_padded_wgrad_bf16_out_and_accumulate(mxq):
+    ms = [40, 3, 0, 200, 57]
+    op = PaddedOps(ms, 256, 256, 98)
+    E, N, K = op.E, op.N, op.K
+    args = (dev_u8(op.sdy["col_q"]), dev_u8(op.sdy["col_s"]), dev_u8(op.sx["col_q"]), dev_u8(op.sx["col_s"]),
+            dev_i64(op.ms))
+    e, n, k = (a.ravel() for a in np.meshgrid(np.arange(E), np.arange(N), np.arange(K), indexing="ij"))
+    ref, mag = orc.wgrad_entries(op.cdy["col_q"], op.cdy["col_s"], op.cx["col_q"], op.cx["col_s"], op.mp, e, n, k)
+    dwb = mxq.grouped_gemm_wgrad(*args, out_bf16=True, pad_experts=True)
+    assert scaled_error(_f64(dwb)[e, n, k], ref, mag) <= TOL_BF16
+    prefill = np.random.default_rng(99).standard_normal((E, N, K)).astype(np.float32)
+    acc = torch.from_numpy(prefill.copy()).cuda()
+    mxq.grouped_gemm_wgrad(*args, accumulate=True, out=acc, pad_experts=True)
+    got = host(acc).astype(np.float64) - prefill.astype(np.float64)
+    # the fp32 read-modify-write adds one rounding of the sum's size on top of the product's tolerance
+    tol = TOL_F32 * mag + 2.0 ** -23 * (np.abs(prefill.astype(np.float64))[e, n, k] + np.abs(ref))
+    assert np.all(np.abs(got[e, n, k] - ref) <= tol + 1e-30)
+    assert np.array_equal(host(acc)[2], prefill[2])  # the empty expert is left as it was
