@@ -54,13 +54,15 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mlp", action="store_true", help="skip the full-MLP step measurement")
-    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp", "padded", "configs", "mma_peak"],
+    p.add_argument("--only", choices=["swiglu_quantize", "scaled_bias", "fused_mlp", "padded", "configs", "mma_peak",
+                                      "mlp_e32"],
                    help="time only one fused kernel family on the MLP workload's shapes and print its line (a "
                         "small footprint for profilers): the SwiGLU->quantize kernels (forward and backward), "
                         "requant of the FC2 gradient with plain dbias vs with the scaled-bias reductions, the "
                         "SwiGLU-fused FC1 fprop and FC2 dgrad vs their unfused pairs, group_quantize with "
                         "expert counts that are not multiples of 128, one grouped-linear step on every "
-                        "synthetic workload, or the tensor-pipe ceiling probe (back-to-back block-scaled MMAs)")
+                        "synthetic workload, the tensor-pipe ceiling probe (back-to-back block-scaled MMAs), or "
+                        "the full SwiGLU MLP step (fwd+bwd) on the 32-expert bf16-input workload")
     return p.parse_args()
 
 
@@ -192,37 +194,34 @@ class NativeStep:
 
 
 MLP_WORKLOAD = "e64_h3072_f1024_t84k_prequant"
-MLP_STAGES = ["requant_x", "quantize_w1_w2", "fc1_fprop_swiglu_quantize_h", "fc2_fprop", "requant_dy2_dbias",
-              "fc2_dgrad", "fc2_wgrad", "swiglu_bwd_quantize_dy1_dbias", "fc1_dgrad", "fc1_wgrad"]
+MLP_WORKLOAD_E32 = "e32_h4096_f1536_t64k_swiglu"
 
 
 class MLPStep:
-    """Forward + backward of a grouped MoE MLP (FC1 -> SwiGLU -> FC2) with
-    per-expert biases; X and the FC2 gradient arrive rowwise-quantized (the
-    expert-parallel dispatch and the combine's backward). Covers every step
-    of the path: requant (+fused dbias), weight and activation quantize
-    (+fused dbias), the three grouped GEMMs of both linears, SwiGLU."""
+    """Forward + backward of a grouped MoE MLP (FC1 -> SwiGLU -> FC2). On the 64-expert workload X
+    and the FC2 gradient arrive rowwise-quantized (the expert-parallel dispatch and the combine's
+    backward) and both linears carry per-expert biases; on the 32-expert workload X and the FC2
+    gradient arrive in bf16 and there are no biases. Covers every step of the path: requant or
+    quantize (+fused dbias), weight quantize, the three grouped GEMMs of both linears, SwiGLU."""
 
-    def __init__(self, dev, seed=0):
+    def __init__(self, dev, workload=MLP_WORKLOAD, seed=0):
         import torch
 
         import moe_expert_grouped_group_gb300 as mxq
         from synth import WORKLOADS, make_inputs
 
         self.torch, self.mxq = torch, mxq
-        w = self.w = WORKLOADS[MLP_WORKLOAD]
-        d = make_inputs(w, seed=seed, which=("x", "w", "dy", "w2", "dy2", "b1", "b2"))
+        w = self.w = WORKLOADS[workload]
+        self.pre_x, self.pre_dy, self.has_bias = w.prequant_x, w.prequant_dy, w.bias
+        which = ("x", "w", "w2", "dy2") + (("b1", "b2") if w.bias else ())
+        d = make_inputs(w, seed=seed, which=which)
         E, H, F, M = w.E, w.K, w.F, w.M
         self.E, self.H, self.F, self.M = E, H, F, M
         tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
         self.ms = torch.from_numpy(d["m_splits"]).to(dev)
         self.w1 = tb(d["w"]).view(E * 2 * F, H)
         self.w2 = tb(d["w2"]).view(E * H, F)
-        self.b1, self.b2 = tb(d["b1"]), tb(d["b2"])
-        qx = mxq.group_quantize(tb(d["x"]), self.ms, rowwise=True, colwise=False, swizzle=False)
-        qd = mxq.group_quantize(tb(d["dy2"]), self.ms, rowwise=True, colwise=False, swizzle=False)
-        self.x_row, self.x_rs = qx["row_data"], qx["row_scale"]
-        self.dy2_row, self.dy2_rs = qd["row_data"], qd["row_scale"]
+        self.b1, self.b2 = (tb(d["b1"]), tb(d["b2"])) if w.bias else (None, None)
         u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
         bf = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=dev)
         sb = mxq.scale_bytes
@@ -231,14 +230,33 @@ class MLPStep:
             return {"row_data": u8((rows, cols)), "row_scale": u8(sb(rows, cols, False)),
                     "col_data": u8((rows, cols)), "col_scale": u8(sb(rows, cols, True))}
 
-        self.rqx = {"col_data": u8((M, H)), "col_scale": u8(sb(M, H, True)), "row_scale_swizzled": u8(sb(M, H, False))}
-        self.rqd = {"col_data": u8((M, H)), "col_scale": u8(sb(M, H, True)), "row_scale_swizzled": u8(sb(M, H, False)),
-                    "dbias": torch.empty((E, H), dtype=torch.float32, device=dev)}
+        def rq(rows, cols):
+            return {"col_data": u8((rows, cols)), "col_scale": u8(sb(rows, cols, True)),
+                    "row_scale_swizzled": u8(sb(rows, cols, False))}
+
+        if self.pre_x:  # the dispatch wire format, made once by the library itself (setup, untimed)
+            qx = mxq.group_quantize(tb(d["x"]), self.ms, rowwise=True, colwise=False, swizzle=False)
+            self.x_row, self.x_rs = qx["row_data"], qx["row_scale"]
+            self.qx = rq(M, H)
+        else:
+            self.x_bf16 = tb(d["x"])
+            self.qx = q(M, H)
+        if self.pre_dy:
+            qd = mxq.group_quantize(tb(d["dy2"]), self.ms, rowwise=True, colwise=False, swizzle=False)
+            self.dy2_row, self.dy2_rs = qd["row_data"], qd["row_scale"]
+            self.qd = rq(M, H)
+        else:
+            self.dy2_bf16 = tb(d["dy2"])
+            self.qd = q(M, H)
+        if w.bias:
+            self.qd["dbias"] = torch.empty((E, H), dtype=torch.float32, device=dev)
         self.qw1, self.qw2 = q(E * 2 * F, H), q(E * H, F)
         self.qh = q(M, F)
         self.qdy1 = q(M, 2 * F)
-        self.qdy1["dbias"] = torch.empty((E, 2 * F), dtype=torch.float32, device=dev)
+        if w.bias:
+            self.qdy1["dbias"] = torch.empty((E, 2 * F), dtype=torch.float32, device=dev)
         self.ws = u8(max(mxq.workspace_bytes(mxq.mxq.OP_REQUANT_COLWISE, M, 0, H, E),
+                         mxq.workspace_bytes(mxq.mxq.OP_GROUP_QUANTIZE, M, 0, H, E),
                          mxq.workspace_bytes(mxq.mxq.OP_SWIGLU_BWD_QUANTIZE, M, 0, F, E)))
         self.y1, self.y2 = bf(M, 2 * F), bf(M, H)
         self.fc1_out = dict(self.qh, y1=self.y1)  # FC1 output saved bf16 + h quantized in its epilogue
@@ -246,7 +264,11 @@ class MLPStep:
         self.dw1 = torch.empty((E, 2 * F, H), dtype=torch.float32, device=dev)
         self.dw2 = torch.empty((E, H, F), dtype=torch.float32, device=dev)
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        self.launches_per_step = 13
+        self.launches_per_step = 11 + (1 if w.bias else 0) * 2
+        b = "_dbias" if w.bias else ""
+        self.stages = [("requant_x" if self.pre_x else "quantize_x"), "quantize_w1_w2", "fc1_fprop_swiglu_quantize_h",
+                       "fc2_fprop", ("requant_dy2" if self.pre_dy else "quantize_dy2") + b, "fc2_dgrad", "fc2_wgrad",
+                       "swiglu_bwd_quantize_dy1" + b, "fc1_dgrad", "fc1_wgrad"]
 
     def flops(self):
         return 6.0 * self.M * (2 * self.F * self.H + self.H * self.F)
@@ -255,48 +277,58 @@ class MLPStep:
         mxq, E, H, F = self.mxq, self.E, self.H, self.F
         rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
         rec(0)
-        mxq.requant_colwise(self.x_row, self.x_rs, self.ms, out=self.rqx)
+        if self.pre_x:
+            mxq.requant_colwise(self.x_row, self.x_rs, self.ms, out=self.qx)
+            x_row, x_rs = self.x_row, self.qx["row_scale_swizzled"]
+        else:
+            mxq.group_quantize(self.x_bf16, self.ms, out=self.qx)
+            x_row, x_rs = self.qx["row_data"], self.qx["row_scale"]
         rec(1)
         mxq.group_quantize(self.w1, None, E=E, out=self.qw1)
         mxq.group_quantize(self.w2, None, E=E, out=self.qw2)
         rec(2)
-        mxq.grouped_gemm_fprop_swiglu(self.x_row, self.rqx["row_scale_swizzled"],
-                                      self.qw1["row_data"].view(E, 2 * F, H), self.qw1["row_scale"], self.ms,
-                                      bias=self.b1, out=self.fc1_out)
+        mxq.grouped_gemm_fprop_swiglu(x_row, x_rs, self.qw1["row_data"].view(E, 2 * F, H), self.qw1["row_scale"],
+                                      self.ms, bias=self.b1, out=self.fc1_out)
         rec(3)
         mxq.grouped_gemm_fprop(self.qh["row_data"], self.qh["row_scale"], self.qw2["row_data"].view(E, H, F),
                                self.qw2["row_scale"], self.ms, bias=self.b2, out=self.y2)
         rec(4)
-        mxq.requant_colwise(self.dy2_row, self.dy2_rs, self.ms, dbias=True, out=self.rqd, workspace=self.ws)
+        if self.pre_dy:
+            mxq.requant_colwise(self.dy2_row, self.dy2_rs, self.ms, dbias=self.has_bias, out=self.qd,
+                                workspace=self.ws)
+            dy2_row, dy2_rs = self.dy2_row, self.qd["row_scale_swizzled"]
+        else:
+            mxq.group_quantize(self.dy2_bf16, self.ms, dbias=self.has_bias, out=self.qd, workspace=self.ws)
+            dy2_row, dy2_rs = self.qd["row_data"], self.qd["row_scale"]
         rec(5)
-        mxq.grouped_gemm_dgrad(self.dy2_row, self.rqd["row_scale_swizzled"], self.qw2["col_data"].view(E, H, F),
-                               self.qw2["col_scale"], self.ms, out=self.dh)
+        mxq.grouped_gemm_dgrad(dy2_row, dy2_rs, self.qw2["col_data"].view(E, H, F), self.qw2["col_scale"], self.ms,
+                               out=self.dh)
         rec(6)
-        mxq.grouped_gemm_wgrad(self.rqd["col_data"], self.rqd["col_scale"], self.qh["col_data"], self.qh["col_scale"],
+        mxq.grouped_gemm_wgrad(self.qd["col_data"], self.qd["col_scale"], self.qh["col_data"], self.qh["col_scale"],
                                self.ms, out=self.dw2)
         rec(7)
-        mxq.swiglu_bwd_quantize(self.dh, self.y1, self.ms, dbias=True, out=self.qdy1, workspace=self.ws)
+        mxq.swiglu_bwd_quantize(self.dh, self.y1, self.ms, dbias=self.has_bias, out=self.qdy1, workspace=self.ws)
         rec(8)
         mxq.grouped_gemm_dgrad(self.qdy1["row_data"], self.qdy1["row_scale"], self.qw1["col_data"].view(E, 2 * F, H),
                                self.qw1["col_scale"], self.ms, out=self.dx)
         rec(9)
-        mxq.grouped_gemm_wgrad(self.qdy1["col_data"], self.qdy1["col_scale"], self.rqx["col_data"],
-                               self.rqx["col_scale"], self.ms, out=self.dw1)
+        mxq.grouped_gemm_wgrad(self.qdy1["col_data"], self.qdy1["col_scale"], self.qx["col_data"],
+                               self.qx["col_scale"], self.ms, out=self.dw1)
         rec(10)
 
     def flush(self):
         self.flush_buf.fill_(1)
 
 
-def time_mlp(dev, steps=10, warmup=3):
+def time_mlp(dev, steps=10, warmup=3, workload=MLP_WORKLOAD):
     import torch
 
-    st = MLPStep(dev)
+    st = MLPStep(dev, workload)
     for _ in range(warmup):
         st.flush()
         st.run()
     torch.cuda.synchronize()
-    n = len(MLP_STAGES) + 1
+    n = len(st.stages) + 1
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(steps)]
     for i in range(steps):
         st.flush()
@@ -304,15 +336,18 @@ def time_mlp(dev, steps=10, warmup=3):
     torch.cuda.synchronize()
     ms = statistics.mean(evs[i][0].elapsed_time(evs[i][n - 1]) for i in range(steps))
     per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
-           for j, k in enumerate(MLP_STAGES)}
+           for j, k in enumerate(st.stages)}
     gemm_ms = sum(v for k, v in per.items() if "prop" in k or "grad" in k)
-
-    return {"workload": MLP_WORKLOAD, "steps": steps, "warmup": warmup, "ms_per_step": ms,
+    bias = " (bias)" if st.has_bias else ""
+    arrive = ("X and dY2 rowwise-prequantized" if st.pre_x and st.pre_dy else
+              "X and dY2 in bf16, quantized rowwise+colwise inside the step")
+    return {"workload": workload, "steps": steps, "warmup": warmup, "ms_per_step": ms,
             "tflops_step": st.flops() / (ms * 1e-3) / 1e12, "gemm_tflops": st.flops() / (gemm_ms * 1e-3) / 1e12,
             "stage_ms": per, "gpu_launches": st.launches_per_step * steps,
-            "step": "fwd+bwd of FC1 (bias) -> SwiGLU -> FC2 (bias), X and dY2 rowwise-prequantized; SwiGLU and "
-                    "the quantization of h in FC1's GEMM epilogue (forward); SwiGLU backward fused with the "
-                    "quantization of dY1 and its dbias (backward)",
+            "step": f"fwd+bwd of FC1{bias} -> SwiGLU -> FC2{bias}, {arrive}; SwiGLU and the quantization of h in "
+                    "FC1's GEMM epilogue (forward); SwiGLU backward fused with the quantization of dY1"
+                    + (" and its dbias" if st.has_bias else "") + " (backward)",
+            "l2": "a 256 MiB buffer written before every step",
             "gemm_note": "gemm_tflops counts the FC1 stage whole (its epilogue also runs SwiGLU and quantizes h)"}
 
 
@@ -956,6 +991,11 @@ def main():
         r = {"metric": "block-scaled MXFP8 tcgen05 MMA stream (128x256x32, one CTA per SM, resident operands)",
              "tflops": t, "unit": "TFLOP/s", "roofline_peak": bf16_peak * MXFP8_OVER_BF16,
              "ratio_to_roofline_peak": t / (bf16_peak * MXFP8_OVER_BF16), "peak_source": src}
+        if rank == 0:
+            print(json.dumps(r), flush=True)
+        return
+    if args.only == "mlp_e32":
+        r = time_mlp(dev, max(1, args.steps), max(1, args.warmup), MLP_WORKLOAD_E32)
         if rank == 0:
             print(json.dumps(r), flush=True)
         return
