@@ -137,7 +137,15 @@ def make_host_workload():
 
 
 class NativeStep:
-    """Device-resident inputs/outputs of one step and the calls that run it."""
+    """Device-resident inputs/outputs of one step and the calls that run it.
+
+    In the order of a training step: the forward's two quantizations, fprop,
+    then the backward's (quantize dY) and dgrad, wgrad. The forward's two are
+    independent, so by default they run concurrently: requant X on a side
+    stream forked from the caller's stream, quantize W on it, joined before
+    fprop. Requant is bound by its arithmetic and quantize W by HBM, and each
+    kernel's last partial wave of CTAs leaves SMs idle that the other fills.
+    The outputs are bit-identical to the serial order."""
 
     def __init__(self, w, d, dev):
         import torch
@@ -167,27 +175,52 @@ class NativeStep:
         self.dw = torch.empty((E, N, K), dtype=torch.float32, device=dev)
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         self.launches_per_step = 6
+        self.s_rq = torch.cuda.Stream(device=dev)
+        self.ev_fork, self.ev_rq = torch.cuda.Event(), torch.cuda.Event()
 
-    def run(self, events=None):
-        mxq, w = self.mxq, self.w
+    def run(self, events=None, concurrent=True):
+        """One step on the current stream. events: STEP_EVENTS timing events, recorded on the stream
+        that runs each kernel (see KERNEL_EVENTS)."""
+        torch, mxq, w = self.torch, self.mxq, self.w
         E, N, K = w.E, w.N, w.K
-        rec = (lambda i: events[i].record()) if events else (lambda i: None)
+        main = torch.cuda.current_stream()
+        rec = (lambda i, st=None: events[i].record(st or main)) if events else (lambda i, st=None: None)
+
+        def requant():
+            mxq.requant_colwise(self.x_row, self.x_row_scale, self.ms, out=self.rq)
+
         rec(0)
-        mxq.requant_colwise(self.x_row, self.x_row_scale, self.ms, out=self.rq)
-        rec(1)
-        mxq.group_quantize(self.wt, None, E=E, out=self.qw)
-        rec(2)
-        mxq.group_quantize(self.dy, self.ms, out=self.qdy)
-        rec(3)
+        if concurrent:
+            self.ev_fork.record(main)
+            self.s_rq.wait_event(self.ev_fork)
+            with torch.cuda.stream(self.s_rq):
+                rec(1, self.s_rq)
+                requant()
+                rec(2, self.s_rq)
+            self.ev_rq.record(self.s_rq)
+            rec(3)
+            mxq.group_quantize(self.wt, None, E=E, out=self.qw)
+            rec(4)
+            main.wait_event(self.ev_rq)
+        else:
+            rec(1)
+            requant()
+            rec(2)
+            rec(3)
+            mxq.group_quantize(self.wt, None, E=E, out=self.qw)
+            rec(4)
+        rec(5)
         mxq.grouped_gemm_fprop(self.x_row, self.rq["row_scale_swizzled"], self.qw["row_data"].view(E, N, K),
                                self.qw["row_scale"], self.ms, out=self.y)
-        rec(4)
+        rec(6)
+        mxq.group_quantize(self.dy, self.ms, out=self.qdy)
+        rec(7)
         mxq.grouped_gemm_dgrad(self.qdy["row_data"], self.qdy["row_scale"], self.qw["col_data"].view(E, N, K),
                                self.qw["col_scale"], self.ms, out=self.dx)
-        rec(5)
+        rec(8)
         mxq.grouped_gemm_wgrad(self.qdy["col_data"], self.qdy["col_scale"], self.rq["col_data"],
                                self.rq["col_scale"], self.ms, out=self.dw)
-        rec(6)
+        rec(9)
 
     def flush(self):
         self.flush_buf.fill_(1)
@@ -202,7 +235,9 @@ class MLPStep:
     and the FC2 gradient arrive rowwise-quantized (the expert-parallel dispatch and the combine's
     backward) and both linears carry per-expert biases; on the 32-expert workload X and the FC2
     gradient arrive in bf16 and there are no biases. Covers every step of the path: requant or
-    quantize (+fused dbias), weight quantize, the three grouped GEMMs of both linears, SwiGLU."""
+    quantize (+fused dbias), weight quantize, the three grouped GEMMs of both linears, SwiGLU.
+    The forward's input quantizations run concurrently (X on a side stream, W1 and W2 on the
+    caller's stream) and join before FC1; the rest runs in order on the caller's stream."""
 
     def __init__(self, dev, workload=MLP_WORKLOAD, seed=0):
         import torch
@@ -265,34 +300,48 @@ class MLPStep:
         self.dw2 = torch.empty((E, H, F), dtype=torch.float32, device=dev)
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         self.launches_per_step = 11 + (1 if w.bias else 0) * 2
+        self.s_x = torch.cuda.Stream(device=dev)
+        self.ev_fork, self.ev_x = torch.cuda.Event(), torch.cuda.Event()
         b = "_dbias" if w.bias else ""
-        self.stages = [("requant_x" if self.pre_x else "quantize_x"), "quantize_w1_w2", "fc1_fprop_swiglu_quantize_h",
-                       "fc2_fprop", ("requant_dy2" if self.pre_dy else "quantize_dy2") + b, "fc2_dgrad", "fc2_wgrad",
-                       "swiglu_bwd_quantize_dy1" + b, "fc1_dgrad", "fc1_wgrad"]
+        # stage name -> (start, end) timing events of run(); event 5 is the forward quantize phase's join
+        names = [("requant_x" if self.pre_x else "quantize_x"), "quantize_w1_w2", "fc1_fprop_swiglu_quantize_h",
+                 "fc2_fprop", ("requant_dy2" if self.pre_dy else "quantize_dy2") + b, "fc2_dgrad", "fc2_wgrad",
+                 "swiglu_bwd_quantize_dy1" + b, "fc1_dgrad", "fc1_wgrad"]
+        self.stages = dict(zip(names, [(1, 2), (3, 4)] + [(k, k + 1) for k in range(5, 13)]))
+        self.n_events = 14
 
     def flops(self):
         return 6.0 * self.M * (2 * self.F * self.H + self.H * self.F)
 
     def run(self, ev=None):
-        mxq, E, H, F = self.mxq, self.E, self.H, self.F
-        rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
+        torch, mxq, E, H, F = self.torch, self.mxq, self.E, self.H, self.F
+        main = torch.cuda.current_stream()
+        rec = (lambda i, st=None: ev[i].record(st or main)) if ev else (lambda i, st=None: None)
         rec(0)
-        if self.pre_x:
-            mxq.requant_colwise(self.x_row, self.x_rs, self.ms, out=self.qx)
-            x_row, x_rs = self.x_row, self.qx["row_scale_swizzled"]
-        else:
-            mxq.group_quantize(self.x_bf16, self.ms, out=self.qx)
-            x_row, x_rs = self.qx["row_data"], self.qx["row_scale"]
-        rec(1)
+        self.ev_fork.record(main)
+        self.s_x.wait_event(self.ev_fork)
+        with torch.cuda.stream(self.s_x):
+            rec(1, self.s_x)
+            if self.pre_x:
+                mxq.requant_colwise(self.x_row, self.x_rs, self.ms, out=self.qx)
+                x_row, x_rs = self.x_row, self.qx["row_scale_swizzled"]
+            else:
+                mxq.group_quantize(self.x_bf16, self.ms, out=self.qx)
+                x_row, x_rs = self.qx["row_data"], self.qx["row_scale"]
+            rec(2, self.s_x)
+        self.ev_x.record(self.s_x)
+        rec(3)
         mxq.group_quantize(self.w1, None, E=E, out=self.qw1)
         mxq.group_quantize(self.w2, None, E=E, out=self.qw2)
-        rec(2)
+        rec(4)
+        main.wait_event(self.ev_x)
+        rec(5)
         mxq.grouped_gemm_fprop_swiglu(x_row, x_rs, self.qw1["row_data"].view(E, 2 * F, H), self.qw1["row_scale"],
                                       self.ms, bias=self.b1, out=self.fc1_out)
-        rec(3)
+        rec(6)
         mxq.grouped_gemm_fprop(self.qh["row_data"], self.qh["row_scale"], self.qw2["row_data"].view(E, H, F),
                                self.qw2["row_scale"], self.ms, bias=self.b2, out=self.y2)
-        rec(4)
+        rec(7)
         if self.pre_dy:
             mxq.requant_colwise(self.dy2_row, self.dy2_rs, self.ms, dbias=self.has_bias, out=self.qd,
                                 workspace=self.ws)
@@ -300,21 +349,21 @@ class MLPStep:
         else:
             mxq.group_quantize(self.dy2_bf16, self.ms, dbias=self.has_bias, out=self.qd, workspace=self.ws)
             dy2_row, dy2_rs = self.qd["row_data"], self.qd["row_scale"]
-        rec(5)
+        rec(8)
         mxq.grouped_gemm_dgrad(dy2_row, dy2_rs, self.qw2["col_data"].view(E, H, F), self.qw2["col_scale"], self.ms,
                                out=self.dh)
-        rec(6)
+        rec(9)
         mxq.grouped_gemm_wgrad(self.qd["col_data"], self.qd["col_scale"], self.qh["col_data"], self.qh["col_scale"],
                                self.ms, out=self.dw2)
-        rec(7)
+        rec(10)
         mxq.swiglu_bwd_quantize(self.dh, self.y1, self.ms, dbias=self.has_bias, out=self.qdy1, workspace=self.ws)
-        rec(8)
+        rec(11)
         mxq.grouped_gemm_dgrad(self.qdy1["row_data"], self.qdy1["row_scale"], self.qw1["col_data"].view(E, 2 * F, H),
                                self.qw1["col_scale"], self.ms, out=self.dx)
-        rec(9)
+        rec(12)
         mxq.grouped_gemm_wgrad(self.qdy1["col_data"], self.qdy1["col_scale"], self.qx["col_data"],
                                self.qx["col_scale"], self.ms, out=self.dw1)
-        rec(10)
+        rec(13)
 
     def flush(self):
         self.flush_buf.fill_(1)
@@ -328,26 +377,29 @@ def time_mlp(dev, steps=10, warmup=3, workload=MLP_WORKLOAD):
         st.flush()
         st.run()
     torch.cuda.synchronize()
-    n = len(st.stages) + 1
+    n = st.n_events
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(steps)]
     for i in range(steps):
         st.flush()
         st.run(evs[i])
     torch.cuda.synchronize()
     ms = statistics.mean(evs[i][0].elapsed_time(evs[i][n - 1]) for i in range(steps))
-    per = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
-           for j, k in enumerate(st.stages)}
+    per = {k: statistics.mean(evs[i][a].elapsed_time(evs[i][b]) for i in range(steps))
+           for k, (a, b) in st.stages.items()}
+    fwd_quant_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][5]) for i in range(steps))
     gemm_ms = sum(v for k, v in per.items() if "prop" in k or "grad" in k)
     bias = " (bias)" if st.has_bias else ""
     arrive = ("X and dY2 rowwise-prequantized" if st.pre_x and st.pre_dy else
               "X and dY2 in bf16, quantized rowwise+colwise inside the step")
     return {"workload": workload, "steps": steps, "warmup": warmup, "ms_per_step": ms,
             "tflops_step": st.flops() / (ms * 1e-3) / 1e12, "gemm_tflops": st.flops() / (gemm_ms * 1e-3) / 1e12,
-            "stage_ms": per, "gpu_launches": st.launches_per_step * steps,
+            "stage_ms": per, "fwd_quantize_phase_ms": fwd_quant_ms, "gpu_launches": st.launches_per_step * steps,
             "step": f"fwd+bwd of FC1{bias} -> SwiGLU -> FC2{bias}, {arrive}; SwiGLU and the quantization of h in "
                     "FC1's GEMM epilogue (forward); SwiGLU backward fused with the quantization of dY1"
                     + (" and its dbias" if st.has_bias else "") + " (backward)",
             "l2": "a 256 MiB buffer written before every step",
+            "streams": "the quantization of X on a side stream concurrent with that of W1 and W2 (stage_ms of the "
+                       "two overlap); the rest in order after the join",
             "gemm_note": "gemm_tflops counts the FC1 stage whole (its epilogue also runs SwiGLU and quantizes h)"}
 
 
@@ -666,6 +718,20 @@ def time_configs(dev, steps, warmup):
 
 
 KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
+# NativeStep.run's timing events: 0 step start, (1, 2) requant X, (3, 4) quantize W, 5 forward quantize
+# phase joined = fprop start, 6 fprop end, 7 quantize dY end, 8 dgrad end, 9 wgrad end (= step end)
+STEP_EVENTS = 10
+KERNEL_EVENTS = {"requant_x": (1, 2), "quantize_w": (3, 4), "fprop": (5, 6), "quantize_dy": (6, 7),
+                 "dgrad": (7, 8), "wgrad": (8, 9)}
+
+
+def step_event_times(evs):
+    """Mean ms per kernel, of the forward quantize phase (requant X with quantize W) and of the step, over
+    a list of STEP_EVENTS-event steps."""
+    per = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in evs) for k, (a, b) in KERNEL_EVENTS.items()}
+    per_step = [e[0].elapsed_time(e[STEP_EVENTS - 1]) for e in evs]
+    phase = statistics.mean(e[0].elapsed_time(e[5]) for e in evs)
+    return per, per_step, phase
 
 
 def algorithmic(w):
@@ -716,16 +782,33 @@ def gemm_bound_us(m_splits, N, K, mx_peak_tflops, hbm_gbs):
 
 def time_warm(st, steps):
     """Per-kernel times of the step with no L2 flush between steps (inputs
-    that fit in the 129 MB L2 may then be served from it)."""
+    that fit in the 129 MB L2 may then be served from it); kernels in order
+    on one stream."""
     torch = st.torch
     for _ in range(3):
-        st.run()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+        st.run(concurrent=False)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(steps)]
     for i in range(steps):
-        st.run(evs[i])
+        st.run(evs[i], concurrent=False)
     torch.cuda.synchronize()
-    return {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
-            for j, k in enumerate(KERNELS)}
+    return step_event_times(evs)[0]
+
+
+def time_serial(st, steps):
+    """The step with its kernels in order on one stream, L2 flushed before
+    each step: every kernel timed alone (the quantize kernels' own HBM
+    rates) and the serial step time."""
+    torch = st.torch
+    for _ in range(3):
+        st.flush()
+        st.run(concurrent=False)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(steps)]
+    for i in range(steps):
+        st.flush()
+        st.run(evs[i], concurrent=False)
+    torch.cuda.synchronize()
+    per, per_step, _ = step_event_times(evs)
+    return per, statistics.mean(per_step)
 
 
 def time_native(st, steps, warmup, sampler):
@@ -734,7 +817,7 @@ def time_native(st, steps, warmup, sampler):
         st.flush()
         st.run()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(steps)]
     if sampler:
         sampler.start()
         time.sleep(0.3)
@@ -748,10 +831,8 @@ def time_native(st, steps, warmup, sampler):
     wall = time.perf_counter() - t0
     barrier()
     clocks = sampler.stop() if sampler else None
-    per_step = [evs[i][0].elapsed_time(evs[i][6]) for i in range(steps)]
-    per_kernel = {k: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
-                  for j, k in enumerate(KERNELS)}
-    return per_step, per_kernel, wall, clocks
+    per_kernel, per_step, phase = step_event_times(evs)
+    return per_step, per_kernel, phase, wall, clocks
 
 
 def time_e2e(st, steps, warmup, d):
@@ -1018,14 +1099,16 @@ def main():
     step_flops = sum(flops.values())
 
     sampler = ClockSampler(local if world > 1 else 0) if rank == 0 else None
-    per_step, per_kernel, wall, clocks = time_native(st, args.steps, max(3, args.warmup), sampler)
+    per_step, per_kernel, phase_ms, wall, clocks = time_native(st, args.steps, max(3, args.warmup), sampler)
     ms_step = statistics.mean(per_step)
     ms_step_max = max_over_ranks(ms_step)
     value = aggregate(step_flops, world, ms_step_max * 1e-3) / 1e12
 
     gemm_ms = per_kernel["fprop"] + per_kernel["dgrad"] + per_kernel["wgrad"]
     gemm_tflops = step_flops / (gemm_ms * 1e-3) / 1e12
-    quant_gbs = {k: bytes_[k] / (per_kernel[k] * 1e-3) / 1e9 for k in bytes_}
+    serial_kernels, serial_ms = time_serial(st, max(10, args.steps // 2))
+    quant_gbs = {k: bytes_[k] / (serial_kernels[k] * 1e-3) / 1e9 for k in bytes_}
+    phase_gbs = (bytes_["requant_x"] + bytes_["quantize_w"]) / (phase_ms * 1e-3) / 1e9
     warm = time_warm(st, max(5, args.steps // 5))
 
     e2e = None
@@ -1094,14 +1177,22 @@ def main():
         "vs_baseline": None, "dtype": "mxfp8_e4m3 (fp32 accumulate)", "data": "synthetic",
         "config": {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
                    "m_splits": [int(v) for v in d["m_splits"]],
-                   "step": "requant X + quantize W (row+col) + quantize dY (row+col) + fprop + dgrad + wgrad (fp32 dW)",
+                   "step": "requant X + quantize W (row+col), fprop, quantize dY (row+col), dgrad, wgrad (fp32 dW)",
+                   "streams": "requant X on a side stream concurrent with quantize W; the rest in order after the "
+                              "join",
                    "l2": "256 MiB buffer written before every timed step (outside the event brackets)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * args.steps,
         "clocks": clocks,
         "kernels_ms": per_kernel, "gemm_tflops": gemm_tflops,
+        "fwd_quantize_phase_ms": phase_ms, "fwd_quantize_phase_gbs": phase_gbs,
+        "fwd_quantize_phase_frac": phase_gbs / hbm_peak,
+        "kernels_ms_serial": serial_kernels, "ms_per_step_serial": serial_ms,
         "group_quantize_gbs": quant_gbs, "hbm_peak_gbs": hbm_peak,
         "group_quantize_frac": {k: v / hbm_peak for k, v in quant_gbs.items()},
+        "group_quantize_note": "each quantize kernel timed alone (serial pass, L2 flushed before each step); in "
+                               "the timed step requant X and quantize W overlap, and kernels_ms holds their "
+                               "concurrent durations",
         "kernels_ms_no_l2_flush": warm,
         "wall_s_timed_region": wall,
         "mlp_step": mlp,

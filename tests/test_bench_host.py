@@ -24,3 +24,23 @@ def test_small_and_empty_experts_are_bound_by_their_bytes():
     wgrad = N * K * 4 / (bw * 1e9) * 1e6 + (128 * N * q + 128 * K * q + N * K * 4) / (bw * 1e9) * 1e6
     assert b["wgrad"] == pytest.approx(wgrad, rel=1e-12)
     assert b["dgrad"] == pytest.approx((128 * N * q + N * K * q + 128 * K * 2) / (bw * 1e9) * 1e6, rel=1e-12)
+
+
+class _FakeEvent:
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_step_event_layout():
+    # one step: requant X 0.1-0.3 on the side stream and quantize W 0.0-0.5 on the main stream, joined at
+    # 0.6, then fprop / quantize dY / dgrad / wgrad ending at 1.0 / 1.3 / 1.8 / 2.4
+    t = [0.0, 0.1, 0.3, 0.0, 0.5, 0.6, 1.0, 1.3, 1.8, 2.4]
+    assert len(t) == bench.STEP_EVENTS
+    per, per_step, phase = bench.step_event_times([[_FakeEvent(v) for v in t]])
+    assert per == pytest.approx({"requant_x": 0.2, "quantize_w": 0.5, "fprop": 0.4, "quantize_dy": 0.3,
+                                 "dgrad": 0.5, "wgrad": 0.6})
+    assert per_step == pytest.approx([2.4]) and phase == pytest.approx(0.6)
+    assert set(per) == set(bench.KERNELS)
