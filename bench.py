@@ -136,6 +136,14 @@ def make_host_workload():
     return w, d
 
 
+def workload_config(w, d, world):
+    """The workload both arms run, as named in their JSON lines."""
+    return {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
+            "m_splits": [int(v) for v in d["m_splits"]],
+            "step": "requant X + quantize W (row+col), fprop, quantize dY (row+col), dgrad, wgrad (fp32 dW)",
+            "parallelism": f"replicas x{world}"}
+
+
 class NativeStep:
     """Device-resident inputs/outputs of one step and the calls that run it.
 
@@ -1021,7 +1029,7 @@ def reference_arm(args, rank, world):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M},
+            "config": workload_config(w, d, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
                              "sample": sample.sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -1175,13 +1183,10 @@ def main():
         "warmup": max(3, args.warmup), "ms_per_step": ms_step_max, "ms_per_step_median": statistics.median(per_step),
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8_e4m3 (fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
-                   "m_splits": [int(v) for v in d["m_splits"]],
-                   "step": "requant X + quantize W (row+col), fprop, quantize dY (row+col), dgrad, wgrad (fp32 dW)",
+        "config": {**workload_config(w, d, world),
                    "streams": "requant X on a side stream concurrent with quantize W; the rest in order after the "
                               "join",
-                   "l2": "256 MiB buffer written before every timed step (outside the event brackets)",
-                   "parallelism": f"replicas x{world}"},
+                   "l2": "256 MiB buffer written before every timed step (outside the event brackets)"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * args.steps,
         "clocks": clocks,
         "kernels_ms": per_kernel, "gemm_tflops": gemm_tflops,
