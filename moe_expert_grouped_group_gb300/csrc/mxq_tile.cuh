@@ -35,6 +35,30 @@ struct TileArgs {
     int32_t* status;
 };
 
+// Packed half-precision steps of the requant fast path (each f16 lane rounds
+// to nearest even, subnormals kept).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)v16));
+    return h;
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t f16x2_max(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// Two f16 (low, high lane) -> two E4M3 bytes (low, high), RNE, saturating finite.
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return (uint32_t)r;
+}
+
 // Byte-wise max of 4 packed 8-bit exponents across the 8 lanes of a group.
 __device__ __forceinline__ uint32_t group8_max_u8x4(uint32_t v) {
 #pragma unroll
@@ -226,6 +250,19 @@ __global__ void __launch_bounds__(kTileThreads)
             if (!kPad || lane < vb)
                 sw = __ldg(reinterpret_cast<const unsigned int*>(a.src_scale + (r0 + lane) * (K / 32) + kt * 4));
         }
+        // requant: the largest and smallest rowwise scale code of this lane's 32-column block over the
+        // warp's 32 rows (the fast paths below need their spread)
+        [[maybe_unused]] uint32_t R = 0, Rmin = 0;
+        if constexpr (kReq) {
+            uint32_t mx = sw, mn = sw;
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                mx = __vmaxu4(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                mn = __vminu4(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            }
+            R = __byte_perm(mx, 0u, sel_blk);
+            Rmin = __byte_perm(mn, 0u, sel_blk);
+        }
         // scaled bias: lane l reads s of row r0 + l and b_e of its 4 columns
         float pw = 0.f, bv[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (kScaled) {
@@ -275,6 +312,15 @@ __global__ void __launch_bounds__(kTileThreads)
         // expert) skips the rows past the expert. Whole warps choose one form.
         auto passes = [&](auto mask_t) {
             [[maybe_unused]] constexpr bool kMask = decltype(mask_t)::value;
+            // Requant fast path, pass 1 (whole warps of 32 rows inside the expert): when every row scale
+            // code of the block is within 5 of the largest, R, |val| 2^(rs - R) is an exact normal f16 for
+            // every nonzero E4M3 val (|val| >= 2^-9), so the colwise maxima can be taken in f16x2.
+            [[maybe_unused]] constexpr bool kFast1 = kReq && kCol && !kBias && !kScaled && !kMask;
+            [[maybe_unused]] constexpr bool kFast2 = kReq && kCol && !kDeq && !kMask;
+            [[maybe_unused]] bool fast1 = false;
+            if constexpr (kFast1) fast1 = __all_sync(0xffffffffu, R - Rmin <= 5u);
+            [[maybe_unused]] uint32_t m16[2] = {0u, 0u};  // fast pass 1: f16x2 maxima of |val| 2^(rs - R)
+            [[maybe_unused]] uint32_t nz = 0u;            // requant: bit j set when column j holds a nonzero
             if constexpr (kCol || kBias) {
                 [[maybe_unused]] uint32_t m[4] = {0, 0, 0, 0};  // packed bf16 |x| bits (bf16 input, no dbias)
                 [[maybe_unused]] float mf[4] = {0.f, 0.f, 0.f, 0.f};  // |v| maxima (every other case)
@@ -299,6 +345,15 @@ __global__ void __launch_bounds__(kTileThreads)
                     }
                     const float dsum = transpose_reduce32(dp, lane);
                     if (!kMask || lane < vb) a.dp_partials[(r0 + lane) * tilesK + kt] = dsum;
+                } else if (kFast1 && fast1) {
+    #pragma unroll 8
+                    for (int r = 0; r < 32; ++r) {
+                        const uint32_t u = ld_row(r).x;
+                        const uint32_t code = __byte_perm(__shfl_sync(0xffffffffu, sw, r), 0u, sel_blk);
+                        const uint32_t s2 = (code + 15u - R) * 0x04000400u;  // 2^(code - R) in both f16 lanes
+                        m16[0] = f16x2_max(m16[0], f16x2_mul(e4m3x2_to_f16x2(u & 0xFFFFu), s2) & 0x7FFF7FFFu);
+                        m16[1] = f16x2_max(m16[1], f16x2_mul(e4m3x2_to_f16x2(u >> 16), s2) & 0x7FFF7FFFu);
+                    }
                 } else {
     #pragma unroll 8
                     for (int r = 0; r < 32; ++r) {
@@ -331,7 +386,16 @@ __global__ void __launch_bounds__(kTileThreads)
                     }
     #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        ccode[j] = (uint32_t)max((int)e[j] - 8, 0);
+                        if (kFast1 && fast1) {
+                            // the column's largest |value| is m16_j 2^(R - 127), whose floor(log2) is
+                            // (ef_j - 15) + (R - 127) for the f16 exponent field ef_j
+                            const uint32_t hb = (m16[j >> 1] >> (16 * (j & 1))) & 0x7FFFu;
+                            ccode[j] = hb ? (uint32_t)max((int)((hb >> 10) + R) - 23, 0) : 0u;
+                            nz |= (uint32_t)(hb != 0u) << j;
+                        } else {
+                            ccode[j] = (uint32_t)max((int)e[j] - 8, 0);
+                            if constexpr (kReq) nz |= (uint32_t)(mf[j] > 0.f) << j;
+                        }
                         cinv[j] = inv_scale_from_code(ccode[j]);
                     }
                     if (a.swizzle) {
@@ -347,6 +411,34 @@ __global__ void __launch_bounds__(kTileThreads)
             if constexpr (kReq && kRow) *reinterpret_cast<uint32_t*>(&s_rs[lane * 16 + rg * 4]) = sw;
 
             // ------------------------------------------------- pass 2: encode
+            if constexpr (kFast2) {
+                // Requant fast path, pass 2: when every rs_r - cs_j lies in [-14, 15] (an all-zero column's
+                // scale taken as R), 2^(rs_r - cs_j) is a normal f16 and val 2^(rs_r - cs_j) is exact in f16
+                // wherever it is at least 2^-14; below that it and the exact value both encode to a signed
+                // zero. One f16x2 product per pair of values then gives the codes of the fp32 steps.
+                uint32_t csm[4];
+                bool ok = true;
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    csm[j] = ((nz >> j) & 1u) ? ccode[j] : R;
+                    ok = ok && (R <= csm[j] + 15u) && (Rmin + 14u >= csm[j]);
+                }
+                if (__all_sync(0xffffffffu, ok)) {
+                    // f16 bits of 2^(rs - cs) for two columns: rs * 0x04000400 plus these, mod 2^32
+                    const uint32_t k01 = (15u - csm[0]) * 1024u + (15u - csm[1]) * 67108864u;
+                    const uint32_t k23 = (15u - csm[2]) * 1024u + (15u - csm[3]) * 67108864u;
+                    uint8_t* cq = a.col_q + r0 * K + col;
+    #pragma unroll 8
+                    for (int r = 0; r < 32; ++r) {
+                        const uint32_t u = ld_row(r).x;
+                        const uint32_t rs2 = __byte_perm(__shfl_sync(0xffffffffu, sw, r), 0u, sel_blk) * 0x04000400u;
+                        const uint32_t lo = f16x2_to_e4m3x2(f16x2_mul(e4m3x2_to_f16x2(u & 0xFFFFu), rs2 + k01));
+                        const uint32_t hi = f16x2_to_e4m3x2(f16x2_mul(e4m3x2_to_f16x2(u >> 16), rs2 + k23));
+                        *reinterpret_cast<uint32_t*>(cq + r * Ku) = lo | (hi << 16);
+                    }
+                    return;
+                }
+            }
             if constexpr ((kRow && !kReq) || kCol || kDeq) {
                 [[maybe_unused]] uint8_t* rq = kRow && !kReq ? a.row_q + r0 * K + col : nullptr;
                 [[maybe_unused]] uint8_t* cq = kCol ? a.col_q + r0 * K + col : nullptr;
