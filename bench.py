@@ -321,28 +321,32 @@ class MLPStep:
     def flops(self):
         return 6.0 * self.M * (2 * self.F * self.H + self.H * self.F)
 
-    def run(self, ev=None):
+    def run(self, ev=None, concurrent=True):
         torch, mxq, E, H, F = self.torch, self.mxq, self.E, self.H, self.F
         main = torch.cuda.current_stream()
         rec = (lambda i, st=None: ev[i].record(st or main)) if ev else (lambda i, st=None: None)
+        side = self.s_x if concurrent else main
         rec(0)
-        self.ev_fork.record(main)
-        self.s_x.wait_event(self.ev_fork)
-        with torch.cuda.stream(self.s_x):
-            rec(1, self.s_x)
+        if concurrent:
+            self.ev_fork.record(main)
+            side.wait_event(self.ev_fork)
+        with torch.cuda.stream(side):
+            rec(1, side)
             if self.pre_x:
                 mxq.requant_colwise(self.x_row, self.x_rs, self.ms, out=self.qx)
                 x_row, x_rs = self.x_row, self.qx["row_scale_swizzled"]
             else:
                 mxq.group_quantize(self.x_bf16, self.ms, out=self.qx)
                 x_row, x_rs = self.qx["row_data"], self.qx["row_scale"]
-            rec(2, self.s_x)
-        self.ev_x.record(self.s_x)
+            rec(2, side)
+        if concurrent:
+            self.ev_x.record(side)
         rec(3)
         mxq.group_quantize(self.w1, None, E=E, out=self.qw1)
         mxq.group_quantize(self.w2, None, E=E, out=self.qw2)
         rec(4)
-        main.wait_event(self.ev_x)
+        if concurrent:
+            main.wait_event(self.ev_x)
         rec(5)
         mxq.grouped_gemm_fprop_swiglu(x_row, x_rs, self.qw1["row_data"].view(E, 2 * F, H), self.qw1["row_scale"],
                                       self.ms, bias=self.b1, out=self.fc1_out)
