@@ -6,16 +6,17 @@ quantized as an expert-parallel FP8 dispatch delivers it). One step is the
 whole hot path over one batch:
 
     requant X (rowwise wire format -> colwise copy + swizzled rowwise scales)
-    group_quantize W (rowwise + colwise, uniform members)
-    group_quantize dY (rowwise + colwise)
+      | group_quantize W (rowwise + colwise, uniform members)   [two streams]
     grouped fprop  Y  = X W_e^T
+    group_quantize dY (rowwise + colwise)
     grouped dgrad  dX = dY W_e
     grouped wgrad  dW = dY_e^T X_e (fp32)
 
 value = GEMM flops of the step (6*M*N*K) / step time (whole step), in
 TFLOP/s. L2 is flushed (256 MiB write) before every timed step; the flush is
 outside the per-step CUDA-event brackets. Per-kernel times come from events
-on the launching stream. `--impl reference` times the CPU oracle instead.
+on the stream that runs each kernel; a serial pass of the same step times
+each quantize kernel alone. `--impl reference` times the CPU oracle instead.
 
 Multi-GPU (torchrun): every rank runs an independent replica of the
 workload (the grouped path has no exchange step of its own); rank 0 prints
