@@ -13,7 +13,8 @@
 // Persistent CTAs of 8 compute warps + 1 TMA producer warp, 128x128 output
 // tiles. A stage holds the 128x128 input tiles a tile needs (g and u; plus
 // dh backward). Warp w turns rows 16w..16w+15 into bf16 h (or dg and du),
-// written back in place -- fp32 steps of mxq_common.cuh, one bf16 rounding
+// written back in place -- the fp32 steps of mxq_common.cuh, two values per
+// packed instruction (bit-identical), one bf16 rounding
 // -- gathering each column's exponent maximum (and dbias sum) in registers
 // on the way. After one exchange of those 16-row statistics through shared
 // memory (a 32-row colwise block is two warps), every warp encodes its own
@@ -28,6 +29,96 @@
 
 namespace mxq {
 namespace swq {
+
+// The fp32 SwiGLU steps of mxq_common.cuh on two values at once. Each packed
+// instruction (add / sub / mul / fma .rn.f32x2) rounds each lane to nearest
+// even without flushing subnormals, exactly as the scalar instruction of the
+// same step does, so every result is bit-identical to swiglu_h / swiglu_grads.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t v) {
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(v));
+    return o;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2splat(float a) { return f2pack(a, a); }
+
+// exp_core_f32 on two lanes (the same steps; (-n) * c is computed as n * (-c), the same product)
+__device__ __forceinline__ uint64_t exp_core_x2(uint64_t x) {
+    const uint64_t magic = f2splat(0x1.8p23f);
+    const uint64_t j = f2fma(x, f2splat(1.44269504f), magic);
+    const uint64_t n = f2sub(j, magic);
+    uint64_t r = f2fma(n, f2splat(-0.693359375f), x);
+    r = f2fma(n, f2splat(2.12194440e-4f), r);
+    uint64_t p = f2fma(f2splat(0x1.a01a02p-13f), r, f2splat(0x1.6c16c2p-10f));
+    p = f2fma(p, r, f2splat(0x1.111112p-7f));
+    p = f2fma(p, r, f2splat(0x1.555556p-5f));
+    p = f2fma(p, r, f2splat(0x1.555556p-3f));
+    p = f2fma(p, r, f2splat(0.5f));
+    p = f2fma(p, r, f2splat(1.0f));
+    p = f2fma(p, r, f2splat(1.0f));
+    const float2 pf = f2unpack(p), jf = f2unpack(j);
+    return f2pack(__uint_as_float(__float_as_uint(pf.x) + (__float_as_uint(jf.x) << 23)),
+                  __uint_as_float(__float_as_uint(pf.y) + (__float_as_uint(jf.y) << 23)));
+}
+// recip_f32_steps on two lanes
+__device__ __forceinline__ uint64_t recip_x2(uint64_t d) {
+    const float2 df = f2unpack(d);
+    uint64_t y = f2pack(__uint_as_float(0x7EF311C3u - __float_as_uint(df.x)),
+                        __uint_as_float(0x7EF311C3u - __float_as_uint(df.y)));
+    const uint64_t nd = f2pack(-df.x, -df.y), one = f2splat(1.0f);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const uint64_t e = f2fma(nd, y, one);
+        y = f2fma(y, e, y);
+    }
+    return y;
+}
+// sigmoid_f32_steps on two lanes
+__device__ __forceinline__ uint64_t sigmoid_x2(float2 g) {
+    const uint64_t y = recip_x2(f2add(f2splat(1.0f), exp_core_x2(f2pack(fmaxf(-g.x, -86.0f), fmaxf(-g.y, -86.0f)))));
+    const float2 yf = f2unpack(y);
+    return f2pack(g.x < -86.0f ? 0.0f : yf.x, g.y < -86.0f ? 0.0f : yf.y);
+}
+// swiglu_h on two lanes: (g * s) * u
+__device__ __forceinline__ float2 swiglu_h_x2(float2 g, float2 u) {
+    return f2unpack(f2mul(f2mul(f2pack(g.x, g.y), sigmoid_x2(g)), f2pack(u.x, u.y)));
+}
+// swiglu_grads on two lanes: dg = ((d * u) * s) * (1 + g * (1 - s)), du = d * (g * s). The factor
+// 1 + g * (1 - s) is a product followed by a sum, which the assembler may fuse when both are packed; it is
+// taken in scalar steps, which never are.
+__device__ __forceinline__ void swiglu_grads_x2(float2 d, float2 g, float2 u, float2& dg, float2& du) {
+    const uint64_t s = sigmoid_x2(g);
+    const uint64_t gp = f2pack(g.x, g.y), dp = f2pack(d.x, d.y);
+    const float2 sf = f2unpack(s);
+    const uint64_t fac = f2pack(__fadd_rn(1.0f, __fmul_rn(g.x, __fsub_rn(1.0f, sf.x))),
+                                __fadd_rn(1.0f, __fmul_rn(g.y, __fsub_rn(1.0f, sf.y))));
+    dg = f2unpack(f2mul(f2mul(f2mul(dp, f2pack(u.x, u.y)), s), fac));
+    du = f2unpack(f2mul(dp, f2mul(gp, s)));
+}
 
 constexpr int kWarps = 8;                       // compute warps
 constexpr int kThreads = (kWarps + 1) * 32;     // + 1 TMA producer warp
@@ -288,7 +379,11 @@ __global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
             if constexpr (!kBwd) {
                 float h[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) h[j] = swiglu_h(g[j], u[j]);
+                for (int j = 0; j < 4; j += 2) {
+                    const float2 h2 = swiglu_h_x2(make_float2(g[j], g[j + 1]), make_float2(u[j], u[j + 1]));
+                    h[j] = h2.x;
+                    h[j + 1] = h2.y;
+                }
                 const uint2 hw = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
                 *gp = hw;
                 if (kCol || kBias) cs[0].add(hw);
@@ -297,7 +392,15 @@ __global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
                 const float d[4] = {bf16lo(dw.x), bf16hi(dw.x), bf16lo(dw.y), bf16hi(dw.y)};
                 float dg[4], du[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) swiglu_grads(d[j], g[j], u[j], dg[j], du[j]);
+                for (int j = 0; j < 4; j += 2) {
+                    float2 dg2, du2;
+                    swiglu_grads_x2(make_float2(d[j], d[j + 1]), make_float2(g[j], g[j + 1]),
+                                    make_float2(u[j], u[j + 1]), dg2, du2);
+                    dg[j] = dg2.x;
+                    dg[j + 1] = dg2.y;
+                    du[j] = du2.x;
+                    du[j + 1] = du2.y;
+                }
                 const uint2 gw2 = make_uint2(pack_bf16x2(dg[0], dg[1]), pack_bf16x2(dg[2], dg[3]));
                 const uint2 uw2 = make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
                 *gp = gw2;
