@@ -44,3 +44,15 @@ def test_step_event_layout():
                                  "dgrad": 0.5, "wgrad": 0.6})
     assert per_step == pytest.approx([2.4]) and phase == pytest.approx(0.6)
     assert set(per) == set(bench.KERNELS)
+
+
+def test_both_arms_name_the_same_workload():
+    from types import SimpleNamespace
+
+    import numpy as np
+
+    w = SimpleNamespace(E=8, K=2048, N=4096, M=16384)
+    d = {"m_splits": np.full(8, 2048, np.int64)}
+    c = bench.workload_config(w, d, 1)
+    assert c["workload"] == bench.WORKLOAD and c["m_splits"] == [2048] * 8 and c["parallelism"] == "replicas x1"
+    assert (c["experts"], c["hidden"], c["out"], c["tokens"]) == (8, 2048, 4096, 16384)
