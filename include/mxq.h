@@ -112,7 +112,8 @@ enum {
                              requant: emit the swizzled copy of the rowwise scales */
     MXQ_COLWISE = 2,      /* emit the colwise copy */
     MXQ_SWIZZLE = 4,      /* scales in the swizzled GEMM layout (else compact) */
-    MXQ_DEQUANT_OUT = 8,  /* requant: also write the dequantized bf16 tensor */
+    MXQ_DEQUANT_OUT = 8,  /* requant: also write the dequantized bf16 tensor; SwiGLU
+                             paths: also write the bf16 values that were quantized */
     MXQ_ACCUMULATE = 16,  /* wgrad: dW += product (else dW = product) */
     MXQ_OUT_BF16 = 32,    /* wgrad: dW in bf16 (else fp32) */
     MXQ_PAD_EXPERTS = 64  /* group_quantize / requant: expert counts need not be
@@ -266,13 +267,16 @@ MXQ_API int mxq_grouped_gemm_dgrad_ex(const void* dy_data, const void* dy_scale,
  *     mxq_swiglu_fwd, quantized rowwise (h_row_data (M, F), h_row_scale) and
  *     colwise (h_col_data (M, F), h_col_scale) exactly as mxq_swiglu_quantize
  *     would quantize it (flags: MXQ_SWIZZLE selects swizzled scales, else
- *     compact).
+ *     compact);
+ *   with MXQ_DEQUANT_OUT, h_bf16_out (M, F): the bf16 h that was quantized
+ *     (else h_bf16_out is ignored and may be NULL).
  * F % 128 == 0, K % 128 == 0. ws may be NULL. */
 MXQ_API int mxq_grouped_gemm_fprop_swiglu(const void* x_data, const void* x_scale, const void* w1_data,
                                           const void* w1_scale, const void* bias_bf16, int64_t M, int64_t K,
                                           int64_t F, int E, const int64_t* d_m_splits, int flags, void* y1_bf16,
                                           void* h_row_data, void* h_row_scale, void* h_col_data, void* h_col_scale,
-                                          int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream);
+                                          void* h_bf16_out, int32_t* d_status, void* ws, size_t ws_bytes,
+                                          mxq_stream_t stream);
 
 /* grouped dgrad [RQ][FM]: dX[m, :] = dY[m, :] . W[e(m)], dY rowwise (M,N)
  * + swizzled rowwise scales; W colwise (E,N,K) E4M3 (W's byte order,
@@ -296,13 +300,15 @@ MXQ_API int mxq_grouped_gemm_dgrad(const void* dy_data, const void* dy_scale, co
  * dbias_out (E, 2F) fp32 or NULL: per-expert column sums of dY1 (fp32 per 32
  * rows in a fixed order, fp64 over blocks; needs ws of
  * mxq_workspace_bytes(MXQ_OP_GEMM_DGRAD_SWIGLU, M, N, F, E, 0) bytes).
+ * With MXQ_DEQUANT_OUT, dy1_bf16_out (M, 2F) gets the bf16 dY1 that was
+ * quantized (else it is ignored and may be NULL).
  * F % 256 == 0, N % 128 == 0. */
 MXQ_API int mxq_grouped_gemm_dgrad_swiglu(const void* dy_data, const void* dy_scale, const void* w_col_data,
                                           const void* w_col_scale, const void* y1_bf16, int64_t M, int64_t N,
                                           int64_t F, int E, const int64_t* d_m_splits, int flags,
                                           void* dy1_row_data, void* dy1_row_scale, void* dy1_col_data,
-                                          void* dy1_col_scale, float* dbias_out, int32_t* d_status, void* ws,
-                                          size_t ws_bytes, mxq_stream_t stream);
+                                          void* dy1_col_scale, float* dbias_out, void* dy1_bf16_out,
+                                          int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream);
 
 /* grouped wgrad [RQ][FM]: dW[e] = dY_e^T . X_e over expert e's tokens,
  * from the colwise copies only: dY colwise (M,N) + per-expert swizzled
@@ -325,8 +331,9 @@ MXQ_API int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_s
  * sums live in a fixed 8 MiB file-scope device array that every GPU loading
  * the library holds until the process exits:
  *   - (M/128) * N must be <= 2,097,152, else MXQ_ERR_SCRATCH_LIMIT;
- *   - the first call on a device looks up the array's device address (once
- *     per device), so make it before any stream capture;
+ *   - the first call in each CUDA context of a device (the first call of the
+ *     process on that device, and again after cudaDeviceReset) looks up the
+ *     array's device address, so make it before any stream capture;
  *   - all calls share the array (it keeps the last call's partials, which the
  *     next call overwrites before reading); calls that overlap on the GPU
  *     race, so serialise them. */

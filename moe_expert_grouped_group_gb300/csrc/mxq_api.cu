@@ -11,7 +11,7 @@
 #include "mxq_internal.h"
 #include "mxq_peak.h"
 
-namespace {
+namespace mxq {
 
 thread_local int g_last_cuda = 0;
 
@@ -24,7 +24,7 @@ bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr
 
 // Device attribute cache: 1 = sm_103 (GB300), -1 = other, 0 = unknown (atomic: calls may come from
 // several host threads).
-int arch_ok() {
+bool arch_ok() {
     static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -51,7 +51,7 @@ bool device_pointer(const void* p) {
     return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
-int check_common(int64_t M, int64_t K, int E, const int64_t* m_splits, bool splits_required, bool padded = false) {
+int check_common(int64_t M, int64_t K, int E, const int64_t* m_splits, bool splits_required, bool padded) {
     if (!arch_ok()) return MXQ_ERR_ARCH;
     if (M < 0 || K <= 0 || (!padded && M % 128) || K % 128) return MXQ_ERR_SHAPE;
     if (padded && !m_splits) return MXQ_ERR_NULL;
@@ -66,7 +66,13 @@ int check_common(int64_t M, int64_t K, int E, const int64_t* m_splits, bool spli
     return MXQ_OK;
 }
 
-}  // namespace
+}  // namespace mxq
+
+using mxq::aligned16;
+using mxq::arch_ok;
+using mxq::check_common;
+using mxq::device_pointer;
+using mxq::fail_cuda;
 
 extern "C" {
 
@@ -329,6 +335,7 @@ static int gemm_common(int mode, const void* a, const void* as, const void* b, c
         c.swizzle = extra->swizzle;
         c.y1 = extra->y1;
         c.dbias_part = extra->dbias_part;
+        c.side_bf16 = extra->side_bf16;
     }
     cudaError_t e = mxq::run_grouped_gemm(c, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
@@ -337,14 +344,17 @@ static int gemm_common(int mode, const void* a, const void* as, const void* b, c
 int mxq_grouped_gemm_fprop_swiglu(const void* x_data, const void* x_scale, const void* w1_data, const void* w1_scale,
                                   const void* bias_bf16, int64_t M, int64_t K, int64_t F, int E,
                                   const int64_t* d_m_splits, int flags, void* y1_bf16, void* h_row_data,
-                                  void* h_row_scale, void* h_col_data, void* h_col_scale, int32_t* d_status,
-                                  void* ws, size_t ws_bytes, mxq_stream_t stream) {
+                                  void* h_row_scale, void* h_col_data, void* h_col_scale, void* h_bf16_out,
+                                  int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
     (void)ws;
     (void)ws_bytes;
-    if (flags & ~MXQ_SWIZZLE) return MXQ_ERR_FLAGS;
+    if (flags & ~(MXQ_SWIZZLE | MXQ_DEQUANT_OUT)) return MXQ_ERR_FLAGS;
+    const bool side = flags & MXQ_DEQUANT_OUT;
     if (F <= 0 || F % 128 || F > ((int64_t)1 << 30)) return MXQ_ERR_SHAPE;
-    if (M != 0 && (!h_row_data || !h_row_scale || !h_col_data || !h_col_scale)) return MXQ_ERR_NULL;
-    if (!aligned16(h_row_data) || !aligned16(h_row_scale) || !aligned16(h_col_data) || !aligned16(h_col_scale))
+    if (M != 0 && (!h_row_data || !h_row_scale || !h_col_data || !h_col_scale || (side && !h_bf16_out)))
+        return MXQ_ERR_NULL;
+    if (!aligned16(h_row_data) || !aligned16(h_row_scale) || !aligned16(h_col_data) || !aligned16(h_col_scale) ||
+        !aligned16(h_bf16_out))
         return MXQ_ERR_ALIGN;
     mxq::GemmExtra x{};
     x.q_row = h_row_data;
@@ -352,6 +362,7 @@ int mxq_grouped_gemm_fprop_swiglu(const void* x_data, const void* x_scale, const
     x.q_col = h_col_data;
     x.q_col_s = h_col_scale;
     x.swizzle = (flags & MXQ_SWIZZLE) != 0;
+    x.side_bf16 = side ? h_bf16_out : nullptr;
     return gemm_common(mxq::kFpropSwiglu, x_data, x_scale, w1_data, w1_scale, bias_bf16, M, 2 * F, K, E, d_m_splits,
                        y1_bf16, 0, 1, d_status, stream, &x);
 }
@@ -360,13 +371,16 @@ int mxq_grouped_gemm_dgrad_swiglu(const void* dy_data, const void* dy_scale, con
                                   const void* w_col_scale, const void* y1_bf16, int64_t M, int64_t N, int64_t F,
                                   int E, const int64_t* d_m_splits, int flags, void* dy1_row_data,
                                   void* dy1_row_scale, void* dy1_col_data, void* dy1_col_scale, float* dbias_out,
-                                  int32_t* d_status, void* ws, size_t ws_bytes, mxq_stream_t stream) {
-    if (flags & ~MXQ_SWIZZLE) return MXQ_ERR_FLAGS;
+                                  void* dy1_bf16_out, int32_t* d_status, void* ws, size_t ws_bytes,
+                                  mxq_stream_t stream) {
+    if (flags & ~(MXQ_SWIZZLE | MXQ_DEQUANT_OUT)) return MXQ_ERR_FLAGS;
+    const bool side = flags & MXQ_DEQUANT_OUT;
     if (F <= 0 || F % 256) return MXQ_ERR_SHAPE;
-    if (M != 0 && (!y1_bf16 || !dy1_row_data || !dy1_row_scale || !dy1_col_data || !dy1_col_scale))
+    if (M != 0 &&
+        (!y1_bf16 || !dy1_row_data || !dy1_row_scale || !dy1_col_data || !dy1_col_scale || (side && !dy1_bf16_out)))
         return MXQ_ERR_NULL;
     if (!aligned16(y1_bf16) || !aligned16(dy1_row_data) || !aligned16(dy1_row_scale) || !aligned16(dy1_col_data) ||
-        !aligned16(dy1_col_scale) || !aligned16(dbias_out) || !aligned16(ws))
+        !aligned16(dy1_col_scale) || !aligned16(dbias_out) || !aligned16(dy1_bf16_out) || !aligned16(ws))
         return MXQ_ERR_ALIGN;
     if (dbias_out && M != 0 && (!ws || ws_bytes < mxq_workspace_bytes(MXQ_OP_GEMM_DGRAD_SWIGLU, M, N, F, E, 0)))
         return MXQ_ERR_WORKSPACE;
@@ -378,6 +392,7 @@ int mxq_grouped_gemm_dgrad_swiglu(const void* dy_data, const void* dy_scale, con
     x.swizzle = (flags & MXQ_SWIZZLE) != 0;
     x.y1 = y1_bf16;
     x.dbias_part = dbias_out ? static_cast<float*>(ws) : nullptr;
+    x.side_bf16 = side ? dy1_bf16_out : nullptr;
     const int r = gemm_common(mxq::kDgradSwiglu, dy_data, dy_scale, w_col_data, w_col_scale, nullptr, M, N, F, E,
                               d_m_splits, nullptr, 0, 1, d_status, stream, &x);
     if (r != MXQ_OK || !dbias_out) return r;
@@ -551,6 +566,6 @@ const char* mxq_error_string(int code) {
     }
 }
 
-int mxq_last_cuda_error(void) { return g_last_cuda; }
+int mxq_last_cuda_error(void) { return mxq::g_last_cuda; }
 
 }  // extern "C"

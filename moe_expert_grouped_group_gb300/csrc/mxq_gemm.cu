@@ -100,6 +100,7 @@ struct Params {
     int swizzle;
     const __nv_bfloat16* y1;  // kDgradSwiglu: saved FC1 output (M, 2K)
     float* dbias_part;        // kDgradSwiglu: (M/32, 2K) per-32-row column sums, or null
+    __nv_bfloat16* side;      // optional bf16 copy of what is quantized: h (M, N/2) or dY1 (M, 2K)
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -416,6 +417,15 @@ __device__ __forceinline__ void swiglu_bwd_tile_epilogue(const Params& p, const 
             dgw[j] = bf16x2_bits(dg0, dg1);
             duw[j] = bf16x2_bits(du0, du1);
         }
+        if (p.side) {
+            uint4* dg_out = reinterpret_cast<uint4*>(p.side + (rb0 + lane) * W + fc);
+            uint4* du_out = reinterpret_cast<uint4*>(p.side + (rb0 + lane) * W + F + fc);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                dg_out[v] = make_uint4(dgw[4 * v], dgw[4 * v + 1], dgw[4 * v + 2], dgw[4 * v + 3]);
+                du_out[v] = make_uint4(duw[4 * v], duw[4 * v + 1], duw[4 * v + 2], duw[4 * v + 3]);
+            }
+        }
         quant_block32(dgw, p, T, W, rb0, fc, lane);
         quant_block32(duw, p, T, W, rb0, F + fc, lane);
 #pragma unroll
@@ -500,6 +510,12 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
 #pragma unroll
     for (int i = 0; i < 32; ++i)
         hw[i] = bf16x2_bits(swiglu_h(bf16lo(y[i]), bf16lo(y[32 + i])), swiglu_h(bf16hi(y[i]), bf16hi(y[32 + i])));
+
+    if (p.side) {
+        uint4* h_out = reinterpret_cast<uint4*>(p.side + (T.a_row + q * 32 + lane) * F + f0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) h_out[v] = make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
+    }
 
     // rowwise and colwise codes of h, two 32-column blocks
     uint32_t w0[16], w1[16];
@@ -1060,6 +1076,7 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     p.swizzle = c.swizzle;
     p.y1 = static_cast<const __nv_bfloat16*>(c.y1);
     p.dbias_part = c.dbias_part;
+    p.side = static_cast<__nv_bfloat16*>(c.side_bf16);
 
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
     if (c.pad) {

@@ -88,6 +88,7 @@ struct GemmCall {
     int swizzle;
     const void* y1;      // kDgradSwiglu: saved FC1 output (M, 2K) bf16
     float* dbias_part;   // kDgradSwiglu: (M/32, 2K) fp32 column sums per 32 rows, or null
+    void* side_bf16;     // SwiGLU modes: optional bf16 copy of h (M, N/2) or dY1 (M, 2K), or null
     int pad;             // fprop/dgrad/wgrad: padded grouping (expert counts not multiples of 128)
 };
 
@@ -97,6 +98,7 @@ struct GemmExtra {
     int swizzle;
     const void* y1;
     float* dbias_part;
+    void* side_bf16;
 };
 
 // Encodes a 2-D row-major tensor map (rows x cols elements of elem_bytes)
@@ -105,6 +107,17 @@ struct GemmExtra {
 // equal it). False on failure.
 bool encode_tmap_2d(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int elem_bytes, int box_cols,
                     int box_rows, int swizzle_bytes);
+
+// Host-side checks shared by the entry points (mxq_api.cu).
+// Records e as this thread's last CUDA error (mxq_last_cuda_error) and returns MXQ_ERR_LAUNCH.
+int fail_cuda(cudaError_t e);
+// The current device is sm_103 (cached per device).
+bool arch_ok();
+bool aligned16(const void* p);
+// p is device (or managed) memory, reachable without a host round trip.
+bool device_pointer(const void* p);
+// Device, shape and m_splits checks of a grouped (M, K) tensor with E experts; MXQ_OK or an error code.
+int check_common(int64_t M, int64_t K, int E, const int64_t* m_splits, bool splits_required, bool padded = false);
 
 cudaError_t run_group_quantize(const QuantCall& c, cudaStream_t s);
 cudaError_t run_requant(const RequantCall& c, cudaStream_t s);

@@ -59,9 +59,9 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_grouped_dbias.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_fprop.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_fprop_swiglu.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P,
-                                                _P, _P, _P, _SZ, _P]
+                                                _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad_swiglu.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _P,
-                                                _P, _P, _P, _SZ, _P]
+                                                _P, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_fprop_ex.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad_ex.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _INT, _P, _P, _P, _SZ, _P]
     L.mxq_grouped_gemm_dgrad.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _P, _P, _P, _SZ, _P]
@@ -391,10 +391,11 @@ def grouped_gemm_fprop(x_data, x_scale, w_data, w_scale, m_splits, bias=None, st
 
 
 def grouped_gemm_fprop_swiglu(x_data, x_scale, w1_data, w1_scale, m_splits, bias=None, swizzle=True, status=None,
-                              out=None):
+                              out=None, h_out=False):
     """FC1 of a SwiGLU MLP with the activation and its quantization in the GEMM epilogue.
     x_data (M, K) u8, w1_data (E, 2F, K) u8 ([gate | up] rows), swizzled scales ->
-    dict(y1 (M, 2F) bf16, row_data, row_scale, col_data, col_scale of h (M, F))."""
+    dict(y1 (M, 2F) bf16, row_data, row_scale, col_data, col_scale of h (M, F)
+    [, h (M, F) bf16: the values that were quantized, with h_out])."""
     M, K = x_data.shape
     E, N2, _ = w1_data.shape
     F = N2 // 2
@@ -406,6 +407,9 @@ def grouped_gemm_fprop_swiglu(x_data, x_scale, w1_data, w1_scale, m_splits, bias
     o.setdefault("row_scale", _u8(scale_bytes(M, F, False), dev))
     o.setdefault("col_data", _u8((M, F), dev))
     o.setdefault("col_scale", _u8(scale_bytes(M, F, True), dev))
+    if h_out:
+        o.setdefault("h", torch.empty((M, F), dtype=torch.bfloat16, device=dev))
+    _need(o.get("h"), "h", M * F * 2, _BF16)
     _need(x_data, "x_data", M * K, _BYTE)
     _need(x_scale, "x_scale", scale_bytes(M, K, False), _BYTE)
     _need(w1_data, "w1_data", E * 2 * F * K, _BYTE)
@@ -418,8 +422,9 @@ def grouped_gemm_fprop_swiglu(x_data, x_scale, w1_data, w1_scale, m_splits, bias
     _need_flags(None, status)
     rc = lib().mxq_grouped_gemm_fprop_swiglu(
         _ptr(x_data), _ptr(x_scale), _ptr(w1_data), _ptr(w1_scale), _ptr(bias), M, K, F, E, _ptr(m_splits),
-        SWIZZLE if swizzle else 0, _ptr(o["y1"]), _ptr(o["row_data"]), _ptr(o["row_scale"]), _ptr(o["col_data"]),
-        _ptr(o["col_scale"]), _ptr(status), None, 0, _stream())
+        (SWIZZLE if swizzle else 0) | (DEQUANT_OUT if "h" in o else 0), _ptr(o["y1"]), _ptr(o["row_data"]),
+        _ptr(o["row_scale"]), _ptr(o["col_data"]), _ptr(o["col_scale"]), _ptr(o.get("h")), _ptr(status), None, 0,
+        _stream())
     _check(rc, "mxq_grouped_gemm_fprop_swiglu")
     return o
 
@@ -446,10 +451,11 @@ def grouped_gemm_dgrad(dy_data, dy_scale, w_col_data, w_col_scale, m_splits, sta
 
 
 def grouped_gemm_dgrad_swiglu(dy_data, dy_scale, w_col_data, w_col_scale, y1, m_splits, swizzle=True, dbias=True,
-                              status=None, out=None, workspace=None):
+                              status=None, out=None, workspace=None, dy_out=False):
     """FC2 dgrad with the SwiGLU backward and the quantization of dY1 in the GEMM epilogue.
     dy_data (M, N) rowwise, w_col_data (E, N, F) colwise, y1 (M, 2F) bf16 saved FC1 output ->
-    dict(row_data, row_scale, col_data, col_scale of dY1 (M, 2F), dbias (E, 2F))."""
+    dict(row_data, row_scale, col_data, col_scale of dY1 (M, 2F), dbias (E, 2F)
+    [, dy (M, 2F) bf16: the values that were quantized, with dy_out])."""
     M, N = dy_data.shape
     E, _, F = w_col_data.shape
     m_splits = _splits(m_splits)
@@ -459,6 +465,9 @@ def grouped_gemm_dgrad_swiglu(dy_data, dy_scale, w_col_data, w_col_scale, y1, m_
     o.setdefault("row_scale", _u8(scale_bytes(M, 2 * F, False), dev))
     o.setdefault("col_data", _u8((M, 2 * F), dev))
     o.setdefault("col_scale", _u8(scale_bytes(M, 2 * F, True), dev))
+    if dy_out:
+        o.setdefault("dy", torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev))
+    _need(o.get("dy"), "dy", M * 2 * F * 2, _BF16)
     ws = None
     if dbias:
         o.setdefault("dbias", torch.empty((E, 2 * F), dtype=torch.float32, device=dev))
@@ -476,8 +485,8 @@ def grouped_gemm_dgrad_swiglu(dy_data, dy_scale, w_col_data, w_col_scale, y1, m_
     _need_flags(None, status)
     rc = lib().mxq_grouped_gemm_dgrad_swiglu(
         _ptr(dy_data), _ptr(dy_scale), _ptr(w_col_data), _ptr(w_col_scale), _ptr(y1), M, N, F, E, _ptr(m_splits),
-        SWIZZLE if swizzle else 0, _ptr(o["row_data"]), _ptr(o["row_scale"]), _ptr(o["col_data"]),
-        _ptr(o["col_scale"]), _ptr(o.get("dbias")), _ptr(status), _ptr(ws),
+        (SWIZZLE if swizzle else 0) | (DEQUANT_OUT if "dy" in o else 0), _ptr(o["row_data"]), _ptr(o["row_scale"]),
+        _ptr(o["col_data"]), _ptr(o["col_scale"]), _ptr(o.get("dbias")), _ptr(o.get("dy")), _ptr(status), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _stream())
     _check(rc, "mxq_grouped_gemm_dgrad_swiglu")
     return o

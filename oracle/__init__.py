@@ -75,14 +75,8 @@ def _declare(L):
     L.orc_wgrad_entries.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P, _I64, _P, _P, _P, _P, _P]
     L.orc_swiglu_fwd.argtypes = [_P, _I64, _I64, _P]
     L.orc_swiglu_bwd.argtypes = [_P, _P, _I64, _I64, _P]
-    L.orc_exp_f32.argtypes = [ctypes.c_float]
-    L.orc_exp_f32.restype = ctypes.c_float
     L.orc_scaled_bias_grads.argtypes = [_P, _I64, _I64, _INT, _P, _P, _P, _P, _P]
     L.orc_scaled_bias_grads.restype = _INT
-    L.orc_recip_f32.argtypes = [ctypes.c_float]
-    L.orc_recip_f32.restype = ctypes.c_float
-    L.orc_swiglu_fwd_f32.argtypes = [_P, _I64, _I64, _P]
-    L.orc_swiglu_bwd_f32.argtypes = [_P, _P, _I64, _I64, _P]
     L.orc_num_threads.restype = _INT
 
 
@@ -436,32 +430,6 @@ def swiglu_bwd(dh_bits, y_bits):
     M, F2 = y.shape
     dy = np.zeros((M, F2), np.uint16)
     lib().orc_swiglu_bwd(_p(_c(dh_bits, np.uint16)), _p(y), M, F2 // 2, _p(dy))
-    return dy
-
-
-def exp_f32(x: float) -> float:
-    return lib().orc_exp_f32(float(x))
-
-
-def recip_f32(d: float) -> float:
-    return lib().orc_recip_f32(float(d))
-
-
-def swiglu_fwd_f32(y_bits):
-    """SwiGLU forward in the kernels' fp32 precision (see mxq_oracle.c)."""
-    y = _c(y_bits, np.uint16)
-    M, F2 = y.shape
-    h = np.zeros((M, F2 // 2), np.uint16)
-    lib().orc_swiglu_fwd_f32(_p(y), M, F2 // 2, _p(h))
-    return h
-
-
-def swiglu_bwd_f32(dh_bits, y_bits):
-    """SwiGLU backward in the kernels' fp32 precision; returns [dg | du]."""
-    y = _c(y_bits, np.uint16)
-    M, F2 = y.shape
-    dy = np.zeros((M, F2), np.uint16)
-    lib().orc_swiglu_bwd_f32(_p(_c(dh_bits, np.uint16)), _p(y), M, F2 // 2, _p(dy))
     return dy
 
 

@@ -543,108 +543,6 @@ ORC_API void orc_swiglu_bwd(const uint16_t* dh, const uint16_t* y, int64_t M, in
         }
 }
 
-/* ------------------------------------------- SwiGLU in kernel precision */
-
-/* The fused SwiGLU + quantize path rounds h (and dY1) to bf16 inside the
- * kernel, in fp32; a quantized code can only be compared bit for bit if the
- * oracle takes that rounding decision in the same precision. These
- * functions define the fp32 computation step by step -- every operation is
- * one IEEE fp32 rounding (this file is built with -ffp-contract=off) -- and
- * the CUDA kernels implement the same steps independently. fmaf is the
- * IEEE fused multiply-add: one rounding of a*b+c.
- *
- * e^x: Cody & Waite argument reduction, x = n*ln2 + r with n the integer
- * nearest to x*log2 e (one fused multiply-add onto 1.5*2^23 rounds the product
- * straight to an integer, ties to even; subtracting 1.5*2^23 is exact) and ln2
- * split into 0.693359375 (exact, so n*ln2hi is exact) + -2.12194440e-4, then
- * the degree-7 Taylor polynomial of e^r (|r| <= ln2/2, truncation < 6e-9
- * relative) by Horner steps of one fmaf each, scaled by 2^n. The
- * coefficients are 1/k! rounded to fp32, written out in hex. Outside
- * [-86, 88] it returns 0 or +inf (so 2^n, n >= -124, keeps p*2^n normal and
- * the scaling exact); NaN stays NaN. */
-static float exp_f32(float x) {
-    if (x != x) return x;
-    if (x > 88.0f) return INFINITY;
-    if (x < -86.0f) return 0.0f;
-    const float n = fmaf(x, 1.44269504f, 0x1.8p23f) - 0x1.8p23f;
-    float r = fmaf(-n, 0.693359375f, x);
-    r = fmaf(-n, -2.12194440e-4f, r);
-    float p = 0x1.a01a02p-13f;        /* 1/5040 */
-    p = fmaf(p, r, 0x1.6c16c2p-10f);  /* 1/720 */
-    p = fmaf(p, r, 0x1.111112p-7f);   /* 1/120 */
-    p = fmaf(p, r, 0x1.555556p-5f);   /* 1/24 */
-    p = fmaf(p, r, 0x1.555556p-3f);   /* 1/6 */
-    p = fmaf(p, r, 0.5f);
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    return ldexpf(p, (int)n);
-}
-
-ORC_API float orc_exp_f32(float x) { return exp_f32(x); }
-
-/* 1/d for d in [1, 2^126): Newton-Raphson iteration y <- y + y*(1 - d*y)
- * (two fmaf per step) from the bit-pattern estimate y0 = as_float(0x7EF311C3
- * - bits(d)), whose relative error is at most 5.1%; three steps square that
- * to below 2^-24 (measured: within 0.5003 ulp of 1/d). Only fp32 adds,
- * multiplies and an integer subtraction: no division. */
-static float recip_f32(float d) {
-    uint32_t b;
-    memcpy(&b, &d, sizeof b);
-    b = 0x7EF311C3u - b;
-    float y;
-    memcpy(&y, &b, sizeof y);
-    for (int i = 0; i < 3; ++i) {
-        const float e = fmaf(-d, y, 1.0f);
-        y = fmaf(y, e, y);
-    }
-    return y;
-}
-
-ORC_API float orc_recip_f32(float d) { return recip_f32(d); }
-
-/* sigmoid(g) = 1/(1 + e^-g); taken as 0 below g = -86, where the true value
- * is under 2^-124 (this also keeps d = 1 + e^-g inside recip_f32's range). */
-static float sigmoid_f32(float g) {
-    if (g < -86.0f) return 0.0f;
-    return recip_f32(1.0f + exp_f32(-g));
-}
-
-static uint16_t bf16_round_f32(float f) { return orc_bf16_round((double)f); }
-
-/* h = (g * sigmoid(g)) * u, fp32 steps as above, rounded once to bf16. */
-ORC_API void orc_swiglu_fwd_f32(const uint16_t* y, int64_t M, int64_t F, uint16_t* h) {
-    #pragma omp parallel for schedule(static)
-    for (int64_t m = 0; m < M; ++m)
-        for (int64_t f = 0; f < F; ++f) {
-            const float g = (float)orc_bf16_value(y[m * 2 * F + f]);
-            const float u = (float)orc_bf16_value(y[m * 2 * F + F + f]);
-            const float sg = sigmoid_f32(g);
-            const float silu = g * sg;
-            h[m * F + f] = bf16_round_f32(silu * u);
-        }
-}
-
-/* dg = ((dh * u) * s) * (1 + g * (1 - s)), du = dh * (g * s), s = sigmoid(g);
- * fp32 steps in that order, each result rounded once to bf16. */
-ORC_API void orc_swiglu_bwd_f32(const uint16_t* dh, const uint16_t* y, int64_t M, int64_t F, uint16_t* dy) {
-    #pragma omp parallel for schedule(static)
-    for (int64_t m = 0; m < M; ++m)
-        for (int64_t f = 0; f < F; ++f) {
-            const float d = (float)orc_bf16_value(dh[m * F + f]);
-            const float g = (float)orc_bf16_value(y[m * 2 * F + f]);
-            const float u = (float)orc_bf16_value(y[m * 2 * F + F + f]);
-            const float sg = sigmoid_f32(g);
-            const float one_minus = 1.0f - sg;
-            const float gt = g * one_minus;
-            const float fac = 1.0f + gt;
-            const float a = d * u;
-            const float b = a * sg;
-            dy[m * 2 * F + f] = bf16_round_f32(b * fac);
-            const float silu = g * sg;
-            dy[m * 2 * F + F + f] = bf16_round_f32(d * silu);
-        }
-}
-
 ORC_API int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

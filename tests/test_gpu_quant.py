@@ -1,14 +1,16 @@
 """GPU parity: group_quantize, requant_colwise, grouped_dbias and SwiGLU
 against the CPU oracle, through the C ABI. Quantized bytes and scales must be
-bit-exact; dbias within 1e-5 * sum|x| per column; SwiGLU within one bf16 ulp
-(fp32 math on the GPU vs fp64 in the oracle, one final rounding each)."""
+bit-exact; dbias within 1e-5 * sum|x| per column; SwiGLU within one bf16 step
+of the oracle's fp64 definition (fp32 math on the GPU, one final rounding each;
+the fp32 sigmoid flush below g = -86 has its own bound, tests/_gpu.py)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as orc
 from synth import WORKLOADS, bf16_bits_from_f32, make_inputs
-from tests._gpu import bf16_to_f64, dev_bf16, dev_i64, dev_u8, first_diff, host, lib, require_gpu
+from tests._gpu import (assert_swiglu_close, bf16_to_f64, dev_bf16, dev_i64, dev_u8, first_diff, host, lib, require_gpu,
+                        swiglu_bwd_slack, swiglu_fwd_slack)
 
 pytestmark = pytest.mark.gpu
 
@@ -217,12 +219,8 @@ def test_swiglu(mxq):
     dh = bf16_bits_from_f32(rng.standard_normal((M, F)).astype(np.float32))
     h = host(mxq.swiglu_fwd(dev_bf16(y)))
     dy = host(mxq.swiglu_bwd(dev_bf16(dh), dev_bf16(y)))
-    for got, ref in ((h, orc.swiglu_fwd(y)), (dy, orc.swiglu_bwd(dh, y))):
-        # within one bf16 ulp: adjacent bit patterns of the same sign
-        d = np.abs(got.astype(np.int32) - ref.astype(np.int32))
-        same_sign = (got >> 15) == (ref >> 15)
-        ok = (d <= 1) & same_sign | ((got & 0x7FFF) <= 1) & ((ref & 0x7FFF) <= 1)
-        assert ok.all(), first_diff(got, ref)
+    assert_swiglu_close(h, orc.swiglu_fwd(y), swiglu_fwd_slack(y), "h")
+    assert_swiglu_close(dy, orc.swiglu_bwd(dh, y), swiglu_bwd_slack(dh, y), "dY1")
 
 
 # ---------------------------------------------------------------- full size
@@ -286,8 +284,5 @@ def test_full_size_swiglu(mxq):
     dh = bf16_bits_from_f32(rng.standard_normal((M, F)).astype(np.float32))
     h = host(mxq.swiglu_fwd(dev_bf16(y)))
     dy = host(mxq.swiglu_bwd(dev_bf16(dh), dev_bf16(y)))
-    for got, ref in ((h, orc.swiglu_fwd(y)), (dy, orc.swiglu_bwd(dh, y))):
-        d_ = np.abs(got.astype(np.int32) - ref.astype(np.int32))
-        same_sign = (got >> 15) == (ref >> 15)
-        ok = (d_ <= 1) & same_sign | ((got & 0x7FFF) <= 1) & ((ref & 0x7FFF) <= 1)
-        assert ok.all(), first_diff(got, ref)
+    assert_swiglu_close(h, orc.swiglu_fwd(y), swiglu_fwd_slack(y), "h")
+    assert_swiglu_close(dy, orc.swiglu_bwd(dh, y), swiglu_bwd_slack(dh, y), "dY1")

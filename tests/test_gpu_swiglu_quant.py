@@ -1,17 +1,22 @@
 """GPU parity: SwiGLU fused with group quantization, forward and backward.
 
-The oracle computes SwiGLU in the kernels' fp32 precision (the rounding of h
-to bf16 decides the E4M3 codes, so both sides take it in the same precision),
-then quantizes with its own group_quantize and reduces dbias in fp64. Codes
-and scales must be bit-exact, the optional bf16 outputs equal, dbias within
-1e-5 * sum|x| per column."""
+Two checks together fix every output (the fused kernels write their bf16 h or
+dY1 on request, as well as its codes):
+  (i)  every bf16 h / dY1 value the kernel produced is within one bf16 step of
+       the oracle's fp64 SwiGLU (or its backward) on the same inputs, or within
+       the bound of the fp32 sigmoid flush below g = -86 (tests/_gpu.py);
+  (ii) the codes and scales equal, byte for byte, the oracle's group_quantize
+       of the kernel's own bf16 values, and dbias is within 1e-5 * sum|x| per
+       column of the oracle's fp64 per-expert sums of them.
+Quantization is exactly defined, so (i) and (ii) leave nothing unchecked."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as orc
 from synth import WORKLOADS, bf16_bits_from_f32, make_inputs
-from tests._gpu import bf16_to_f64, dev_bf16, dev_i64, first_diff, host, lib, require_gpu
+from tests._gpu import (assert_swiglu_close, bf16_to_f64, dev_bf16, dev_i64, first_diff, host, lib, require_gpu,
+                        swiglu_bwd_slack, swiglu_fwd_slack)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +30,7 @@ def mxq():
 def _inputs(M, F, seed):
     rng = np.random.default_rng(seed)
     y = (3 * rng.standard_normal((M, 2 * F))).astype(np.float32)
-    y[rng.random((M, 2 * F)) < 0.002] *= 100.0       # saturated gates and big ups
+    y[rng.random((M, 2 * F)) < 0.002] *= 100.0       # saturated gates (some below -86) and big ups
     y[:32, :32] = 0.0                                 # all-zero blocks
     y[32:64, F:F + 32] = np.float32(1e-39)            # bf16 subnormal ups
     dh = rng.standard_normal((M, F)).astype(np.float32)
@@ -41,6 +46,28 @@ def _cmp(q, o, what):
         assert np.array_equal(got, o[k]), (what, k, first_diff(got, o[k]))
 
 
+def check_forward(q, y, ms, swizzled, rowwise=True, colwise=True, what="fwd"):
+    """(i) q["h"] against the fp64 definition; (ii) codes == group_quantize(q["h"])."""
+    h = host(q["h"])
+    assert_swiglu_close(h, orc.swiglu_fwd(y), swiglu_fwd_slack(y), what + " h")
+    _cmp(q, orc.group_quantize(h, np.asarray(ms), rowwise=rowwise, colwise=colwise, swizzled=swizzled), what)
+
+
+def check_backward(q, dh, y, ms, swizzled, rowwise=True, colwise=True, dbias=True, what="bwd"):
+    """(i) q["dy"] against the fp64 backward; (ii) codes == group_quantize(q["dy"]), dbias of q["dy"]."""
+    ms = np.asarray(ms)
+    dy = host(q["dy"])
+    assert_swiglu_close(dy, orc.swiglu_bwd(dh, y), swiglu_bwd_slack(dh, y), what + " dY1")
+    _cmp(q, orc.group_quantize(dy, ms, rowwise=rowwise, colwise=colwise, swizzled=swizzled), what)
+    if dbias:
+        ref = orc.grouped_dbias(dy, ms)
+        got = host(q["dbias"]).astype(np.float64)
+        f = np.abs(bf16_to_f64(dy))
+        off = np.concatenate([[0], np.cumsum(ms)])
+        for e in range(len(ms)):
+            assert np.all(np.abs(got[e] - ref[e]) <= 1e-5 * f[off[e]:off[e + 1]].sum(axis=0) + 1e-30), (what, e)
+
+
 CASES = [(512, 256, [128, 256, 0, 128]), (384, 128, [384]), (640, 384, [0, 256, 128, 0, 256])]
 
 
@@ -49,10 +76,9 @@ CASES = [(512, 256, [128, 256, 0, 128]), (384, 128, [384]), (640, 384, [0, 256, 
 def test_swiglu_quantize_forward(mxq, case, swz):
     M, F, ms = case
     y, _ = _inputs(M, F, M + F)
+    assert (bf16_to_f64(y)[:, :F] < -86).any()        # the flush branch is exercised
     q = mxq.swiglu_quantize(dev_bf16(y), dev_i64(ms), swizzle=swz, h_out=True)
-    h = orc.swiglu_fwd_f32(y)
-    assert np.array_equal(host(q["h"]), h), first_diff(host(q["h"]), h)
-    _cmp(q, orc.group_quantize(h, np.array(ms), swizzled=swz), "fwd")
+    check_forward(q, y, ms, swz)
 
 
 @pytest.mark.parametrize("swz", [True, False])
@@ -61,34 +87,34 @@ def test_swiglu_quantize_backward(mxq, case, swz):
     M, F, ms = case
     y, dh = _inputs(M, F, 7 * M + F)
     q = mxq.swiglu_bwd_quantize(dev_bf16(dh), dev_bf16(y), dev_i64(ms), swizzle=swz, dbias=True, dy_out=True)
-    dy = orc.swiglu_bwd_f32(dh, y)
-    assert np.array_equal(host(q["dy"]), dy), first_diff(host(q["dy"]), dy)
-    _cmp(q, orc.group_quantize(dy, np.array(ms), swizzled=swz), "bwd")
-    ref = orc.grouped_dbias(dy, np.array(ms))
-    got = host(q["dbias"]).astype(np.float64)
-    f = np.abs(bf16_to_f64(dy))
-    off = np.concatenate([[0], np.cumsum(ms)])
-    for e in range(len(ms)):
-        assert np.all(np.abs(got[e] - ref[e]) <= 1e-5 * f[off[e]:off[e + 1]].sum(axis=0) + 1e-30), e
+    check_backward(q, dh, y, ms, swz)
 
 
 @pytest.mark.parametrize("rowwise,colwise", [(True, False), (False, True)])
 def test_swiglu_quantize_single_direction(mxq, rowwise, colwise):
     M, F, ms = 512, 256, [256, 256]
     y, dh = _inputs(M, F, 3)
-    q = mxq.swiglu_quantize(dev_bf16(y), dev_i64(ms), rowwise=rowwise, colwise=colwise)
-    _cmp(q, orc.group_quantize(orc.swiglu_fwd_f32(y), np.array(ms), rowwise=rowwise, colwise=colwise,
-                               swizzled=True), "fwd1")
-    q = mxq.swiglu_bwd_quantize(dev_bf16(dh), dev_bf16(y), dev_i64(ms), rowwise=rowwise, colwise=colwise)
-    _cmp(q, orc.group_quantize(orc.swiglu_bwd_f32(dh, y), np.array(ms), rowwise=rowwise, colwise=colwise,
-                               swizzled=True), "bwd1")
+    q = mxq.swiglu_quantize(dev_bf16(y), dev_i64(ms), rowwise=rowwise, colwise=colwise, h_out=True)
+    check_forward(q, y, ms, True, rowwise=rowwise, colwise=colwise, what="fwd1")
+    q = mxq.swiglu_bwd_quantize(dev_bf16(dh), dev_bf16(y), dev_i64(ms), rowwise=rowwise, colwise=colwise,
+                                dbias=False, dy_out=True)
+    check_backward(q, dh, y, ms, True, rowwise=rowwise, colwise=colwise, dbias=False, what="bwd1")
 
 
-def test_unfused_swiglu_equals_kernel_precision_definition(mxq):
+def test_unfused_swiglu_equals_fused(mxq):
+    """The unfused kernels run the same fp32 steps: their outputs equal the fused kernels' bf16
+    side outputs bit for bit, and both are within the tolerance of the fp64 definition."""
     M, F = 512, 384
     y, dh = _inputs(M, F, 5)
-    assert np.array_equal(host(mxq.swiglu_fwd(dev_bf16(y))), orc.swiglu_fwd_f32(y))
-    assert np.array_equal(host(mxq.swiglu_bwd(dev_bf16(dh), dev_bf16(y))), orc.swiglu_bwd_f32(dh, y))
+    ms = [M]
+    h = host(mxq.swiglu_fwd(dev_bf16(y)))
+    dy = host(mxq.swiglu_bwd(dev_bf16(dh), dev_bf16(y)))
+    assert_swiglu_close(h, orc.swiglu_fwd(y), swiglu_fwd_slack(y), "h")
+    assert_swiglu_close(dy, orc.swiglu_bwd(dh, y), swiglu_bwd_slack(dh, y), "dY1")
+    qf = mxq.swiglu_quantize(dev_bf16(y), dev_i64(ms), h_out=True)
+    qb = mxq.swiglu_bwd_quantize(dev_bf16(dh), dev_bf16(y), dev_i64(ms), dbias=False, dy_out=True)
+    assert np.array_equal(h, host(qf["h"]))
+    assert np.array_equal(dy, host(qb["dy"]))
 
 
 def test_noop_and_bad_splits(mxq):
@@ -114,15 +140,8 @@ def test_full_size(mxq, name):
     rng = np.random.default_rng(w.wid)
     y = bf16_bits_from_f32((2 * rng.standard_normal((w.M, 2 * w.F))).astype(np.float32))
     dh = bf16_bits_from_f32(rng.standard_normal((w.M, w.F)).astype(np.float32))
-    q = mxq.swiglu_quantize(dev_bf16(y), dev_i64(ms))
-    _cmp(q, orc.group_quantize(orc.swiglu_fwd_f32(y), ms, swizzled=True), name + " fwd")
+    q = mxq.swiglu_quantize(dev_bf16(y), dev_i64(ms), h_out=True)
+    check_forward(q, y, ms, True, what=name + " fwd")
     del q
-    q = mxq.swiglu_bwd_quantize(dev_bf16(dh), dev_bf16(y), dev_i64(ms), dbias=True)
-    dy = orc.swiglu_bwd_f32(dh, y)
-    _cmp(q, orc.group_quantize(dy, ms, swizzled=True), name + " bwd")
-    ref = orc.grouped_dbias(dy, ms)
-    got = host(q["dbias"]).astype(np.float64)
-    f = np.abs(bf16_to_f64(dy))
-    off = np.concatenate([[0], np.cumsum(ms)])
-    for e in range(w.E):
-        assert np.all(np.abs(got[e] - ref[e]) <= 1e-5 * f[off[e]:off[e + 1]].sum(axis=0) + 1e-30), e
+    q = mxq.swiglu_bwd_quantize(dev_bf16(dh), dev_bf16(y), dev_i64(ms), dbias=True, dy_out=True)
+    check_backward(q, dh, y, ms, True, what=name + " bwd")

@@ -38,3 +38,26 @@ def test_random_codes_are_finite_e4m3():
     assert len(np.unique(codes)) == 254  # every finite code appears
     s = random_scales(np.random.default_rng(6), (64, 64))
     assert s.min() >= 118 and s.max() <= 136
+
+
+def test_weight_slab_atom_mapping():
+    """The full-size weight test compares 128-row slabs: slab j of expert e, quantized by the
+    oracle as a member of its own, must equal the same rows and scale atoms of the whole
+    weight's quantization (rowwise atoms contiguous, colwise atom kb at
+    e K N / 32 + (kb (N / 128) + j) * 512)."""
+    import oracle as orc
+
+    E, N, K = 3, 384, 512
+    w = bf16_bits_from_f32((0.02 * np.random.default_rng(1).standard_normal((E, N, K))).astype(np.float32))
+    full = orc.quantize_weights(w, swizzled=True)
+    nkb = K // 128
+    for e in range(E):
+        for j in range(N // 128):
+            r0 = e * N + 128 * j
+            o = orc.quantize_weights(w[e, 128 * j:128 * j + 128][None], swizzled=True)
+            assert np.array_equal(full["row_q"][r0:r0 + 128], o["row_q"])
+            assert np.array_equal(full["col_q"][r0:r0 + 128], o["col_q"])
+            a = (r0 // 128) * nkb * 512
+            assert np.array_equal(full["row_s"][a:a + nkb * 512], o["row_s"])
+            idx = e * K * N // 32 + (np.arange(nkb)[:, None] * (N // 128) + j) * 512 + np.arange(512)[None, :]
+            assert np.array_equal(full["col_s"][idx.ravel()], o["col_s"])

@@ -1,15 +1,15 @@
 """mxq_grouped_dbias_noalloc: per-expert dbias for callers that cannot
 allocate device memory (its scratch is a fixed file-scope device array).
 
-Called through the C ABI and compared with mxq_grouped_dbias (which takes a
-caller workspace) within the dbias tolerance of the other tests,
-1e-5 * sum|dY| per column, on two calls in a row with different inputs and
-groupings so that a stale partial from the first call would show up in the
-second. Collected last so that a run stopping at the first failure has run
-every other test; it also passes alone in a fresh process.
+Called through the C ABI on two calls in a row with different inputs and
+groupings, so that a stale partial from the first call would show up in the
+second. It runs the same kernels in the same order as mxq_grouped_dbias
+(which takes a caller workspace), so the two results must be identical bit
+for bit; both must also be within the dbias tolerance of the other tests,
+1e-5 * sum|dY| per column, of the oracle's fp64 per-expert sums. Collected
+last so that a run stopping at the first failure has run every other test;
+it also passes alone in a fresh process.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
@@ -31,7 +31,8 @@ def _call_with_workspace(L, dy, ms, out):
 
 
 def test_noalloc_dbias_matches_workspace_dbias_twice():
-    from tests._gpu import lib, require_gpu
+    import oracle as orc
+    from tests._gpu import bf16_to_f64, lib, require_gpu
 
     require_gpu()
     L = lib().mxq.lib()
@@ -51,12 +52,16 @@ def test_noalloc_dbias_matches_workspace_dbias_twice():
         assert _call_with_workspace(L, dy, ms, ref) == 0
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        a = dy.float().abs()
+        assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), (M, N, "not bit-identical")
+        bits = dy.view(torch.int16).cpu().numpy().view(np.uint16)
+        want = orc.grouped_dbias(bits, np.array(splits, np.int64))
+        a = np.abs(bf16_to_f64(bits))
         off = np.concatenate([[0], np.cumsum(splits)])
         for e in range(E):
-            tol = 1e-5 * a[off[e]:off[e + 1]].sum(dim=0).double() + 1e-30
-            diff = (got[e].double() - ref[e].double()).abs()
-            assert bool((diff <= tol).all()), (M, N, e)
+            tol = 1e-5 * a[off[e]:off[e + 1]].sum(axis=0) + 1e-30
+            for name, t in (("noalloc", got), ("workspace", ref)):
+                diff = np.abs(t[e].double().cpu().numpy() - want[e])
+                assert np.all(diff <= tol), (name, M, N, e)
             if splits[e] == 0:
                 assert bool((got[e] == 0).all())
 
