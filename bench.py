@@ -1,22 +1,32 @@
 """Benchmark: one grouped MXFP8 linear training step of an MoE expert layer.
 
-Workload (8 experts, hidden 2048, out 4096, 16384 routed tokens, uniform
-multinomial routing rounded to 128-token multiples, X arriving rowwise-
-quantized as an expert-parallel FP8 dispatch delivers it). One step is the
-whole hot path over one batch:
+Headline workload: 128 experts (32 of them empty, the rest with Pareto(1.2)
+loads rounded to 128-token multiples), hidden 7168, out 2048, 131072 routed
+tokens, bf16 activations with x1000 outliers and all-zero 32x32 tiles. One
+step is the whole hot path over one batch:
 
-    requant X (rowwise wire format -> colwise copy + swizzled rowwise scales)
-      | group_quantize W (rowwise + colwise, uniform members)   [two streams]
+    group_quantize X (rowwise + colwise)      | group_quantize W (rowwise +
+                                              | colwise, uniform members)
+                                              [two streams, joined]
     grouped fprop  Y  = X W_e^T
     group_quantize dY (rowwise + colwise)
     grouped dgrad  dX = dY W_e
     grouped wgrad  dW = dY_e^T X_e (fp32)
 
+(On a workload whose X arrives rowwise-quantized, as an expert-parallel FP8
+dispatch delivers it, the first call is requant_colwise instead.)
+
 value = GEMM flops of the step (6*M*N*K) / step time (whole step), in
-TFLOP/s. L2 is flushed (256 MiB write) before every timed step; the flush is
-outside the per-step CUDA-event brackets. Per-kernel times come from events
-on the stream that runs each kernel; a serial pass of the same step times
-each quantize kernel alone. `--impl reference` times the CPU oracle instead.
+TFLOP/s. L2 is flushed (256 MiB write) before every pass; the flush is outside
+the per-pass CUDA-event brackets. The timed region runs K steps, each as R
+back-to-back passes (R chosen so the region lasts over a second; ms_per_step
+is one pass). Per-kernel times come from events on the stream that runs each
+kernel; a serial pass of the same step times each quantize kernel alone. The
+line also carries one grouped-linear step of every other synthetic workload
+("configs"), the full SwiGLU MLP step on the 64-expert workload ("mlp_step"),
+an end-to-end leg through pinned host buffers ("e2e") and the CPU oracle on a
+bounded fraction of the step ("cpu_baseline"). `--impl reference` times the
+CPU oracle alone.
 
 Multi-GPU (torchrun): every rank runs an independent replica of the
 workload (the grouped path has no exchange step of its own); rank 0 prints
@@ -38,7 +48,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "e8_h2048_n4096_t16k_prequant"
+WORKLOAD = "e128_h7168_n2048_t128k_skew"
+TIMED_REGION_S = 1.2    # the timed region lasts at least this long (inner repeat of each step)
 METRIC = "grouped MXFP8 GEMM TFLOPS (fprop+dgrad+wgrad); group_quantize HBM GB/s"
 UNIT = "TFLOP/s"
 MXFP8_OVER_BF16 = 2.0   # nominal dense MXFP8 / BF16 tensor-core ratio (4.5 / 2.25 PFLOP/s)
@@ -51,6 +62,9 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--repeat", type=int, default=0,
+                   help="passes per timed step (0: enough for a timed region of at least TIMED_REGION_S)")
+    p.add_argument("--no-configs", action="store_true", help="skip the other workloads' grouped-linear steps")
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -137,12 +151,19 @@ def make_host_workload():
     return w, d
 
 
+def x_kernel(w) -> str:
+    return "requant_x" if w.prequant_x else "quantize_x"
+
+
 def workload_config(w, d, world):
     """The workload both arms run, as named in their JSON lines."""
+    first = ("requant X (rowwise wire format -> colwise copy + swizzled rowwise scales)" if w.prequant_x
+             else "quantize X (row+col)")
     return {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
             "m_splits": [int(v) for v in d["m_splits"]],
-            "step": "requant X + quantize W (row+col), fprop, quantize dY (row+col), dgrad, wgrad (fp32 dW)",
-            "parallelism": f"replicas x{world}"}
+            "step": f"{first} + quantize W (row+col), fprop, quantize dY (row+col), dgrad, wgrad (fp32 dW)",
+            "parallelism": f"replicas x{world}",
+            "l2": "GPU arm: a 256 MiB buffer written before every timed pass (outside the event brackets)"}
 
 
 class NativeStep:
@@ -150,9 +171,9 @@ class NativeStep:
 
     In the order of a training step: the forward's two quantizations, fprop,
     then the backward's (quantize dY) and dgrad, wgrad. The forward's two are
-    independent, so by default they run concurrently: requant X on a side
-    stream forked from the caller's stream, quantize W on it, joined before
-    fprop. Requant is bound by its arithmetic and quantize W by HBM, and each
+    independent, so by default they run concurrently: the quantization of X
+    (or its requant, when X arrives rowwise-quantized) on a side stream forked
+    from the caller's stream, quantize W on it, joined before fprop. Each
     kernel's last partial wave of CTAs leaves SMs idle that the other fills.
     The outputs are bit-identical to the serial order."""
 
@@ -162,19 +183,26 @@ class NativeStep:
         import moe_expert_grouped_group_gb300 as mxq
 
         self.torch, self.mxq, self.w, self.dev = torch, mxq, w, dev
+        self.pre_x = w.prequant_x
         E, N, K, M = w.E, w.N, w.K, w.M
         tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
         self.ms = torch.from_numpy(d["m_splits"]).to(dev)
         self.x_bf16 = tb(d["x"])
         self.wt = tb(d["w"]).view(E * N, K)
         self.dy = tb(d["dy"])
-        # The dispatch wire format (rowwise E4M3 + compact scales), made once
-        # by the library itself (setup, untimed).
-        q = mxq.group_quantize(self.x_bf16, self.ms, rowwise=True, colwise=False, swizzle=False)
-        self.x_row, self.x_row_scale = q["row_data"], q["row_scale"]
         u8 = lambda n: torch.empty(n, dtype=torch.uint8, device=dev)
-        self.rq = {"col_data": u8((M, K)), "col_scale": u8(mxq.scale_bytes(M, K, True)),
-                   "row_scale_swizzled": u8(mxq.scale_bytes(M, K, False))}
+        if self.pre_x:
+            # The dispatch wire format (rowwise E4M3 + compact scales), made once
+            # by the library itself (setup, untimed).
+            q = mxq.group_quantize(self.x_bf16, self.ms, rowwise=True, colwise=False, swizzle=False)
+            self.x_row, self.x_row_scale = q["row_data"], q["row_scale"]
+            self.qx = {"col_data": u8((M, K)), "col_scale": u8(mxq.scale_bytes(M, K, True)),
+                       "row_scale_swizzled": u8(mxq.scale_bytes(M, K, False))}
+            self.e2e_inputs = ("x_row", "x_row_scale", "wt", "dy", "ms")
+        else:
+            self.qx = {"row_data": u8((M, K)), "row_scale": u8(mxq.scale_bytes(M, K, False)),
+                       "col_data": u8((M, K)), "col_scale": u8(mxq.scale_bytes(M, K, True))}
+            self.e2e_inputs = ("x_bf16", "wt", "dy", "ms")
         self.qw = {"row_data": u8((E * N, K)), "row_scale": u8(mxq.scale_bytes(E * N, K, False)),
                    "col_data": u8((E * N, K)), "col_scale": u8(mxq.scale_bytes(E * N, K, True))}
         self.qdy = {"row_data": u8((M, N)), "row_scale": u8(mxq.scale_bytes(M, N, False)),
@@ -184,51 +212,61 @@ class NativeStep:
         self.dw = torch.empty((E, N, K), dtype=torch.float32, device=dev)
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         self.launches_per_step = 6
-        self.s_rq = torch.cuda.Stream(device=dev)
-        self.ev_fork, self.ev_rq = torch.cuda.Event(), torch.cuda.Event()
+        self.kernel_events = kernel_events(self.pre_x)
+        self.s_x = torch.cuda.Stream(device=dev)
+        self.ev_fork, self.ev_x = torch.cuda.Event(), torch.cuda.Event()
+
+    def x_operands(self):
+        """(rowwise codes, swizzled rowwise scales, colwise codes, colwise scales) of X."""
+        if self.pre_x:
+            return self.x_row, self.qx["row_scale_swizzled"], self.qx["col_data"], self.qx["col_scale"]
+        return self.qx["row_data"], self.qx["row_scale"], self.qx["col_data"], self.qx["col_scale"]
 
     def run(self, events=None, concurrent=True):
         """One step on the current stream. events: STEP_EVENTS timing events, recorded on the stream
-        that runs each kernel (see KERNEL_EVENTS)."""
+        that runs each kernel (see kernel_events)."""
         torch, mxq, w = self.torch, self.mxq, self.w
         E, N, K = w.E, w.N, w.K
         main = torch.cuda.current_stream()
         rec = (lambda i, st=None: events[i].record(st or main)) if events else (lambda i, st=None: None)
 
-        def requant():
-            mxq.requant_colwise(self.x_row, self.x_row_scale, self.ms, out=self.rq)
+        def quant_x():
+            if self.pre_x:
+                mxq.requant_colwise(self.x_row, self.x_row_scale, self.ms, out=self.qx)
+            else:
+                mxq.group_quantize(self.x_bf16, self.ms, out=self.qx)
 
         rec(0)
         if concurrent:
             self.ev_fork.record(main)
-            self.s_rq.wait_event(self.ev_fork)
-            with torch.cuda.stream(self.s_rq):
-                rec(1, self.s_rq)
-                requant()
-                rec(2, self.s_rq)
-            self.ev_rq.record(self.s_rq)
+            self.s_x.wait_event(self.ev_fork)
+            with torch.cuda.stream(self.s_x):
+                rec(1, self.s_x)
+                quant_x()
+                rec(2, self.s_x)
+            self.ev_x.record(self.s_x)
             rec(3)
             mxq.group_quantize(self.wt, None, E=E, out=self.qw)
             rec(4)
-            main.wait_event(self.ev_rq)
+            main.wait_event(self.ev_x)
         else:
             rec(1)
-            requant()
+            quant_x()
             rec(2)
             rec(3)
             mxq.group_quantize(self.wt, None, E=E, out=self.qw)
             rec(4)
         rec(5)
-        mxq.grouped_gemm_fprop(self.x_row, self.rq["row_scale_swizzled"], self.qw["row_data"].view(E, N, K),
-                               self.qw["row_scale"], self.ms, out=self.y)
+        x_row, x_rs, x_col, x_cs = self.x_operands()
+        mxq.grouped_gemm_fprop(x_row, x_rs, self.qw["row_data"].view(E, N, K), self.qw["row_scale"], self.ms,
+                               out=self.y)
         rec(6)
         mxq.group_quantize(self.dy, self.ms, out=self.qdy)
         rec(7)
         mxq.grouped_gemm_dgrad(self.qdy["row_data"], self.qdy["row_scale"], self.qw["col_data"].view(E, N, K),
                                self.qw["col_scale"], self.ms, out=self.dx)
         rec(8)
-        mxq.grouped_gemm_wgrad(self.qdy["col_data"], self.qdy["col_scale"], self.rq["col_data"],
-                               self.rq["col_scale"], self.ms, out=self.dw)
+        mxq.grouped_gemm_wgrad(self.qdy["col_data"], self.qdy["col_scale"], x_col, x_cs, self.ms, out=self.dw)
         rec(9)
 
     def flush(self):
@@ -644,11 +682,12 @@ def time_padded(dev, steps, warmup):
     return res
 
 
-def time_configs(dev, steps, warmup):
+def time_configs(dev, steps, warmup, skip=()):
     """One grouped-linear step (the first linear: FC1 for the SwiGLU MLPs) on every synthetic
-    workload: X quantized row+col (or, prequantized, requantized colwise), W and dY quantized
-    row+col, fprop, dgrad, wgrad (fp32 dW); per-kernel CUDA-event times, GEMM TFLOP/s and
-    quantize GB/s with their roofline fractions."""
+    workload but those in `skip`: X quantized row+col (or, prequantized, requantized colwise), W and
+    dY quantized row+col, fprop, dgrad, wgrad (fp32 dW), each call timed alone (CUDA events, L2
+    flushed before each step); per-kernel times, GEMM TFLOP/s and quantize GB/s with their
+    roofline fractions."""
     import torch
 
     import moe_expert_grouped_group_gb300 as mxq
@@ -660,6 +699,8 @@ def time_configs(dev, steps, warmup):
     tb = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     out = {}
     for name, w in WORKLOADS.items():
+        if name in skip:
+            continue
         d = make_inputs(w, which=("x", "w", "dy"))
         E, N, K, M = w.E, w.N, w.K, w.M
         ms = torch.from_numpy(d["m_splits"]).to(dev)
@@ -679,12 +720,10 @@ def time_configs(dev, steps, warmup):
         if w.prequant_x:
             xq = lambda: mxq.requant_colwise(wire["row_data"], wire["row_scale"], ms, out={
                 "col_data": qx["col_data"], "col_scale": qx["col_scale"], "row_scale_swizzled": qx["row_scale"]})
-            xbytes = M * K * (2 + 3 / 32)
         else:
             xq = lambda: mxq.group_quantize(x, ms, out=qx)
-            xbytes = M * K * (4 + 2 / 32)
-        calls = [("x", xq), ("w", lambda: mxq.group_quantize(wt, None, E=E, out=qw)),
-                 ("dy", lambda: mxq.group_quantize(dy, ms, out=qd)),
+        calls = [(x_kernel(w), xq), ("quantize_w", lambda: mxq.group_quantize(wt, None, E=E, out=qw)),
+                 ("quantize_dy", lambda: mxq.group_quantize(dy, ms, out=qd)),
                  ("fprop", lambda: mxq.grouped_gemm_fprop(qx["row_data"], qx["row_scale"], qw["row_data"].view(E, N, K),
                                                           qw["row_scale"], ms, out=y)),
                  ("dgrad", lambda: mxq.grouped_gemm_dgrad(qd["row_data"], qd["row_scale"], qw["col_data"].view(E, N, K),
@@ -710,18 +749,7 @@ def time_configs(dev, steps, warmup):
             wev[i][3].record()
         torch.cuda.synchronize()
         us_warm = {calls[j][0]: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in wev) * 1e3 for j in range(3)}
-        bound = gemm_bound_us(ms.cpu().numpy(), N, K, mx_peak, hbm)
-        flops = 6.0 * M * N * K
-        gemm_us = us["fprop"] + us["dgrad"] + us["wgrad"]
-        qb = {"x": xbytes, "w": E * N * K * (4 + 2 / 32), "dy": M * N * (4 + 2 / 32)}
-        out[name] = {"us": {k: round(v, 1) for k, v in us.items()},
-                     "gemm_tflops": flops / (gemm_us * 1e-6) / 1e12,
-                     "gemm_frac": flops / (gemm_us * 1e-6) / 1e12 / mx_peak,
-                     "gemm_per_expert_bound_us": {k: round(v, 1) for k, v in bound.items()},
-                     "gemm_frac_of_per_expert_bound": sum(bound.values()) / gemm_us,
-                     "us_no_l2_flush": {k: round(v, 1) for k, v in us_warm.items()},
-                     "quant_frac": {k: qb[k] / (us[k] * 1e-6) / 1e9 / hbm for k in qb},
-                     "x_path": "requant" if w.prequant_x else "quantize"}
+        out[name] = config_record(w, ms.cpu().numpy(), us, us_warm, mx_peak, hbm)
         del x, wt, dy, qx, qw, qd, y, dx, dw
         if w.prequant_x:
             del wire
@@ -730,18 +758,20 @@ def time_configs(dev, steps, warmup):
             "peak_tflops": mx_peak, "peak_gbs": hbm, "configs": out}
 
 
-KERNELS = ["requant_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"]
-# NativeStep.run's timing events: 0 step start, (1, 2) requant X, (3, 4) quantize W, 5 forward quantize
-# phase joined = fprop start, 6 fprop end, 7 quantize dY end, 8 dgrad end, 9 wgrad end (= step end)
+# NativeStep.run's timing events: 0 step start, (1, 2) quantize or requant X, (3, 4) quantize W, 5 forward
+# quantize phase joined = fprop start, 6 fprop end, 7 quantize dY end, 8 dgrad end, 9 wgrad end (= step end)
 STEP_EVENTS = 10
-KERNEL_EVENTS = {"requant_x": (1, 2), "quantize_w": (3, 4), "fprop": (5, 6), "quantize_dy": (6, 7),
-                 "dgrad": (7, 8), "wgrad": (8, 9)}
 
 
-def step_event_times(evs):
-    """Mean ms per kernel, of the forward quantize phase (requant X with quantize W) and of the step, over
-    a list of STEP_EVENTS-event steps."""
-    per = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in evs) for k, (a, b) in KERNEL_EVENTS.items()}
+def kernel_events(pre_x: bool) -> dict:
+    return {("requant_x" if pre_x else "quantize_x"): (1, 2), "quantize_w": (3, 4), "fprop": (5, 6),
+            "quantize_dy": (6, 7), "dgrad": (7, 8), "wgrad": (8, 9)}
+
+
+def step_event_times(evs, kev):
+    """Mean ms per kernel (kev: kernel -> (start, end) event), of the forward quantize phase (X with
+    quantize W) and of the step, over a list of STEP_EVENTS-event steps."""
+    per = {k: statistics.mean(e[a].elapsed_time(e[b]) for e in evs) for k, (a, b) in kev.items()}
     per_step = [e[0].elapsed_time(e[STEP_EVENTS - 1]) for e in evs]
     phase = statistics.mean(e[0].elapsed_time(e[5]) for e in evs)
     return per, per_step, phase
@@ -750,7 +780,8 @@ def step_event_times(evs):
 def algorithmic(w):
     M, N, K, E = w.M, w.N, w.K, w.E
     flops = {"fprop": 2.0 * M * N * K, "dgrad": 2.0 * M * N * K, "wgrad": 2.0 * M * N * K}
-    bytes_ = {"requant_x": 2.09375 * M * K, "quantize_w": 4.0625 * E * N * K, "quantize_dy": 4.0625 * M * N}
+    bytes_ = {x_kernel(w): (2.09375 if w.prequant_x else 4.0625) * M * K, "quantize_w": 4.0625 * E * N * K,
+              "quantize_dy": 4.0625 * M * N}
     return flops, bytes_
 
 
@@ -804,7 +835,7 @@ def time_warm(st, steps):
     for i in range(steps):
         st.run(evs[i], concurrent=False)
     torch.cuda.synchronize()
-    return step_event_times(evs)[0]
+    return step_event_times(evs, st.kernel_events)[0]
 
 
 def time_serial(st, steps):
@@ -820,38 +851,59 @@ def time_serial(st, steps):
         st.flush()
         st.run(evs[i], concurrent=False)
     torch.cuda.synchronize()
-    per, per_step, _ = step_event_times(evs)
+    per, per_step, _ = step_event_times(evs, st.kernel_events)
     return per, statistics.mean(per_step)
 
 
-def time_native(st, steps, warmup, sampler):
+def inner_repeat(st, steps, requested):
+    """Passes per timed step: `requested` if > 0, else enough for a timed region of TIMED_REGION_S."""
+    if requested > 0:
+        return requested
+    torch = st.torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        st.flush()
+        st.run()
+    b.record()
+    torch.cuda.synchronize()
+    pass_s = a.elapsed_time(b) * 1e-3 / 3
+    return max(1, int(np.ceil(TIMED_REGION_S / (max(1, steps) * pass_s))))
+
+
+def time_native(st, steps, warmup, sampler, repeat_requested):
+    """K steps of R passes each (R = inner_repeat after the warm-up); every pass is one step of the hot
+    path over the batch, preceded by its L2 flush (outside its event brackets)."""
     torch = st.torch
     for _ in range(warmup):
         st.flush()
         st.run()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(steps)]
+    repeat = inner_repeat(st, steps, repeat_requested)
+    n = steps * repeat
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(STEP_EVENTS)] for _ in range(n)]
     if sampler:
         sampler.start()
         time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for i in range(steps):
+    for i in range(n):
         st.flush()
         st.run(evs[i])
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier()
     clocks = sampler.stop() if sampler else None
-    per_kernel, per_step, phase = step_event_times(evs)
-    return per_step, per_kernel, phase, wall, clocks
+    per_kernel, per_step, phase = step_event_times(evs, st.kernel_events)
+    return per_step, per_kernel, phase, wall, clocks, repeat
 
 
 def time_e2e(st, steps, warmup, d):
     """Through the public API from pinned host memory: every step copies its
-    inputs (wire-format X, its scales, W, dY, m_splits) host -> device, runs
-    the six calls and copies its results (Y, dX, dW) device -> host.
+    inputs (X -- bf16, or the wire format and its scales --, W, dY, m_splits)
+    host -> device, runs the six calls and copies its results (Y, dX, dW)
+    device -> host.
 
     Pipelined: the copies run on their own streams, so step i+1's inputs go
     up and step i-1's results come down while step i's kernels run; inputs
@@ -862,7 +914,7 @@ def time_e2e(st, steps, warmup, d):
     import copy
 
     torch = st.torch
-    names_in, names_out = ("x_row", "x_row_scale", "wt", "dy", "ms"), ("y", "dx", "dw")
+    names_in, names_out = st.e2e_inputs, ("y", "dx", "dw")
     host_in = {k: getattr(st, k).cpu().pin_memory() for k in names_in}
     host_out = {k: torch.empty_like(getattr(st, k), device="cpu").pin_memory() for k in names_out}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -925,68 +977,93 @@ def time_e2e(st, steps, warmup, d):
     return ms_pipe, ms_serial, h2d, d2h
 
 
+def config_record(w, ms, us, us_warm, mx_peak, hbm):
+    """One workload's row of the five-workload table: per-kernel times (us), GEMM TFLOP/s and quantize GB/s
+    with their roofline fractions."""
+    E, N, K, M = w.E, w.N, w.K, w.M
+    bound = gemm_bound_us(ms, N, K, mx_peak, hbm)
+    flops = 6.0 * M * N * K
+    gemm_us = us["fprop"] + us["dgrad"] + us["wgrad"]
+    _, qb = algorithmic(w)
+    return {"us": {k: round(v, 1) for k, v in us.items()},
+            "gemm_tflops": flops / (gemm_us * 1e-6) / 1e12,
+            "gemm_frac": flops / (gemm_us * 1e-6) / 1e12 / mx_peak,
+            "gemm_per_expert_bound_us": {k: round(v, 1) for k, v in bound.items()},
+            "gemm_frac_of_per_expert_bound": sum(bound.values()) / gemm_us,
+            "us_no_l2_flush": {k: round(v, 1) for k, v in us_warm.items()},
+            "quant_gbs": {k: qb[k] / (us[k] * 1e-6) / 1e9 for k in qb},
+            "quant_frac": {k: qb[k] / (us[k] * 1e-6) / 1e9 / hbm for k in qb},
+            "x_path": "requant" if w.prequant_x else "quantize"}
+
+
 # ------------------------------------------------------------- CPU oracle
 class OracleSample:
-    """The CPU oracle on a bounded sample of one step, scaled to a full step.
+    """The CPU oracle on a bounded fraction f of one step's GEMM work.
 
-    Sample: quantize/requant on a 1/32 row slice of X and dY and of W's rows;
-    each GEMM on `entries` output entries, each a full-length dot product.
-    The sampled rows all belong to one expert (so only that expert's weights
-    are needed); per-entry cost does not depend on which expert it is."""
+    The GEMMs: f*M*N fprop entries (full-length dot products over K), f*M*K
+    dgrad entries (over N) and f*M*N*K/r wgrad entries, each reducing over r
+    sampled tokens -- f of each GEMM's 2*M*N*K flops. The quantizations run on
+    r rows of X and dY and on f of W's rows, rounded up to whole 128-row
+    blocks (at least f of that work). The r sampled rows are treated as one
+    expert's (so only one expert's weights are needed); the cost per entry does
+    not depend on which expert it is. f * step flops / its measured time is
+    therefore a lower bound of the oracle's rate in the step's metric."""
 
-    def __init__(self, w, d, frac_rows=1 / 32, entries=1 << 18):
+    def __init__(self, w, d, frac):
         import oracle as orc
 
         self.orc, self.w, self.d = orc, w, d
         M, N, K, E = w.M, w.N, w.K, w.E
-        self.frac = frac_rows
-        self.rows = int(M * frac_rows) // 128 * 128
-        self.wrows = int(E * N * frac_rows) // 128 * 128
+        self.frac = frac
+        self.rows = max(128, int(round(M * frac / 128)) * 128)
+        self.wrows = max(128, int(round(E * N * frac / 128)) * 128)
         rows = self.rows
         self.wire = orc.group_quantize(d["x"][:rows], [rows], rowwise=True, colwise=False)
         self.cx = orc.group_quantize(d["x"][:rows], [rows])
         self.cdy = orc.group_quantize(d["dy"][:rows], [rows])
         self.cw = orc.quantize_weights(d["w"][:1])
         rng = np.random.default_rng(0)
-        self.r = rng.integers(0, rows, entries)
-        self.cn = rng.integers(0, N, entries)
-        self.ck = rng.integers(0, K, entries)
-        self.n_w = max(16, entries // 8)
-        self.wn = rng.integers(0, N, self.n_w)
-        self.wk = rng.integers(0, K, self.n_w)
+        self.nf, self.nd = int(round(frac * M * N)), int(round(frac * M * K))
+        self.nw = int(round(frac * M * N * K / rows))
+        self.fr, self.fc = rng.integers(0, rows, self.nf), rng.integers(0, N, self.nf)
+        self.dr, self.dc = rng.integers(0, rows, self.nd), rng.integers(0, K, self.nd)
+        self.wn, self.wk = rng.integers(0, N, self.nw), rng.integers(0, K, self.nw)
         self.cores = orc.num_threads()
-        self.sample = (f"quantize/requant on {rows}/{M} activation rows and {self.wrows}/{E * N} weight rows; "
-                       f"{entries} fprop and dgrad entries and {self.n_w} wgrad entries (full-length dot "
-                       f"products); scaled to one full step")
+        first = "requant" if w.prequant_x else "quantize"
+        self.sample = (f"f = {frac:.3g} of one step's GEMM work: {self.nf} fprop and {self.nd} dgrad entries "
+                       f"(full-length dot products), {self.nw} wgrad entries over {rows} tokens; {first} X and "
+                       f"quantize dY on {rows} rows, quantize W on {self.wrows}/{E * N} rows")
 
     def run(self):
+        """Seconds per part of the sampled step."""
         orc, w, d = self.orc, self.w, self.d
-        M, N, K, E = w.M, w.N, w.K, w.E
+        N, K = w.N, w.K
         rows, t = self.rows, {}
         t1 = time.perf_counter()
-        orc.requant_colwise(self.wire["row_q"], self.wire["row_s"], [rows], swizzled=True)
-        t["requant_x"] = (time.perf_counter() - t1) * M / rows
+        if w.prequant_x:
+            orc.requant_colwise(self.wire["row_q"], self.wire["row_s"], [rows], swizzled=True)
+        else:
+            orc.group_quantize(d["x"][:rows], [rows], swizzled=True)
+        t[x_kernel(w)] = time.perf_counter() - t1
         t1 = time.perf_counter()
-        orc.group_quantize(d["w"].reshape(E * N, K)[:self.wrows], [self.wrows], swizzled=True)
-        t["quantize_w"] = (time.perf_counter() - t1) * (E * N) / self.wrows
+        orc.group_quantize(d["w"].reshape(-1, K)[:self.wrows], [self.wrows], swizzled=True)
+        t["quantize_w"] = time.perf_counter() - t1
         t1 = time.perf_counter()
         orc.group_quantize(d["dy"][:rows], [rows], swizzled=True)
-        t["quantize_dy"] = (time.perf_counter() - t1) * M / rows
+        t["quantize_dy"] = time.perf_counter() - t1
         cx, cdy, cw = self.cx, self.cdy, self.cw
         t1 = time.perf_counter()
         orc.fprop_entries(cx["row_q"], cx["row_s"], cw["row_q"].reshape(1, N, K), cw["row_s"], [rows],
-                          self.r, self.cn)
-        t["fprop"] = (time.perf_counter() - t1) * (M * N) / self.r.size
+                          self.fr, self.fc)
+        t["fprop"] = time.perf_counter() - t1
         t1 = time.perf_counter()
         orc.dgrad_entries(cdy["row_q"], cdy["row_s"], cw["col_q"].reshape(1, N, K), cw["col_s"], [rows],
-                          self.r, self.ck)
-        t["dgrad"] = (time.perf_counter() - t1) * (M * K) / self.r.size
+                          self.dr, self.dc)
+        t["dgrad"] = time.perf_counter() - t1
         t1 = time.perf_counter()
         orc.wgrad_entries(cdy["col_q"], cdy["col_s"], cx["col_q"], cx["col_s"], [rows],
-                          np.zeros(self.n_w, np.int64), self.wn, self.wk)
-        # a sampled wgrad entry reduces over `rows` tokens, a full-size one
-        # over m_e = M/E tokens on average
-        t["wgrad"] = (time.perf_counter() - t1) * (E * N * K) / self.n_w * (M / E) / rows
+                          np.zeros(self.nw, np.int64), self.wn, self.wk)
+        t["wgrad"] = time.perf_counter() - t1
         return t
 
 
@@ -1019,25 +1096,35 @@ def aggregate(per_rank_units: float, world: int, t_max_s: float) -> float:
     return per_rank_units * world / t_max_s
 
 
+REFERENCE_FRAC = 1 / 8192   # fraction of a step's GEMM work the reference arm's oracle runs per timed step
+CPU_BASELINE_FRAC = 1 / 2048  # fraction in the GPU line's cpu_baseline (10-30 s of CPU work)
+
+
 def reference_arm(args, rank, world):
+    """The CPU oracle as the reference implementation: each timed step is the oracle on a fixed
+    fraction f of the workload's step; value = f * step flops / measured step time."""
     if rank != 0:
         return
     w, d = make_host_workload()
     flops, _ = algorithmic(w)
     step_flops = sum(flops.values())
-    sample = OracleSample(w, d, entries=1 << 16)
+    sample = OracleSample(w, d, REFERENCE_FRAC)
     for _ in range(args.warmup):
         sample.run()
+    t0 = time.perf_counter()
     times = [sum(sample.run().values()) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
     ms = statistics.mean(times) * 1e3
-    value = step_flops / (ms * 1e-3) / 1e12
+    value = sample.frac * step_flops / (ms * 1e-3) / 1e12
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": workload_config(w, d, world),
+            "step_fraction": sample.frac,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
                              "sample": sample.sample},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s_timed_region": wall}
     print(json.dumps(line), flush=True)
 
 
@@ -1106,13 +1193,16 @@ def main():
         if rank == 0:
             print(json.dumps(r), flush=True)
         return
+    bf16_peak, hbm_peak, src = peaks()
+    mx_peak = bf16_peak * MXFP8_OVER_BF16
     w, d = make_host_workload()
     st = NativeStep(w, d, dev)
     flops, bytes_ = algorithmic(w)
     step_flops = sum(flops.values())
+    warmup = max(3, args.warmup)
 
     sampler = ClockSampler(local if world > 1 else 0) if rank == 0 else None
-    per_step, per_kernel, phase_ms, wall, clocks = time_native(st, args.steps, max(3, args.warmup), sampler)
+    per_step, per_kernel, phase_ms, wall, clocks, repeat = time_native(st, args.steps, warmup, sampler, args.repeat)
     ms_step = statistics.mean(per_step)
     ms_step_max = max_over_ranks(ms_step)
     value = aggregate(step_flops, world, ms_step_max * 1e-3) / 1e12
@@ -1121,8 +1211,11 @@ def main():
     gemm_tflops = step_flops / (gemm_ms * 1e-3) / 1e12
     serial_kernels, serial_ms = time_serial(st, max(10, args.steps // 2))
     quant_gbs = {k: bytes_[k] / (serial_kernels[k] * 1e-3) / 1e9 for k in bytes_}
-    phase_gbs = (bytes_["requant_x"] + bytes_["quantize_w"]) / (phase_ms * 1e-3) / 1e9
+    xk = x_kernel(w)
+    phase_gbs = (bytes_[xk] + bytes_["quantize_w"]) / (phase_ms * 1e-3) / 1e9
     warm = time_warm(st, max(5, args.steps // 5))
+    headline_record = config_record(w, d["m_splits"], {k: v * 1e3 for k, v in serial_kernels.items()},
+                                    {k: warm[k] * 1e3 for k in bytes_}, mx_peak, hbm_peak)
 
     e2e = None
     if not args.no_e2e:
@@ -1135,20 +1228,21 @@ def main():
                         "outputs double-buffered",
                "serial_ms_per_step": ms_serial,
                "serial_value": aggregate(step_flops, world, ms_serial * 1e-3) / 1e12}
+    del st
+    torch.cuda.empty_cache()
 
-    mlp = None
-    if not args.no_mlp and rank == 0:
-        del st
-        torch.cuda.empty_cache()
-        try:  # a secondary leg: a failure is reported in the line instead of losing the line
-            mlp = time_mlp(dev)
-        except Exception as ex:  # noqa: BLE001
-            mlp = {"error": f"{type(ex).__name__}: {ex}"}
-    if rank != 0:
-        return
-    bf16_peak, hbm_peak, src = peaks()
-    mx_peak = bf16_peak * MXFP8_OVER_BF16
-    traffic = None
+    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": mx_peak, "unit": "TFLOP/s",
+                "frac": gemm_tflops / mx_peak, "traffic": None,
+                "kernel": "grouped_gemm_kernel (fprop+dgrad+wgrad launches of one step)",
+                "peak_source": f"{src} bf16 burst {bf16_peak} TFLOP/s x {MXFP8_OVER_BF16} (nominal MXFP8/BF16)"}
+    sustained = None
+    ppath = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(ppath):
+        with open(ppath) as f:
+            sustained = json.load(f).get("bf16_tflops_sustained")
+    if sustained:
+        roofline["peak_sustained"] = sustained * MXFP8_OVER_BF16
+        roofline["frac_of_sustained"] = gemm_tflops / (sustained * MXFP8_OVER_BF16)
     tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
     if os.path.exists(tpath):
         from moe_expert_grouped_group_gb300.build import source_stamp
@@ -1156,43 +1250,61 @@ def main():
         with open(tpath) as f:
             tj = json.load(f)
         if tj.get("source_stamp") == source_stamp() and tj.get("workload") == WORKLOAD:
-            traffic = tj.get("dram_bytes_per_launch")
-    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": mx_peak, "unit": "TFLOP/s",
-                "frac": gemm_tflops / mx_peak, "traffic": traffic,
-                "kernel": "grouped_gemm_kernel (fprop+dgrad+wgrad launches of one step)",
-                "peak_source": f"{src} bf16 burst {bf16_peak} TFLOP/s x {MXFP8_OVER_BF16} (nominal MXFP8/BF16)"}
-    try:
-        stream_tflops = time_mma_stream()
-        roofline["mma_stream_tflops"] = stream_tflops
-        roofline["frac_of_mma_stream"] = gemm_tflops / stream_tflops
-    except Exception as ex:  # noqa: BLE001
-        roofline["mma_stream_tflops"] = {"error": f"{type(ex).__name__}: {ex}"}
+            roofline["traffic"] = tj.get("dram_bytes_per_launch")
+            roofline["traffic_note"] = tj.get("note")
+    if rank == 0:
+        try:
+            stream_tflops = time_mma_stream()
+            roofline["mma_stream_tflops"] = stream_tflops
+            roofline["frac_of_mma_stream"] = gemm_tflops / stream_tflops
+        except Exception as ex:  # noqa: BLE001
+            roofline["mma_stream_tflops"] = {"error": f"{type(ex).__name__}: {ex}"}
     bound = gemm_bound_us(d["m_splits"], w.N, w.K, mx_peak, hbm_peak)
     roofline["per_expert_bound_us"] = bound
     roofline["frac_of_per_expert_bound"] = sum(bound.values()) / (gemm_ms * 1e3)
+
+    configs = None
+    mlp = None
+    if rank == 0:
+        # secondary legs: a failure is reported in the line instead of losing the line
+        if not args.no_configs:
+            try:
+                configs = time_configs(dev, min(10, max(1, args.steps)), 2, skip=(WORKLOAD,))
+                configs["configs"][WORKLOAD] = dict(headline_record, note="from the headline run's serial pass")
+            except Exception as ex:  # noqa: BLE001
+                configs = {"error": f"{type(ex).__name__}: {ex}"}
+            torch.cuda.empty_cache()
+        if not args.no_mlp:
+            try:
+                mlp = time_mlp(dev)
+            except Exception as ex:  # noqa: BLE001
+                mlp = {"error": f"{type(ex).__name__}: {ex}"}
+            torch.cuda.empty_cache()
+    if rank != 0:
+        return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         t0 = time.perf_counter()
         try:
-            sample = OracleSample(w, d, frac_rows=1 / 8, entries=1 << 21)
+            sample = OracleSample(w, d, CPU_BASELINE_FRAC)
             t = sample.run()
-            cpu_ms = sum(t.values()) * 1e3
-            cpu = {"value": step_flops / (cpu_ms * 1e-3) / 1e12, "unit": UNIT, "cores": sample.cores,
-                   "kind": "oracle", "sample": sample.sample, "ms_per_step_extrapolated": cpu_ms,
-                   "per_kernel_ms_extrapolated": {k: v * 1e3 for k, v in t.items()},
-                   "wall_s": time.perf_counter() - t0}
+            cpu_s = sum(t.values())
+            cpu = {"value": sample.frac * step_flops / cpu_s / 1e12, "unit": UNIT, "cores": sample.cores,
+                   "kind": "oracle", "sample": sample.sample, "step_fraction": sample.frac,
+                   "sample_s": cpu_s, "per_part_s": t, "wall_s": time.perf_counter() - t0}
         except Exception as ex:  # noqa: BLE001
             cpu = {"error": f"{type(ex).__name__}: {ex}", "kind": "oracle"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms_step_max, "ms_per_step_median": statistics.median(per_step),
+        "warmup": warmup, "ms_per_step": ms_step_max, "ms_per_step_median": statistics.median(per_step),
+        "inner_repeat": repeat, "timed_passes": args.steps * repeat,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8_e4m3 (fp32 accumulate)", "data": "synthetic",
-        "config": {**workload_config(w, d, world),
-                   "streams": "requant X on a side stream concurrent with quantize W; the rest in order after the "
-                              "join",
-                   "l2": "256 MiB buffer written before every timed step (outside the event brackets)"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * args.steps,
+        "config": workload_config(w, d, world),
+        "streams": "the quantization of X on a side stream concurrent with quantize W; the rest in order after "
+                   "the join",
+        "timing": f"{args.steps} timed steps of {repeat} back-to-back passes each; ms_per_step is the mean pass",
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 6 * args.steps * repeat,
         "clocks": clocks,
         "kernels_ms": per_kernel, "gemm_tflops": gemm_tflops,
         "fwd_quantize_phase_ms": phase_ms, "fwd_quantize_phase_gbs": phase_gbs,
@@ -1201,10 +1313,11 @@ def main():
         "group_quantize_gbs": quant_gbs, "hbm_peak_gbs": hbm_peak,
         "group_quantize_frac": {k: v / hbm_peak for k, v in quant_gbs.items()},
         "group_quantize_note": "each quantize kernel timed alone (serial pass, L2 flushed before each step); in "
-                               "the timed step requant X and quantize W overlap, and kernels_ms holds their "
+                               "the timed step the quantizations of X and W overlap, and kernels_ms holds their "
                                "concurrent durations",
         "kernels_ms_no_l2_flush": warm,
         "wall_s_timed_region": wall,
+        "configs": configs,
         "mlp_step": mlp,
     }
     print(json.dumps(line), flush=True)

@@ -35,15 +35,16 @@ class _FakeEvent:
 
 
 def test_step_event_layout():
-    # one step: requant X 0.1-0.3 on the side stream and quantize W 0.0-0.5 on the main stream, joined at
+    # one step: quantize X 0.1-0.3 on the side stream and quantize W 0.0-0.5 on the main stream, joined at
     # 0.6, then fprop / quantize dY / dgrad / wgrad ending at 1.0 / 1.3 / 1.8 / 2.4
     t = [0.0, 0.1, 0.3, 0.0, 0.5, 0.6, 1.0, 1.3, 1.8, 2.4]
     assert len(t) == bench.STEP_EVENTS
-    per, per_step, phase = bench.step_event_times([[_FakeEvent(v) for v in t]])
-    assert per == pytest.approx({"requant_x": 0.2, "quantize_w": 0.5, "fprop": 0.4, "quantize_dy": 0.3,
-                                 "dgrad": 0.5, "wgrad": 0.6})
-    assert per_step == pytest.approx([2.4]) and phase == pytest.approx(0.6)
-    assert set(per) == set(bench.KERNELS)
+    for pre_x, xk in ((False, "quantize_x"), (True, "requant_x")):
+        kev = bench.kernel_events(pre_x)
+        per, per_step, phase = bench.step_event_times([[_FakeEvent(v) for v in t]], kev)
+        assert per == pytest.approx({xk: 0.2, "quantize_w": 0.5, "fprop": 0.4, "quantize_dy": 0.3,
+                                     "dgrad": 0.5, "wgrad": 0.6})
+        assert per_step == pytest.approx([2.4]) and phase == pytest.approx(0.6)
 
 
 def test_both_arms_name_the_same_workload():
@@ -51,8 +52,42 @@ def test_both_arms_name_the_same_workload():
 
     import numpy as np
 
-    w = SimpleNamespace(E=8, K=2048, N=4096, M=16384)
-    d = {"m_splits": np.full(8, 2048, np.int64)}
+    w = SimpleNamespace(E=128, K=7168, N=2048, M=131072, prequant_x=False)
+    d = {"m_splits": np.full(128, 1024, np.int64)}
     c = bench.workload_config(w, d, 1)
-    assert c["workload"] == bench.WORKLOAD and c["m_splits"] == [2048] * 8 and c["parallelism"] == "replicas x1"
-    assert (c["experts"], c["hidden"], c["out"], c["tokens"]) == (8, 2048, 4096, 16384)
+    assert c["workload"] == bench.WORKLOAD and c["m_splits"] == [1024] * 128 and c["parallelism"] == "replicas x1"
+    assert (c["experts"], c["hidden"], c["out"], c["tokens"]) == (128, 7168, 2048, 131072)
+    assert c["step"].startswith("quantize X (row+col)")
+
+
+def test_headline_is_the_largest_workload():
+    from synth import WORKLOADS
+
+    w = WORKLOADS[bench.WORKLOAD]
+    assert all(6 * v.M * v.N * v.K <= 6 * w.M * w.N * w.K for v in WORKLOADS.values())
+
+
+def test_oracle_sample_is_the_stated_fraction_of_the_gemm_work():
+    """The reference arm's step: f of each GEMM's flops, so f * step flops / time is its rate."""
+    from types import SimpleNamespace
+
+    import numpy as np
+
+    w = SimpleNamespace(E=2, K=256, N=256, M=1024, prequant_x=False)
+    rng = np.random.default_rng(0)
+    bits = lambda *sh: (rng.standard_normal(sh).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    d = {"x": bits(1024, 256), "dy": bits(1024, 256), "w": bits(2, 256, 256)}
+    f = 1 / 4
+    s = bench.OracleSample(w, d, f)
+    M, N, K = w.M, w.N, w.K
+    gemm_flops = 2 * s.nf * K + 2 * s.nd * N + 2 * s.nw * s.rows
+    assert gemm_flops == pytest.approx(f * 6 * M * N * K, rel=1e-9)
+    t = s.run()
+    assert set(t) == {"quantize_x", "quantize_w", "quantize_dy", "fprop", "dgrad", "wgrad"}
+
+
+def test_inner_repeat_reaches_the_timed_region():
+    class _St:
+        pass
+
+    assert bench.inner_repeat(_St(), 20, 7) == 7

@@ -1,7 +1,8 @@
 """The steps bench.py times, run through the C ABI: the concurrent schedule
 of each (the forward's quantizations on two streams) gives outputs bit-
-identical to the same calls in order on one stream, for the 8-expert
-grouped-linear training step and the 64-expert SwiGLU MLP step. The calls
+identical to the same calls in order on one stream, for the grouped-linear
+training step of the headline workload (128 experts, hidden 7168) and the
+64-expert SwiGLU MLP step. The calls
 themselves are checked against the oracle by the other GPU tests; this pins
 the streams and events of the timed steps."""
 import numpy as np
@@ -35,7 +36,7 @@ def test_grouped_linear_step_concurrent_equals_serial():
 
     def outs():
         o = {"y": st.y, "dx": st.dx, "dw": st.dw}
-        o.update({f"rq.{k}": v for k, v in st.rq.items()})
+        o.update({f"qx.{k}": v for k, v in st.qx.items()})
         o.update({f"qw.{k}": v for k, v in st.qw.items()})
         o.update({f"qdy.{k}": v for k, v in st.qdy.items()})
         return o
