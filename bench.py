@@ -65,6 +65,9 @@ def parse():
     p.add_argument("--repeat", type=int, default=0,
                    help="passes per timed step (0: enough for a timed region of at least TIMED_REGION_S)")
     p.add_argument("--no-configs", action="store_true", help="skip the other workloads' grouped-linear steps")
+    p.add_argument("--workload", default=None,
+                   help="run the timed step on this workload instead of the headline one (a small footprint for "
+                        "profilers)")
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -143,10 +146,10 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- workload
-def make_host_workload():
+def make_host_workload(name=None):
     from synth import WORKLOADS, make_inputs
 
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[name or WORKLOAD]
     d = make_inputs(w, which=("x", "w", "dy"))
     return w, d
 
@@ -159,7 +162,7 @@ def workload_config(w, d, world):
     """The workload both arms run, as named in their JSON lines."""
     first = ("requant X (rowwise wire format -> colwise copy + swizzled rowwise scales)" if w.prequant_x
              else "quantize X (row+col)")
-    return {"workload": WORKLOAD, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
+    return {"workload": w.name, "experts": w.E, "hidden": w.K, "out": w.N, "tokens": w.M,
             "m_splits": [int(v) for v in d["m_splits"]],
             "step": f"{first} + quantize W (row+col), fprop, quantize dY (row+col), dgrad, wgrad (fp32 dW)",
             "parallelism": f"replicas x{world}",
@@ -1195,7 +1198,7 @@ def main():
         return
     bf16_peak, hbm_peak, src = peaks()
     mx_peak = bf16_peak * MXFP8_OVER_BF16
-    w, d = make_host_workload()
+    w, d = make_host_workload(args.workload)
     st = NativeStep(w, d, dev)
     flops, bytes_ = algorithmic(w)
     step_flops = sum(flops.values())
@@ -1249,7 +1252,7 @@ def main():
 
         with open(tpath) as f:
             tj = json.load(f)
-        if tj.get("source_stamp") == source_stamp() and tj.get("workload") == WORKLOAD:
+        if tj.get("source_stamp") == source_stamp() and tj.get("workload") == w.name:
             roofline["traffic"] = tj.get("dram_bytes_per_launch")
             roofline["traffic_note"] = tj.get("note")
     if rank == 0:
@@ -1269,8 +1272,8 @@ def main():
         # secondary legs: a failure is reported in the line instead of losing the line
         if not args.no_configs:
             try:
-                configs = time_configs(dev, min(10, max(1, args.steps)), 2, skip=(WORKLOAD,))
-                configs["configs"][WORKLOAD] = dict(headline_record, note="from the headline run's serial pass")
+                configs = time_configs(dev, min(10, max(1, args.steps)), 2, skip=(w.name,))
+                configs["configs"][w.name] = dict(headline_record, note="from the headline run's serial pass")
             except Exception as ex:  # noqa: BLE001
                 configs = {"error": f"{type(ex).__name__}: {ex}"}
             torch.cuda.empty_cache()

@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -924,6 +925,507 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ============================================================ two-SM tiles
+// The plain fprop / dgrad / wgrad (128-aligned experts) run on CTA pairs:
+// a cluster of two CTAs on two SMs computes one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 32). Each CTA stages its own
+// 128 rows of A and its own 128-wide half of B (plain TMA loads into its own
+// shared memory, completing on the leader CTA's stage barrier), so a
+// 32 KB stage covers as many MMA cycles as a 48 KB stage of the one-SM tile
+// and the ring is six stages deep. The leader (cluster rank 0) issues the
+// scale copies and MMAs for both SMs; every CTA holds the accumulator of its
+// own 128 rows (all 256 columns) in its TMEM and drains it with its own eight
+// epilogue warps. Semantics used (PTX ISA, tcgen05 with .cta_group::2):
+// one warp in each CTA allocates the 512 TMEM columns collectively (both
+// get the same address); a tcgen05.cp issued by the leader copies each CTA's
+// shared memory into that CTA's TMEM at the same addresses; each CTA's TMEM
+// holds the scale factors of its own 128 A rows and of all 256 B columns;
+// tcgen05.commit with .multicast::cluster arrives on the barrier at the same
+// offset in both CTAs.
+//
+// Row tiles of fprop / dgrad pair 256 rows of one expert (both halves use
+// the same expert's weights); when an expert holds an odd number of 128-row
+// blocks, its last pair tile's second CTA recomputes the first CTA's rows and
+// does not store them. wgrad tiles pair 256 rows of N with 256 columns of K
+// of one expert.
+namespace pair {
+
+constexpr int PSTAGES = 6;
+constexpr int PSTAGE_BYTES = 32768;               // A 16 KB + B half 16 KB
+constexpr int PSF_BYTES = 1536;                   // scale atoms: A (512), B both halves (2 x 512)
+constexpr uint32_t PTX_CTA = PSTAGE_BYTES + PSF_BYTES;
+constexpr int PSF_REGION = PSTAGES * PSTAGE_BYTES;
+constexpr int PBAR_REGION = PSF_REGION + PSTAGES * PSF_BYTES;
+constexpr int PEPI_REGION = (PBAR_REGION + 256 + 511) / 512 * 512;
+constexpr int PTABLE_REGION = PEPI_REGION + EPI_WARPS * EPI_STAGE_BYTES;
+constexpr int MAX_EXPERTS = 512;
+__host__ __device__ constexpr int smem_bytes(int E) { return 1024 + PTABLE_REGION + 8 * (E + 1) + 4 * (E + 1); }
+static_assert(smem_bytes(MAX_EXPERTS) <= 232448, "shared memory over the per-block limit");
+static_assert(PEPI_REGION % 512 == 0, "the 64-byte swizzle of the staging boxes repeats every 512 bytes");
+
+__device__ __forceinline__ uint32_t cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of the variable at shared::cta address `a` in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+// Arrive on a barrier of the other CTA without a cluster-scope release: the callers only need
+// the arrive to follow their completed tcgen05.ld (tcgen05.wait::ld), which it does in program
+// order. A release at cluster scope costs about 1.5k cycles here, a relaxed arrive about 65.
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// TMA tile load into this CTA's shared memory, completing on the leader's barrier
+__device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* map, uint32_t lead_bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+        "%4}], [%2];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(lead_bar), "r"(x), "r"(y)
+        : "memory");
+}
+// Non-blocking test of two barrier phases at once: both test_waits issue before either result is
+// used, so a pair of ready stages costs the issuing thread one barrier latency, not two.
+__device__ __forceinline__ bool mbar_test2(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+        "and.pred p, p, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(a), "r"(pa), "r"(b), "r"(pb)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint32_t idesc_pair(uint32_t a_mn, uint32_t b_mn, uint32_t sf_id) {
+    return (sf_id << 4) | (a_mn << 15) | (b_mn << 16) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(256 >> 4) << 24) | (sf_id << 29);
+}
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(id), "r"(accum), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+__device__ __forceinline__ void cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// arrive on the barrier at this offset in both CTAs once the leader's prior tcgen05 work completes
+__device__ __forceinline__ void commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"((uint16_t)3)
+                 : "memory");
+}
+
+// One pair tile as seen by CTA `rank`.
+struct PTile {
+    bool valid;
+    int e;
+    int64_t off, me;
+    int nk;           // 128-deep K blocks
+    int64_t a0;       // fprop/dgrad: this CTA's first A (token) row; wgrad: its first N row
+    int64_t out_row;  // first output row of this CTA (dW: e*N + N row)
+    int64_t c0;       // first output column of the tile (256 wide)
+    bool store;       // this CTA writes its rows (false: the duplicate half of an odd row block)
+};
+
+struct PSched {
+    int mode;
+    int64_t M, N, K;
+    int E;
+    const int64_t* off;   // token offsets (E+1)
+    const int32_t* aux;   // fprop/dgrad: pair row-tile offsets (E+1); wgrad: experts heaviest first (E)
+    int64_t tiles_n, total;
+    uint32_t rank;
+
+    __device__ int64_t pick(int64_t i, int c, int nc) const {
+        const int64_t base = i * nc;
+        return (i & 1) ? base + (nc - 1 - c) : base + c;
+    }
+    __device__ PTile get(int64_t t) const {
+        PTile T;
+        T.valid = t < total;
+        if (!T.valid) return T;
+        if (mode != kWgrad) {
+            const int64_t prt = t / tiles_n, nt = t % tiles_n;
+            int lo = 0, hi = E - 1;  // first e with aux[e + 1] > prt
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (aux[mid + 1] > prt) hi = mid;
+                else lo = mid + 1;
+            }
+            T.e = lo;
+            T.off = off[lo];
+            T.me = off[lo + 1] - T.off;
+            const int64_t r0 = T.off + 256 * (prt - aux[lo]);
+            const int64_t left = T.off + T.me - r0;  // rows of the expert from r0 on (128 or >= 256)
+            T.store = left > 128 * (int64_t)rank;
+            T.a0 = T.store ? r0 + 128 * rank : r0;
+            T.out_row = T.a0;
+            T.c0 = nt * 256;
+            T.nk = (int)((mode == kDgrad ? N : K) / BK);
+        } else {
+            const int64_t ei = t / tiles_n, r = t % tiles_n;
+            const int64_t kt = K / 256;
+            T.e = aux[ei];
+            T.off = off[T.e];
+            T.me = off[T.e + 1] - T.off;
+            T.a0 = (r / kt) * 256 + 128 * rank;
+            T.out_row = (int64_t)T.e * N + T.a0;
+            T.c0 = (r % kt) * 256;
+            T.nk = (int)(T.me / BK);
+            T.store = true;
+        }
+        return T;
+    }
+};
+
+template <int kMode>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                             const __grid_constant__ CUtensorMap tmOut, Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_align<1024>(smem_raw);
+    int64_t* s_off = reinterpret_cast<int64_t*>(smem + PTABLE_REGION);
+    int32_t* s_aux = reinterpret_cast<int32_t*>(s_off + p.E + 1);
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cta_rank();
+    const bool leader = rank == 0;
+    // every CTA validates the same m_splits; a bad split stops both CTAs of every pair before any
+    // cluster-wide step
+    const int bad = load_offsets(p.m_splits, p.E, p.M, s_off);
+    if (bad) {
+        report_status(p.status, bad);
+        return;
+    }
+    if (kMode == kWgrad) {
+        for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+            const int64_t me = s_off[e + 1] - s_off[e];
+            int rk = 0;
+            for (int f = 0; f < p.E; ++f) {
+                const int64_t mf = s_off[f + 1] - s_off[f];
+                rk += (mf > me) || (mf == me && f < e);
+            }
+            s_aux[rk] = e;
+        }
+    } else if (threadIdx.x < 32) {
+        // exclusive prefix of ceil(m_e / 256), the pair row tiles of each expert
+        const int per = (p.E + 31) / 32;
+        const int lo = min(p.E, lane * per), hi = min(p.E, lo + per);
+        int32_t local = 0;
+        for (int e = lo; e < hi; ++e) local += (int32_t)((s_off[e + 1] - s_off[e] + 255) / 256);
+        int32_t incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int32_t run = incl - local;
+        for (int e = lo; e < hi; ++e) {
+            s_aux[e] = run;
+            run += (int32_t)((s_off[e + 1] - s_off[e] + 255) / 256);
+        }
+        if (lane == 31) s_aux[p.E] = incl;
+    }
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PBAR_REGION);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + PSTAGES);
+    const uint32_t acc_full = smem_u32(bars + 2 * PSTAGES), acc_empty = smem_u32(bars + 2 * PSTAGES + 1);
+    volatile int* abort_flag = &s_abort;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int st = 0; st < PSTAGES; ++st) {
+            mbar_init(full0 + 8 * st, 1);
+            mbar_init(empty0 + 8 * st, 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 2 * EPI_WARPS);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmB) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmSA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmSB) : "memory");
+        if (p.tma_store) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmOut) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any load completes on the leader's
+    fence_after();
+    const uint32_t tmem = s_tmem;
+
+    PSched S;
+    S.mode = kMode; S.M = p.M; S.N = p.N; S.K = p.K; S.E = p.E; S.off = s_off; S.aux = s_aux; S.rank = rank;
+    if (kMode == kFprop) { S.tiles_n = p.N / 256; S.total = (int64_t)s_aux[p.E] * S.tiles_n; }
+    else if (kMode == kDgrad) { S.tiles_n = p.K / 256; S.total = (int64_t)s_aux[p.E] * S.tiles_n; }
+    else { S.tiles_n = (p.N / 256) * (p.K / 256); S.total = (int64_t)p.E * S.tiles_n; }
+    const int ncl = gridDim.x / 2, cl = blockIdx.x / 2;
+    const uint32_t a_mn = (kMode == kWgrad) ? 1u : 0u;
+    const uint32_t b_mn = (kMode == kFprop) ? 0u : 1u;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t i = 0;; ++i) {
+                const PTile T = S.get(S.pick(i, cl, ncl));
+                if (!T.valid) break;
+                int ax, ay, bx, by, adx, ady, bdx, bdy;
+                int sa, sb0, sb1;  // scale atom rows (512 B each) of K block 0; +1 per block
+                if (kMode == kFprop) {
+                    const int64_t kbs = p.K / BK, wrow = (int64_t)T.e * p.N + T.c0;
+                    ax = 0; ay = (int)T.a0; adx = BK; ady = 0;
+                    bx = 0; by = (int)(wrow + 128 * rank); bdx = BK; bdy = 0;
+                    sa = (int)((T.a0 / 128) * kbs);
+                    sb0 = (int)((wrow / 128) * kbs);
+                    sb1 = sb0 + (int)kbs;
+                } else if (kMode == kDgrad) {
+                    const int64_t kbs = p.N / BK;
+                    const int64_t wb = (int64_t)T.e * (p.K / 128) * kbs;  // expert e's colwise atoms
+                    ax = 0; ay = (int)T.a0; adx = BK; ady = 0;
+                    bx = (int)(T.c0 + 128 * rank); by = (int)((int64_t)T.e * p.N); bdx = 0; bdy = BK;
+                    sa = (int)((T.a0 / 128) * kbs);
+                    sb0 = (int)(wb + (T.c0 / 128) * kbs);
+                    sb1 = sb0 + (int)kbs;
+                } else {
+                    const int64_t kbs = T.me / BK;
+                    const int64_t ab = (p.N / 128) * (T.off / 128), bb = (p.K / 128) * (T.off / 128);
+                    ax = (int)T.a0; ay = (int)T.off; adx = 0; ady = BK;
+                    bx = (int)(T.c0 + 128 * rank); by = (int)T.off; bdx = 0; bdy = BK;
+                    sa = (int)(ab + (T.a0 / 128) * kbs);
+                    sb0 = (int)(bb + (T.c0 / 128) * kbs);
+                    sb1 = sb0 + (int)kbs;
+                }
+                for (int kb = 0; kb < T.nk; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) goto done_producer;
+                    const uint32_t sbuf = smem_u32(smem + stage * PSTAGE_BYTES);
+                    const uint32_t fb = full0 + 8 * stage;
+                    if (leader) mbar_expect_tx(fb, 2 * PTX_CTA);
+                    const uint32_t lead = mapa(fb, 0);
+                    tma_load_pair(sbuf, &tmA, lead, ax, ay);
+                    tma_load_pair(sbuf + 16384, &tmB, lead, bx, by);
+                    const uint32_t sfs = smem_u32(smem + PSF_REGION + stage * PSF_BYTES);
+                    tma_load_pair(sfs, &tmSA, lead, 0, sa + kb);
+                    tma_load_pair(sfs + 512, &tmSB, lead, 0, sb0 + kb);
+                    tma_load_pair(sfs + 1024, &tmSB, lead, 0, sb1 + kb);
+                    ax += adx; ay += ady; bx += bdx; by += bdy;
+                    if (++stage == PSTAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+        done_producer:;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, aphase = 0;
+            const uint32_t base = smem_u32(smem);
+            const uint64_t a_desc0 = a_mn ? smem_desc(base, BK * 128, 1024, 2) : smem_desc(base, 16, 1024, 2);
+            const uint64_t b_desc0 =
+                b_mn ? smem_desc(base + 16384, BK * 128, 1024, 2) : smem_desc(base + 16384, 16, 1024, 2);
+            const uint64_t sf_desc0 = smem_desc(smem_u32(smem + PSF_REGION), 0, 128, 0);
+            const uint32_t a_step16 = a_mn ? 4096u / 16 : 32u / 16, b_step16 = b_mn ? 4096u / 16 : 32u / 16;
+            uint32_t id[BK / UMMA_K];
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) id[k] = idesc_pair(a_mn, b_mn, (uint32_t)k);
+            for (int64_t i = 0;; ++i) {
+                const PTile T = S.get(S.pick(i, cl, ncl));
+                if (!T.valid) break;
+                if (T.nk == 0) continue;  // empty wgrad expert: the epilogues write zeros without the accumulator
+                if (!mbar_wait(acc_empty, aphase ^ 1, abort_flag)) break;
+                fence_after();
+                // K blocks in pairs: one barrier test per two stages (eight MMAs). Any wait on
+                // this thread between MMAs idles the tensor pipe for about its latency.
+                for (int kb = 0; kb < T.nk; kb += 2) {
+                    const int n2 = (kb + 1 < T.nk) ? 2 : 1;
+                    const int st1 = (stage + 1 == PSTAGES) ? 0 : stage + 1;
+                    const uint32_t ph1 = (st1 == 0) ? (phase ^ 1) : phase;
+                    const bool ready = n2 == 2 ? mbar_test2(full0 + 8 * stage, phase, full0 + 8 * st1, ph1)
+                                               : mbar_try(full0 + 8 * stage, phase);
+                    if (!ready) {
+                        if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) goto done_mma;
+                        if (n2 == 2 && !mbar_wait(full0 + 8 * st1, ph1, abort_flag)) goto done_mma;
+                    }
+                    fence_after();
+                    for (int h = 0; h < n2; ++h) {
+                        const uint64_t sfd = sf_desc0 + (uint64_t)(stage * (PSF_BYTES / 16));
+                        cp_sf_pair(tmem + TMEM_SFA, sfd);
+                        cp_sf_pair(tmem + TMEM_SFB, sfd + 512 / 16);
+                        cp_sf_pair(tmem + TMEM_SFB + 4, sfd + 1024 / 16);
+                        const uint64_t ad = a_desc0 + (uint64_t)(stage * (PSTAGE_BYTES / 16));
+                        const uint64_t bd = b_desc0 + (uint64_t)(stage * (PSTAGE_BYTES / 16));
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            mma_pair(tmem, ad + k * a_step16, bd + k * b_step16, id[k], tmem + TMEM_SFA,
+                                     tmem + TMEM_SFB, ((kb + h) | k) != 0);
+                        commit_pair(empty0 + 8 * stage);
+                        if (++stage == PSTAGES) { stage = 0; phase ^= 1; }
+                    }
+                }
+                commit_pair(acc_full);
+                aphase ^= 1;
+            }
+        done_mma:;
+        }
+    } else {
+        // ------------------------------------------------------ epilogue (both CTAs, own 128 rows)
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int col0 = half * (BN / 2);
+        uint8_t* epi_buf = smem + PEPI_REGION + (warp - 2) * EPI_STAGE_BYTES;
+        const uint32_t lead_acc_empty = mapa(acc_empty, 0);
+        uint32_t aphase = 0;
+        for (int64_t i = 0;; ++i) {
+            const PTile T = S.get(S.pick(i, cl, ncl));
+            if (!T.valid) break;
+            uint32_t r[BN / 2];
+            const bool zero = (kMode == kWgrad && T.nk == 0);
+            if (!zero) {
+                const bool ok = mbar_wait(acc_full, aphase, abort_flag);
+                __syncwarp();
+                if (!ok || *abort_flag) break;
+                fence_after();
+                const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + col0;
+                TMEM_LD32(tbase + 0, (r + 0));
+                TMEM_LD32(tbase + 32, (r + 32));
+                TMEM_LD32(tbase + 64, (r + 64));
+                TMEM_LD32(tbase + 96, (r + 96));
+                tmem_wait_ld();
+                fence_before();
+                __syncwarp();
+                // this warp's slice is in registers: the leader may overwrite the accumulator
+                if (lane == 0) {
+                    if (leader) mbar_arrive(acc_empty);
+                    else arrive_remote_relaxed(lead_acc_empty);
+                }
+                aphase ^= 1;
+            } else {
+                if (p.accumulate) continue;  // an empty expert's dW stays as it is
+#pragma unroll
+                for (int j = 0; j < BN / 2; ++j) r[j] = 0u;
+            }
+            if (!T.store) continue;
+            const int64_t row = T.out_row + q * 32 + lane;
+            if (p.tma_store) {
+                const bool f32 = (kMode == kWgrad && !p.out_bf16);
+                const int out_row0 = (int)(T.out_row + q * 32);
+                const __nv_bfloat16* bias =
+                    (kMode == kFprop && p.bias) ? p.bias + (int64_t)T.e * p.N + T.c0 + col0 : nullptr;
+#pragma unroll
+                for (int c = 0; c < BN / 2; c += 16) {
+                    if (!f32 && (c & 31)) continue;
+                    uint32_t w16[16];
+                    if (f32) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w16[j] = r[c + j];
+                    } else {
+                        float f[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[(c + j) & (BN / 2 - 1)]);
+                        if (bias) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                const uint4 bw = __ldg(reinterpret_cast<const uint4*>(bias + c) + v);
+                                const uint32_t ws[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    f[8 * v + 2 * j] += __uint_as_float(ws[j] << 16);
+                                    f[8 * v + 2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) w16[j] = bf16x2_bits(f[2 * j], f[2 * j + 1]);
+                    }
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                    __syncwarp();
+                    uint4* dst = reinterpret_cast<uint4*>(epi_buf + lane * 64);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v ^ ((lane >> 1) & 3)] = make_uint4(w16[4 * v], w16[4 * v + 1], w16[4 * v + 2], w16[4 * v + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        asm volatile(
+                            "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                                (uint64_t)&tmOut),
+                            "r"((int)(T.c0 + col0 + c)), "r"(out_row0), "r"(smem_u32(epi_buf))
+                            : "memory");
+                        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    }
+                }
+            } else if (kMode == kWgrad) {
+                // accumulate into dW: read-modify-write with plain loads and stores
+                const int64_t base = row * p.K + T.c0 + col0;
+                if (p.out_bf16) {
+                    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base;
+#pragma unroll
+                    for (int c = 0; c < BN / 2; c += 8) {
+                        float f[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[c + j]);
+                        uint4* dst = reinterpret_cast<uint4*>(out + c);
+                        const uint4 o = *dst;
+                        const uint32_t ws[4] = {o.x, o.y, o.z, o.w};
+                        uint32_t h[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            h[j] = bf16x2_bits(f[2 * j] + __uint_as_float(ws[j] << 16),
+                                               f[2 * j + 1] + __uint_as_float(ws[j] & 0xFFFF0000u));
+                        *dst = make_uint4(h[0], h[1], h[2], h[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base);
+#pragma unroll
+                    for (int v = 0; v < BN / 8; ++v) {
+                        const float4 old = dst[v];
+                        dst[v] = make_float4(__uint_as_float(r[4 * v]) + old.x, __uint_as_float(r[4 * v + 1]) + old.y,
+                                             __uint_as_float(r[4 * v + 2]) + old.z,
+                                             __uint_as_float(r[4 * v + 3]) + old.w);
+                    }
+                }
+            }
+        }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
+    }
+
+    fence_before();
+    __syncthreads();
+    if (s_abort && threadIdx.x == 0 && p.status) atomicOr(p.status, MXQ_STATUS_WAIT_TIMEOUT);
+    cluster_sync();  // the leader's MMAs have read this CTA's shared memory for the last time
+    if (warp == 1) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace pair
+
 // ------------------------------------------------------------------ host side
 // 2-D uint8 tensor (outer rows x inner cols, row-major), box 128 x 128, 128B swizzle.
 static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
@@ -978,6 +1480,103 @@ static int sm_count() {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
     return v;
+}
+
+}  // namespace gemm
+
+namespace gemm {
+
+// The plain fprop / dgrad / wgrad on 128-aligned experts run on CTA pairs when the shapes allow:
+// 256-wide output tiles along N (fprop, wgrad) and K (dgrad, wgrad), at most pair::MAX_EXPERTS
+// experts (the offset tables' shared-memory budget).
+static bool pair_eligible(const GemmCall& c) {
+    if (c.pad || c.E > pair::MAX_EXPERTS) return false;
+    if (c.mode == kFprop) return c.N % 256 == 0;
+    if (c.mode == kDgrad) return c.K % 256 == 0;
+    if (c.mode == kWgrad) return c.N % 256 == 0 && c.K % 256 == 0;
+    return false;
+}
+
+// 2-D uint32 view of a swizzled scale buffer: one 512-byte atom (128 words) per row, box = one atom.
+static bool make_atom_map(CUtensorMap* m, const void* base, int64_t bytes) {
+    return encode_tmap_2d(m, base, bytes / 512, 128, 4, 128, 1, 0);
+}
+
+// Largest number of co-resident CTA pairs of the pair kernel for `mode` on the current device.
+template <int kMode>
+static int max_pairs() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64) {
+        const int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::smem_bytes(pair::MAX_EXPERTS);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)pair::grouped_gemm_pair_kernel<kMode>, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = sm_count() / 2;
+    }
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+template <int kMode>
+static cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                               const CUtensorMap& tsb, const CUtensorMap& to, const Params& p, int64_t tiles,
+                               cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(pair::grouped_gemm_pair_kernel<kMode>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         pair::smem_bytes(pair::MAX_EXPERTS));
+    if (e != cudaSuccess) return e;
+    const int pairs = (int)std::min<int64_t>(tiles, max_pairs<kMode>());
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::smem_bytes(p.E);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, pair::grouped_gemm_pair_kernel<kMode>, ta, tb, tsa, tsb, to, p);
+}
+
+static cudaError_t run_pair(const GemmCall& c, const Params& p, const CUtensorMap& to, cudaStream_t s) {
+    // pair tiles, an upper bound of the device-side count (row tiles per expert are rounded up)
+    int64_t tiles;
+    if (c.mode == kFprop) tiles = (c.M / 256 + c.E) * (c.N / 256);
+    else if (c.mode == kDgrad) tiles = (c.M / 256 + c.E) * (c.K / 256);
+    else tiles = (int64_t)c.E * (c.N / 256) * (c.K / 256);
+    CUtensorMap ta, tb, tsa, tsb;
+    bool ok;
+    if (c.mode == kFprop)
+        ok = make_map(&ta, c.a_data, c.M, c.K) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K) &&
+             make_atom_map(&tsa, c.a_scale, c.M * c.K / 32) && make_atom_map(&tsb, c.b_scale, (int64_t)c.E * c.N * c.K / 32);
+    else if (c.mode == kDgrad)
+        ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K) &&
+             make_atom_map(&tsa, c.a_scale, c.M * c.N / 32) && make_atom_map(&tsb, c.b_scale, (int64_t)c.E * c.N * c.K / 32);
+    else
+        ok = make_map(&ta, c.a_data, c.M, c.N) && make_map(&tb, c.b_data, c.M, c.K) &&
+             make_atom_map(&tsa, c.a_scale, c.M * c.N / 32) && make_atom_map(&tsb, c.b_scale, c.M * c.K / 32);
+    if (!ok) return cudaErrorInvalidValue;
+    if (c.mode == kFprop) return launch_pair<kFprop>(ta, tb, tsa, tsb, to, p, tiles, s);
+    if (c.mode == kDgrad) return launch_pair<kDgrad>(ta, tb, tsa, tsb, to, p, tiles, s);
+    return launch_pair<kWgrad>(ta, tb, tsa, tsb, to, p, tiles, s);
 }
 
 }  // namespace gemm
@@ -1054,6 +1653,8 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
         if (!ok) return cudaErrorInvalidValue;
     }
 
+    const bool use_pair = pair_eligible(c);
+
     Params p{};
     p.mode = c.mode;
     p.M = c.M;
@@ -1077,6 +1678,8 @@ cudaError_t run_grouped_gemm(const GemmCall& c, cudaStream_t s) {
     p.y1 = static_cast<const __nv_bfloat16*>(c.y1);
     p.dbias_part = c.dbias_part;
     p.side = static_cast<__nv_bfloat16*>(c.side_bf16);
+
+    if (use_pair) return run_pair(c, p, to, s);
 
     const int grid = (int)std::min<int64_t>(tiles, sm_count());
     if (c.pad) {

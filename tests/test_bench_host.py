@@ -52,7 +52,7 @@ def test_both_arms_name_the_same_workload():
 
     import numpy as np
 
-    w = SimpleNamespace(E=128, K=7168, N=2048, M=131072, prequant_x=False)
+    w = SimpleNamespace(name=bench.WORKLOAD, E=128, K=7168, N=2048, M=131072, prequant_x=False)
     d = {"m_splits": np.full(128, 1024, np.int64)}
     c = bench.workload_config(w, d, 1)
     assert c["workload"] == bench.WORKLOAD and c["m_splits"] == [1024] * 128 and c["parallelism"] == "replicas x1"
