@@ -959,6 +959,8 @@ constexpr int PBAR_REGION = PSF_REGION + PSTAGES * PSF_BYTES;
 constexpr int PEPI_REGION = (PBAR_REGION + 256 + 511) / 512 * 512;
 constexpr int PTABLE_REGION = PEPI_REGION + EPI_WARPS * EPI_STAGE_BYTES;
 constexpr int MAX_EXPERTS = 512;
+// producer, MMA, 8 epilogue warps, and one warp that writes the zero dW tiles of empty experts
+constexpr int PAIR_THREADS = NUM_THREADS + 32;
 __host__ __device__ constexpr int smem_bytes(int E) { return 1024 + PTABLE_REGION + 8 * (E + 1) + 4 * (E + 1); }
 static_assert(smem_bytes(MAX_EXPERTS) <= 232448, "shared memory over the per-block limit");
 static_assert(PEPI_REGION % 512 == 0, "the 64-byte swizzle of the staging boxes repeats every 512 bytes");
@@ -1095,7 +1097,7 @@ struct PSched {
 };
 
 template <int kMode>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                              const __grid_constant__ CUtensorMap tmOut, Params p) {
@@ -1291,6 +1293,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         done_mma:;
         }
+    } else if (warp == 2 + EPI_WARPS) {
+        // ------------------------------------------------------ zero dW of empty experts (wgrad)
+        // Plain coalesced stores, independent of the accumulator pipeline, so that these writes
+        // overlap the MMAs of the heavy experts' tiles instead of queueing behind their epilogues.
+        if (kMode == kWgrad && !p.accumulate) {
+            const int64_t esz = p.out_bf16 ? 2 : 4;
+            const int64_t row_bytes = 256 * esz, vec_per_row = row_bytes / 16;
+            uint8_t* out = static_cast<uint8_t*>(p.out);
+            for (int64_t i = 0;; ++i) {
+                const PTile T = S.get(S.pick(i, cl, ncl));
+                if (!T.valid) break;
+                if (T.nk != 0) continue;
+                uint8_t* base = out + (T.out_row * p.K + T.c0) * esz;
+                for (int64_t v = lane; v < 128 * vec_per_row; v += 32) {
+                    const int64_t rr = v / vec_per_row, cc = v % vec_per_row;
+                    *reinterpret_cast<uint4*>(base + rr * p.K * esz + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------ epilogue (both CTAs, own 128 rows)
         const int q = warp & 3;
@@ -1303,8 +1324,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const PTile T = S.get(S.pick(i, cl, ncl));
             if (!T.valid) break;
             uint32_t r[BN / 2];
-            const bool zero = (kMode == kWgrad && T.nk == 0);
-            if (!zero) {
+            if (kMode == kWgrad && T.nk == 0) continue;  // an empty expert: written by the zero warp
+            {
                 const bool ok = mbar_wait(acc_full, aphase, abort_flag);
                 __syncwarp();
                 if (!ok || *abort_flag) break;
@@ -1323,10 +1344,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     else arrive_remote_relaxed(lead_acc_empty);
                 }
                 aphase ^= 1;
-            } else {
-                if (p.accumulate) continue;  // an empty expert's dW stays as it is
-#pragma unroll
-                for (int j = 0; j < BN / 2; ++j) r[j] = 0u;
             }
             if (!T.store) continue;
             const int64_t row = T.out_row + q * 32 + lane;
@@ -1514,7 +1531,7 @@ static int max_pairs() {
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(pair::PAIR_THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::smem_bytes(pair::MAX_EXPERTS);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1543,7 +1560,7 @@ static cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, con
     const int pairs = (int)std::min<int64_t>(tiles, max_pairs<kMode>());
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(pair::PAIR_THREADS, 1, 1);
     cfg.dynamicSmemBytes = pair::smem_bytes(p.E);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

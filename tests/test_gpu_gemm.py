@@ -156,6 +156,22 @@ def test_wgrad_bf16_out_and_accumulate(mxq):
     assert bool((acc[1] == 0).all())
 
 
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_wgrad_overwrites_a_prefilled_output(mxq, out_bf16):
+    """Without MXQ_ACCUMULATE every dW entry is written: the empty experts' with exact zeros, the
+    others with their products (the output buffer starts as NaN)."""
+    op = rand_case([0, 384, 0, 128, 0], 512, 768, 8)
+    dt = torch.bfloat16 if out_bf16 else torch.float32
+    dw = torch.full((op.E, op.N, op.K), float("nan"), dtype=dt, device="cuda")
+    op.gpu_wgrad(mxq, out_bf16=out_bf16, out=dw)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(dw).all())
+    for e in (0, 2, 4):
+        assert bool((dw[e] == 0).all()), e
+    ref = op.gpu_wgrad(mxq, out_bf16=out_bf16)
+    assert torch.equal(dw, ref)
+
+
 def test_deterministic(mxq):
     op = rand_case([512, 128, 384], 512, 512, 5)
     for fn in (op.gpu_fprop, op.gpu_dgrad, op.gpu_wgrad):
