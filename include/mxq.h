@@ -344,12 +344,12 @@ MXQ_API int mxq_grouped_dbias_noalloc(const void* dy_bf16, int64_t M, int64_t N,
  * first F columns of the FC1 output are the gate):
  *   fwd: y (M, 2F) bf16 -> h (M, F) bf16, h = silu(g) * u;
  *   bwd: dh (M, F), y (M, 2F) -> dy (M, 2F) = [dh*u*silu'(g) | dh*silu(g)].
- * bf16 I/O; the math is a fixed sequence of fp32 IEEE operations, each
- * rounded once: e^x by Cody-Waite reduction and the degree-7 Taylor
- * polynomial (fused multiply-adds), sigmoid(g) = 1/(1 + e^-g) with the
- * reciprocal by three Newton-Raphson steps, taken as 0 below g = -86;
- * h = (g*s)*u, dg = ((dh*u)*s)*(1 + g*(1 - s)), du = dh*(g*s). The result
- * is reproducible bit for bit on any IEEE fp32 machine. F % 8 == 0. */
+ * bf16 I/O; the math is fp32: sigmoid(g) = 1 / (1 + 2^(-g log2 e)) with the
+ * hardware base-2 exponential and reciprocal (relative errors near 2^-22),
+ * h = (g*s)*u, dg = ((dh*u)*s)*(1 + g*(1 - s)), du = dh*(g*s), each result
+ * rounded once to bf16: within one bf16 step of the exact value. Every
+ * SwiGLU path of this library runs the same steps and agrees bit for bit.
+ * F % 8 == 0. */
 MXQ_API int mxq_swiglu_fwd(const void* y_bf16, int64_t M, int64_t F, void* h_bf16, mxq_stream_t stream);
 MXQ_API int mxq_swiglu_bwd(const void* dh_bf16, const void* y_bf16, int64_t M, int64_t F, void* dy_bf16,
                    mxq_stream_t stream);
@@ -357,8 +357,8 @@ MXQ_API int mxq_swiglu_bwd(const void* dh_bf16, const void* y_bf16, int64_t M, i
 /* SwiGLU fused with group_quantize [FM][RQ][DI] (the fused grouped MLP's
  * FC1 -> activation -> FC2, with the activation's output quantized where it
  * is produced). y (M, 2F) bf16 is the FC1 output [gate | up]; h = silu(g)*u
- * is computed in fp32 (fixed sequence of IEEE operations: the same steps as
- * mxq_swiglu_fwd, so the results agree bit for bit), rounded to bf16 and
+ * is computed in fp32 (the same steps as mxq_swiglu_fwd, so the results
+ * agree bit for bit), rounded to bf16 and
  * quantized exactly as mxq_group_quantize would quantize that bf16 h.
  * flags: MXQ_ROWWISE / MXQ_COLWISE / MXQ_SWIZZLE as for group_quantize;
  * MXQ_DEQUANT_OUT also writes h in bf16 to h_bf16_out (M, F). Outputs are

@@ -168,65 +168,40 @@ __device__ __forceinline__ void report_status(int32_t* d_status, int bits) {
     if (d_status && bits && blockIdx.x == 0 && threadIdx.x == 0) atomicOr(d_status, bits);
 }
 
-// ------------------------------------------------ SwiGLU in fp32 steps
+// ------------------------------------------------ SwiGLU in fp32
 // SwiGLU between FC1 and FC2 of a fused grouped MoE MLP (TransformerEngine
 // PR #3545, "Fix distributed BF16 weights and trim NVFP4 saved state in the
 // fused grouped MLP": FC1 -> activation -> FC2; gate = first half of FC1's
-// output). Every step is one IEEE fp32 operation with one rounding (__f*_rn
-// are never contracted; __fmaf_rn is an explicit fused multiply-add) so that
-// the bf16 rounding of h, and the E4M3 codes chosen from it, are
-// reproducible exactly. All of it is branch-free (range limits are selects)
-// so the unrolled element loops keep their instruction-level parallelism.
-// e^x for x in [-86, 88]: Cody & Waite argument reduction x = n*ln2 + r, n
-// the integer nearest to x*log2 e (one fused multiply-add onto 1.5*2^23
-// rounds the product to an integer, whose value then sits in the low
-// mantissa bits of j), ln2 = 0.693359375 + -2.12194440e-4; the degree-7
-// Taylor polynomial of e^r by fused Horner steps with coefficients 1/k!
-// rounded to fp32; then 2^n applied by adding n to p's exponent field
-// (exact: n >= -124 keeps the result normal). Outside [-86, 88] the value is
-// meaningless; callers clamp or select.
-__device__ __forceinline__ float exp_core_f32(float x) {
-    const float j = __fmaf_rn(x, 1.44269504f, 0x1.8p23f);
-    const float n = __fsub_rn(j, 0x1.8p23f);
-    float r = __fmaf_rn(-n, 0.693359375f, x);
-    r = __fmaf_rn(-n, -2.12194440e-4f, r);
-    float p = 0x1.a01a02p-13f;             // 1/5040
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/720
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/120
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/24
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/6
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    // bits(j) = bits(1.5*2^23) + n, and bits(1.5*2^23) << 23 wraps to 0
-    return __uint_as_float(__float_as_uint(p) + (__float_as_uint(j) << 23));
-}
-// 1/d for d in [1, 2^126): Newton-Raphson y <- y + y*(1 - d*y), three steps
-// from the bit-pattern estimate as_float(0x7EF311C3 - bits(d)) (relative
-// error <= 5.1%, squared by each step to below 2^-24 after the third).
-__device__ __forceinline__ float recip_f32_steps(float d) {
-    float y = __uint_as_float(0x7EF311C3u - __float_as_uint(d));
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        const float e = __fmaf_rn(-d, y, 1.0f);
-        y = __fmaf_rn(y, e, y);
-    }
+// output). The sigmoid is 1 / (1 + 2^(-g log2 e)) with the hardware base-2
+// exponential and reciprocal (ex2.approx, rcp.approx; relative errors near
+// 2^-22), the products are single IEEE fp32 roundings (__f*_rn, never
+// contracted). Every fp32 step errs far below half a bf16 ulp (2^-9), so the
+// bf16-rounded h, dg and du sit within one bf16 step of the exact values.
+// All SwiGLU paths (unfused, fused with quantization, both GEMM epilogues)
+// run these same steps and agree bit for bit. Below g = -88.7 the
+// exponential overflows to +inf and the sigmoid is 0 (its exact value is
+// under 2^-127 there).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// sigmoid(g) = 1/(1 + e^-g), 0 below g = -86 (true value under 2^-124).
-// e^-g is taken at max(-g, -86): above g = 86 that is e^-86 instead of 0,
-// and 1 + e^-86 rounds to 1 exactly as 1 + 0 does.
-__device__ __forceinline__ float sigmoid_f32_steps(float g) {
-    const float y = recip_f32_steps(__fadd_rn(1.0f, exp_core_f32(fmaxf(-g, -86.0f))));
-    return g < -86.0f ? 0.0f : y;
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kNegLog2e = -1.44269504088896341f;  // -log2(e), rounded to fp32
+__device__ __forceinline__ float sigmoid_f32(float g) {
+    return rcp_approx(__fadd_rn(1.0f, ex2_approx(__fmul_rn(g, kNegLog2e))));
 }
 // h = (g * s) * u
 __device__ __forceinline__ float swiglu_h(float g, float u) {
-    return __fmul_rn(__fmul_rn(g, sigmoid_f32_steps(g)), u);
+    return __fmul_rn(__fmul_rn(g, sigmoid_f32(g)), u);
 }
 // dg = ((dh * u) * s) * (1 + g * (1 - s)), du = dh * (g * s)
 __device__ __forceinline__ void swiglu_grads(float d, float g, float u, float& dg, float& du) {
-    const float s = sigmoid_f32_steps(g);
+    const float s = sigmoid_f32(g);
     const float fac = __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s)));
     dg = __fmul_rn(__fmul_rn(__fmul_rn(d, u), s), fac);
     du = __fmul_rn(d, __fmul_rn(g, s));

@@ -31,9 +31,9 @@ namespace mxq {
 namespace swq {
 
 // The fp32 SwiGLU steps of mxq_common.cuh on two values at once. Each packed
-// instruction (add / sub / mul / fma .rn.f32x2) rounds each lane to nearest
-// even without flushing subnormals, exactly as the scalar instruction of the
-// same step does, so every result is bit-identical to swiglu_h / swiglu_grads.
+// instruction (add / sub / mul .rn.f32x2) rounds each lane to nearest even
+// without flushing subnormals, exactly as the scalar instruction of the same
+// step does, so every result is bit-identical to swiglu_h / swiglu_grads.
 __device__ __forceinline__ uint64_t f2pack(float a, float b) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
@@ -43,11 +43,6 @@ __device__ __forceinline__ float2 f2unpack(uint64_t v) {
     float2 o;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(v));
     return o;
-}
-__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
 }
 __device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
     uint64_t r;
@@ -59,49 +54,13 @@ __device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 __device__ __forceinline__ uint64_t f2splat(float a) { return f2pack(a, a); }
 
-// exp_core_f32 on two lanes (the same steps; (-n) * c is computed as n * (-c), the same product)
-__device__ __forceinline__ uint64_t exp_core_x2(uint64_t x) {
-    const uint64_t magic = f2splat(0x1.8p23f);
-    const uint64_t j = f2fma(x, f2splat(1.44269504f), magic);
-    const uint64_t n = f2sub(j, magic);
-    uint64_t r = f2fma(n, f2splat(-0.693359375f), x);
-    r = f2fma(n, f2splat(2.12194440e-4f), r);
-    uint64_t p = f2fma(f2splat(0x1.a01a02p-13f), r, f2splat(0x1.6c16c2p-10f));
-    p = f2fma(p, r, f2splat(0x1.111112p-7f));
-    p = f2fma(p, r, f2splat(0x1.555556p-5f));
-    p = f2fma(p, r, f2splat(0x1.555556p-3f));
-    p = f2fma(p, r, f2splat(0.5f));
-    p = f2fma(p, r, f2splat(1.0f));
-    p = f2fma(p, r, f2splat(1.0f));
-    const float2 pf = f2unpack(p), jf = f2unpack(j);
-    return f2pack(__uint_as_float(__float_as_uint(pf.x) + (__float_as_uint(jf.x) << 23)),
-                  __uint_as_float(__float_as_uint(pf.y) + (__float_as_uint(jf.y) << 23)));
-}
-// recip_f32_steps on two lanes
-__device__ __forceinline__ uint64_t recip_x2(uint64_t d) {
-    const float2 df = f2unpack(d);
-    uint64_t y = f2pack(__uint_as_float(0x7EF311C3u - __float_as_uint(df.x)),
-                        __uint_as_float(0x7EF311C3u - __float_as_uint(df.y)));
-    const uint64_t nd = f2pack(-df.x, -df.y), one = f2splat(1.0f);
-#pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        const uint64_t e = f2fma(nd, y, one);
-        y = f2fma(y, e, y);
-    }
-    return y;
-}
-// sigmoid_f32_steps on two lanes
+// sigmoid_f32 on two lanes: the product and the sum packed, the exponential and reciprocal per lane
 __device__ __forceinline__ uint64_t sigmoid_x2(float2 g) {
-    const uint64_t y = recip_x2(f2add(f2splat(1.0f), exp_core_x2(f2pack(fmaxf(-g.x, -86.0f), fmaxf(-g.y, -86.0f)))));
-    const float2 yf = f2unpack(y);
-    return f2pack(g.x < -86.0f ? 0.0f : yf.x, g.y < -86.0f ? 0.0f : yf.y);
+    const float2 t = f2unpack(f2mul(f2pack(g.x, g.y), f2splat(kNegLog2e)));
+    const float2 d = f2unpack(f2add(f2splat(1.0f), f2pack(ex2_approx(t.x), ex2_approx(t.y))));
+    return f2pack(rcp_approx(d.x), rcp_approx(d.y));
 }
 // swiglu_h on two lanes: (g * s) * u
 __device__ __forceinline__ float2 swiglu_h_x2(float2 g, float2 u) {

@@ -62,13 +62,14 @@ def first_diff(a: np.ndarray, b: np.ndarray):
 
 # ------------------------------------------------------------ SwiGLU tolerance
 # The kernels evaluate SwiGLU in fp32; the oracle's definition is fp64 with one
-# final rounding to bf16. Every fp32 step rounds with a relative error far below
-# half a bf16 ulp (2^-9), so after the final rounding the two may differ by one
-# bf16 step at most (a rounding boundary between them). The one exception is
-# the sigmoid below g = -86, where it is under 2^-124 and the fp32 steps take it
-# as 0: there the results may differ by the dropped term, at most
-# |g u| 2^-124 for h, |dh u| (1 + |g|) 2^-124 for dg and |dh g| 2^-124 for du,
-# each allowed twice over to cover the final rounding of the fp64 result.
+# final rounding to bf16. Every fp32 step errs by far less than half a bf16 ulp
+# (2^-9) relative, so after the final rounding the two may differ by one bf16
+# step at most (a rounding boundary between them). The one exception is the
+# sigmoid below g = -86: its exact value is under 2^-124 there, where fp32 has
+# only subnormals (or, below g = -88.7, 0) to hold it. The results may then be off
+# by up to the whole term, at most |g u| 2^-124 for h, |dh u| (1 + |g|) 2^-124
+# for dg and |dh g| 2^-124 for du, each allowed twice over to cover the final
+# rounding of the fp64 result.
 SIGMOID_FLUSH_G = -86.0
 SIGMOID_FLUSH_BOUND = 2.0 ** -123
 
