@@ -1082,13 +1082,16 @@ struct PSched {
             T.nk = (int)((mode == kDgrad ? N : K) / BK);
         } else {
             const int64_t ei = t / tiles_n, r = t % tiles_n;
-            const int64_t kt = K / 256;
+            // consecutive tiles of an expert share the block of the wider operand and step through
+            // the narrower one, so the wider colwise copy (dY's N or X's K columns) is read once
+            const int64_t nt = N / 256, kt = K / 256;
+            const int64_t nb = N <= K ? r % nt : r / kt, kb = N <= K ? r / nt : r % kt;
             T.e = aux[ei];
             T.off = off[T.e];
             T.me = off[T.e + 1] - T.off;
-            T.a0 = (r / kt) * 256 + 128 * rank;
+            T.a0 = nb * 256 + 128 * rank;
             T.out_row = (int64_t)T.e * N + T.a0;
-            T.c0 = (r % kt) * 256;
+            T.c0 = kb * 256;
             T.nk = (int)(T.me / BK);
             T.store = true;
         }
