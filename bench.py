@@ -1253,7 +1253,8 @@ def main():
         with open(tpath) as f:
             tj = json.load(f)
         if tj.get("source_stamp") == source_stamp() and tj.get("workload") == w.name:
-            roofline["traffic"] = tj.get("dram_bytes_per_launch")
+            roofline["traffic"] = tj.get("dram_bytes_per_step")
+            roofline["traffic_per_launch"] = tj.get("dram_bytes_per_launch")
             roofline["traffic_note"] = tj.get("note")
     if rank == 0:
         try:
