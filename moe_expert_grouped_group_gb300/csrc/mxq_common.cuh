@@ -199,10 +199,10 @@ __device__ __forceinline__ float sigmoid_f32(float g) {
 __device__ __forceinline__ float swiglu_h(float g, float u) {
     return __fmul_rn(__fmul_rn(g, sigmoid_f32(g)), u);
 }
-// dg = ((dh * u) * s) * (1 + g * (1 - s)), du = dh * (g * s)
+// dg = ((dh * u) * s) * (1 + g * (1 - s)), the factor by one fused multiply-add; du = dh * (g * s)
 __device__ __forceinline__ void swiglu_grads(float d, float g, float u, float& dg, float& du) {
     const float s = sigmoid_f32(g);
-    const float fac = __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s)));
+    const float fac = __fmaf_rn(g, __fsub_rn(1.0f, s), 1.0f);
     dg = __fmul_rn(__fmul_rn(__fmul_rn(d, u), s), fac);
     du = __fmul_rn(d, __fmul_rn(g, s));
 }

@@ -44,6 +44,16 @@ __device__ __forceinline__ float2 f2unpack(uint64_t v) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(v));
     return o;
 }
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
 __device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
     uint64_t r;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -66,15 +76,11 @@ __device__ __forceinline__ uint64_t sigmoid_x2(float2 g) {
 __device__ __forceinline__ float2 swiglu_h_x2(float2 g, float2 u) {
     return f2unpack(f2mul(f2mul(f2pack(g.x, g.y), sigmoid_x2(g)), f2pack(u.x, u.y)));
 }
-// swiglu_grads on two lanes: dg = ((d * u) * s) * (1 + g * (1 - s)), du = d * (g * s). The factor
-// 1 + g * (1 - s) is a product followed by a sum, which the assembler may fuse when both are packed; it is
-// taken in scalar steps, which never are.
+// swiglu_grads on two lanes: dg = ((d * u) * s) * fma(g, 1 - s, 1), du = d * (g * s)
 __device__ __forceinline__ void swiglu_grads_x2(float2 d, float2 g, float2 u, float2& dg, float2& du) {
     const uint64_t s = sigmoid_x2(g);
-    const uint64_t gp = f2pack(g.x, g.y), dp = f2pack(d.x, d.y);
-    const float2 sf = f2unpack(s);
-    const uint64_t fac = f2pack(__fadd_rn(1.0f, __fmul_rn(g.x, __fsub_rn(1.0f, sf.x))),
-                                __fadd_rn(1.0f, __fmul_rn(g.y, __fsub_rn(1.0f, sf.y))));
+    const uint64_t gp = f2pack(g.x, g.y), dp = f2pack(d.x, d.y), one = f2splat(1.0f);
+    const uint64_t fac = f2fma(gp, f2sub(one, s), one);
     dg = f2unpack(f2mul(f2mul(f2mul(dp, f2pack(u.x, u.y)), s), fac));
     du = f2unpack(f2mul(dp, f2mul(gp, s)));
 }
@@ -126,22 +132,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Colwise statistics of one output tile over a warp's 16 rows, gathered as
-// the bf16 results are produced: per column the largest |bits| (two
-// columns per word) and, for dbias, the fp32 sum.
-template <bool kBias>
+// Colwise exponent statistics of one output tile over a warp's 16 rows,
+// gathered as the bf16 results are produced: per column the largest |bits|
+// (two columns per word).
 struct ColStats {
     uint32_t m[2] = {0u, 0u};
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
     __device__ __forceinline__ void add(uint2 w) {
         m[0] = __vmaxu2(m[0], w.x & 0x7FFF7FFFu);
         m[1] = __vmaxu2(m[1], w.y & 0x7FFF7FFFu);
-        if constexpr (kBias) {
-            sum[0] += bf16lo(w.x);
-            sum[1] += bf16hi(w.x);
-            sum[2] += bf16lo(w.y);
-            sum[3] += bf16hi(w.y);
-        }
     }
     // the four biased exponents, one byte per column
     __device__ __forceinline__ uint32_t exps() const {
@@ -155,8 +153,10 @@ struct ColStats {
 // column tile `kt` of an (M, Kout) tensor. The colwise scale of each 32-row
 // block comes from the exponent maxima of warps w and w^1 (the two halves of
 // the block); the rowwise scale of each row from the 8 lanes of its
-// 32-column block. Swizzled scale bytes are staged in `sc` for flush_scratch.
-template <bool kRow, bool kCol, bool kDeq>
+// 32-column block. Swizzled scale bytes are staged in `sc` for flush_scratch;
+// with kBias the lane's four column sums over the 16 rows (fp32, in row order)
+// go to sc.red[w].
+template <bool kRow, bool kCol, bool kDeq, bool kBias>
 __device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, int64_t mt, int64_t kt,
                                             int64_t Kout, Scratch& sc, int w, int lane) {
     auto o = [&](int r) { return *reinterpret_cast<const uint2*>(rows + r * (kTile * 2)); };
@@ -189,6 +189,7 @@ __device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, 
     uint8_t* rq = kRow ? a.row_q + r0 * Kout + col : nullptr;
     uint8_t* cq = kCol ? a.col_q + r0 * Kout + col : nullptr;
     __nv_bfloat16* dq = kDeq ? a.bf16_out + r0 * Kout + col : nullptr;
+    float bsum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
     for (int r4 = 0; r4 < kPreRows; r4 += 4) {
         uint2 ow[4];
@@ -209,6 +210,10 @@ __device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, 
             const int r = r4 + k;
             const uint2 u = ow[k];
             const float v[4] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y)};
+            if constexpr (kBias) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bsum[j] += v[j];
+            }
             if constexpr (kRow) {
                 const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
                 const float inv = inv_scale_from_code(code);
@@ -226,6 +231,8 @@ __device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, 
             if constexpr (kDeq) *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = u;
         }
     }
+    if constexpr (kBias)
+        *reinterpret_cast<float4*>(&sc.red[w][lane * 4]) = make_float4(bsum[0], bsum[1], bsum[2], bsum[3]);
 }
 
 // Write out one tile's scratch: the dbias partial of each of its 128 columns
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
         // SwiGLU of this warp's 16 rows, rounded to bf16 and written back in
         // place (h or dg over the gate tile, du over the up tile), with the
         // colwise statistics of each output tile
-        ColStats<kBias> cs[kOut];
+        ColStats cs[kOut];
         uint8_t* g_row = stage + (warp * kPreRows) * (kTile * 2) + lane * 8;
         uint8_t* u_row = g_row + kTileBytes;
 #pragma unroll 4
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
                 }
                 const uint2 hw = make_uint2(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]));
                 *gp = hw;
-                if (kCol || kBias) cs[0].add(hw);
+                if (kCol) cs[0].add(hw);
             } else {
                 const uint2 dw = *reinterpret_cast<const uint2*>(g_row + 2 * kTileBytes + r * (kTile * 2));
                 const float d[4] = {bf16lo(dw.x), bf16hi(dw.x), bf16lo(dw.y), bf16hi(dw.y)};
@@ -364,26 +371,22 @@ __global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
                 const uint2 uw2 = make_uint2(pack_bf16x2(du[0], du[1]), pack_bf16x2(du[2], du[3]));
                 *gp = gw2;
                 *up = uw2;
-                if (kCol || kBias) {
+                if (kCol) {
                     cs[0].add(gw2);
                     cs[kOut - 1].add(uw2);
                 }
             }
         }
 #pragma unroll
-        for (int q = 0; q < kOut; ++q) {
+        for (int q = 0; q < kOut; ++q)
             if constexpr (kCol) s_sc[q].xexp[warp][lane] = cs[q].exps();
-            if constexpr (kBias)
-                *reinterpret_cast<float4*>(&s_sc[q].red[warp][lane * 4]) =
-                    make_float4(cs[q].sum[0], cs[q].sum[1], cs[q].sum[2], cs[q].sum[3]);
-        }
         bar_compute();  // every warp's colwise statistics are in
 
         const int64_t Kout = kBwd ? 2 * a.F : a.F;
 #pragma unroll
         for (int q = 0; q < kOut; ++q)
-            encode_rows<kRow, kCol, kDeq>(g_row + q * kTileBytes, a, mt, q ? tilesF + ft : ft, Kout, s_sc[q], warp,
-                                          lane);
+            encode_rows<kRow, kCol, kDeq, kBias>(g_row + q * kTileBytes, a, mt, q ? tilesF + ft : ft, Kout, s_sc[q],
+                                                 warp, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty);  // this warp is done with the stage
         bar_compute();                      // scratch complete
