@@ -443,9 +443,12 @@ __device__ __forceinline__ void swiglu_bwd_tile_epilogue(const Params& p, const 
 // steps of mxq_common.cuh, and quantizes h as group_quantize does: rowwise
 // over the lane's two 32-column blocks, colwise over the warp's 32 rows (a
 // byte-wise max of exponents across the lanes), E4M3 by the same cast.
+// `release(lane)` hands the accumulator back once this warp's slice is in registers; with
+// store == false (the duplicate half of a pair tile) nothing is written.
+template <class Release>
 __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile& T, uint32_t tmem, int q, int half,
-                                                     int lane, uint8_t* epi_buf, uint32_t acc_empty,
-                                                     const CUtensorMap* tmOut) {
+                                                     int lane, uint8_t* epi_buf, Release release,
+                                                     const CUtensorMap* tmOut, bool store = true) {
     const int64_t F = p.N / 2;
     uint32_t r[BN / 2];
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + 64 * half;
@@ -456,7 +459,8 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
     tmem_wait_ld();
     fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(acc_empty);  // the MMA warp may start the next tile
+    release(lane);  // the MMA warp may start the next tile
+    if (!store) return;
 
     const int64_t f0 = T.b_col + 64 * half;  // first gate (and h) column of this warp
 
@@ -746,7 +750,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok || *abort_flag) break;
             fence_after();
             if constexpr (kMode == kFpropSwiglu) {
-                swiglu_tile_epilogue(p, T, tmem, q, half, lane, epi_buf, acc_empty, &tmOut);
+                swiglu_tile_epilogue(p, T, tmem, q, half, lane, epi_buf,
+                                     [&](int l) { if (l == 0) mbar_arrive(acc_empty); }, &tmOut);
                 aphase ^= 1;
                 continue;
             }
@@ -1078,7 +1083,7 @@ struct PSched {
             T.store = left > 128 * (int64_t)rank;
             T.a0 = T.store ? r0 + 128 * rank : r0;
             T.out_row = T.a0;
-            T.c0 = nt * 256;
+            T.c0 = nt * (mode == kFpropSwiglu ? 128 : 256);  // SwiGLU: 128 gate columns (and their up columns)
             T.nk = (int)((mode == kDgrad ? N : K) / BK);
         } else {
             const int64_t ei = t / tiles_n, r = t % tiles_n;
@@ -1184,12 +1189,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
 
     PSched S;
     S.mode = kMode; S.M = p.M; S.N = p.N; S.K = p.K; S.E = p.E; S.off = s_off; S.aux = s_aux; S.rank = rank;
-    if (kMode == kFprop) { S.tiles_n = p.N / 256; S.total = (int64_t)s_aux[p.E] * S.tiles_n; }
+    if (kMode == kFprop || kMode == kFpropSwiglu) { S.tiles_n = p.N / 256; S.total = (int64_t)s_aux[p.E] * S.tiles_n; }
     else if (kMode == kDgrad) { S.tiles_n = p.K / 256; S.total = (int64_t)s_aux[p.E] * S.tiles_n; }
     else { S.tiles_n = (p.N / 256) * (p.K / 256); S.total = (int64_t)p.E * S.tiles_n; }
     const int ncl = gridDim.x / 2, cl = blockIdx.x / 2;
     const uint32_t a_mn = (kMode == kWgrad) ? 1u : 0u;
-    const uint32_t b_mn = (kMode == kFprop) ? 0u : 1u;
+    const uint32_t b_mn = (kMode == kFprop || kMode == kFpropSwiglu) ? 0u : 1u;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer (both CTAs)
@@ -1208,6 +1213,15 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                     sa = (int)((T.a0 / 128) * kbs);
                     sb0 = (int)((wrow / 128) * kbs);
                     sb1 = sb0 + (int)kbs;
+                } else if (kMode == kFpropSwiglu) {
+                    // CTA 0 stages 128 gate rows of W1, CTA 1 the matching up rows F further: the
+                    // accumulator's columns 0..127 are gate, 128..255 up, for the same 128 columns of F
+                    const int64_t kbs = p.K / BK, grow = (int64_t)T.e * p.N + T.c0, urow = grow + p.N / 2;
+                    ax = 0; ay = (int)T.a0; adx = BK; ady = 0;
+                    bx = 0; by = (int)(rank ? urow : grow); bdx = BK; bdy = 0;
+                    sa = (int)((T.a0 / 128) * kbs);
+                    sb0 = (int)((grow / 128) * kbs);
+                    sb1 = (int)((urow / 128) * kbs);
                 } else if (kMode == kDgrad) {
                     const int64_t kbs = p.N / BK;
                     const int64_t wb = (int64_t)T.e * (p.K / 128) * kbs;  // expert e's colwise atoms
@@ -1326,6 +1340,28 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         for (int64_t i = 0;; ++i) {
             const PTile T = S.get(S.pick(i, cl, ncl));
             if (!T.valid) break;
+            if constexpr (kMode == kFpropSwiglu) {
+                const bool ok = mbar_wait(acc_full, aphase, abort_flag);
+                __syncwarp();
+                if (!ok || *abort_flag) break;
+                fence_after();
+                Tile ST;
+                ST.a_row = T.out_row;
+                ST.b_col = T.c0;
+                ST.e = T.e;
+                ST.off = T.off;
+                ST.me = T.me;
+                swiglu_tile_epilogue(p, ST, tmem, q, half, lane, epi_buf,
+                                     [&](int l) {
+                                         if (l == 0) {
+                                             if (leader) mbar_arrive(acc_empty);
+                                             else arrive_remote_relaxed(lead_acc_empty);
+                                         }
+                                     },
+                                     &tmOut, T.store);
+                aphase ^= 1;
+                continue;
+            }
             uint32_t r[BN / 2];
             if (kMode == kWgrad && T.nk == 0) continue;  // an empty expert: written by the zero warp
             {
@@ -1511,7 +1547,7 @@ namespace gemm {
 // experts (the offset tables' shared-memory budget).
 static bool pair_eligible(const GemmCall& c) {
     if (c.pad || c.E > pair::MAX_EXPERTS) return false;
-    if (c.mode == kFprop) return c.N % 256 == 0;
+    if (c.mode == kFprop || c.mode == kFpropSwiglu) return c.N % 256 == 0;
     if (c.mode == kDgrad) return c.K % 256 == 0;
     if (c.mode == kWgrad) return c.N % 256 == 0 && c.K % 256 == 0;
     return false;
@@ -1579,12 +1615,12 @@ static cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, con
 static cudaError_t run_pair(const GemmCall& c, const Params& p, const CUtensorMap& to, cudaStream_t s) {
     // pair tiles, an upper bound of the device-side count (row tiles per expert are rounded up)
     int64_t tiles;
-    if (c.mode == kFprop) tiles = (c.M / 256 + c.E) * (c.N / 256);
+    if (c.mode == kFprop || c.mode == kFpropSwiglu) tiles = (c.M / 256 + c.E) * (c.N / 256);
     else if (c.mode == kDgrad) tiles = (c.M / 256 + c.E) * (c.K / 256);
     else tiles = (int64_t)c.E * (c.N / 256) * (c.K / 256);
     CUtensorMap ta, tb, tsa, tsb;
     bool ok;
-    if (c.mode == kFprop)
+    if (c.mode == kFprop || c.mode == kFpropSwiglu)
         ok = make_map(&ta, c.a_data, c.M, c.K) && make_map(&tb, c.b_data, (int64_t)c.E * c.N, c.K) &&
              make_atom_map(&tsa, c.a_scale, c.M * c.K / 32) && make_atom_map(&tsb, c.b_scale, (int64_t)c.E * c.N * c.K / 32);
     else if (c.mode == kDgrad)
@@ -1595,6 +1631,7 @@ static cudaError_t run_pair(const GemmCall& c, const Params& p, const CUtensorMa
              make_atom_map(&tsa, c.a_scale, c.M * c.N / 32) && make_atom_map(&tsb, c.b_scale, c.M * c.K / 32);
     if (!ok) return cudaErrorInvalidValue;
     if (c.mode == kFprop) return launch_pair<kFprop>(ta, tb, tsa, tsb, to, p, tiles, s);
+    if (c.mode == kFpropSwiglu) return launch_pair<kFpropSwiglu>(ta, tb, tsa, tsb, to, p, tiles, s);
     if (c.mode == kDgrad) return launch_pair<kDgrad>(ta, tb, tsa, tsb, to, p, tiles, s);
     return launch_pair<kWgrad>(ta, tb, tsa, tsb, to, p, tiles, s);
 }
