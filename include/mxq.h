@@ -392,6 +392,16 @@ MXQ_API int mxq_swiglu_bwd_quantize(const void* dh_bf16, const void* y_bf16, int
  * mmas_per_sm in [0, 2^31); MXQ_ERR_SHAPE otherwise. */
 MXQ_API int mxq_probe_mma_stream(int64_t mmas_per_sm, int32_t* d_status, mxq_stream_t stream);
 
+/* The same probe with a choice of operands: MXQ_PROBE_ZEROS (as above) or
+ * MXQ_PROBE_RANDOM, pseudo-random E4M3 bytes (exponent field <= 6, so no NaN
+ * and finite sums) with unit E8M0 scales. The tensor pipe draws more power
+ * multiplying random bits than zeros; a stream of random operands long
+ * enough to reach the board's power limit (about a second) measures the
+ * sustained ceiling a GEMM on real data meets. Any other `operands` value:
+ * MXQ_ERR_FLAGS. */
+enum { MXQ_PROBE_ZEROS = 0, MXQ_PROBE_RANDOM = 1 };
+MXQ_API int mxq_probe_mma_stream_ex(int64_t mmas_per_sm, int operands, int32_t* d_status, mxq_stream_t stream);
+
 /* Self-test of the failure path every kernel shares: one CTA waits, limit_ns
  * long, on an mbarrier that nothing arrives on, with the kernels' bounded wait;
  * the wait expires, the CTA's other waiter is released through the abort flag,

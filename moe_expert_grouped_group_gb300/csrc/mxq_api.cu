@@ -452,11 +452,16 @@ int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_scale, co
                        nullptr, (flags & MXQ_PAD_EXPERTS) != 0);
 }
 
-int mxq_probe_mma_stream(int64_t mmas_per_sm, int32_t* d_status, mxq_stream_t stream) {
+int mxq_probe_mma_stream_ex(int64_t mmas_per_sm, int operands, int32_t* d_status, mxq_stream_t stream) {
+    if (operands != MXQ_PROBE_ZEROS && operands != MXQ_PROBE_RANDOM) return MXQ_ERR_FLAGS;
     if (!arch_ok()) return MXQ_ERR_ARCH;
     if (mmas_per_sm < 0 || mmas_per_sm >= ((int64_t)1 << 31)) return MXQ_ERR_SHAPE;
-    cudaError_t e = mxq::run_mma_stream(mmas_per_sm, d_status, (cudaStream_t)stream);
+    cudaError_t e = mxq::run_mma_stream(mmas_per_sm, operands == MXQ_PROBE_RANDOM, d_status, (cudaStream_t)stream);
     return e == cudaSuccess ? MXQ_OK : fail_cuda(e);
+}
+
+int mxq_probe_mma_stream(int64_t mmas_per_sm, int32_t* d_status, mxq_stream_t stream) {
+    return mxq_probe_mma_stream_ex(mmas_per_sm, MXQ_PROBE_ZEROS, d_status, stream);
 }
 
 int mxq_selftest_wait_timeout(int64_t limit_ns, int32_t* d_status, mxq_stream_t stream) {

@@ -8,6 +8,10 @@
 // copies, four MMAs and a commit per 128-deep K block) without the loads,
 // the waits between blocks, the tile boundaries or the epilogue. Its rate is
 // the most any kernel built from these instructions can reach on this GPU.
+// The operands are zeros, or pseudo-random E4M3 bytes with unit scales: the
+// tensor pipe's power grows with the bits it multiplies, so a long stream of
+// random operands (as a GEMM on real data) meets the board's power limit and
+// runs at a lower clock than a stream of zeros.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,14 +37,23 @@ __device__ __forceinline__ uint32_t peak_idesc(uint32_t k) {
     return (k << 4) | ((uint32_t)(256 >> 3) << 17) | (1u << 23) | ((uint32_t)(128 >> 4) << 24) | (k << 29);
 }
 
-__global__ void __launch_bounds__(kPeakThreads) mma_stream_kernel(int64_t mmas, int32_t* status) {
+__global__ void __launch_bounds__(kPeakThreads) mma_stream_kernel(int64_t mmas, int random, int32_t* status) {
     extern __shared__ uint8_t peak_raw[];
     uint8_t* smem = smem_align<1024>(peak_raw);
     __shared__ uint32_t s_tmem;
     __shared__ __align__(8) uint64_t s_bar[2];  // [0]: per-K-block commits (never waited on), [1]: all done
     __shared__ int s_abort;
-    for (int i = threadIdx.x; i < (kOperandBytes + kScaleBytes) / 16; i += blockDim.x)
-        reinterpret_cast<uint4*>(smem)[i] = make_uint4(0u, 0u, 0u, 0u);
+    // random operands: a multiplicative hash of the word index and the SM, each byte's exponent
+    // field kept at most 6 (no NaN code; products and sums stay finite); scales 127 (2^0)
+    for (int i = threadIdx.x; i < kOperandBytes / 4; i += blockDim.x) {
+        uint32_t h = (uint32_t)(i + 1) * 2654435761u ^ ((uint32_t)blockIdx.x << 20);
+        h ^= h >> 13;
+        h *= 0x5bd1e995u;
+        h ^= h >> 15;
+        reinterpret_cast<uint32_t*>(smem)[i] = random ? (h & 0xB7B7B7B7u) : 0u;
+    }
+    for (int i = threadIdx.x; i < kScaleBytes / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(smem + kOperandBytes)[i] = random ? 0x7F7F7F7Fu : 0u;
     if (threadIdx.x == 0) {
         s_abort = 0;
         mbar_init(smem_u32(&s_bar[0]), 1);
@@ -124,14 +137,14 @@ cudaError_t run_wait_timeout(int64_t limit_ns, int32_t* status, cudaStream_t s) 
     return cudaGetLastError();
 }
 
-cudaError_t run_mma_stream(int64_t mmas_per_sm, int32_t* status, cudaStream_t s) {
+cudaError_t run_mma_stream(int64_t mmas_per_sm, int random, int32_t* status, cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const cudaError_t attr =
         cudaFuncSetAttribute(mma_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPeakSmem);
     if (attr != cudaSuccess) return attr;
-    mma_stream_kernel<<<sms, kPeakThreads, kPeakSmem, s>>>(mmas_per_sm, status);
+    mma_stream_kernel<<<sms, kPeakThreads, kPeakSmem, s>>>(mmas_per_sm, random, status);
     return cudaGetLastError();
 }
 

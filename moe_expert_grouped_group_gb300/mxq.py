@@ -21,6 +21,7 @@ ROWWISE, COLWISE, SWIZZLE, DEQUANT_OUT, ACCUMULATE, OUT_BF16, PAD_EXPERTS = 1, 2
 OP_GROUP_QUANTIZE, OP_REQUANT_COLWISE, OP_GROUPED_DBIAS = 1, 2, 3
 OP_GEMM_FPROP, OP_GEMM_DGRAD, OP_GEMM_WGRAD, OP_SWIGLU_BWD_QUANTIZE, OP_SCALED_BIAS = 4, 5, 6, 7, 8
 OP_GEMM_DGRAD_SWIGLU = 9
+PROBE_ZEROS, PROBE_RANDOM = 0, 1
 STATUS_SPLIT_UNALIGNED, STATUS_SPLIT_NEGATIVE, STATUS_SPLIT_SUM, STATUS_WAIT_TIMEOUT = 1, 2, 4, 8
 
 SYMBOLS = [
@@ -29,7 +30,7 @@ SYMBOLS = [
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
     "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu", "mxq_grouped_gemm_dgrad_swiglu",
-    "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex", "mxq_probe_mma_stream",
+    "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex", "mxq_probe_mma_stream", "mxq_probe_mma_stream_ex",
     "mxq_selftest_wait_timeout",
 ]
 
@@ -80,6 +81,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.mxq_status_read.argtypes = [_P, _P, _P]
     L.mxq_probe_mma_stream.argtypes = [_I64, _P, _P]
     L.mxq_probe_mma_stream.restype = _INT
+    L.mxq_probe_mma_stream_ex.argtypes = [_I64, _INT, _P, _P]
+    L.mxq_probe_mma_stream_ex.restype = _INT
     L.mxq_selftest_wait_timeout.argtypes = [_I64, _P, _P]
     L.mxq_selftest_wait_timeout.restype = _INT
     L.mxq_error_string.argtypes = [_INT]
@@ -515,12 +518,15 @@ def grouped_gemm_wgrad(dy_col_data, dy_col_scale, x_col_data, x_col_scale, m_spl
     return out
 
 
-def probe_mma_stream(mmas_per_sm=8192, status=None):
+def probe_mma_stream(mmas_per_sm=8192, status=None, random=False):
     """Launch the tensor-pipe ceiling probe (not part of the MXFP8 path): one CTA per SM issues
-    mmas_per_sm block-scaled 128x256x32 MMAs from resident shared memory. Returns its FLOPs
-    (2*128*256*32*mmas_per_sm*SMs); time it with CUDA events on the current stream."""
+    mmas_per_sm block-scaled 128x256x32 MMAs from resident shared memory, zero operands or (random)
+    pseudo-random E4M3 ones. Returns its FLOPs (2*128*256*32*mmas_per_sm*SMs); time it with CUDA
+    events on the current stream."""
     _need_flags(None, status)
-    _check(lib().mxq_probe_mma_stream(int(mmas_per_sm), _ptr(status), _stream()), "mxq_probe_mma_stream")
+    rc = lib().mxq_probe_mma_stream_ex(int(mmas_per_sm), PROBE_RANDOM if random else PROBE_ZEROS, _ptr(status),
+                                       _stream())
+    _check(rc, "mxq_probe_mma_stream_ex")
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     return 2.0 * 128 * 256 * 32 * mmas_per_sm * sms
 

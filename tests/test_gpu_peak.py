@@ -23,6 +23,21 @@ def test_probe_runs_and_reports_no_timeout(mxq):
     assert mxq.status_read(status) == 0
 
 
+def test_probe_with_random_operands_runs_and_reports_no_timeout(mxq):
+    status = mxq.new_status()
+    for n in (0, 4, 1024):
+        flops = mxq.probe_mma_stream(n, status=status, random=True)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert flops == 2.0 * 128 * 256 * 32 * n * sms
+    torch.cuda.synchronize()
+    assert mxq.status_read(status) == 0
+
+
+def test_probe_rejects_an_unknown_operand_mode(mxq):
+    rc = mxq.mxq.lib().mxq_probe_mma_stream_ex(4, 2, None, None)
+    assert rc == -7  # MXQ_ERR_FLAGS
+
+
 def test_probe_rejects_bad_counts(mxq):
     with pytest.raises(mxq.MXQError):
         mxq.probe_mma_stream(-1)
