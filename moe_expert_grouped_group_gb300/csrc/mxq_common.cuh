@@ -181,14 +181,19 @@ __device__ __forceinline__ void report_status(int32_t* d_status, int bits) {
 // run these same steps and agree bit for bit. Below g = -88.7 the
 // exponential overflows to +inf and the sigmoid is 0 (its exact value is
 // under 2^-127 there).
+// The hardware approximations with subnormal inputs and results flushed to
+// zero (.ftz), which spares their subnormal handling. In the sigmoid below
+// this changes nothing but s for g below about -87.3, where the exact
+// sigmoid is under 2^-126: s is then 0 instead of a subnormal. (A subnormal
+// ex2 result is absorbed by 1 + x either way.)
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 constexpr float kNegLog2e = -1.44269504088896341f;  // -log2(e), rounded to fp32

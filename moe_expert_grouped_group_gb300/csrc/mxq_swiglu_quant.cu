@@ -189,50 +189,56 @@ __device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, 
     uint8_t* rq = kRow ? a.row_q + r0 * Kout + col : nullptr;
     uint8_t* cq = kCol ? a.col_q + r0 * Kout + col : nullptr;
     __nv_bfloat16* dq = kDeq ? a.bf16_out + r0 * Kout + col : nullptr;
-    float bsum[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint64_t cinv01 = f2pack(cinv[0], cinv[1]), cinv23 = f2pack(cinv[2], cinv[3]);
+    uint64_t bsum01 = f2splat(0.f), bsum23 = f2splat(0.f);  // column sums, two columns per packed add
 #pragma unroll 2
     for (int r4 = 0; r4 < kPreRows; r4 += 4) {
         uint2 ow[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) ow[k] = o(r4 + k);
-        uint32_t packed = 0;
+        uint32_t packed = 0;  // rowwise codes of the four rows, one byte each
         if constexpr (kRow) {
+            uint32_t m[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t m = __vmaxu2(ow[k].x & 0x7FFF7FFFu, ow[k].y & 0x7FFF7FFFu);
-                packed |= (max(m & 0xFFFFu, m >> 16) >> 7) << (8 * k);
-            }
+            for (int k = 0; k < 4; ++k) m[k] = __vmaxu2(ow[k].x & 0x7FFF7FFFu, ow[k].y & 0x7FFF7FFFu);
+            // |bits| maxima of rows (0, 1) and (2, 3) as 16-bit halves, then their exponent bytes
+            const uint32_t v01 = __vmaxu2(__byte_perm(m[0], m[1], 0x5410), __byte_perm(m[0], m[1], 0x7632));
+            const uint32_t v23 = __vmaxu2(__byte_perm(m[2], m[3], 0x5410), __byte_perm(m[2], m[3], 0x7632));
+            packed = __byte_perm((v01 >> 7) & 0x00FF00FFu, (v23 >> 7) & 0x00FF00FFu, 0x6420);
 #pragma unroll
             for (int s = 4; s >= 1; s >>= 1) packed = __vmaxu4(packed, __shfl_xor_sync(0xffffffffu, packed, s));
+            packed = __vsubus4(packed, 0x08080808u);  // code = max(exponent - 8, 0), per byte
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = r4 + k;
             const uint2 u = ow[k];
-            const float v[4] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y)};
+            const uint64_t v01 = f2pack(bf16lo(u.x), bf16hi(u.x)), v23 = f2pack(bf16lo(u.y), bf16hi(u.y));
             if constexpr (kBias) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) bsum[j] += v[j];
+                bsum01 = f2add(bsum01, v01);
+                bsum23 = f2add(bsum23, v23);
             }
             if constexpr (kRow) {
-                const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
-                const float inv = inv_scale_from_code(code);
-                *reinterpret_cast<uint32_t*>(rq + r * Ku) =
-                    cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+                const uint32_t code = (packed >> (8 * k)) & 0xFFu;
+                const uint64_t inv = f2splat(inv_scale_from_code(code));
+                const float2 s01 = f2unpack(f2mul(v01, inv)), s23 = f2unpack(f2mul(v23, inv));
+                *reinterpret_cast<uint32_t*>(rq + r * Ku) = cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
                 if ((lane & 7) == 0) {
                     if (a.swizzle) sc.rs[((w & 1) * kPreRows + r) * 16 + rg * 4 + blk] = (uint8_t)code;
                     else a.row_s[(r0 + r) * (Kout / 32) + kt * 4 + blk] = (uint8_t)code;
                 }
             }
             if constexpr (kCol) {
-                *reinterpret_cast<uint32_t*>(cq + r * Ku) =
-                    cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) | (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
+                const float2 s01 = f2unpack(f2mul(v01, cinv01)), s23 = f2unpack(f2mul(v23, cinv23));
+                *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
             }
             if constexpr (kDeq) *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = u;
         }
     }
-    if constexpr (kBias)
-        *reinterpret_cast<float4*>(&sc.red[w][lane * 4]) = make_float4(bsum[0], bsum[1], bsum[2], bsum[3]);
+    if constexpr (kBias) {
+        const float2 s01 = f2unpack(bsum01), s23 = f2unpack(bsum23);
+        *reinterpret_cast<float4*>(&sc.red[w][lane * 4]) = make_float4(s01.x, s01.y, s23.x, s23.y);
+    }
 }
 
 // Write out one tile's scratch: the dbias partial of each of its 128 columns

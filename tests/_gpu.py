@@ -66,10 +66,11 @@ def first_diff(a: np.ndarray, b: np.ndarray):
 # (2^-9) relative, so after the final rounding the two may differ by one bf16
 # step at most (a rounding boundary between them). The one exception is the
 # sigmoid below g = -86: its exact value is under 2^-124 there, where fp32 has
-# only subnormals (or, below g = -88.7, 0) to hold it. The results may then be off
-# by up to the whole term, at most |g u| 2^-124 for h, |dh u| (1 + |g|) 2^-124
-# for dg and |dh g| 2^-124 for du, each allowed twice over to cover the final
-# rounding of the fp64 result.
+# only subnormals to hold it, and the kernels' flush-to-zero approximations
+# give 0 below g = -87.3 (and every fp32 sigmoid is 0 below g = -103.3). The
+# results may then be off by up to the whole term, at most |g u| 2^-124 for h,
+# |dh u| (1 + |g|) 2^-124 for dg and |dh g| 2^-124 for du, each allowed twice
+# over to cover the final rounding of the fp64 result.
 SIGMOID_FLUSH_G = -86.0
 SIGMOID_FLUSH_BOUND = 2.0 ** -123
 
