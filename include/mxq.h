@@ -333,7 +333,7 @@ MXQ_API int mxq_grouped_gemm_wgrad(const void* dy_col_data, const void* dy_col_s
  *   - (M/128) * N must be <= 2,097,152, else MXQ_ERR_SCRATCH_LIMIT;
  *   - the first call in each CUDA context of a device (the first call of the
  *     process on that device, and again after cudaDeviceReset) looks up the
- *     array's device address, so make it before any stream capture;
+ *     array's device address with a host-side symbol query;
  *   - all calls share the array (it keeps the last call's partials, which the
  *     next call overwrites before reading); calls that overlap on the GPU
  *     race, so serialise them. */

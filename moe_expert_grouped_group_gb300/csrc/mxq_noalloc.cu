@@ -17,8 +17,7 @@
 //     the device current, on the first call in each CUDA context of a device:
 //     the first call of the process on that device, and the first call after
 //     the device's context was destroyed and re-created (cudaDeviceReset), in
-//     which the module and its array may have moved. Make that first call
-//     before any stream capture;
+//     which the module and its array may have moved;
 //   - every call shares the one array and it keeps the last call's partials;
 //     the tile kernel overwrites every partial it later reads, so nothing
 //     needs clearing between calls;
