@@ -148,96 +148,123 @@ struct ColStats {
     }
 };
 
-// Encode the 16 rows of one output tile that warp w produced (bf16 in shared
-// memory, row r at rows + r*256, lane l reading columns 4l..4l+3) into output
-// column tile `kt` of an (M, Kout) tensor. The colwise scale of each 32-row
-// block comes from the exponent maxima of warps w and w^1 (the two halves of
-// the block); the rowwise scale of each row from the 8 lanes of its
-// 32-column block. Swizzled scale bytes are staged in `sc` for flush_scratch;
-// with kBias the lane's four column sums over the 16 rows (fp32, in row order)
-// go to sc.red[w].
-template <bool kRow, bool kCol, bool kDeq, bool kBias>
-__device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, int64_t mt, int64_t kt,
-                                            int64_t Kout, Scratch& sc, int w, int lane) {
-    auto o = [&](int r) { return *reinterpret_cast<const uint2*>(rows + r * (kTile * 2)); };
+// Encode the 16 rows of the kN output tiles that warp w produced (h, or dg and du; bf16 in shared
+// memory, tile q at rows + q*kTileBytes, row r at + r*256, lane l reading columns 4l..4l+3) into output
+// column tiles kt0 + q*kt_step of an (M, Kout) tensor, the tiles' rows side by side in each step so that
+// their independent chains overlap. The colwise scale of each 32-row block comes from the exponent maxima
+// of warps w and w^1 (the two halves of the block); the rowwise scale of each row from the 8 lanes of its
+// 32-column block. Swizzled scale bytes are staged in sc[q] for flush_scratch; with kBias the lane's four
+// column sums over the 16 rows (fp32, in row order) go to sc[q].red[w].
+template <int kN, bool kRow, bool kCol, bool kDeq, bool kBias>
+__device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, int64_t mt, int64_t kt0,
+                                            int64_t kt_step, int64_t Kout, Scratch* sc, int w, int lane) {
+    auto o = [&](int q, int r) { return *reinterpret_cast<const uint2*>(rows + q * kTileBytes + r * (kTile * 2)); };
     const int blk = lane >> 3;
     const int rg = w >> 1;                          // 32-row block of the tile
     const int64_t r0 = mt * kTile + w * kPreRows;   // first row of this warp
-    const int64_t col = kt * kTile + lane * 4;
     const uint32_t Ku = (uint32_t)Kout;
 
-    uint32_t ccode[4] = {0, 0, 0, 0};
-    float cinv[4] = {1.f, 1.f, 1.f, 1.f};
-    if constexpr (kCol) {
-        const uint32_t e = __vmaxu4(sc.xexp[w][lane], sc.xexp[w ^ 1][lane]);
-        uint32_t packed = 0;
+    uint64_t cinv01[kN], cinv23[kN], bsum01[kN], bsum23[kN];
+    uint8_t *rq[kN], *cq[kN];
+    __nv_bfloat16* dq[kN];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            ccode[j] = (uint32_t)max((int)((e >> (8 * j)) & 0xFFu) - 8, 0);
-            cinv[j] = inv_scale_from_code(ccode[j]);
-            packed |= ccode[j] << (8 * j);
-        }
-        if ((w & 1) == 0) {
-            if (a.swizzle) {
+    for (int q = 0; q < kN; ++q) {
+        const int64_t kt = kt0 + q * kt_step;
+        const int64_t col = kt * kTile + lane * 4;
+        uint32_t ccode[4] = {0, 0, 0, 0};
+        float cinv[4] = {1.f, 1.f, 1.f, 1.f};
+        if constexpr (kCol) {
+            const uint32_t e = __vmaxu4(sc[q].xexp[w][lane], sc[q].xexp[w ^ 1][lane]);
+            uint32_t packed = 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) sc.cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
-            } else {
-                *reinterpret_cast<uint32_t*>(a.col_s + (mt * 4 + rg) * Kout + col) = packed;
+            for (int j = 0; j < 4; ++j) {
+                ccode[j] = (uint32_t)max((int)((e >> (8 * j)) & 0xFFu) - 8, 0);
+                cinv[j] = inv_scale_from_code(ccode[j]);
+                packed |= ccode[j] << (8 * j);
+            }
+            if ((w & 1) == 0) {
+                if (a.swizzle) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sc[q].cs[(4 * (lane & 7) + j) * 16 + blk * 4 + rg] = (uint8_t)ccode[j];
+                } else {
+                    *reinterpret_cast<uint32_t*>(a.col_s + (mt * 4 + rg) * Kout + col) = packed;
+                }
             }
         }
+        rq[q] = kRow ? a.row_q + r0 * Kout + col : nullptr;
+        cq[q] = kCol ? a.col_q + r0 * Kout + col : nullptr;
+        dq[q] = kDeq ? a.bf16_out + r0 * Kout + col : nullptr;
+        cinv01[q] = f2pack(cinv[0], cinv[1]);
+        cinv23[q] = f2pack(cinv[2], cinv[3]);
+        bsum01[q] = bsum23[q] = f2splat(0.f);  // column sums, two columns per packed add
     }
-    uint8_t* rq = kRow ? a.row_q + r0 * Kout + col : nullptr;
-    uint8_t* cq = kCol ? a.col_q + r0 * Kout + col : nullptr;
-    __nv_bfloat16* dq = kDeq ? a.bf16_out + r0 * Kout + col : nullptr;
-    const uint64_t cinv01 = f2pack(cinv[0], cinv[1]), cinv23 = f2pack(cinv[2], cinv[3]);
-    uint64_t bsum01 = f2splat(0.f), bsum23 = f2splat(0.f);  // column sums, two columns per packed add
 #pragma unroll 2
     for (int r4 = 0; r4 < kPreRows; r4 += 4) {
-        uint2 ow[4];
+        uint2 ow[kN][4];
+        uint32_t packed[kN];  // rowwise codes of the four rows, one byte each
 #pragma unroll
-        for (int k = 0; k < 4; ++k) ow[k] = o(r4 + k);
-        uint32_t packed = 0;  // rowwise codes of the four rows, one byte each
+        for (int q = 0; q < kN; ++q) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ow[q][k] = o(q, r4 + k);
+            packed[q] = 0;
+            if constexpr (kRow) {
+                uint32_t m[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    m[k] = __vmaxu2(ow[q][k].x & 0x7FFF7FFFu, ow[q][k].y & 0x7FFF7FFFu);
+                // |bits| maxima of rows (0, 1) and (2, 3) as 16-bit halves, then their exponent bytes
+                const uint32_t v01 = __vmaxu2(__byte_perm(m[0], m[1], 0x5410), __byte_perm(m[0], m[1], 0x7632));
+                const uint32_t v23 = __vmaxu2(__byte_perm(m[2], m[3], 0x5410), __byte_perm(m[2], m[3], 0x7632));
+                packed[q] = __byte_perm((v01 >> 7) & 0x00FF00FFu, (v23 >> 7) & 0x00FF00FFu, 0x6420);
+            }
+        }
         if constexpr (kRow) {
-            uint32_t m[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) m[k] = __vmaxu2(ow[k].x & 0x7FFF7FFFu, ow[k].y & 0x7FFF7FFFu);
-            // |bits| maxima of rows (0, 1) and (2, 3) as 16-bit halves, then their exponent bytes
-            const uint32_t v01 = __vmaxu2(__byte_perm(m[0], m[1], 0x5410), __byte_perm(m[0], m[1], 0x7632));
-            const uint32_t v23 = __vmaxu2(__byte_perm(m[2], m[3], 0x5410), __byte_perm(m[2], m[3], 0x7632));
-            packed = __byte_perm((v01 >> 7) & 0x00FF00FFu, (v23 >> 7) & 0x00FF00FFu, 0x6420);
+            for (int s = 4; s >= 1; s >>= 1)
 #pragma unroll
-            for (int s = 4; s >= 1; s >>= 1) packed = __vmaxu4(packed, __shfl_xor_sync(0xffffffffu, packed, s));
-            packed = __vsubus4(packed, 0x08080808u);  // code = max(exponent - 8, 0), per byte
+                for (int q = 0; q < kN; ++q)
+                    packed[q] = __vmaxu4(packed[q], __shfl_xor_sync(0xffffffffu, packed[q], s));
+#pragma unroll
+            for (int q = 0; q < kN; ++q) packed[q] = __vsubus4(packed[q], 0x08080808u);  // max(exponent - 8, 0)
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int r = r4 + k;
-            const uint2 u = ow[k];
-            const uint64_t v01 = f2pack(bf16lo(u.x), bf16hi(u.x)), v23 = f2pack(bf16lo(u.y), bf16hi(u.y));
-            if constexpr (kBias) {
-                bsum01 = f2add(bsum01, v01);
-                bsum23 = f2add(bsum23, v23);
-            }
-            if constexpr (kRow) {
-                const uint32_t code = (packed >> (8 * k)) & 0xFFu;
-                const uint64_t inv = f2splat(inv_scale_from_code(code));
-                const float2 s01 = f2unpack(f2mul(v01, inv)), s23 = f2unpack(f2mul(v23, inv));
-                *reinterpret_cast<uint32_t*>(rq + r * Ku) = cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
-                if ((lane & 7) == 0) {
-                    if (a.swizzle) sc.rs[((w & 1) * kPreRows + r) * 16 + rg * 4 + blk] = (uint8_t)code;
-                    else a.row_s[(r0 + r) * (Kout / 32) + kt * 4 + blk] = (uint8_t)code;
+#pragma unroll
+            for (int q = 0; q < kN; ++q) {
+                const uint2 u = ow[q][k];
+                const uint64_t v01 = f2pack(bf16lo(u.x), bf16hi(u.x)), v23 = f2pack(bf16lo(u.y), bf16hi(u.y));
+                if constexpr (kBias) {
+                    bsum01[q] = f2add(bsum01[q], v01);
+                    bsum23[q] = f2add(bsum23[q], v23);
                 }
+                if constexpr (kRow) {
+                    const uint32_t code = (packed[q] >> (8 * k)) & 0xFFu;
+                    const uint64_t inv = f2splat(inv_scale_from_code(code));
+                    const float2 s01 = f2unpack(f2mul(v01, inv)), s23 = f2unpack(f2mul(v23, inv));
+                    *reinterpret_cast<uint32_t*>(rq[q] + r * Ku) =
+                        cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
+                    if ((lane & 7) == 0) {
+                        if (a.swizzle) sc[q].rs[((w & 1) * kPreRows + r) * 16 + rg * 4 + blk] = (uint8_t)code;
+                        else a.row_s[(r0 + r) * (Kout / 32) + (kt0 + q * kt_step) * 4 + blk] = (uint8_t)code;
+                    }
+                }
+                if constexpr (kCol) {
+                    const float2 s01 = f2unpack(f2mul(v01, cinv01[q])), s23 = f2unpack(f2mul(v23, cinv23[q]));
+                    *reinterpret_cast<uint32_t*>(cq[q] + r * Ku) =
+                        cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
+                }
+                if constexpr (kDeq) *reinterpret_cast<uint2*>(dq[q] + (size_t)r * Ku) = u;
             }
-            if constexpr (kCol) {
-                const float2 s01 = f2unpack(f2mul(v01, cinv01)), s23 = f2unpack(f2mul(v23, cinv23));
-                *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
-            }
-            if constexpr (kDeq) *reinterpret_cast<uint2*>(dq + (size_t)r * Ku) = u;
         }
     }
     if constexpr (kBias) {
-        const float2 s01 = f2unpack(bsum01), s23 = f2unpack(bsum23);
-        *reinterpret_cast<float4*>(&sc.red[w][lane * 4]) = make_float4(s01.x, s01.y, s23.x, s23.y);
+#pragma unroll
+        for (int q = 0; q < kN; ++q) {
+            const float2 s01 = f2unpack(bsum01[q]), s23 = f2unpack(bsum23[q]);
+            *reinterpret_cast<float4*>(&sc[q].red[w][lane * 4]) = make_float4(s01.x, s01.y, s23.x, s23.y);
+        }
     }
 }
 
@@ -389,10 +416,7 @@ __global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
         bar_compute();  // every warp's colwise statistics are in
 
         const int64_t Kout = kBwd ? 2 * a.F : a.F;
-#pragma unroll
-        for (int q = 0; q < kOut; ++q)
-            encode_rows<kRow, kCol, kDeq, kBias>(g_row + q * kTileBytes, a, mt, q ? tilesF + ft : ft, Kout, s_sc[q],
-                                                 warp, lane);
+        encode_rows<kOut, kRow, kCol, kDeq, kBias>(g_row, a, mt, ft, tilesF, Kout, s_sc, warp, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty);  // this warp is done with the stage
         bar_compute();                      // scratch complete
