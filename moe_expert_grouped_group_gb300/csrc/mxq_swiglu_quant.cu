@@ -150,14 +150,18 @@ struct ColStats {
 
 // Encode the 16 rows of the kN output tiles that warp w produced (h, or dg and du; bf16 in shared
 // memory, tile q at rows + q*kTileBytes, row r at + r*256, lane l reading columns 4l..4l+3) into output
-// column tiles kt0 + q*kt_step of an (M, Kout) tensor, the tiles' rows side by side in each step so that
-// their independent chains overlap. The colwise scale of each 32-row block comes from the exponent maxima
+// column tiles kt0 + q*kt_step of an (M, Kout) tensor. Each step encodes four rows of every tile, and with
+// one tile four rows of each half of the warp's rows, so that the step holds two independent chains for
+// the warp's instructions to overlap. The colwise scale of each 32-row block comes from the exponent maxima
 // of warps w and w^1 (the two halves of the block); the rowwise scale of each row from the 8 lanes of its
 // 32-column block. Swizzled scale bytes are staged in sc[q] for flush_scratch; with kBias the lane's four
 // column sums over the 16 rows (fp32, in row order) go to sc[q].red[w].
 template <int kN, bool kRow, bool kCol, bool kDeq, bool kBias>
 __device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, int64_t mt, int64_t kt0,
                                             int64_t kt_step, int64_t Kout, Scratch* sc, int w, int lane) {
+    // chains per step: tile q = c / kG, rows from g * (kPreRows / kG) on, g = c % kG
+    constexpr int kG = kN == 1 && !kBias ? 2 : 1;  // the column sums keep row order: one chain per tile
+    constexpr int kC = kN * kG, kSpan = kPreRows / kG;
     auto o = [&](int q, int r) { return *reinterpret_cast<const uint2*>(rows + q * kTileBytes + r * (kTile * 2)); };
     const int blk = lane >> 3;
     const int rg = w >> 1;                          // 32-row block of the tile
@@ -200,47 +204,48 @@ __device__ __forceinline__ void encode_rows(const uint8_t* rows, const Args& a, 
         bsum01[q] = bsum23[q] = f2splat(0.f);  // column sums, two columns per packed add
     }
 #pragma unroll 2
-    for (int r4 = 0; r4 < kPreRows; r4 += 4) {
-        uint2 ow[kN][4];
-        uint32_t packed[kN];  // rowwise codes of the four rows, one byte each
+    for (int r4 = 0; r4 < kSpan; r4 += 4) {
+        uint2 ow[kC][4];
+        uint32_t packed[kC];  // rowwise codes of the chain's four rows, one byte each
 #pragma unroll
-        for (int q = 0; q < kN; ++q) {
+        for (int c = 0; c < kC; ++c) {
+            const int q = c / kG, rb = (c % kG) * kSpan + r4;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) ow[q][k] = o(q, r4 + k);
-            packed[q] = 0;
+            for (int k = 0; k < 4; ++k) ow[c][k] = o(q, rb + k);
+            packed[c] = 0;
             if constexpr (kRow) {
                 uint32_t m[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    m[k] = __vmaxu2(ow[q][k].x & 0x7FFF7FFFu, ow[q][k].y & 0x7FFF7FFFu);
+                    m[k] = __vmaxu2(ow[c][k].x & 0x7FFF7FFFu, ow[c][k].y & 0x7FFF7FFFu);
                 // |bits| maxima of rows (0, 1) and (2, 3) as 16-bit halves, then their exponent bytes
                 const uint32_t v01 = __vmaxu2(__byte_perm(m[0], m[1], 0x5410), __byte_perm(m[0], m[1], 0x7632));
                 const uint32_t v23 = __vmaxu2(__byte_perm(m[2], m[3], 0x5410), __byte_perm(m[2], m[3], 0x7632));
-                packed[q] = __byte_perm((v01 >> 7) & 0x00FF00FFu, (v23 >> 7) & 0x00FF00FFu, 0x6420);
+                packed[c] = __byte_perm((v01 >> 7) & 0x00FF00FFu, (v23 >> 7) & 0x00FF00FFu, 0x6420);
             }
         }
         if constexpr (kRow) {
 #pragma unroll
             for (int s = 4; s >= 1; s >>= 1)
 #pragma unroll
-                for (int q = 0; q < kN; ++q)
-                    packed[q] = __vmaxu4(packed[q], __shfl_xor_sync(0xffffffffu, packed[q], s));
+                for (int c = 0; c < kC; ++c)
+                    packed[c] = __vmaxu4(packed[c], __shfl_xor_sync(0xffffffffu, packed[c], s));
 #pragma unroll
-            for (int q = 0; q < kN; ++q) packed[q] = __vsubus4(packed[q], 0x08080808u);  // max(exponent - 8, 0)
+            for (int c = 0; c < kC; ++c) packed[c] = __vsubus4(packed[c], 0x08080808u);  // max(exponent - 8, 0)
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int r = r4 + k;
 #pragma unroll
-            for (int q = 0; q < kN; ++q) {
-                const uint2 u = ow[q][k];
+            for (int c = 0; c < kC; ++c) {
+                const int q = c / kG, r = (c % kG) * kSpan + r4 + k;
+                const uint2 u = ow[c][k];
                 const uint64_t v01 = f2pack(bf16lo(u.x), bf16hi(u.x)), v23 = f2pack(bf16lo(u.y), bf16hi(u.y));
                 if constexpr (kBias) {
                     bsum01[q] = f2add(bsum01[q], v01);
                     bsum23[q] = f2add(bsum23[q], v23);
                 }
                 if constexpr (kRow) {
-                    const uint32_t code = (packed[q] >> (8 * k)) & 0xFFu;
+                    const uint32_t code = (packed[c] >> (8 * k)) & 0xFFu;
                     const uint64_t inv = f2splat(inv_scale_from_code(code));
                     const float2 s01 = f2unpack(f2mul(v01, inv)), s23 = f2unpack(f2mul(v23, inv));
                     *reinterpret_cast<uint32_t*>(rq[q] + r * Ku) =
