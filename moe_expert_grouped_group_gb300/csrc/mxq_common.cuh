@@ -212,6 +212,61 @@ __device__ __forceinline__ void swiglu_grads(float d, float g, float u, float& d
     du = __fmul_rn(d, __fmul_rn(g, s));
 }
 
+// The fp32 SwiGLU steps of mxq_common.cuh on two values at once. Each packed
+// instruction (add / sub / mul .rn.f32x2) rounds each lane to nearest even
+// without flushing subnormals, exactly as the scalar instruction of the same
+// step does, so every result is bit-identical to swiglu_h / swiglu_grads.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t v) {
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(v));
+    return o;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2splat(float a) { return f2pack(a, a); }
+
+// sigmoid_f32 on two lanes: the product and the sum packed, the exponential and reciprocal per lane
+__device__ __forceinline__ uint64_t sigmoid_x2(float2 g) {
+    const float2 t = f2unpack(f2mul(f2pack(g.x, g.y), f2splat(kNegLog2e)));
+    const float2 d = f2unpack(f2add(f2splat(1.0f), f2pack(ex2_approx(t.x), ex2_approx(t.y))));
+    return f2pack(rcp_approx(d.x), rcp_approx(d.y));
+}
+// swiglu_h on two lanes: (g * s) * u
+__device__ __forceinline__ float2 swiglu_h_x2(float2 g, float2 u) {
+    return f2unpack(f2mul(f2mul(f2pack(g.x, g.y), sigmoid_x2(g)), f2pack(u.x, u.y)));
+}
+// swiglu_grads on two lanes: dg = ((d * u) * s) * fma(g, 1 - s, 1), du = d * (g * s)
+__device__ __forceinline__ void swiglu_grads_x2(float2 d, float2 g, float2 u, float2& dg, float2& du) {
+    const uint64_t s = sigmoid_x2(g);
+    const uint64_t gp = f2pack(g.x, g.y), dp = f2pack(d.x, d.y), one = f2splat(1.0f);
+    const uint64_t fac = f2fma(gp, f2sub(one, s), one);
+    dg = f2unpack(f2mul(f2mul(f2mul(dp, f2pack(u.x, u.y)), s), fac));
+    du = f2unpack(f2mul(dp, f2mul(gp, s)));
+}
+
 // ------------------------------------------ mbarrier and TMA wrappers (PTX)
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bound on any on-chip wait
 

@@ -289,12 +289,14 @@ __device__ __forceinline__ void quant_block32(const uint32_t (&w)[16], const Par
 #pragma unroll
         for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
         const uint32_t code = (uint32_t)max((int)(max(m & 0xFFFFu, m >> 16) >> 7) - 8, 0);
-        const float inv = inv_scale_from_code(code);
+        const uint64_t inv = f2splat(inv_scale_from_code(code));
         uint32_t o[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t w0 = w[2 * k], w1 = w[2 * k + 1];
-            o[k] = cvt_e4m3x2(bf16lo(w0) * inv, bf16hi(w0) * inv) | (cvt_e4m3x2(bf16lo(w1) * inv, bf16hi(w1) * inv) << 16);
+            const float2 a = f2unpack(f2mul(f2pack(bf16lo(w0), bf16hi(w0)), inv));
+            const float2 b = f2unpack(f2mul(f2pack(bf16lo(w1), bf16hi(w1)), inv));
+            o[k] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
         }
         uint4* d = reinterpret_cast<uint4*>(p.q_row + row * W + col0);
         d[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -309,10 +311,8 @@ __device__ __forceinline__ void quant_block32(const uint32_t (&w)[16], const Par
     // colwise
     uint32_t e4[8];  // four columns per word, one exponent byte each
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t a = w[2 * i], b = w[2 * i + 1];
-        e4[i] = ((a >> 7) & 0xFFu) | (((a >> 23) & 0xFFu) << 8) | (((b >> 7) & 0xFFu) << 16) | (((b >> 23) & 0xFFu) << 24);
-    }
+    for (int i = 0; i < 8; ++i)  // the exponent fields of both halves of two words: bytes 0 and 2 of each
+        e4[i] = __byte_perm((w[2 * i] >> 7) & 0x00FF00FFu, (w[2 * i + 1] >> 7) & 0x00FF00FFu, 0x6420);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)
 #pragma unroll
@@ -326,11 +326,13 @@ __device__ __forceinline__ void quant_block32(const uint32_t (&w)[16], const Par
         for (int k = 0; k < 4; ++k) {
             const uint32_t cw = e4[4 * v + k];
             const uint32_t w0 = w[8 * v + 2 * k], w1 = w[8 * v + 2 * k + 1];
-            o[k] = cvt_e4m3x2(bf16lo(w0) * inv_scale_from_code(cw & 0xFFu),
-                              bf16hi(w0) * inv_scale_from_code((cw >> 8) & 0xFFu)) |
-                   (cvt_e4m3x2(bf16lo(w1) * inv_scale_from_code((cw >> 16) & 0xFFu),
-                               bf16hi(w1) * inv_scale_from_code(cw >> 24))
-                    << 16);
+            const float2 a = f2unpack(f2mul(f2pack(bf16lo(w0), bf16hi(w0)),
+                                            f2pack(inv_scale_from_code(cw & 0xFFu),
+                                                   inv_scale_from_code((cw >> 8) & 0xFFu))));
+            const float2 b = f2unpack(f2mul(f2pack(bf16lo(w1), bf16hi(w1)),
+                                            f2pack(inv_scale_from_code((cw >> 16) & 0xFFu),
+                                                   inv_scale_from_code(cw >> 24))));
+            o[k] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
         }
         *reinterpret_cast<uint4*>(p.q_col + row * W + col0 + 16 * v) = make_uint4(o[0], o[1], o[2], o[3]);
     }
@@ -471,20 +473,21 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
         const __nv_bfloat16* bias = p.bias ? p.bias + (int64_t)T.e * p.N + hp * F + f0 : nullptr;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-            float f[8];
+            uint64_t f2[4];  // accumulator pairs, plus the bias pairs in one packed add each
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(r[64 * hp + 8 * v + j]);
+            for (int j = 0; j < 4; ++j)
+                f2[j] = f2pack(__uint_as_float(r[64 * hp + 8 * v + 2 * j]), __uint_as_float(r[64 * hp + 8 * v + 2 * j + 1]));
             if (bias) {
                 const uint4 bw = __ldg(reinterpret_cast<const uint4*>(bias) + v);
                 const uint32_t ws[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    f[2 * j] += __uint_as_float(ws[j] << 16);
-                    f[2 * j + 1] += __uint_as_float(ws[j] & 0xFFFF0000u);
-                }
+                for (int j = 0; j < 4; ++j) f2[j] = f2add(f2[j], f2pack(bf16lo(ws[j]), bf16hi(ws[j])));
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) y[32 * hp + 4 * v + j] = bf16x2_bits(f[2 * j], f[2 * j + 1]);
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = f2unpack(f2[j]);
+                y[32 * hp + 4 * v + j] = bf16x2_bits(f.x, f.y);
+            }
         }
     }
     // y1 through four staged 32x32 boxes: gate f0, f0+32; up F+f0, F+f0+32
@@ -513,8 +516,11 @@ __device__ __forceinline__ void swiglu_tile_epilogue(const Params& p, const Tile
     // h = silu(g) * u, rounded to bf16
     uint32_t hw[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        hw[i] = bf16x2_bits(swiglu_h(bf16lo(y[i]), bf16lo(y[32 + i])), swiglu_h(bf16hi(y[i]), bf16hi(y[32 + i])));
+    for (int i = 0; i < 32; ++i) {
+        const float2 h2 = swiglu_h_x2(make_float2(bf16lo(y[i]), bf16hi(y[i])),
+                                      make_float2(bf16lo(y[32 + i]), bf16hi(y[32 + i])));
+        hw[i] = bf16x2_bits(h2.x, h2.y);
+    }
 
     if (p.side) {
         uint4* h_out = reinterpret_cast<uint4*>(p.side + (T.a_row + q * 32 + lane) * F + f0);
