@@ -11,6 +11,7 @@ m_splits is a CUDA int64 tensor (host m_splits are rejected by the library).
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 
 import torch
@@ -30,8 +31,8 @@ SYMBOLS = [
     "mxq_swiglu_fwd", "mxq_swiglu_bwd", "mxq_status_read", "mxq_error_string", "mxq_last_cuda_error",
     "mxq_grouped_dbias_noalloc", "mxq_swiglu_quantize", "mxq_swiglu_bwd_quantize", "mxq_group_quantize_scaled_bias",
     "mxq_requant_colwise_scaled_bias", "mxq_grouped_gemm_fprop_swiglu", "mxq_grouped_gemm_dgrad_swiglu",
-    "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex", "mxq_probe_mma_stream", "mxq_probe_mma_stream_ex",
-    "mxq_selftest_wait_timeout",
+    "mxq_scale_bytes_grouped", "mxq_grouped_gemm_fprop_ex", "mxq_grouped_gemm_dgrad_ex", "mxq_probe_mma_stream",
+    "mxq_probe_mma_stream_ex", "mxq_selftest_wait_timeout",
 ]
 
 
@@ -114,7 +115,14 @@ def _ptr(t):
     return t.data_ptr()
 
 
+# The current stream's raw handle without building a torch Stream object (about 3 us a call
+# otherwise, as much as a small kernel); torch's public call where the fast one is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream():
+    if _raw_stream is not None:
+        return _raw_stream(torch.cuda.current_device())
     return torch.cuda.current_stream().cuda_stream
 
 
@@ -163,15 +171,18 @@ def _splits(m_splits):
     return m_splits
 
 
+@functools.lru_cache(maxsize=4096)
 def scale_bytes(rows: int, cols: int, colwise: bool) -> int:
     return int(lib().mxq_scale_bytes(rows, cols, int(colwise)))
 
 
+@functools.lru_cache(maxsize=4096)
 def scale_bytes_grouped(rows: int, cols: int, E: int, colwise: bool) -> int:
     """A scale-buffer size that holds the per-expert padded layout for any split of `rows`."""
     return int(lib().mxq_scale_bytes_grouped(rows, cols, E, int(colwise)))
 
 
+@functools.lru_cache(maxsize=4096)
 def workspace_bytes(op: int, M: int, N: int, K: int, E: int, flags: int = 0) -> int:
     return int(lib().mxq_workspace_bytes(op, M, N, K, E, flags))
 
@@ -190,6 +201,13 @@ def _u8(n, dev):
     return torch.empty(n, dtype=torch.uint8, device=dev)
 
 
+def _fill(o, key, make):
+    """o[key] = make() unless the caller supplied it (setdefault with the default built only when needed:
+    an eager default would allocate every output buffer on every call)."""
+    if key not in o:
+        o[key] = make()
+
+
 def group_quantize(x, m_splits=None, E=None, rowwise=True, colwise=True, swizzle=True, dbias=False,
                    noop=None, status=None, out=None, workspace=None, pad_experts=False):
     """bf16 x (M, K) -> dict(row_data, row_scale, col_data, col_scale, dbias).
@@ -205,16 +223,16 @@ def group_quantize(x, m_splits=None, E=None, rowwise=True, colwise=True, swizzle
              | (PAD_EXPERTS if pad_experts else 0))
     o = dict(out or {})
     if rowwise:
-        o.setdefault("row_data", _u8((M, K), dev))
+        _fill(o, "row_data", lambda: _u8((M, K), dev))
         rs = scale_bytes_grouped(M, K, E, False) if (pad_experts and swizzle) else scale_bytes(M, K, False)
-        o.setdefault("row_scale", _u8(rs, dev))
+        _fill(o, "row_scale", lambda: _u8(rs, dev))
     if colwise:
-        o.setdefault("col_data", _u8((M, K), dev))
-        o.setdefault("col_scale", _u8(scale_bytes_grouped(M, K, E, True) if pad_experts else scale_bytes(M, K, True),
-                                      dev))
+        _fill(o, "col_data", lambda: _u8((M, K), dev))
+        cs = scale_bytes_grouped(M, K, E, True) if pad_experts else scale_bytes(M, K, True)
+        _fill(o, "col_scale", lambda: _u8(cs, dev))
     ws = None
     if dbias:
-        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+        _fill(o, "dbias", lambda: torch.empty((E, K), dtype=torch.float32, device=dev))
         ws = workspace if workspace is not None else _u8(
             max(16, workspace_bytes(OP_GROUP_QUANTIZE, M, 0, K, E, flags)), dev)
     _need(x, "x", M * K * 2, _BF16)
@@ -246,15 +264,15 @@ def requant_colwise(row_data, row_scale_compact, m_splits, colwise=True, swizzle
     sb = (lambda r, c, cw: scale_bytes_grouped(r, c, E, cw)) if pad_experts else scale_bytes
     o = dict(out or {})
     if colwise:
-        o.setdefault("col_data", _u8((M, K), dev))
-        o.setdefault("col_scale", _u8(sb(M, K, True), dev))
+        _fill(o, "col_data", lambda: _u8((M, K), dev))
+        _fill(o, "col_scale", lambda: _u8(sb(M, K, True), dev))
     if row_scale_swizzled:
-        o.setdefault("row_scale_swizzled", _u8(sb(M, K, False), dev))
+        _fill(o, "row_scale_swizzled", lambda: _u8(sb(M, K, False), dev))
     if dequant:
-        o.setdefault("dequant", torch.empty((M, K), dtype=torch.bfloat16, device=dev))
+        _fill(o, "dequant", lambda: torch.empty((M, K), dtype=torch.bfloat16, device=dev))
     ws = None
     if dbias:
-        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+        _fill(o, "dbias", lambda: torch.empty((E, K), dtype=torch.float32, device=dev))
         ws = workspace if workspace is not None else _u8(
             max(16, workspace_bytes(OP_REQUANT_COLWISE, M, 0, K, E, flags)), dev)
     _need(row_data, "row_data", M * K, _BYTE)
@@ -284,15 +302,15 @@ def group_quantize_scaled_bias(x, m_splits, probs, bias, rowwise=True, colwise=T
     flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
     o = dict(out or {})
     if rowwise:
-        o.setdefault("row_data", _u8((M, K), dev))
-        o.setdefault("row_scale", _u8(scale_bytes(M, K, False), dev))
+        _fill(o, "row_data", lambda: _u8((M, K), dev))
+        _fill(o, "row_scale", lambda: _u8(scale_bytes(M, K, False), dev))
     if colwise:
-        o.setdefault("col_data", _u8((M, K), dev))
-        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+        _fill(o, "col_data", lambda: _u8((M, K), dev))
+        _fill(o, "col_scale", lambda: _u8(scale_bytes(M, K, True), dev))
     if dbias:
-        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+        _fill(o, "dbias", lambda: torch.empty((E, K), dtype=torch.float32, device=dev))
     if dprobs:
-        o.setdefault("dprobs", torch.empty((M,), dtype=torch.float32, device=dev))
+        _fill(o, "dprobs", lambda: torch.empty((M,), dtype=torch.float32, device=dev))
     ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SCALED_BIAS, M, 0, K, E)), dev)
     _need(x, "x", M * K * 2, _BF16)
     _need(probs, "probs", M * 4, _F32)
@@ -324,16 +342,16 @@ def requant_colwise_scaled_bias(row_data, row_scale_compact, m_splits, probs, bi
              | (DEQUANT_OUT if dequant else 0))
     o = dict(out or {})
     if colwise:
-        o.setdefault("col_data", _u8((M, K), dev))
-        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+        _fill(o, "col_data", lambda: _u8((M, K), dev))
+        _fill(o, "col_scale", lambda: _u8(scale_bytes(M, K, True), dev))
     if row_scale_swizzled:
-        o.setdefault("row_scale_swizzled", _u8(scale_bytes(M, K, False), dev))
+        _fill(o, "row_scale_swizzled", lambda: _u8(scale_bytes(M, K, False), dev))
     if dequant:
-        o.setdefault("dequant", torch.empty((M, K), dtype=torch.bfloat16, device=dev))
+        _fill(o, "dequant", lambda: torch.empty((M, K), dtype=torch.bfloat16, device=dev))
     if dbias:
-        o.setdefault("dbias", torch.empty((E, K), dtype=torch.float32, device=dev))
+        _fill(o, "dbias", lambda: torch.empty((E, K), dtype=torch.float32, device=dev))
     if dprobs:
-        o.setdefault("dprobs", torch.empty((M,), dtype=torch.float32, device=dev))
+        _fill(o, "dprobs", lambda: torch.empty((M,), dtype=torch.float32, device=dev))
     ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SCALED_BIAS, M, 0, K, E)), dev)
     _need(row_data, "row_data", M * K, _BYTE)
     _need(row_scale_compact, "row_scale_compact", M * (K // 32), _BYTE)
@@ -405,13 +423,13 @@ def grouped_gemm_fprop_swiglu(x_data, x_scale, w1_data, w1_scale, m_splits, bias
     m_splits = _splits(m_splits)
     dev = x_data.device
     o = dict(out or {})
-    o.setdefault("y1", torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev))
-    o.setdefault("row_data", _u8((M, F), dev))
-    o.setdefault("row_scale", _u8(scale_bytes(M, F, False), dev))
-    o.setdefault("col_data", _u8((M, F), dev))
-    o.setdefault("col_scale", _u8(scale_bytes(M, F, True), dev))
+    _fill(o, "y1", lambda: torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev))
+    _fill(o, "row_data", lambda: _u8((M, F), dev))
+    _fill(o, "row_scale", lambda: _u8(scale_bytes(M, F, False), dev))
+    _fill(o, "col_data", lambda: _u8((M, F), dev))
+    _fill(o, "col_scale", lambda: _u8(scale_bytes(M, F, True), dev))
     if h_out:
-        o.setdefault("h", torch.empty((M, F), dtype=torch.bfloat16, device=dev))
+        _fill(o, "h", lambda: torch.empty((M, F), dtype=torch.bfloat16, device=dev))
     _need(o.get("h"), "h", M * F * 2, _BF16)
     _need(x_data, "x_data", M * K, _BYTE)
     _need(x_scale, "x_scale", scale_bytes(M, K, False), _BYTE)
@@ -464,16 +482,16 @@ def grouped_gemm_dgrad_swiglu(dy_data, dy_scale, w_col_data, w_col_scale, y1, m_
     m_splits = _splits(m_splits)
     dev = dy_data.device
     o = dict(out or {})
-    o.setdefault("row_data", _u8((M, 2 * F), dev))
-    o.setdefault("row_scale", _u8(scale_bytes(M, 2 * F, False), dev))
-    o.setdefault("col_data", _u8((M, 2 * F), dev))
-    o.setdefault("col_scale", _u8(scale_bytes(M, 2 * F, True), dev))
+    _fill(o, "row_data", lambda: _u8((M, 2 * F), dev))
+    _fill(o, "row_scale", lambda: _u8(scale_bytes(M, 2 * F, False), dev))
+    _fill(o, "col_data", lambda: _u8((M, 2 * F), dev))
+    _fill(o, "col_scale", lambda: _u8(scale_bytes(M, 2 * F, True), dev))
     if dy_out:
-        o.setdefault("dy", torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev))
+        _fill(o, "dy", lambda: torch.empty((M, 2 * F), dtype=torch.bfloat16, device=dev))
     _need(o.get("dy"), "dy", M * 2 * F * 2, _BF16)
     ws = None
     if dbias:
-        o.setdefault("dbias", torch.empty((E, 2 * F), dtype=torch.float32, device=dev))
+        _fill(o, "dbias", lambda: torch.empty((E, 2 * F), dtype=torch.float32, device=dev))
         ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_GEMM_DGRAD_SWIGLU, M, N, F, E)),
                                                          dev)
     _need(dy_data, "dy_data", M * N, _BYTE)
@@ -559,11 +577,11 @@ def swiglu_bwd(dh, y, out=None):
 
 def _quant_outputs(o, M, K, rowwise, colwise, dev):
     if rowwise:
-        o.setdefault("row_data", _u8((M, K), dev))
-        o.setdefault("row_scale", _u8(scale_bytes(M, K, False), dev))
+        _fill(o, "row_data", lambda: _u8((M, K), dev))
+        _fill(o, "row_scale", lambda: _u8(scale_bytes(M, K, False), dev))
     if colwise:
-        o.setdefault("col_data", _u8((M, K), dev))
-        o.setdefault("col_scale", _u8(scale_bytes(M, K, True), dev))
+        _fill(o, "col_data", lambda: _u8((M, K), dev))
+        _fill(o, "col_scale", lambda: _u8(scale_bytes(M, K, True), dev))
     return o
 
 
@@ -578,7 +596,7 @@ def swiglu_quantize(y, m_splits, rowwise=True, colwise=True, swizzle=True, h_out
     dev = y.device
     o = _quant_outputs(dict(out or {}), M, F, rowwise, colwise, dev)
     if h_out:
-        o.setdefault("h", torch.empty((M, F), dtype=torch.bfloat16, device=dev))
+        _fill(o, "h", lambda: torch.empty((M, F), dtype=torch.bfloat16, device=dev))
     flags = ((ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
              | (DEQUANT_OUT if h_out else 0))
     _need(y, "y", M * F2 * 2, _BF16)
@@ -605,10 +623,10 @@ def swiglu_bwd_quantize(dh, y, m_splits, rowwise=True, colwise=True, swizzle=Tru
     dev = y.device
     o = _quant_outputs(dict(out or {}), M, F2, rowwise, colwise, dev)
     if dy_out:
-        o.setdefault("dy", torch.empty((M, F2), dtype=torch.bfloat16, device=dev))
+        _fill(o, "dy", lambda: torch.empty((M, F2), dtype=torch.bfloat16, device=dev))
     ws = None
     if dbias:
-        o.setdefault("dbias", torch.empty((E, F2), dtype=torch.float32, device=dev))
+        _fill(o, "dbias", lambda: torch.empty((E, F2), dtype=torch.float32, device=dev))
         ws = workspace if workspace is not None else _u8(max(16, workspace_bytes(OP_SWIGLU_BWD_QUANTIZE, M, 0, F, E)),
                                                          dev)
     flags = ((ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (SWIZZLE if swizzle else 0)
