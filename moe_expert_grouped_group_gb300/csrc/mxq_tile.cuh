@@ -443,32 +443,52 @@ __global__ void __launch_bounds__(kTileThreads)
                 [[maybe_unused]] uint8_t* rq = kRow && !kReq ? a.row_q + r0 * K + col : nullptr;
                 [[maybe_unused]] uint8_t* cq = kCol ? a.col_q + r0 * K + col : nullptr;
                 [[maybe_unused]] __nv_bfloat16* dq = kDeq ? a.deq_out + r0 * K + col : nullptr;
-    #pragma unroll 2
-                for (int r4 = 0; r4 < 32; r4 += 4) {
-                    uint2 u[4];
+    #pragma unroll 1
+                for (int r8 = 0; r8 < 32; r8 += 8) {
+                    // eight rows in flight: the loads of both four-row groups before any store (the stores
+                    // go through pointers the compiler cannot tell apart from the shared tile)
+                    uint2 u[8];
     #pragma unroll
-                    for (int k = 0; k < 4; ++k) u[k] = ld_row(r4 + k);
-                    [[maybe_unused]] uint32_t packed = 0;
+                    for (int k = 0; k < 8; ++k) u[k] = ld_row(r8 + k);
+                    [[maybe_unused]] uint32_t packed[2] = {0u, 0u};  // rowwise codes, one byte per row
                     if constexpr (kRow && !kReq) {
     #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t w2 = __vmaxu2(u[k].x & 0x7FFF7FFFu, u[k].y & 0x7FFF7FFFu);
-                            packed |= (max(w2 & 0xFFFFu, w2 >> 16) >> 7) << (8 * k);  // bf16 exponent field
-                        }
-                        packed = group8_max_u8x4(packed);
-                    }
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t m[4];
     #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int r = r4 + k;
+                            for (int k = 0; k < 4; ++k)
+                                m[k] = __vmaxu2(u[4 * h + k].x & 0x7FFF7FFFu, u[4 * h + k].y & 0x7FFF7FFFu);
+                            // |bits| maxima of rows (0, 1) and (2, 3) as 16-bit halves, then their bf16
+                            // exponent fields, one byte per row
+                            const uint32_t v01 =
+                                __vmaxu2(__byte_perm(m[0], m[1], 0x5410), __byte_perm(m[0], m[1], 0x7632));
+                            const uint32_t v23 =
+                                __vmaxu2(__byte_perm(m[2], m[3], 0x5410), __byte_perm(m[2], m[3], 0x7632));
+                            packed[h] = __byte_perm((v01 >> 7) & 0x00FF00FFu, (v23 >> 7) & 0x00FF00FFu, 0x6420);
+                        }
+    #pragma unroll
+                        for (int o = 4; o >= 1; o >>= 1)
+    #pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                packed[h] = __vmaxu4(packed[h], __shfl_xor_sync(0xffffffffu, packed[h], o));
+    #pragma unroll
+                        for (int h = 0; h < 2; ++h) packed[h] = __vsubus4(packed[h], 0x08080808u);  // max(e - 8, 0)
+                    }
+                    [[maybe_unused]] const uint64_t cinv01 = f2pack(cinv[0], cinv[1]), cinv23 = f2pack(cinv[2], cinv[3]);
+    #pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int r = r8 + k;
                         const bool valid = !kMask || r < vb;  // kPad: rows past the expert are not written
                         float v[4];
                         vals(r, u[k], v);
+                        const uint64_t v01 = f2pack(v[0], v[1]), v23 = f2pack(v[2], v[3]);
                         if constexpr (kRow && !kReq) {
-                            const uint32_t code = (uint32_t)max((int)((packed >> (8 * k)) & 0xFFu) - 8, 0);
-                            const float inv = inv_scale_from_code(code);
+                            const uint32_t code = (packed[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+                            const uint64_t inv = f2splat(inv_scale_from_code(code));
+                            const float2 s01 = f2unpack(f2mul(v01, inv)), s23 = f2unpack(f2mul(v23, inv));
                             if (valid)
                                 *reinterpret_cast<uint32_t*>(rq + r * Ku) =
-                                    cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+                                    cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
                             if ((lane & 7) == 0) {
                                 if (a.swizzle) s_rs[r * 16 + rg * 4 + blk] = valid ? (uint8_t)code : (uint8_t)0;
                                 else if (valid) a.row_s[(r0 + r) * (K / 32) + kt * 4 + blk] = (uint8_t)code;
@@ -476,8 +496,9 @@ __global__ void __launch_bounds__(kTileThreads)
                         }
                         if (!valid) continue;
                         if constexpr (kCol) {
-                            *reinterpret_cast<uint32_t*>(cq + r * Ku) = cvt_e4m3x2(v[0] * cinv[0], v[1] * cinv[1]) |
-                                                                        (cvt_e4m3x2(v[2] * cinv[2], v[3] * cinv[3]) << 16);
+                            const float2 s01 = f2unpack(f2mul(v01, cinv01)), s23 = f2unpack(f2mul(v23, cinv23));
+                            *reinterpret_cast<uint32_t*>(cq + r * Ku) =
+                                cvt_e4m3x2(s01.x, s01.y) | (cvt_e4m3x2(s23.x, s23.y) << 16);
                         }
                         if constexpr (kDeq) {
                             __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]);
