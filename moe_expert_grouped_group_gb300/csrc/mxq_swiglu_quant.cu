@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, kBwd ? 2 : 3)
         ColStats cs[kOut];
         uint8_t* g_row = stage + (warp * kPreRows) * (kTile * 2) + lane * 8;
         uint8_t* u_row = g_row + kTileBytes;
-#pragma unroll 4
+#pragma unroll 8
         for (int r = 0; r < kPreRows; ++r) {
             uint2* gp = reinterpret_cast<uint2*>(g_row + r * (kTile * 2));
             uint2* up = reinterpret_cast<uint2*>(u_row + r * (kTile * 2));
