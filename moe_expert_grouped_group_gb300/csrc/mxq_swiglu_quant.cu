@@ -18,8 +18,10 @@
 // -- gathering each column's exponent maximum (and dbias sum) in registers
 // on the way. After one exchange of those 16-row statistics through shared
 // memory (a 32-row colwise block is two warps), every warp encodes its own
-// rows rowwise and colwise: the same codes as "SwiGLU, then group_quantize"
-// bit for bit, while h (or dY1) never makes a round trip through HBM.
+// rows rowwise and colwise (the backward's dg and du rows side by side, two
+// independent chains per step): the same codes as "SwiGLU, then
+// group_quantize" bit for bit, while h (or dY1) never makes a round trip
+// through HBM.
 #include <cuda_bf16.h>
 
 #include <algorithm>
