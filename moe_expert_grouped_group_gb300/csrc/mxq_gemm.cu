@@ -959,6 +959,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // blocks, its last pair tile's second CTA recomputes the first CTA's rows and
 // does not store them. wgrad tiles pair 256 rows of N with 256 columns of K
 // of one expert.
+//
+// Clusters take tiles in rounds of one tile each, serpentine within a round.
+// wgrad's tiles are listed heaviest expert first, and the rounds are walked
+// alternately from the two ends of that list (first, last, second, second
+// last, ...): every cluster then interleaves light tiles, whose time is their
+// dW stores, with heavy tiles, whose time is their MMAs.
 namespace pair {
 
 constexpr int PSTAGES = 6;
@@ -1068,6 +1074,11 @@ struct PSched {
     __device__ int64_t pick(int64_t i, int c, int nc) const {
         const int64_t base = i * nc;
         return (i & 1) ? base + (nc - 1 - c) : base + c;
+    }
+    // wgrad walk: step i takes round i/2 of the heaviest-first list when i is even, round
+    // rounds-1-i/2 when odd (a round's slot past the last tile is invalid and skipped)
+    __device__ int64_t pick_alt(int64_t i, int c, int nc, int64_t rounds) const {
+        return pick((i & 1) ? rounds - 1 - (i >> 1) : (i >> 1), c, nc);
     }
     __device__ PTile get(int64_t t) const {
         PTile T;
@@ -1199,6 +1210,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     else if (kMode == kDgrad) { S.tiles_n = p.K / 256; S.total = (int64_t)s_aux[p.E] * S.tiles_n; }
     else { S.tiles_n = (p.N / 256) * (p.K / 256); S.total = (int64_t)p.E * S.tiles_n; }
     const int ncl = gridDim.x / 2, cl = blockIdx.x / 2;
+    constexpr bool kAlt = kMode == kWgrad;
+    const int64_t rounds = (S.total + ncl - 1) / ncl;
+    // the i-th tile of this cluster's walk (invalid: none in that slot)
+    auto walk = [&](int64_t i) -> PTile { return S.get(kAlt ? S.pick_alt(i, cl, ncl, rounds) : S.pick(i, cl, ncl)); };
     const uint32_t a_mn = (kMode == kWgrad) ? 1u : 0u;
     const uint32_t b_mn = (kMode == kFprop || kMode == kFpropSwiglu) ? 0u : 1u;
 
@@ -1208,8 +1223,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             for (int64_t i = 0;; ++i) {
-                const PTile T = S.get(S.pick(i, cl, ncl));
-                if (!T.valid) break;
+                if (kAlt && i >= rounds) break;
+                const PTile T = walk(i);
+                if (!T.valid) {
+                    if (kAlt) continue;
+                    break;
+                }
                 int ax, ay, bx, by, adx, ady, bdx, bdy;
                 int sa, sb0, sb1;  // scale atom rows (512 B each) of K block 0; +1 per block
                 if (kMode == kFprop) {
@@ -1278,8 +1297,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) id[k] = idesc_pair(a_mn, b_mn, (uint32_t)k);
             for (int64_t i = 0;; ++i) {
-                const PTile T = S.get(S.pick(i, cl, ncl));
-                if (!T.valid) break;
+                if (kAlt && i >= rounds) break;
+                const PTile T = walk(i);
+                if (!T.valid) {
+                    if (kAlt) continue;
+                    break;
+                }
                 if (T.nk == 0) continue;  // empty wgrad expert: the epilogues write zeros without the accumulator
                 if (!mbar_wait(acc_empty, aphase ^ 1, abort_flag)) break;
                 fence_after();
@@ -1325,8 +1348,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             const int64_t row_bytes = 256 * esz, vec_per_row = row_bytes / 16;
             uint8_t* out = static_cast<uint8_t*>(p.out);
             for (int64_t i = 0;; ++i) {
-                const PTile T = S.get(S.pick(i, cl, ncl));
-                if (!T.valid) break;
+                if (kAlt && i >= rounds) break;
+                const PTile T = walk(i);
+                if (!T.valid) {
+                    if (kAlt) continue;
+                    break;
+                }
                 if (T.nk != 0) continue;
                 uint8_t* base = out + (T.out_row * p.K + T.c0) * esz;
                 for (int64_t v = lane; v < 128 * vec_per_row; v += 32) {
@@ -1344,8 +1371,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         const uint32_t lead_acc_empty = mapa(acc_empty, 0);
         uint32_t aphase = 0;
         for (int64_t i = 0;; ++i) {
-            const PTile T = S.get(S.pick(i, cl, ncl));
-            if (!T.valid) break;
+            if (kAlt && i >= rounds) break;
+            const PTile T = walk(i);
+            if (!T.valid) {
+                if (kAlt) continue;
+                break;
+            }
             if constexpr (kMode == kFpropSwiglu) {
                 const bool ok = mbar_wait(acc_full, aphase, abort_flag);
                 __syncwarp();
