@@ -156,6 +156,27 @@ def test_wgrad_bf16_out_and_accumulate(mxq):
     assert bool((acc[1] == 0).all())
 
 
+@pytest.mark.parametrize("splits,N,K", [
+    ([128], 256, 256),                                # one tile, one pair
+    ([256, 128, 0, 384, 128], 768, 1280),             # 75 tiles: as many pairs, one full round
+    ([256, 128, 0, 384, 128], 1024, 1024),            # 80 tiles: a round of 76 pairs and a partial one
+    ([128, 384, 0, 256, 0, 128, 256], 256, 5632),     # 154 tiles: two rounds and a partial third
+])
+def test_wgrad_round_walk_all_entries(mxq, splits, N, K):
+    """wgrad deals its heaviest-first tiles in rounds of one tile per cluster pair (76 pairs on a
+    GB300; fewer tiles launch fewer pairs) and walks the rounds alternately from both ends of the list,
+    the last round possibly partial. Every dW entry is checked, so each tile must be computed exactly
+    once, and every empty expert's dW must be zero."""
+    op = rand_case(splits, N, K, 11 + N + K)
+    e, n, k = np.meshgrid(np.arange(op.E), np.arange(N), np.arange(K), indexing="ij")
+    dw = f64(op.gpu_wgrad(mxq))
+    ref, mag = op.ref_wgrad(e.ravel(), n.ravel(), k.ravel())
+    assert scaled_error(dw.ravel(), ref, mag) <= TOL_F32
+    for ee, m in enumerate(splits):
+        if m == 0:
+            assert not dw[ee].any(), ee
+
+
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_wgrad_overwrites_a_prefilled_output(mxq, out_bf16):
     """Without MXQ_ACCUMULATE every dW entry is written: the empty experts' with exact zeros, the
