@@ -10,7 +10,13 @@
 // grouped linear module with single grouped weight support": device m_splits
 // read without a host sync, one grouped weight (E,out,in), 2-D grouped bias.)
 //
-// Kernel: persistent, one CTA (320 threads) per SM, warp-specialised.
+// Two kernels. The plain fprop, dgrad and wgrad on 128-aligned experts, and
+// FC1 with the SwiGLU epilogue, run on two-SM pair tiles (namespace pair
+// below: tcgen05 cta_group::2, 256 x 256 tiles). The one-SM kernel described
+// here serves padded grouping, the FC2 dgrad with the SwiGLU-backward
+// epilogue, more than 512 experts and wgrad with N not a multiple of 256.
+//
+// One-SM kernel: persistent, one CTA (320 threads) per SM, warp-specialised.
 //   warp 0      TMA producer: 128x128-byte E4M3 boxes (128B swizzle) for A and
 //               two for B per 128-deep K block, plus the 512-byte scale atoms
 //               (already in the tensor-core 128x4 layout) by bulk copy;
