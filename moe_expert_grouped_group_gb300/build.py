@@ -50,13 +50,39 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source with its comments removed and trailing blanks trimmed, so that editing a comment
+    leaves the stamp of the code alone. String and character literals are kept whole."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).split("\n")]
+    return "\n".join(ln for ln in lines if ln)
+
+
 def source_stamp(files=("mxq_gemm.cu", "mxq_common.cuh", "mxq_internal.h")) -> str:
-    """Hash of the named kernel sources (identifies the code an ncu capture measured)."""
+    """Hash of the named kernel sources without their comments (identifies the code an ncu capture
+    measured; a comment edit does not change it)."""
     h = hashlib.sha256()
     for name in files:
-        with open(os.path.join(CSRC, name), "rb") as f:
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

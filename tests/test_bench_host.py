@@ -1,4 +1,6 @@
-"""Host-side arithmetic of bench.py: the per-expert GEMM roofline."""
+"""Host-side arithmetic of bench.py: the per-expert GEMM roofline, the step layout, the source stamp."""
+import pathlib
+
 import pytest
 
 import bench
@@ -91,3 +93,25 @@ def test_inner_repeat_reaches_the_timed_region():
         pass
 
     assert bench.inner_repeat(_St(), 20, 7) == 7
+
+
+def test_source_stamp_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    """The GEMM traffic record is matched to the code by a stamp of the kernel sources without their
+    comments: editing a comment keeps it, editing code changes it, and string literals (PTX) stay whole."""
+    from moe_expert_grouped_group_gb300 import build as B
+
+    text = 'int a = 1;  // note\n/* block\n comment */ asm("mov.b32 %0, 1; // kept");\nchar c = \'"\';\n'
+    code = B._code_only(text)
+    assert "note" not in code and "block" not in code
+    assert 'asm("mov.b32 %0, 1; // kept");' in code and "char c = '\"';" in code
+
+    for n in ("mxq_gemm.cu", "mxq_common.cuh", "mxq_internal.h"):
+        (tmp_path / n).write_text(pathlib.Path(B.CSRC, n).read_text())
+    monkeypatch.setattr(B, "CSRC", str(tmp_path))
+    base = B.source_stamp()
+    gemm = tmp_path / "mxq_gemm.cu"
+    src = gemm.read_text()
+    gemm.write_text("// a new comment line\n" + src.replace("// One-SM kernel", "// The one-SM kernel", 1))
+    assert B.source_stamp() == base
+    gemm.write_text(src + "\nstatic int mxq_stamp_probe = 1;\n")
+    assert B.source_stamp() != base
