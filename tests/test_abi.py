@@ -61,3 +61,28 @@ def test_no_cpu_fallback_in_the_product_path():
             src = open(os.path.join(pkg, name)).read()
             assert "oracle" not in src, name
             assert "numpy" not in src, name
+
+
+def test_compute_entry_points_refuse_without_a_gb300(L):
+    """On a host without a GB300 every compute entry point of the hot path returns MXQ_ERR_ARCH, with
+    well-formed arguments, before any pointer is used: nothing runs on the host in its place. The
+    addresses below are never dereferenced."""
+    import torch
+
+    if torch.cuda.is_available() and torch.cuda.get_device_capability(0) == (10, 3):
+        pytest.skip("a GB300 is present: the GPU tests cover these calls")
+    P, WS = 1 << 20, 1 << 30                     # a 16-byte-aligned address; a workspace size large enough
+    M = N = K = 256
+    E = 2
+    ROW, COL, SWZ, ARCH = 1, 2, 4, -4
+    calls = {
+        "mxq_group_quantize": (P, M, K, E, P, ROW | COL | SWZ, P, P, P, P, None, None, P, P, WS, None),
+        "mxq_requant_colwise": (P, P, M, K, E, P, COL | SWZ, P, P, P, None, None, None, P, P, WS, None),
+        "mxq_grouped_dbias": (P, M, N, E, P, P, P, P, WS, None),
+        "mxq_grouped_gemm_fprop": (P, P, P, P, None, M, N, K, E, P, P, P, P, WS, None),
+        "mxq_grouped_gemm_dgrad": (P, P, P, P, M, N, K, E, P, P, P, P, WS, None),
+        "mxq_grouped_gemm_wgrad": (P, P, P, P, M, N, K, E, P, 0, P, P, P, WS, None),
+        "mxq_swiglu_fwd": (P, M, K, P, None),
+    }
+    for name, args in calls.items():
+        assert getattr(L, name)(*args) == ARCH, name
